@@ -1,0 +1,338 @@
+"""fp64 definition of causal grouped-query attention, paged split-K decode and
+the LSE merge (TEST INFRASTRUCTURE: tests, smoke check and CPU baseline only).
+
+Sources, by page title and section:
+
+* ``causal_forward_kernel.py`` (flash-attention-scratch),
+  ``_flash_attention_forward_gqa_kernel``: the GQA head map
+  (``kv_head = q_head // (Hq // Hkv)``) and what the blockwise loop computes.
+* ``gpt-o3 / triton6fd1ef`` (FlashInfer-style GQA prefill), ``_gqa_prefill_kernel``,
+  "Number of KV tokens visible to this query": bottom-right causal alignment,
+  a key j is visible to query i iff ``j < min(kv_len, i + 1 + delta)`` with
+  ``delta = kv_len - q_len``.
+* ``splitk_kernels.py`` (xformers), ``_fwd_kernel_splitK``: split-K chunks,
+  block-table indirection, the empty-chunk convention (O = 0, LSE = -inf) and
+  the natural-log LSE written by its epilogue; its docstring and
+  ``cast_uint32_to_half2`` / ``dequantize``: the int4 row format;
+  ``_splitK_reduce``: the LSE-weighted merge.
+
+Readings taken where the pages disagree or are silent:
+
+* LSE is the natural log-sum-exp of the scaled scores, with no epsilon.
+* Rows with no visible key yield O = 0 and LSE = -inf.
+* Inputs are the exact low-precision values upcast to float64; nothing here
+  rounds intermediate values.
+"""
+
+import math
+
+import numpy as np
+
+NEG_INF = -np.inf
+
+
+# --------------------------------------------------------------------------
+# Dense causal GQA prefill
+# --------------------------------------------------------------------------
+
+def visible_mask(q_len, kv_len, rows=None):
+    """Boolean visibility matrix ``[len(rows), kv_len]``.
+
+    Bottom-right causal alignment (``gpt-o3 / triton6fd1ef``,
+    ``_gqa_prefill_kernel``, the ``kv_allowed`` computation): with
+    ``delta = kv_len - q_len`` key ``j`` is visible to query ``i`` iff
+    ``j <= i + delta`` (and ``j < kv_len``, which the range of ``j`` gives).
+    """
+    delta = kv_len - q_len
+    i = np.arange(q_len) if rows is None else np.asarray(rows, dtype=np.int64)
+    j = np.arange(kv_len)
+    return j[None, :] <= (i[:, None] + delta)
+
+
+def attend(q, k, v, mask, scale):
+    """Masked softmax attention of one head, materialised in full.
+
+    ``q [M, D]``, ``k [N, D]``, ``v [N, Dv]``, ``mask`` bool ``[M, N]``.
+    Returns ``o [M, Dv]`` and the natural-log ``lse [M]``:
+
+    1. ``S = scale * q k^T``, masked entries set to -inf;
+    2. ``lse = m + log(sum_j exp(S - m))`` with ``m`` the row maximum;
+    3. ``P = exp(S - lse)``, ``O = P v``;
+    4. a row with no visible key gets ``O = 0`` and ``lse = -inf``.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    m_rows, n_keys = q.shape[0], k.shape[0]
+    s = scale * (q @ k.T)
+    s = np.where(mask, s, NEG_INF)
+    if n_keys == 0:
+        return np.zeros((m_rows, v.shape[1])), np.full(m_rows, NEG_INF)
+    m = s.max(axis=1)
+    has_key = np.isfinite(m)
+    m_safe = np.where(has_key, m, 0.0)
+    l = np.exp(s - m_safe[:, None]).sum(axis=1)
+    lse = np.where(has_key, m_safe + np.log(np.where(has_key, l, 1.0)), NEG_INF)
+    p = np.where(has_key[:, None], np.exp(s - np.where(has_key, lse, 0.0)[:, None]), 0.0)
+    return p @ v, lse
+
+
+def _default_scale(d):
+    # 1/sqrt(D), the wrappers' default softmax scale on every page.
+    return 1.0 / math.sqrt(d)
+
+
+def prefill(q, k, v, scale=None):
+    """Causal GQA prefill: ``q [B, Hq, q_len, D]``, ``k, v [B, Hkv, kv_len, D]``.
+
+    Returns ``o [B, Hq, q_len, D]`` and ``lse [B, Hq, q_len]`` in float64.
+    K and V are expanded to Hq heads with an explicit ``np.repeat`` so that
+    query head ``h`` reads key/value head ``h // (Hq // Hkv)``
+    (``causal_forward_kernel.py``, "map the current query head to its shared
+    key/value head").
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    bsz, hq, q_len, d = q.shape
+    hkv, kv_len = k.shape[1], k.shape[2]
+    if hq % hkv != 0:
+        raise ValueError("Hq must be a multiple of Hkv")
+    group = hq // hkv
+    scale = _default_scale(d) if scale is None else float(scale)
+    k_rep = np.repeat(k, group, axis=1)
+    v_rep = np.repeat(v, group, axis=1)
+    mask = visible_mask(q_len, kv_len)
+    o = np.zeros((bsz, hq, q_len, v.shape[3]))
+    lse = np.zeros((bsz, hq, q_len))
+    for b in range(bsz):
+        for h in range(hq):
+            o[b, h], lse[b, h] = attend(q[b, h], k_rep[b, h], v_rep[b, h], mask, scale)
+    return o, lse
+
+
+def prefill_rows(q, k, v, b, h, rows, scale=None):
+    """The same definition as :func:`prefill`, for selected query rows
+    ``rows`` of one (batch ``b``, query head ``h``); used to check sampled
+    outputs of workloads too large to materialise whole."""
+    d = q.shape[3]
+    hq, hkv = q.shape[1], k.shape[1]
+    q_len, kv_len = q.shape[2], k.shape[2]
+    if hq % hkv != 0:
+        raise ValueError("Hq must be a multiple of Hkv")
+    group = hq // hkv
+    scale = _default_scale(d) if scale is None else float(scale)
+    rows = np.asarray(rows, dtype=np.int64)
+    # explicit repeat of this batch entry's key/value heads
+    k_rep = np.repeat(np.asarray(k[b], dtype=np.float64), group, axis=0)
+    v_rep = np.repeat(np.asarray(v[b], dtype=np.float64), group, axis=0)
+    qb = np.asarray(q[b, h], dtype=np.float64)[rows]
+    return attend(qb, k_rep[h], v_rep[h], visible_mask(q_len, kv_len, rows), scale)
+
+
+# --------------------------------------------------------------------------
+# int4 row format (splitk_kernels.py: docstring of _fwd_kernel_splitK,
+# cast_uint32_to_half2, dequantize)
+# --------------------------------------------------------------------------
+
+def fp16_from_bits(bits):
+    """IEEE binary16 values from their 16-bit patterns, as float64."""
+    return np.asarray(bits, dtype=np.uint16).view(np.float16).astype(np.float64)
+
+
+def unpack_coef_word(word):
+    """One quantisation coefficient word: the low 16 bits are the fp16 scale,
+    the high 16 bits the fp16 offset (``cast_uint32_to_half2``)."""
+    w = int(np.uint32(np.int64(word) & 0xFFFFFFFF))
+    return float(fp16_from_bits(w & 0xFFFF)), float(fp16_from_bits(w >> 16))
+
+
+def dequant_int4_row(words, d, n_groups):
+    """Dequantise one packed row, element by element.
+
+    ``words``: ``n_groups + d // 8`` 32-bit words.  The first ``n_groups`` are
+    coefficient words (group order); then come the code words, group by group,
+    ``d // 8 // n_groups`` words per group.  Inside a code word nibble ``j``
+    (bits ``4j .. 4j+3``) holds element ``word_in_group * 8 + j`` of the group,
+    and group ``g`` covers elements ``[g*d/n_groups, (g+1)*d/n_groups)``.
+    Value = ``scale * code + offset`` in exact arithmetic.
+    """
+    if n_groups not in (1, 2, 4, 8) or d % (8 * n_groups) != 0:
+        raise ValueError("unsupported int4 layout")
+    words = [int(np.uint32(np.int64(x) & 0xFFFFFFFF)) for x in words]
+    if len(words) != n_groups + d // 8:
+        raise ValueError("row has the wrong number of words")
+    per_group = d // n_groups
+    words_per_group = per_group // 8
+    out = np.zeros(d)
+    for g in range(n_groups):
+        scale, offset = unpack_coef_word(words[g])
+        for w in range(words_per_group):
+            word = words[n_groups + g * words_per_group + w]
+            for j in range(8):
+                code = (word >> (4 * j)) & 0xF
+                out[g * per_group + w * 8 + j] = scale * code + offset
+    return out
+
+
+def dequant_int4_rows(words, d, n_groups):
+    """The same layout as :func:`dequant_int4_row`, for an array of rows
+    ``words [..., n_groups + d // 8]``, written with numpy broadcasting."""
+    if n_groups not in (1, 2, 4, 8) or d % (8 * n_groups) != 0:
+        raise ValueError("unsupported int4 layout")
+    w = np.asarray(words).astype(np.int64) & 0xFFFFFFFF
+    if w.shape[-1] != n_groups + d // 8:
+        raise ValueError("row has the wrong number of words")
+    coef = w[..., :n_groups]
+    scale = fp16_from_bits(coef & 0xFFFF)                     # [..., G]
+    offset = fp16_from_bits(coef >> 16)                       # [..., G]
+    code_words = w[..., n_groups:]                            # [..., d/8]
+    shifts = 4 * np.arange(8)
+    codes = (code_words[..., :, None] >> shifts) & 0xF        # [..., d/8, 8]
+    codes = codes.reshape(w.shape[:-1] + (d,)).astype(np.float64)
+    per_group = d // n_groups
+    scale_e = np.repeat(scale, per_group, axis=-1)
+    offset_e = np.repeat(offset, per_group, axis=-1)
+    return scale_e * codes + offset_e
+
+
+# --------------------------------------------------------------------------
+# Paged split-K decode (splitk_kernels.py: _fwd_kernel_splitK)
+# --------------------------------------------------------------------------
+
+def paged_row_index(block_table, b, t, page_size):
+    """Physical row of logical token ``t`` of sequence ``b``:
+    ``block_table[b, t // page_size] * page_size + t % page_size``
+    ("Offset in integer pages" / ``physical_page_idx`` in ``_fwd_kernel_splitK``)."""
+    return int(block_table[b][t // page_size]) * page_size + t % page_size
+
+
+def gather_paged_rows(cache, block_table, b, t_lo, t_hi, page_size):
+    """Rows ``[t_lo, t_hi)`` of sequence ``b`` from a paged pool
+    ``cache [num_pages, page_size, Hkv, W]``, one token at a time."""
+    out = []
+    for t in range(t_lo, t_hi):
+        page = int(block_table[b][t // page_size])
+        out.append(np.asarray(cache[page, t % page_size]))
+    if not out:
+        return np.zeros((0,) + tuple(cache.shape[2:]), dtype=np.asarray(cache[:0]).dtype)
+    return np.stack(out)
+
+
+def _kv_rows(cache, block_table, b, lo, hi, page_size, kv_format, d, n_groups):
+    rows = gather_paged_rows(cache, block_table, b, lo, hi, page_size)
+    if kv_format == "int4":
+        return dequant_int4_rows(rows, d, n_groups)
+    if kv_format != "dense":
+        raise ValueError("kv_format must be 'dense' or 'int4'")
+    return rows.astype(np.float64)
+
+
+def num_splits(max_kv_len, split_tokens):
+    """Number of split-K chunks for the longest sequence (at least one)."""
+    return max(1, -(-int(max_kv_len) // int(split_tokens)))
+
+
+def decode_split_partials(q, k_cache, v_cache, block_table, seq_lens, page_size,
+                          split_tokens, scale=None, kv_format="dense", n_groups=1,
+                          max_kv_len=None, batches=None):
+    """Per-split partial results of single-query decode.
+
+    ``q [B, Hq, D]``; caches ``[num_pages, page_size, Hkv, D]`` (dense values)
+    or ``[num_pages, page_size, Hkv, n_groups + D/8]`` (int4 words).
+    Split ``s`` of sequence ``b`` covers tokens
+    ``[s*split_tokens, min((s+1)*split_tokens, len_b))``; with one query per
+    sequence every cached token is visible.  An empty split gives ``O_s = 0``
+    and ``LSE_s = -inf`` (the early exit and the ``l == 0`` guard of
+    ``_fwd_kernel_splitK``).  Returns ``o_part [B, Hq, S, D]`` and
+    ``lse_part [B, Hq, S]``; ``batches`` restricts the work to some sequences
+    (the other entries stay zero / -inf).
+    """
+    q = np.asarray(q, dtype=np.float64)
+    bsz, hq, d = q.shape
+    hkv = k_cache.shape[2]
+    if hq % hkv != 0:
+        raise ValueError("Hq must be a multiple of Hkv")
+    group = hq // hkv
+    scale = _default_scale(d) if scale is None else float(scale)
+    lens = [int(x) for x in np.asarray(seq_lens).reshape(-1)]
+    if max_kv_len is None:
+        max_kv_len = max(lens) if lens else 0
+    n_split = num_splits(max_kv_len, split_tokens)
+    o_part = np.zeros((bsz, hq, n_split, d))
+    lse_part = np.full((bsz, hq, n_split), NEG_INF)
+    for b in (range(bsz) if batches is None else batches):
+        for s in range(n_split):
+            lo = s * split_tokens
+            hi = min(lo + split_tokens, lens[b])
+            if hi <= lo:
+                continue
+            k_rows = _kv_rows(k_cache, block_table, b, lo, hi, page_size, kv_format, d, n_groups)
+            v_rows = _kv_rows(v_cache, block_table, b, lo, hi, page_size, kv_format, d, n_groups)
+            k_rep = np.repeat(k_rows, group, axis=1)          # [n, Hq, D]
+            v_rep = np.repeat(v_rows, group, axis=1)
+            every = np.ones((1, hi - lo), dtype=bool)
+            for h in range(hq):
+                o, lse = attend(q[b, h][None, :], k_rep[:, h], v_rep[:, h], every, scale)
+                o_part[b, h, s] = o[0]
+                lse_part[b, h, s] = lse[0]
+    return o_part, lse_part
+
+
+def decode_unsplit(q, k_cache, v_cache, block_table, seq_lens, page_size, scale=None,
+                   kv_format="dense", n_groups=1, batches=None):
+    """Single-query decode over each whole sequence in one piece (no split)."""
+    q = np.asarray(q, dtype=np.float64)
+    bsz, hq, d = q.shape
+    hkv = k_cache.shape[2]
+    group = hq // hkv
+    scale = _default_scale(d) if scale is None else float(scale)
+    lens = [int(x) for x in np.asarray(seq_lens).reshape(-1)]
+    o_out = np.zeros((bsz, hq, d))
+    lse_out = np.full((bsz, hq), NEG_INF)
+    for b in (range(bsz) if batches is None else batches):
+        k_rows = _kv_rows(k_cache, block_table, b, 0, lens[b], page_size, kv_format, d, n_groups)
+        v_rows = _kv_rows(v_cache, block_table, b, 0, lens[b], page_size, kv_format, d, n_groups)
+        k_rep = np.repeat(k_rows, group, axis=1)
+        v_rep = np.repeat(v_rows, group, axis=1)
+        every = np.ones((1, lens[b]), dtype=bool)
+        for h in range(hq):
+            o, lse = attend(q[b, h][None, :], k_rep[:, h], v_rep[:, h], every, scale)
+            o_out[b, h], lse_out[b, h] = o[0], lse[0]
+    return o_out, lse_out
+
+
+# --------------------------------------------------------------------------
+# LSE-weighted merge (splitk_kernels.py: _splitK_reduce)
+# --------------------------------------------------------------------------
+
+def lse_merge(o_part, lse_part):
+    """Merge split partials ``o_part [..., S, D]``, ``lse_part [..., S]``.
+
+    ``M = max_s LSE_s``; ``w_s = exp(LSE_s - M)``;
+    ``O = sum_s w_s O_s / sum_s w_s``; ``LSE = M + log(sum_s w_s)``;
+    when every ``LSE_s`` is -inf the result is ``O = 0``, ``LSE = -inf``.
+    """
+    o_part = np.asarray(o_part, dtype=np.float64)
+    lse_part = np.asarray(lse_part, dtype=np.float64)
+    if lse_part.shape[-1] == 0:
+        return np.zeros(o_part.shape[:-2] + o_part.shape[-1:]), np.full(lse_part.shape[:-1], NEG_INF)
+    m = lse_part.max(axis=-1)
+    alive = np.isfinite(m)
+    m_safe = np.where(alive, m, 0.0)
+    w = np.where(alive[..., None], np.exp(lse_part - m_safe[..., None]), 0.0)
+    wsum = w.sum(axis=-1)
+    o = np.where(alive[..., None],
+                 (w[..., None] * o_part).sum(axis=-2) / np.where(alive, wsum, 1.0)[..., None],
+                 0.0)
+    lse = np.where(alive, m_safe + np.log(np.where(alive, wsum, 1.0)), NEG_INF)
+    return o, lse
+
+
+def decode(q, k_cache, v_cache, block_table, seq_lens, page_size, split_tokens, scale=None,
+           kv_format="dense", n_groups=1, max_kv_len=None, batches=None):
+    """Split-K decode: the per-split partials merged by :func:`lse_merge`."""
+    o_part, lse_part = decode_split_partials(q, k_cache, v_cache, block_table, seq_lens,
+                                             page_size, split_tokens, scale, kv_format,
+                                             n_groups, max_kv_len, batches)
+    return lse_merge(o_part, lse_part)
