@@ -1,0 +1,467 @@
+"""Benchmark of the causal GQA attention hot path on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input,
+inputs resident in HBM:
+  1. causal GQA prefill, Llama-style workload: B=1, Hq=32, Hkv=4, q_len=2048,
+     kv_len=4096 (bottom-right, delta=2048), D=128, bf16;
+  2. paged split-K decode, bf16 cache: B=64, Hq=32, Hkv=8, D=128, lengths
+     U[512, 32768], 256-token pages, split 2048, then the LSE merge;
+  3. paged split-K decode, int4 cache (N_GROUPS=4): B=16, length 16384, then
+     the LSE merge.
+Each kernel is timed with CUDA events on the stream it runs on; a 256 MiB
+buffer is written before each kernel to flush the 129 MB L2 (the flush is
+outside the kernel timings).  The headline value is prefill TFLOP/s with
+causal-halved FLOPs = 2*B*Hq*D*(visible pairs)*2; decode is reported in GB/s
+of algorithmic bytes.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Under torchrun every rank runs its own replica of the step (independent
+problems, no collective on the data path); rank 0 prints one JSON line.
+"""
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "causal GQA prefill TFLOP/s and paged decode KV GB/s, % of GB300 roofline"
+L2_FLUSH_BYTES = 256 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------- accounting
+
+def visible_pairs(q_len, kv_len):
+    """Number of (query, key) pairs with key <= query + (kv_len - q_len)."""
+    delta = kv_len - q_len
+    return sum(max(0, min(kv_len, i + delta + 1)) for i in range(q_len))
+
+
+def prefill_flops(shape):
+    return 2 * shape.B * shape.Hq * shape.D * visible_pairs(shape.q_len, shape.kv_len) * 2
+
+
+def decode_bytes(shape, lens):
+    """Algorithmic bytes of one decode: every cached K and V row once, Q, the
+    block-table entries and lengths read; O and LSE written.  The split
+    partials (kernel-to-kernel scratch) are not counted."""
+    row = shape.D * 2 if shape.kv_format == "dense" else (shape.n_groups + shape.D // 8) * 4
+    kv = sum(lens) * shape.Hkv * row * 2
+    pages = sum(-(-n // shape.page_size) for n in lens)
+    q = shape.B * shape.Hq * shape.D * 2
+    o = shape.B * shape.Hq * shape.D * 2 + shape.B * shape.Hq * 4
+    return {"kv": kv, "q": q, "o": o, "table": pages * 4 + shape.B * 4,
+            "kernel": kv + q + pages * 4 + shape.B * 4, "path": kv + q + o + pages * 4 + shape.B * 4}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return {k: float(pk[k]) for k in FALLBACK_PEAKS}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def load_traffic():
+    """Per-launch DRAM bytes from the committed ncu summary, keyed by kernel,
+    kept only while the kernel's source is unchanged since the capture."""
+    out = {}
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return out
+    for line in open(path):
+        parts = line.split()
+        if len(parts) != 4 or line.startswith("#"):
+            continue
+        name, nbytes, src, digest = parts
+        srcp = os.path.join(ROOT, "causal_gqa_flashattention_attn_gb300", "csrc", src)
+        if os.path.exists(srcp) and hashlib.sha256(open(srcp, "rb").read()).hexdigest()[:16] == digest:
+            out[name] = float(nbytes)
+    return out
+
+
+def aggregate(per_rank_ms, world):
+    """Whole-job timing: the slowest rank's time for each kernel."""
+    return {k: max(v[k] for v in per_rank_ms) for k in per_rank_ms[0]}
+
+
+# ------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", str(gpu_id)], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sms, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sms.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        if not sms:
+            return None
+        sms.sort()
+        return {"sm_mhz": sms[len(sms) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sms)}
+
+
+def gpu_id_for_smi(torch, dev):
+    try:
+        uuid = torch.cuda.get_device_properties(dev).uuid
+        s = str(uuid)
+        return s if s.startswith("GPU-") else "GPU-" + s
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        ids = [x for x in vis.split(",") if x.strip()]
+        return ids[dev.index or 0] if ids else str(dev.index or 0)
+
+
+# ------------------------------------------------------------- CPU baseline
+
+def oracle_prefill_sample(seconds, shape):
+    """The oracle as it stands on the host cores: whole heads of the prefill
+    workload (every query row of head h of batch 0) until `seconds` pass."""
+    import oracle
+    import synth
+    q, k, v = synth.prefill_inputs(shape, seed=0)
+    qn = q[:1].double().numpy()
+    kn, vn = k[:1].double().numpy(), v[:1].double().numpy()
+    per_head = 2 * shape.D * visible_pairs(shape.q_len, shape.kv_len) * 2
+    rows = list(range(shape.q_len))
+    heads, t0 = 0, time.perf_counter()
+    while True:
+        oracle.prefill_rows(qn, kn, vn, 0, heads % shape.Hq, rows)
+        heads += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return per_head * heads / el / 1e12, heads, el
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+# --------------------------------------------------------------- the bench
+
+def run_ours(args, rank, world, dist):
+    import torch
+
+    import causal_gqa_flashattention_attn_gb300 as attn
+    import synth
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    attn.lib()
+    stream = torch.cuda.current_stream(dev)
+
+    pf = synth.LLAMA_GQA_PREFILL
+    d16 = synth.PAGED_DECODE_BF16
+    d4 = synth.PAGED_DECODE_INT4
+    seed = 1000 * rank
+    q, k, v = (t.to(dev) for t in synth.prefill_inputs(pf, seed=seed))
+    o = torch.empty_like(q)
+    lse = torch.empty(pf.B, pf.Hq, pf.q_len, dtype=torch.float32, device=dev)
+    dec = {}
+    for name, shape in (("decode_bf16", d16), ("decode_int4", d4)):
+        inp = synth.decode_inputs(shape, seed=seed)
+        t = {kk: vv.to(dev) for kk, vv in inp.items() if torch.is_tensor(vv)}
+        max_len = shape.len_hi
+        ws = torch.empty(attn.attn_decode_workspace_bytes(shape.B, shape.Hq, max_len, shape.split_tokens, shape.D),
+                         dtype=torch.uint8, device=dev)
+        o_part, lse_part = attn.decode_partials_view(ws, shape.B, shape.Hq, max_len, shape.split_tokens, shape.D)
+        dec[name] = dict(shape=shape, t=t, lens=inp["lens"], max_len=max_len, ws=ws,
+                         o_part=o_part.view(shape.B * shape.Hq, -1, shape.D),
+                         lse_part=lse_part.view(shape.B * shape.Hq, -1),
+                         o=torch.empty(shape.B * shape.Hq, shape.D, dtype=torch.bfloat16, device=dev),
+                         lse=torch.empty(shape.B * shape.Hq, dtype=torch.float32, device=dev),
+                         bytes=decode_bytes(shape, inp["lens"]))
+        del inp
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    kernels = ["prefill", "decode_bf16", "merge_bf16", "decode_int4", "merge_int4"]
+    launches_per_step = len(kernels)
+
+    def step(ev):
+        flush.fill_(1.0)
+        ev["prefill"][0].record(stream)
+        attn.attn_prefill_fwd(q, k, v, o=o, lse=lse, dev_status=status, stream=stream)
+        ev["prefill"][1].record(stream)
+        for name in ("decode_bf16", "decode_int4"):
+            d = dec[name]
+            sh, t = d["shape"], d["t"]
+            flush.fill_(1.0)
+            ev[name][0].record(stream)
+            attn.attn_decode_paged_splitk(t["q"], t["k_cache"], t["v_cache"], t["block_table"], t["seq_lens"],
+                                          sh.split_tokens, d["max_len"], n_groups=sh.n_groups, workspace=d["ws"],
+                                          dev_status=status, stream=stream, write_output=False)
+            ev[name][1].record(stream)
+            mname = name.replace("decode", "merge")
+            ev[mname][0].record(stream)
+            attn.attn_lse_merge(d["o_part"], d["lse_part"], o=d["o"], lse=d["lse"], stream=stream)
+            ev[mname][1].record(stream)
+
+    def new_events():
+        return {kn: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for kn in kernels}
+
+    for _ in range(args.warmup):
+        step(new_events())
+    torch.cuda.synchronize(dev)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(gpu_id_for_smi(torch, dev)) if rank == 0 else None
+    region0 = torch.cuda.Event(enable_timing=True)
+    region1 = torch.cuda.Event(enable_timing=True)
+    evs = [new_events() for _ in range(args.steps)]
+    region0.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    region1.record(stream)
+    torch.cuda.synchronize(dev)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop() if sampler is not None else None
+    assert status.item() == 0, f"device status {status.item()}"
+
+    ms = {kn: sum(e[kn][0].elapsed_time(e[kn][1]) for e in evs) / args.steps for kn in kernels}
+    region_ms = region0.elapsed_time(region1) / args.steps
+    if dist is not None:
+        import torch.distributed as tdist
+        vals = torch.tensor([ms[kn] for kn in kernels] + [region_ms], dtype=torch.float64)
+        vals = vals.to(dev) if tdist.get_backend() == "nccl" else vals
+        tdist.all_reduce(vals, op=tdist.ReduceOp.MAX)
+        vals = vals.cpu().tolist()
+        ms = dict(zip(kernels, vals[:-1]))
+        region_ms = vals[-1]
+
+    # ---------------------------------------------------------------- e2e
+    # the same prefill through the public call with host buffers: pinned
+    # host -> device copies of Q, K, V and a device -> host read of O and LSE
+    # inside the timed region, every step
+    hq_, hk_, hv_ = (t.cpu().pin_memory() for t in (q, k, v))
+    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+    def e2e_step():
+        dq.copy_(hq_, non_blocking=True)
+        dk.copy_(hk_, non_blocking=True)
+        dv.copy_(hv_, non_blocking=True)
+        attn.attn_prefill_fwd(dq, dk, dv, o=o, lse=lse, stream=stream)
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    h2d = sum(t.numel() * t.element_size() for t in (q, k, v))
+    d2h = o.numel() * o.element_size() + lse.numel() * lse.element_size()
+
+    if rank != 0:
+        return None
+
+    # ------------------------------------------------------------ report
+    peaks, peak_src = load_peaks()
+    traffic = load_traffic()
+    flops = prefill_flops(pf)
+    tflops = world * flops / (ms["prefill"] * 1e-3) / 1e12
+    rep = {}
+    rep["prefill"] = dict(bound="tensor", achieved=flops / (ms["prefill"] * 1e-3) / 1e12,
+                          peak=peaks["bf16_tflops"], unit="TFLOP/s", work=flops, src="prefill_tc.cu",
+                          kernel="prefill_tc_kernel")
+    for name in ("decode_bf16", "decode_int4"):
+        d = dec[name]
+        kb = d["bytes"]["kernel"]
+        rep[name] = dict(bound="hbm", achieved=kb / (ms[name] * 1e-3) / 1e9, peak=peaks["hbm_gbs"], unit="GB/s",
+                         work=kb, src="decode.cu" if name == "decode_bf16" else "decode_int4.cu",
+                         kernel="decode_bf16_kernel" if name == "decode_bf16" else "decode_int4_kernel")
+        mname = name.replace("decode", "merge")
+        n_rows = d["shape"].B * d["shape"].Hq
+        s_max = d["o_part"].shape[1]
+        mb = n_rows * s_max * (d["shape"].D + 1) * 4 + n_rows * (d["shape"].D * 2 + 4)
+        rep[mname] = dict(bound="hbm", achieved=mb / (ms[mname] * 1e-3) / 1e9, peak=peaks["hbm_gbs"], unit="GB/s",
+                          work=mb, src="merge.cu", kernel="lse_merge_kernel")
+    kernels_out = []
+    for kn in kernels:
+        r = rep[kn]
+        kernels_out.append({"name": kn, "kernel": r["kernel"], "ms": round(ms[kn], 5), "bound": r["bound"],
+                            "achieved": round(r["achieved"], 2), "peak": r["peak"], "unit": r["unit"],
+                            "frac": round(r["achieved"] / r["peak"], 4),
+                            "traffic": traffic.get(kn)})
+    dominant = max(kernels, key=lambda kn: ms[kn])
+    dom = rep[dominant]
+    path = {}
+    for name in ("decode_bf16", "decode_int4"):
+        d = dec[name]
+        t_ms = ms[name] + ms[name.replace("decode", "merge")]
+        path[name] = {"value": round(world * d["bytes"]["path"] / (t_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                      "ms": round(t_ms, 5), "kv_bytes": d["bytes"]["kv"], "algorithmic_bytes": d["bytes"]["path"],
+                      "frac_of_hbm": round(d["bytes"]["path"] / (t_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        val, heads, el = oracle_prefill_sample(args.cpu_seconds, pf)
+        cpu = {"value": val, "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
+               "sample": f"{heads} whole heads (all {pf.q_len} query rows x {pf.kv_len} keys) of the prefill "
+                         f"workload, {el:.1f} s of numpy float64 on the host"}
+    line = {
+        "metric": METRIC,
+        "value": round(tflops, 3),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(sum(ms.values()), 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": "prefill B1 Hq32 Hkv4 q2048 kv4096 D128 bf16 (bottom-right causal) + paged split-K decode "
+                        "bf16 B64 Hq32 Hkv8 D128 len U[512,32768] page256 split2048 + int4 (N_GROUPS=4) paged "
+                        "decode B16 len16384",
+            "prefill": {"B": pf.B, "Hq": pf.Hq, "Hkv": pf.Hkv, "q_len": pf.q_len, "kv_len": pf.kv_len, "D": pf.D,
+                        "flops": flops},
+            "decode_bf16": {"B": d16.B, "Hq": d16.Hq, "Hkv": d16.Hkv, "D": d16.D, "tokens": sum(dec["decode_bf16"]["lens"]),
+                            "page": d16.page_size, "split": d16.split_tokens},
+            "decode_int4": {"B": d4.B, "Hq": d4.Hq, "Hkv": d4.Hkv, "D": d4.D, "tokens": sum(dec["decode_int4"]["lens"]),
+                            "n_groups": d4.n_groups, "page": d4.page_size, "split": d4.split_tokens},
+            "global_batch": world,
+            "parallelism": f"replicas x{world}",
+            "l2": "256 MiB buffer written before each kernel; flush excluded from kernel times",
+            "peaks": peak_src,
+        },
+        "decode": path,
+        "roofline": {"kernel": dominant, "bound": dom["bound"], "achieved": round(dom["achieved"], 2),
+                     "peak": dom["peak"], "unit": dom["unit"], "frac": round(dom["achieved"] / dom["peak"], 4),
+                     "traffic": traffic.get(dominant), "peak_source": f"{peak_src} (MEASURED_PEAKS.json)"
+                     if peak_src == "measured" else "fallback"},
+        "prefill_roofline": {"bound": "tensor", "achieved": round(rep["prefill"]["achieved"], 2),
+                             "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                             "frac": round(rep["prefill"]["achieved"] / peaks["bf16_tflops"], 4),
+                             "traffic": traffic.get("prefill")},
+        "kernels": kernels_out,
+        "region_ms_per_step_incl_flush": round(region_ms, 5),
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms": round(e2e_ms, 5),
+                "what": "prefill through attn_prefill_fwd with pinned host Q/K/V copied in and O/LSE copied out "
+                        "each step"},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    return line
+
+
+def run_reference(args, rank):
+    """The oracle arm: the CPU oracle as it stands, timed on the host cores on
+    a bounded sample of the same prefill workload (one head per step)."""
+    import synth
+    if rank != 0:
+        return None
+    pf = synth.LLAMA_GQA_PREFILL
+    per_head = 2 * pf.D * visible_pairs(pf.q_len, pf.kv_len) * 2
+    import oracle
+    q, k, v = synth.prefill_inputs(pf, seed=0)
+    qn, kn, vn = q[:1].double().numpy(), k[:1].double().numpy(), v[:1].double().numpy()
+    rows = list(range(pf.q_len))
+    for i in range(args.warmup):
+        oracle.prefill_rows(qn, kn, vn, 0, i % pf.Hq, rows)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        oracle.prefill_rows(qn, kn, vn, 0, i % pf.Hq, rows)
+    el = time.perf_counter() - t0
+    val = per_head * args.steps / el / 1e12
+    sample = f"one whole head (all {pf.q_len} query rows x {pf.kv_len} keys) of the prefill workload per step"
+    return {"impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "prefill B1 Hq32 Hkv4 q2048 kv4096 D128 (bottom-right causal), CPU oracle"},
+            "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist = None
+    if args.impl == "reference":
+        line = run_reference(args, rank)
+    else:
+        if world > 1:
+            import torch
+            import torch.distributed as tdist
+            tdist.init_process_group(backend="nccl" if torch.cuda.is_available() else "gloo")
+            dist = tdist
+        line = run_ours(args, rank, world, dist)
+        if dist is not None:
+            dist.destroy_process_group()
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,186 @@
+"""GB300 (sm_103a) causal grouped-query attention: Python binding of libattn.so.
+
+This module only marshals arguments: it takes torch tensors that already live
+on the GPU, passes their device pointers and sizes to the C ABI declared in
+``include/attn.h`` and raises on a non-OK status.  Every step of the
+computation runs in the library's CUDA kernels; there is no fallback of any
+kind, and importing a function of this module fails loudly when the library
+has not been built.
+
+Entry points (names as in the C ABI):
+  attn_prefill_fwd          causal GQA prefill -> (O, LSE)
+  attn_decode_workspace_bytes
+  attn_decode_paged_splitk  single-query split-K decode over a paged cache
+  attn_lse_merge            LSE-weighted merge of split partials
+  attn_status_string
+"""
+
+import ctypes
+import math
+import os
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libattn.so")
+
+# status and dtype codes of include/attn.h
+ATTN_OK = 0
+ATTN_F32, ATTN_BF16, ATTN_F16, ATTN_INT4_PACKED = 0, 1, 2, 3
+ATTN_DEV_PAGE_OUT_OF_RANGE = 0x1
+ATTN_DEV_SEQ_TOO_LONG = 0x2
+ATTN_DEV_WAIT_TIMEOUT = 0x4
+
+EXPORTED = ("attn_prefill_fwd", "attn_decode_workspace_bytes", "attn_decode_paged_splitk",
+            "attn_lse_merge", "attn_status_string", "attn_abi_version")
+
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__(f"{fn} failed: {attn_status_string(status)} ({status})")
+
+
+def lib():
+    """The loaded library (ctypes), with argument and result types declared."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+                           "(or python causal_gqa_flashattention_attn_gb300/_build.py)")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    L.attn_prefill_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32, vp, vp]
+    L.attn_prefill_fwd.restype = i32
+    L.attn_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
+    L.attn_decode_workspace_bytes.restype = sz
+    L.attn_decode_paged_splitk.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, i32, i32, i32,
+                                           i32, f32, vp, sz, vp, vp, vp, vp]
+    L.attn_decode_paged_splitk.restype = i32
+    L.attn_lse_merge.argtypes = [vp, vp, i32, i32, i32, vp, vp, i32, vp]
+    L.attn_lse_merge.restype = i32
+    L.attn_status_string.argtypes = [i32]
+    L.attn_status_string.restype = ctypes.c_char_p
+    L.attn_abi_version.argtypes = []
+    L.attn_abi_version.restype = i32
+    _lib = L
+    return L
+
+
+def attn_status_string(status):
+    return lib().attn_status_string(int(status)).decode()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_ptr(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(fn, status):
+    if status != ATTN_OK:
+        raise AttnError(fn, status)
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+_DT = {torch.float32: ATTN_F32, torch.bfloat16: ATTN_BF16, torch.float16: ATTN_F16}
+
+
+def attn_prefill_fwd(q, k, v, o=None, lse=None, scale=None, dev_status=None, stream=None, want_lse=True):
+    """Causal GQA prefill (bottom-right alignment).
+
+    ``q [B, Hq, q_len, D]``, ``k, v [B, Hkv, kv_len, D]`` (bf16 or fp32).
+    Returns ``(o, lse)`` with ``o`` like ``q`` and ``lse [B, Hq, q_len]``
+    float32 (natural log), allocating them when not given.
+    """
+    _need_cuda(q, k, v, o, lse, dev_status)
+    bsz, hq, q_len, d = q.shape
+    hkv, kv_len = k.shape[1], k.shape[2]
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty(bsz, hq, q_len, dtype=torch.float32, device=q.device)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    st = lib().attn_prefill_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _DT.get(q.dtype, -1), bsz, hq,
+                                hkv, q_len, kv_len, d, float(scale), _ptr(dev_status), _stream_ptr(stream))
+    _check("attn_prefill_fwd", st)
+    return o, lse
+
+
+def attn_decode_workspace_bytes(B, Hq, max_kv_len, split_tokens, D):
+    return int(lib().attn_decode_workspace_bytes(B, Hq, max_kv_len, split_tokens, D))
+
+
+def attn_decode_paged_splitk(q, k_cache, v_cache, block_table, seq_lens, split_tokens, max_kv_len, scale=None,
+                             n_groups=1, workspace=None, o=None, lse=None, dev_status=None, stream=None,
+                             write_output=True):
+    """Single-query split-K decode over a paged KV cache.
+
+    ``q [B, Hq, D]`` bf16; caches ``[num_pages, page_size, Hkv, D]`` bf16 or
+    ``[num_pages, page_size, Hkv, n_groups + D/8]`` int32 (int4 rows);
+    ``block_table [B, max_pages]`` and ``seq_lens [B]`` int32.  Returns
+    ``(o, lse, workspace)``; with ``write_output=False`` only the split
+    partials are produced in ``workspace`` (``o`` and ``lse`` are None).
+    """
+    _need_cuda(q, k_cache, v_cache, block_table, seq_lens, workspace, o, lse, dev_status)
+    bsz, hq, d = q.shape
+    num_pages, page_size, hkv = k_cache.shape[0], k_cache.shape[1], k_cache.shape[2]
+    kv_dtype = ATTN_INT4_PACKED if k_cache.dtype == torch.int32 else _DT.get(k_cache.dtype, -1)
+    need = attn_decode_workspace_bytes(bsz, hq, max_kv_len, split_tokens, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    if write_output:
+        if o is None:
+            o = torch.empty(bsz, hq, d, dtype=q.dtype, device=q.device)
+        if lse is None:
+            lse = torch.empty(bsz, hq, dtype=torch.float32, device=q.device)
+    else:
+        o = lse = None
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    st = lib().attn_decode_paged_splitk(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1], _ptr(seq_lens), kv_dtype,
+        n_groups, bsz, hq, hkv, d, num_pages, page_size, split_tokens, max_kv_len, float(scale), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(o), _ptr(lse), _ptr(dev_status), _stream_ptr(stream))
+    _check("attn_decode_paged_splitk", st)
+    return o, lse, workspace
+
+
+def decode_partials_view(workspace, B, Hq, max_kv_len, split_tokens, D):
+    """Views ``(o_part [B, Hq, S, D], lse_part [B, Hq, S])`` of a decode
+    workspace, in the layout documented for attn_decode_workspace_bytes."""
+    S = max(1, -(-max_kv_len // split_tokens))
+    n_o = B * Hq * S * D
+    off = ((n_o * 4 + 15) // 16) * 16
+    f = workspace.view(torch.uint8)
+    o_part = f[:n_o * 4].view(torch.float32).view(B, Hq, S, D)
+    lse_part = f[off:off + B * Hq * S * 4].view(torch.float32).view(B, Hq, S)
+    return o_part, lse_part
+
+
+def attn_lse_merge(o_part, lse_part, o=None, lse=None, o_dtype=torch.float32, stream=None):
+    """Merge ``o_part [N, S, D]`` / ``lse_part [N, S]`` (float32) by LSE weight.
+    Returns ``(o [N, D], lse [N])``."""
+    _need_cuda(o_part, lse_part, o, lse)
+    n, s, d = o_part.shape
+    if o is None:
+        o = torch.empty(n, d, dtype=o_dtype, device=o_part.device)
+    if lse is None:
+        lse = torch.empty(n, dtype=torch.float32, device=o_part.device)
+    st = lib().attn_lse_merge(_ptr(o_part), _ptr(lse_part), n, s, d, _ptr(o), _ptr(lse), _DT.get(o.dtype, -1),
+                              _stream_ptr(stream))
+    _check("attn_lse_merge", st)
+    return o, lse

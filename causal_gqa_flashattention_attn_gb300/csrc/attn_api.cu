@@ -1,0 +1,177 @@
+// attn_api.cu - the C ABI declared in include/attn.h: argument validation,
+// workspace accounting, TMA descriptor encoding and kernel dispatch.
+//
+// The errors the pages' Python wrappers raise become status codes: the
+// Hq % Hkv assertion of "causal_forward_kernel.py" flash_attention_forward,
+// the shape checks of "gpt-o3 / triton6fd1ef" run, and the static_asserts of
+// "splitk_kernels.py" _fwd_kernel_splitK (N_GROUPS in {1, 2, 4, 8}).
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace gb300 {
+
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+void load_encode() {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+}
+
+constexpr int kMaxDevices = 64;
+int g_sm_count[kMaxDevices] = {0};
+}  // namespace
+
+bool encode_tiled_map(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base,
+                      const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                      CUtensorMapSwizzle swizzle) {
+    std::call_once(g_encode_once, load_encode);
+    if (g_encode == nullptr) return false;
+    cuuint32_t elem_strides[5] = {1, 1, 1, 1, 1};
+    cuuint64_t d[5], s[4];
+    cuuint32_t bx[5];
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        bx[i] = box[i];
+    }
+    for (int i = 0; i + 1 < rank; ++i) s[i] = strides_bytes[i];
+    const CUresult r = g_encode(map, dtype, static_cast<cuuint32_t>(rank), const_cast<void*>(base), d, s, bx,
+                                elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+int device_sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < kMaxDevices && g_sm_count[dev] > 0) return g_sm_count[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < kMaxDevices) g_sm_count[dev] = n;
+    return n;
+}
+
+}  // namespace gb300
+
+using namespace gb300;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+attn_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
+
+int split_count(int max_kv_len, int split_tokens) {
+    const long long s = (static_cast<long long>(max_kv_len) + split_tokens - 1) / split_tokens;
+    return s < 1 ? 1 : static_cast<int>(s);
+}
+
+size_t round16(size_t x) { return (x + 15) & ~static_cast<size_t>(15); }
+
+}  // namespace
+
+extern "C" {
+
+const char* attn_status_string(attn_status_t status) {
+    switch (status) {
+        case ATTN_OK: return "ok";
+        case ATTN_ERR_INVALID_ARG: return "invalid argument";
+        case ATTN_ERR_UNSUPPORTED: return "unsupported configuration";
+        case ATTN_ERR_WORKSPACE: return "workspace missing or too small";
+        case ATTN_ERR_CUDA: return "CUDA error";
+        case ATTN_ERR_DEVICE_FAULT: return "device-side fault";
+        default: return "unknown status";
+    }
+}
+
+int attn_abi_version(void) { return 100; }
+
+attn_status_t attn_prefill_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                               attn_dtype_t dtype, int B, int Hq, int Hkv, int q_len, int kv_len, int D,
+                               float scale, int32_t* dev_status, void* stream) {
+    if (q == nullptr || k == nullptr || v == nullptr || o == nullptr) return ATTN_ERR_INVALID_ARG;
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || q_len <= 0 || kv_len <= 0 || D <= 0) return ATTN_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return ATTN_ERR_INVALID_ARG;
+    if (dtype != ATTN_F32 && dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
+    if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+    if (static_cast<long long>(B) * Hq * q_len >= (1LL << 31) || static_cast<long long>(B) * Hkv * kv_len >= (1LL << 31))
+        return ATTN_ERR_UNSUPPORTED;
+    PrefillArgs a{q, k, v, o, lse, static_cast<int>(dtype), B, Hq, Hkv, q_len, kv_len, D, scale, dev_status};
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (dtype == ATTN_BF16 && prefill_tc_supported(a)) return from_cuda(launch_prefill_tc(a, s));
+    return from_cuda(launch_prefill_simt(a, s));
+}
+
+size_t attn_decode_workspace_bytes(int B, int Hq, int max_kv_len, int split_tokens, int D) {
+    if (B <= 0 || Hq <= 0 || max_kv_len < 0 || split_tokens <= 0 || D <= 0) return 0;
+    const size_t S = static_cast<size_t>(split_count(max_kv_len, split_tokens));
+    const size_t rows = static_cast<size_t>(B) * Hq;
+    return round16(rows * S * D * sizeof(float)) + round16(rows * S * sizeof(float));
+}
+
+attn_status_t attn_decode_paged_splitk(const void* q, const void* k_cache, const void* v_cache,
+                                       const int32_t* block_table, int max_pages_per_seq,
+                                       const int32_t* seq_lens, attn_dtype_t kv_dtype, int n_groups, int B,
+                                       int Hq, int Hkv, int D, int num_pages, int page_size, int split_tokens,
+                                       int max_kv_len, float scale, void* workspace, size_t workspace_bytes,
+                                       void* o, float* lse, int32_t* dev_status, void* stream) {
+    if (q == nullptr || k_cache == nullptr || v_cache == nullptr || block_table == nullptr || seq_lens == nullptr)
+        return ATTN_ERR_INVALID_ARG;
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || num_pages <= 0 || page_size <= 0 || split_tokens <= 0 ||
+        max_kv_len < 0 || max_pages_per_seq <= 0)
+        return ATTN_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0 || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || (o != nullptr && !aligned16(o)))
+        return ATTN_ERR_INVALID_ARG;
+    if (D != 128) return ATTN_ERR_UNSUPPORTED;
+    const int G = Hq / Hkv;
+    if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return ATTN_ERR_UNSUPPORTED;
+    if (page_size % 64 != 0 || split_tokens % 64 != 0) return ATTN_ERR_UNSUPPORTED;
+    if (static_cast<long long>(num_pages) * page_size >= (1LL << 31)) return ATTN_ERR_UNSUPPORTED;
+    int fmt = 0;
+    if (kv_dtype == ATTN_BF16) {
+        fmt = 0;
+    } else if (kv_dtype == ATTN_INT4_PACKED) {
+        fmt = 1;
+        if (n_groups != 1 && n_groups != 2 && n_groups != 4 && n_groups != 8) return ATTN_ERR_UNSUPPORTED;
+        if ((static_cast<long long>(Hkv) * (n_groups + D / 8)) % 4 != 0) return ATTN_ERR_UNSUPPORTED;
+    } else {
+        return ATTN_ERR_UNSUPPORTED;
+    }
+    const size_t need = attn_decode_workspace_bytes(B, Hq, max_kv_len, split_tokens, D);
+    if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return ATTN_ERR_WORKSPACE;
+    const int S = split_count(max_kv_len, split_tokens);
+    const size_t rows = static_cast<size_t>(B) * Hq;
+    float* o_part = static_cast<float*>(workspace);
+    float* lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + round16(rows * S * D * sizeof(float)));
+    DecodeArgs a{q,        k_cache, v_cache, block_table, max_pages_per_seq, seq_lens, fmt, n_groups, B, Hq, Hkv,
+                 D,        num_pages, page_size, split_tokens, max_kv_len, S, scale, o_part, lse_part, dev_status};
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_decode(a, s);
+    if (e != cudaSuccess) return ATTN_ERR_CUDA;
+    if (o != nullptr) e = launch_merge(o_part, lse_part, static_cast<int>(rows), S, D, o, lse, ATTN_BF16, s);
+    return from_cuda(e);
+}
+
+attn_status_t attn_lse_merge(const float* o_part, const float* lse_part, int N, int S, int D, void* o, float* lse,
+                             attn_dtype_t o_dtype, void* stream) {
+    if (o_part == nullptr || lse_part == nullptr || o == nullptr) return ATTN_ERR_INVALID_ARG;
+    if (N < 0 || S < 1 || D < 4 || D % 4 != 0) return ATTN_ERR_INVALID_ARG;
+    if (D > 1024) return ATTN_ERR_UNSUPPORTED;
+    if (o_dtype != ATTN_F32 && o_dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
+    if (!aligned16(o_part) || !aligned16(o)) return ATTN_ERR_INVALID_ARG;
+    return from_cuda(launch_merge(o_part, lse_part, N, S, D, o, lse, o_dtype, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

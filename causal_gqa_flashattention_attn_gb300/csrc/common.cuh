@@ -1,0 +1,76 @@
+// common.cuh - host/device declarations shared by the kernels and the C ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/attn.h"
+
+namespace gb300 {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Records a device-side error bit (never traps).
+__device__ __forceinline__ void flag_status(int32_t* status, int32_t bit) {
+    if (status != nullptr) atomicOr(status, bit);
+}
+
+__device__ __forceinline__ uint8_t* align_1024(uint8_t* p) {
+    return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+__device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// ---------------------------------------------------------------- host side
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// dependency on libcuda).  Returns false on failure.
+bool encode_tiled_map(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base,
+                      const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                      CUtensorMapSwizzle swizzle);
+
+int device_sm_count();
+
+// Launchers (return a cudaError_t from the launch).
+struct DecodeArgs {
+    const void* q;
+    const void* k_cache;
+    const void* v_cache;
+    const int32_t* block_table;
+    int max_pages;
+    const int32_t* seq_lens;
+    int kv_format;   // 0 bf16, 1 int4
+    int n_groups;
+    int B, Hq, Hkv, D, num_pages, page_size, split_tokens, max_kv_len, n_split;
+    float scale;
+    float* o_part;
+    float* lse_part;
+    int32_t* dev_status;
+};
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+
+cudaError_t launch_merge(const float* o_part, const float* lse_part, int N, int S, int D, void* o,
+                         float* lse, int o_dtype, cudaStream_t stream);
+
+struct PrefillArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    void* o;
+    float* lse;
+    int dtype;  // ATTN_F32 / ATTN_BF16
+    int B, Hq, Hkv, q_len, kv_len, D;
+    float scale;
+    int32_t* dev_status;
+};
+cudaError_t launch_prefill_simt(const PrefillArgs& a, cudaStream_t stream);
+bool prefill_tc_supported(const PrefillArgs& a);
+cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream);
+
+}  // namespace gb300

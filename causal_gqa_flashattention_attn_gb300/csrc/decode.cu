@@ -1,0 +1,349 @@
+// decode.cu - single-query split-K decode over a paged KV cache.
+//
+// Follows "splitk_kernels.py" (xformers), _fwd_kernel_splitK: one program per
+// (split, sequence, head), a chunk of split_tokens keys per split, the block
+// table giving the physical page of each page_size tokens, an online softmax
+// in the exp2 domain, and an epilogue that writes the split's O already
+// divided by its own l plus the split's natural-log LSE (O = 0, LSE = -inf for
+// an empty split).
+//
+// GB300 design (not the pages' design):
+//   * one CTA per (split, kv head, sequence) serves all G = Hq/Hkv query heads
+//     of the group, so each K/V byte is read from HBM exactly once;
+//   * a producer warp streams 64-token K/V tiles with TMA (128-byte swizzle)
+//     through a ring of shared-memory stages, guided by the block table;
+//   * four consumer warps each take 16 tokens of a tile and compute the G
+//     score rows and the P.V update with m16n8k16 bf16 tensor-core MMAs
+//     (heads padded to 16 rows), keeping the online-softmax state in
+//     registers; row max / sum reductions are warp shuffles;
+//   * the four warps' partial states are merged through shared memory.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace gb300 {
+namespace {
+
+constexpr int kD = 128;                         // head dim handled here
+constexpr int kTileTok = 64;                    // tokens per pipeline stage
+constexpr int kConsumers = 4;                   // consumer warps
+constexpr int kThreads = 32 * (kConsumers + 1); // + 1 producer warp
+constexpr int kHalfBytes = kTileTok * 128;      // one 64-column half of a K or V tile
+constexpr int kKVTileBytes = 2 * kHalfBytes;    // 16 KB per K (or V) tile
+constexpr int kStageBytes = 2 * kKVTileBytes;   // K + V
+
+struct Params {
+    const __nv_bfloat16* q;  // [B, Hq, D]
+    const int32_t* block_table;
+    const int32_t* seq_lens;
+    int max_pages, B, Hq, Hkv, num_pages, page_size, split_tokens, max_kv_len, n_split;
+    float scale_log2;
+    float* o_part;    // [B, Hq, S, D]
+    float* lse_part;  // [B, Hq, S]
+    int32_t* status;
+};
+
+// Byte offset of 16-byte chunk `c` (0..15 across D) of token row `r` inside a
+// K or V tile written by TMA with 128-byte swizzle (two 64-column halves).
+__device__ __forceinline__ uint32_t tile_off(int r, int c) {
+    return (c >> 3) * kHalfBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+}
+
+template <int G, int NS>
+__global__ void __launch_bounds__(kThreads) decode_bf16_kernel(const __grid_constant__ CUtensorMap k_map,
+                                                               const __grid_constant__ CUtensorMap v_map,
+                                                               const Params p) {
+    static_assert(G == 1 || G == 2 || G == 4 || G == 8 || G == 16, "group size");
+    constexpr bool kTwoRows = (G > 8);  // rows g+8 of the m16 fragment hold real heads
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align_1024(smem_raw);
+    __shared__ __align__(8) uint64_t full_bar[NS];
+    __shared__ __align__(8) uint64_t empty_bar[NS];
+    __shared__ int s_abort;
+
+    const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const size_t head_stride = static_cast<size_t>(p.n_split) * kD;
+    float* o_base = p.o_part + ((static_cast<size_t>(b) * p.Hq + kvh * G) * p.n_split + split) * kD;
+    float* lse_base = p.lse_part + (static_cast<size_t>(b) * p.Hq + kvh * G) * p.n_split + split;
+
+    int len = p.seq_lens[b];
+    const int cap = min(p.max_kv_len, p.max_pages * p.page_size);
+    if (len < 0 || len > cap) {
+        if (threadIdx.x == 0) flag_status(p.status, ATTN_DEV_SEQ_TOO_LONG);
+        len = len < 0 ? 0 : cap;
+    }
+    const int lo = split * p.split_tokens;
+    const int hi = min(lo + p.split_tokens, len);
+    if (lo >= hi) {  // empty split: O = 0, LSE = -inf
+        for (int i = threadIdx.x; i < G * kD; i += kThreads) o_base[(i / kD) * head_stride + (i % kD)] = 0.f;
+        if (threadIdx.x < G) lse_base[threadIdx.x * p.n_split] = -INFINITY;
+        return;
+    }
+    const int n_tiles = (hi - lo + kTileTok - 1) / kTileTok;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], kConsumers);
+        }
+        s_abort = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == kConsumers) {
+        // ---------------------------------------------------------------- producer
+        if (lane == 0) {
+            tma_prefetch_desc(&k_map);
+            tma_prefetch_desc(&v_map);
+            const int32_t* table = p.block_table + static_cast<size_t>(b) * p.max_pages;
+            for (int t = 0; t < n_tiles; ++t) {
+                const int slot = t % NS;
+                if (t >= NS && !mbar_wait(&empty_bar[slot], ((t / NS) - 1) & 1)) {
+                    flag_status(p.status, ATTN_DEV_WAIT_TIMEOUT);
+                    atomicExch(&s_abort, 1);
+                    break;
+                }
+                const int tok = lo + t * kTileTok;
+                const int page = table[tok / p.page_size];
+                if (page < 0 || page >= p.num_pages) {
+                    flag_status(p.status, ATTN_DEV_PAGE_OUT_OF_RANGE);
+                    mbar_arrive(&full_bar[slot]);  // release the consumers; the tile is not loaded
+                    continue;
+                }
+                const int row = page * p.page_size + tok % p.page_size;
+                uint8_t* st = smem + slot * kStageBytes;
+                mbar_arrive_expect_tx(&full_bar[slot], kStageBytes);
+                tma_load_3d(st, &k_map, &full_bar[slot], 0, kvh, row);
+                tma_load_3d(st + kHalfBytes, &k_map, &full_bar[slot], 64, kvh, row);
+                tma_load_3d(st + kKVTileBytes, &v_map, &full_bar[slot], 0, kvh, row);
+                tma_load_3d(st + kKVTileBytes + kHalfBytes, &v_map, &full_bar[slot], 64, kvh, row);
+            }
+        }
+        return;
+    }
+
+    // -------------------------------------------------------------------- consumers
+    const int g = lane >> 2, t4 = lane & 3;
+    // Q fragments (A operand, rows = heads of the group, zero past G).
+    uint32_t qa[8][4];
+    {
+        const __nv_bfloat16* qh = p.q + (static_cast<size_t>(b) * p.Hq + kvh * G) * kD;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            const int d0 = kk * 16 + 2 * t4;
+            qa[kk][0] = g < G ? *reinterpret_cast<const uint32_t*>(qh + g * kD + d0) : 0u;
+            qa[kk][2] = g < G ? *reinterpret_cast<const uint32_t*>(qh + g * kD + d0 + 8) : 0u;
+            qa[kk][1] = (kTwoRows && g + 8 < G) ? *reinterpret_cast<const uint32_t*>(qh + (g + 8) * kD + d0) : 0u;
+            qa[kk][3] =
+                (kTwoRows && g + 8 < G) ? *reinterpret_cast<const uint32_t*>(qh + (g + 8) * kD + d0 + 8) : 0u;
+        }
+    }
+    float o_acc[16][4];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) o_acc[i][0] = o_acc[i][1] = o_acc[i][2] = o_acc[i][3] = 0.f;
+    float m_run[2] = {-INFINITY, -INFINITY};
+    float l_part[2] = {0.f, 0.f};
+    const float sl2 = p.scale_log2;
+
+    for (int t = 0; t < n_tiles; ++t) {
+        const int slot = t % NS;
+        if (!mbar_wait(&full_bar[slot], (t / NS) & 1)) {
+            flag_status(p.status, ATTN_DEV_WAIT_TIMEOUT);
+            break;
+        }
+        if (s_abort) break;
+        const int tok0 = lo + t * kTileTok + warp * 16;
+        const int n_valid = min(max(hi - tok0, 0), 16);
+        const uint32_t k_s = smem_u32(smem + slot * kStageBytes);
+        const uint32_t v_s = k_s + kKVTileBytes;
+        if (n_valid > 0) {
+            if (n_valid < 16) {
+                // rows past the end of the sequence: zero V so 0 * garbage stays 0
+                uint8_t* vt = smem + slot * kStageBytes + kKVTileBytes;
+                for (int i = lane; i < (16 - n_valid) * 16; i += 32) {
+                    const int r = warp * 16 + n_valid + i / 16, c = i % 16;
+                    *reinterpret_cast<uint4*>(vt + tile_off(r, c)) = make_uint4(0, 0, 0, 0);
+                }
+                __syncwarp();
+            }
+            // S = Q K^T for 16 tokens (two n8 tiles), fp32.
+            float s[2][4];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+            {
+                const int mi = lane >> 3, r = warp * 16 + (mi >> 1) * 8 + (lane & 7);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    uint32_t b0, b1, b2, b3;
+                    ldmatrix_x4(b0, b1, b2, b3, k_s + tile_off(r, 2 * kk + (mi & 1)));
+                    mma_bf16_16816(s[0], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
+                    mma_bf16_16816(s[1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b2, b3);
+                }
+            }
+            // mask tokens past the end, scale to the log2 domain
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int tok = nt * 8 + 2 * t4 + (e & 1);
+                    s[nt][e] = tok < n_valid ? s[nt][e] * sl2 : -INFINITY;
+                }
+            }
+            // online softmax per row (row g: e = 0,1; row g+8: e = 2,3)
+            uint32_t pa[4];
+            bool need_rescale = false;
+            float alpha[2] = {1.f, 1.f};
+#pragma unroll
+            for (int rr = 0; rr < (kTwoRows ? 2 : 1); ++rr) {
+                float mx = fmaxf(fmaxf(s[0][2 * rr], s[0][2 * rr + 1]), fmaxf(s[1][2 * rr], s[1][2 * rr + 1]));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                // lazy rescale: keep a stale max unless the new one exceeds it by 2^8
+                if (mx > m_run[rr] + 8.f) {
+                    alpha[rr] = ex2(m_run[rr] - mx);  // 0 when m_run = -inf
+                    m_run[rr] = mx;
+                    need_rescale = true;
+                }
+                const float m_use = m_run[rr] == -INFINITY ? 0.f : m_run[rr];
+                const float p0 = ex2(s[0][2 * rr] - m_use), p1 = ex2(s[0][2 * rr + 1] - m_use);
+                const float p2 = ex2(s[1][2 * rr] - m_use), p3 = ex2(s[1][2 * rr + 1] - m_use);
+                l_part[rr] = l_part[rr] * alpha[rr] + ((p0 + p1) + (p2 + p3));
+                pa[rr] = pack_bf16x2(p0, p1);
+                pa[rr + 2] = pack_bf16x2(p2, p3);
+            }
+            if (!kTwoRows) {
+                pa[1] = 0u;
+                pa[3] = 0u;
+            }
+            if (__any_sync(0xffffffffu, need_rescale)) {
+#pragma unroll
+                for (int dn = 0; dn < 16; ++dn) {
+                    o_acc[dn][0] *= alpha[0];
+                    o_acc[dn][1] *= alpha[0];
+                    o_acc[dn][2] *= alpha[1];
+                    o_acc[dn][3] *= alpha[1];
+                }
+            }
+            // O += P V (A = P from registers, B = V^T via ldmatrix.trans)
+            {
+                const int mi = lane >> 3, r = warp * 16 + (mi & 1) * 8 + (lane & 7);
+#pragma unroll
+                for (int dn = 0; dn < 16; dn += 2) {
+                    uint32_t b0, b1, b2, b3;
+                    ldmatrix_x4_trans(b0, b1, b2, b3, v_s + tile_off(r, dn + (mi >> 1)));
+                    mma_bf16_16816(o_acc[dn], pa[0], pa[1], pa[2], pa[3], b0, b1);
+                    mma_bf16_16816(o_acc[dn + 1], pa[0], pa[1], pa[2], pa[3], b2, b3);
+                }
+            }
+            if (n_valid < 16) fence_proxy_async_smem();  // generic writes before the next TMA fill
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[slot]);
+    }
+
+    // ------------------------------------------------------- merge the 4 warps
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+        l_part[rr] += __shfl_xor_sync(0xffffffffu, l_part[rr], 1);
+        l_part[rr] += __shfl_xor_sync(0xffffffffu, l_part[rr], 2);
+    }
+    named_barrier_sync(1, 32 * kConsumers);  // every consumer is done with the stages
+    float* red_o = reinterpret_cast<float*>(smem);                 // [warp][G][kD]
+    float* red_m = red_o + kConsumers * G * kD;                    // [warp][G]
+    float* red_l = red_m + kConsumers * G;                         // [warp][G]
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+        const int row = g + rr * 8;
+        if (row < G) {
+#pragma unroll
+            for (int dn = 0; dn < 16; ++dn) {
+                const int d = dn * 8 + 2 * t4;
+                red_o[(warp * G + row) * kD + d] = o_acc[dn][2 * rr];
+                red_o[(warp * G + row) * kD + d + 1] = o_acc[dn][2 * rr + 1];
+            }
+            if (t4 == 0) {
+                red_m[warp * G + row] = m_run[rr];
+                red_l[warp * G + row] = l_part[rr];
+            }
+        }
+    }
+    named_barrier_sync(1, 32 * kConsumers);
+    const int d = threadIdx.x;  // 0..127
+    for (int row = 0; row < G; ++row) {
+        float mx = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kConsumers; ++w) mx = fmaxf(mx, red_m[w * G + row]);
+        float acc = 0.f, l = 0.f;
+        if (mx != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < kConsumers; ++w) {
+                const float c = ex2(red_m[w * G + row] - mx);
+                l += c * red_l[w * G + row];
+                acc += c * red_o[(w * G + row) * kD + d];
+            }
+        }
+        const bool alive = l > 0.f;
+        o_base[row * head_stride + d] = alive ? acc / l : 0.f;
+        if (d == 0) lse_base[row * p.n_split] = alive ? (mx * kLn2 + logf(l)) : -INFINITY;
+    }
+}
+
+template <int G>
+cudaError_t launch_bf16(const DecodeArgs& a, cudaStream_t stream) {
+    constexpr int NS = 3;
+    CUtensorMap k_map, v_map;
+    const uint64_t rows = static_cast<uint64_t>(a.num_pages) * a.page_size;
+    const uint64_t dims[3] = {static_cast<uint64_t>(a.D), static_cast<uint64_t>(a.Hkv), rows};
+    const uint64_t strides[2] = {static_cast<uint64_t>(a.D) * 2, static_cast<uint64_t>(a.Hkv) * a.D * 2};
+    const uint32_t box[3] = {64, 1, kTileTok};
+    if (!encode_tiled_map(&k_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.k_cache, dims, strides, box,
+                          CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tiled_map(&v_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.v_cache, dims, strides, box,
+                          CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    Params p;
+    p.q = static_cast<const __nv_bfloat16*>(a.q);
+    p.block_table = a.block_table;
+    p.seq_lens = a.seq_lens;
+    p.max_pages = a.max_pages;
+    p.B = a.B;
+    p.Hq = a.Hq;
+    p.Hkv = a.Hkv;
+    p.num_pages = a.num_pages;
+    p.page_size = a.page_size;
+    p.split_tokens = a.split_tokens;
+    p.max_kv_len = a.max_kv_len;
+    p.n_split = a.n_split;
+    p.scale_log2 = a.scale * kLog2e;
+    p.o_part = a.o_part;
+    p.lse_part = a.lse_part;
+    p.status = a.dev_status;
+    const size_t smem = NS * kStageBytes + 1024;
+    auto kern = decode_bf16_kernel<G, NS>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    dim3 grid(a.n_split, a.Hkv, a.B);
+    kern<<<grid, kThreads, smem, stream>>>(k_map, v_map, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode_int4(const DecodeArgs& a, cudaStream_t stream);
+
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
+    if (a.kv_format == 1) return launch_decode_int4(a, stream);
+    switch (a.Hq / a.Hkv) {
+        case 1: return launch_bf16<1>(a, stream);
+        case 2: return launch_bf16<2>(a, stream);
+        case 4: return launch_bf16<4>(a, stream);
+        case 8: return launch_bf16<8>(a, stream);
+        case 16: return launch_bf16<16>(a, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace gb300

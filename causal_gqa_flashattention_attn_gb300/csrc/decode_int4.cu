@@ -1,0 +1,467 @@
+// decode_int4.cu - split-K paged decode over an int4 group-quantised KV cache.
+//
+// Row format ("splitk_kernels.py", docstring of _fwd_kernel_splitK,
+// cast_uint32_to_half2, dequantize): per (token, kv head) a row of int32
+// words, first n_groups coefficient words (fp16 scale in the low half, fp16
+// offset in the high half), then D/8 code words group by group; nibble j of
+// code word w of a group is element 8w+j of that group; value = scale*code +
+// offset.
+//
+// The dequantisation is fused into the tensor-core operands instead of being
+// materialised: a code c becomes the exact bf16 value 128 + c by OR-ing the
+// nibble into the bit pattern 0x4300 (no conversion instruction), and the
+// affine map is applied where it is cheap:
+//   s[h,t]   = sum_g scale_g(t) * (sum_{d in g} q_hd c_td)  +  sum_g offset_g(t) * Qsum_g[h]
+//              (the MMA accumulator of group g starts at -128 * Qsum_g[h])
+//   O[h,d]   = sum_t (p_ht scale_g(t)) (128 + c_td) - 128 SP_g[h] + OFF_g[h],
+//              SP_g = sum_t bf16(p_ht scale_g(t)),  OFF_g = sum_t p_ht offset_g(t)
+// so per element only one bit operation feeds the MMA; the per-group affine
+// terms cost a few FMAs per (token, head).
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace gb300 {
+namespace {
+
+constexpr int kD = 128;
+constexpr int kTileTok = 64;
+constexpr int kConsumers = 4;
+constexpr int kThreads = 32 * (kConsumers + 1);
+
+struct Params {
+    const __nv_bfloat16* q;
+    const int32_t* block_table;
+    const int32_t* seq_lens;
+    int max_pages, B, Hq, Hkv, num_pages, page_size, split_tokens, max_kv_len, n_split;
+    int row_words;   // n_groups + D/8
+    float scale_log2;
+    float* o_part;
+    float* lse_part;
+    int32_t* status;
+};
+
+__device__ __forceinline__ float lo_half(uint32_t w) { return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xFFFFu))); }
+__device__ __forceinline__ float hi_half(uint32_t w) { return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16))); }
+
+// bf16x2 (128 + nibble q of the low half, 128 + nibble q of the high half)
+__device__ __forceinline__ uint32_t nib_pair(uint32_t x, int q) {
+    return ((x >> (4 * q)) & 0x000F000Fu) | 0x43004300u;
+}
+
+// Coordinates of the K-side operand of group-local k-step `ks` for lane
+// quad index t: the code word (within the group) and the first nibble pair.
+template <int NG>
+__device__ __forceinline__ void k_word_of(int t, int ks, int& word, int& j0) {
+    constexpr int E = kD / NG;        // elements per group
+    if constexpr (E == 16) {          // half a word per thread
+        word = t >> 1;
+        j0 = 2 * (t & 1);
+    } else {
+        constexpr int WPT = E / 32;   // words per thread per group
+        word = t * WPT + (ks >> 1);
+        j0 = 2 * (ks & 1);
+    }
+}
+
+template <int G, int NG, int NS>
+__global__ void __launch_bounds__(kThreads) decode_int4_kernel(const __grid_constant__ CUtensorMap k_map,
+                                                               const __grid_constant__ CUtensorMap v_map,
+                                                               const Params p) {
+    constexpr bool kTwoRows = (G > 8);
+    constexpr int E = kD / NG;                 // elements per group
+    constexpr int KS = E / 16;                 // k-steps per group
+    constexpr int EPT = E / 8;                 // V elements per lane column per group
+    constexpr int BW = (NG <= 4) ? 20 : 24;    // words per smem row (box width)
+    constexpr int kTileBytes = kTileTok * BW * 4;
+    constexpr int kStageBytes = 2 * kTileBytes;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align_1024(smem_raw);
+    __shared__ __align__(8) uint64_t full_bar[NS];
+    __shared__ __align__(8) uint64_t empty_bar[NS];
+    __shared__ int s_abort;
+
+    const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const size_t head_stride = static_cast<size_t>(p.n_split) * kD;
+    float* o_base = p.o_part + ((static_cast<size_t>(b) * p.Hq + kvh * G) * p.n_split + split) * kD;
+    float* lse_base = p.lse_part + (static_cast<size_t>(b) * p.Hq + kvh * G) * p.n_split + split;
+
+    int len = p.seq_lens[b];
+    const int cap = min(p.max_kv_len, p.max_pages * p.page_size);
+    if (len < 0 || len > cap) {
+        if (threadIdx.x == 0) flag_status(p.status, ATTN_DEV_SEQ_TOO_LONG);
+        len = len < 0 ? 0 : cap;
+    }
+    const int lo = split * p.split_tokens;
+    const int hi = min(lo + p.split_tokens, len);
+    if (lo >= hi) {
+        for (int i = threadIdx.x; i < G * kD; i += kThreads) o_base[(i / kD) * head_stride + (i % kD)] = 0.f;
+        if (threadIdx.x < G) lse_base[threadIdx.x * p.n_split] = -INFINITY;
+        return;
+    }
+    const int n_tiles = (hi - lo + kTileTok - 1) / kTileTok;
+    const int x0 = (kvh * p.row_words) & ~3;      // 16-byte aligned box start
+    const int woff = kvh * p.row_words - x0;      // this head's row inside the box
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], kConsumers);
+        }
+        s_abort = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == kConsumers) {
+        if (lane == 0) {
+            tma_prefetch_desc(&k_map);
+            tma_prefetch_desc(&v_map);
+            const int32_t* table = p.block_table + static_cast<size_t>(b) * p.max_pages;
+            for (int t = 0; t < n_tiles; ++t) {
+                const int slot = t % NS;
+                if (t >= NS && !mbar_wait(&empty_bar[slot], ((t / NS) - 1) & 1)) {
+                    flag_status(p.status, ATTN_DEV_WAIT_TIMEOUT);
+                    atomicExch(&s_abort, 1);
+                    break;
+                }
+                const int tok = lo + t * kTileTok;
+                const int page = table[tok / p.page_size];
+                if (page < 0 || page >= p.num_pages) {
+                    flag_status(p.status, ATTN_DEV_PAGE_OUT_OF_RANGE);
+                    mbar_arrive(&full_bar[slot]);
+                    continue;
+                }
+                const int row = page * p.page_size + tok % p.page_size;
+                uint8_t* st = smem + slot * kStageBytes;
+                mbar_arrive_expect_tx(&full_bar[slot], kStageBytes);
+                tma_load_2d(st, &k_map, &full_bar[slot], x0, row);
+                tma_load_2d(st + kTileBytes, &v_map, &full_bar[slot], x0, row);
+            }
+        }
+        return;
+    }
+
+    // ------------------------------------------------------------ consumers
+    const int g = lane >> 2, t4 = lane & 3;
+    // Q fragments in the nibble order of the K operand, and per-group sums of q.
+    uint32_t qa[NG][KS][4];
+    float qsum[NG][2];
+    {
+        const __nv_bfloat16* qh = p.q + (static_cast<size_t>(b) * p.Hq + kvh * G) * kD;
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+            const int row = g + 8 * rr;
+            const bool real = (rr == 0 || kTwoRows) && row < G;
+#pragma unroll
+            for (int gr = 0; gr < NG; ++gr) {
+                float qs = 0.f;
+                if (real) {
+                    for (int e = 0; e < E; ++e) qs += __bfloat162float(qh[row * kD + gr * E + e]);
+                }
+                qsum[gr][rr] = qs;
+#pragma unroll
+                for (int ks = 0; ks < KS; ++ks) {
+                    int word, j0;
+                    k_word_of<NG>(t4, ks, word, j0);
+                    const int e0 = gr * E + 8 * word + j0;  // element of nibble j0
+                    uint32_t lo_pair = 0u, hi_pair = 0u;
+                    if (real) {
+                        const __nv_bfloat16* qr = qh + row * kD;
+                        __nv_bfloat162 a = __halves2bfloat162(qr[e0], qr[e0 + 4]);
+                        __nv_bfloat162 c = __halves2bfloat162(qr[e0 + 1], qr[e0 + 5]);
+                        lo_pair = *reinterpret_cast<uint32_t*>(&a);
+                        hi_pair = *reinterpret_cast<uint32_t*>(&c);
+                    }
+                    qa[gr][ks][rr] = lo_pair;        // a0 (row g) / a1 (row g+8): k = 2t, 2t+1
+                    qa[gr][ks][rr + 2] = hi_pair;    // a2 / a3: k = 2t+8, 2t+9
+                }
+            }
+        }
+    }
+    float o_acc[16][4];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) o_acc[i][0] = o_acc[i][1] = o_acc[i][2] = o_acc[i][3] = 0.f;
+    float sp[NG][2], off_acc[NG][2];
+#pragma unroll
+    for (int gr = 0; gr < NG; ++gr) sp[gr][0] = sp[gr][1] = off_acc[gr][0] = off_acc[gr][1] = 0.f;
+    float m_run[2] = {-INFINITY, -INFINITY};
+    float l_part[2] = {0.f, 0.f};
+    const float sl2 = p.scale_log2;
+
+    for (int t = 0; t < n_tiles; ++t) {
+        const int slot = t % NS;
+        if (!mbar_wait(&full_bar[slot], (t / NS) & 1)) {
+            flag_status(p.status, ATTN_DEV_WAIT_TIMEOUT);
+            break;
+        }
+        if (s_abort) break;
+        const int tok0 = lo + t * kTileTok + warp * 16;
+        const int n_valid = min(max(hi - tok0, 0), 16);
+        if (n_valid > 0) {
+            const uint32_t* kt = reinterpret_cast<const uint32_t*>(smem + slot * kStageBytes) + woff;
+            const uint32_t* vt = reinterpret_cast<const uint32_t*>(smem + slot * kStageBytes + kTileBytes) + woff;
+            // tokens this lane's accumulator entries refer to (relative to the warp's 16)
+            const int tk[4] = {2 * t4, 2 * t4 + 1, 8 + 2 * t4, 9 + 2 * t4};
+            // ---- scores in code space
+            float s[2][4];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+#pragma unroll
+            for (int gr = 0; gr < NG; ++gr) {
+                float acc[2][4];
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    acc[nt][0] = acc[nt][1] = -128.f * qsum[gr][0];
+                    acc[nt][2] = acc[nt][3] = -128.f * qsum[gr][1];
+                }
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const uint32_t* krow = kt + (warp * 16 + nt * 8 + g) * BW + NG + gr * (E / 8);
+#pragma unroll
+                    for (int ks = 0; ks < KS; ++ks) {
+                        int word, j0;
+                        k_word_of<NG>(t4, ks, word, j0);
+                        const uint32_t w = krow[word];
+                        mma_bf16_16816(acc[nt], qa[gr][ks][0], qa[gr][ks][1], qa[gr][ks][2], qa[gr][ks][3],
+                                       nib_pair(w, j0), nib_pair(w, j0 + 1));
+                    }
+                }
+                // affine map of group gr for this lane's four tokens
+#pragma unroll
+                for (int e4 = 0; e4 < 4; ++e4) {
+                    const int nt = e4 >> 1, e = e4 & 1;
+                    const uint32_t cw = kt[(warp * 16 + tk[e4]) * BW + gr];
+                    const float sc = lo_half(cw), of = hi_half(cw);
+                    s[nt][e] += sc * acc[nt][e] + of * qsum[gr][0];
+                    if (kTwoRows) s[nt][e + 2] += sc * acc[nt][e + 2] + of * qsum[gr][1];
+                }
+            }
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int tok = nt * 8 + 2 * t4 + (e & 1);
+                    s[nt][e] = tok < n_valid ? s[nt][e] * sl2 : -INFINITY;
+                }
+            }
+            // ---- online softmax (same as the bf16 path)
+            float pv[2][4];   // [row][token slot e4]
+            bool need_rescale = false;
+            float alpha[2] = {1.f, 1.f};
+#pragma unroll
+            for (int rr = 0; rr < (kTwoRows ? 2 : 1); ++rr) {
+                float mx = fmaxf(fmaxf(s[0][2 * rr], s[0][2 * rr + 1]), fmaxf(s[1][2 * rr], s[1][2 * rr + 1]));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                if (mx > m_run[rr] + 8.f) {
+                    alpha[rr] = ex2(m_run[rr] - mx);
+                    m_run[rr] = mx;
+                    need_rescale = true;
+                }
+                const float m_use = m_run[rr] == -INFINITY ? 0.f : m_run[rr];
+                pv[rr][0] = ex2(s[0][2 * rr] - m_use);
+                pv[rr][1] = ex2(s[0][2 * rr + 1] - m_use);
+                pv[rr][2] = ex2(s[1][2 * rr] - m_use);
+                pv[rr][3] = ex2(s[1][2 * rr + 1] - m_use);
+                l_part[rr] = l_part[rr] * alpha[rr] + ((pv[rr][0] + pv[rr][1]) + (pv[rr][2] + pv[rr][3]));
+            }
+            if (__any_sync(0xffffffffu, need_rescale)) {
+#pragma unroll
+                for (int dn = 0; dn < 16; ++dn) {
+                    o_acc[dn][0] *= alpha[0];
+                    o_acc[dn][1] *= alpha[0];
+                    o_acc[dn][2] *= alpha[1];
+                    o_acc[dn][3] *= alpha[1];
+                }
+#pragma unroll
+                for (int gr = 0; gr < NG; ++gr) {
+                    sp[gr][0] *= alpha[0];
+                    sp[gr][1] *= alpha[1];
+                    off_acc[gr][0] *= alpha[0];
+                    off_acc[gr][1] *= alpha[1];
+                }
+            }
+            // ---- O += (P * scale_g) (128 + codes), group by group
+#pragma unroll
+            for (int gr = 0; gr < NG; ++gr) {
+                float sc[4], of[4];
+#pragma unroll
+                for (int e4 = 0; e4 < 4; ++e4) {
+                    // rows past the end of the sequence may hold any bits: weight 0 there
+                    const bool ok = tk[e4] < n_valid;
+                    const uint32_t cw = vt[(warp * 16 + tk[e4]) * BW + gr];
+                    sc[e4] = ok ? lo_half(cw) : 0.f;
+                    of[e4] = ok ? hi_half(cw) : 0.f;
+                }
+                uint32_t pa[4];
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr) {
+                    if (rr == 1 && !kTwoRows) {
+                        pa[1] = pa[3] = 0u;
+                        break;
+                    }
+                    const __nv_bfloat162 lo2 = __floats2bfloat162_rn(pv[rr][0] * sc[0], pv[rr][1] * sc[1]);
+                    const __nv_bfloat162 hi2 = __floats2bfloat162_rn(pv[rr][2] * sc[2], pv[rr][3] * sc[3]);
+                    pa[rr] = *reinterpret_cast<const uint32_t*>(&lo2);
+                    pa[rr + 2] = *reinterpret_cast<const uint32_t*>(&hi2);
+                    const float2 lf = __bfloat1622float2(lo2), hf = __bfloat1622float2(hi2);
+                    sp[gr][rr] += (lf.x + lf.y) + (hf.x + hf.y);
+                    off_acc[gr][rr] += pv[rr][0] * of[0] + pv[rr][1] * of[1] + pv[rr][2] * of[2] + pv[rr][3] * of[3];
+                }
+                // B operand: this lane's column c = g owns elements [g*EPT, g*EPT + EPT) of the group.
+                const uint32_t* v_a = vt + (warp * 16 + 2 * t4) * BW + NG + gr * (E / 8);      // token 2t
+                const uint32_t* v_c = vt + (warp * 16 + 8 + 2 * t4) * BW + NG + gr * (E / 8);  // token 2t+8
+#pragma unroll
+                for (int j = 0; j < EPT; j += 4) {
+                    // nibbles [g*EPT + j, +4) (or +2 when EPT == 2) lie in one 16-bit half
+                    const int nib = g * EPT + j;
+                    const int word = nib >> 3;
+                    const uint32_t sel = (nib & 4) ? 0x7632u : 0x5410u;
+                    const uint32_t xa = __byte_perm(v_a[word], v_a[word + BW], sel);  // tokens 2t, 2t+1
+                    const uint32_t xc = __byte_perm(v_c[word], v_c[word + BW], sel);  // tokens 2t+8, 2t+9
+                    const int q0 = nib & 3;
+#pragma unroll
+                    for (int jj = 0; jj < (EPT < 4 ? EPT : 4); ++jj) {
+                        const int dn = gr * (E / 8) + j + jj;   // n-tile index across D
+                        mma_bf16_16816(o_acc[dn], pa[0], pa[1], pa[2], pa[3], nib_pair(xa, q0 + jj),
+                                       nib_pair(xc, q0 + jj));
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[slot]);
+    }
+
+    // ------------------------------------------- corrections and warp merge
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+        l_part[rr] += __shfl_xor_sync(0xffffffffu, l_part[rr], 1);
+        l_part[rr] += __shfl_xor_sync(0xffffffffu, l_part[rr], 2);
+#pragma unroll
+        for (int gr = 0; gr < NG; ++gr) {
+            float corr = off_acc[gr][rr] - 128.f * sp[gr][rr];
+            corr += __shfl_xor_sync(0xffffffffu, corr, 1);
+            corr += __shfl_xor_sync(0xffffffffu, corr, 2);
+            off_acc[gr][rr] = corr;
+        }
+    }
+    named_barrier_sync(1, 32 * kConsumers);
+    float* red_o = reinterpret_cast<float*>(smem);
+    float* red_m = red_o + kConsumers * G * kD;
+    float* red_l = red_m + kConsumers * G;
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+        const int row = g + rr * 8;
+        if (row < G) {
+#pragma unroll
+            for (int dn = 0; dn < 16; ++dn) {
+                const int gr = dn / (E / 8), j = dn % (E / 8);
+                // column 2t -> element (2t)*EPT + j of group gr; column 2t+1 -> (2t+1)*EPT + j
+                const int d0 = gr * E + (2 * t4) * EPT + j;
+                const int d1 = gr * E + (2 * t4 + 1) * EPT + j;
+                red_o[(warp * G + row) * kD + d0] = o_acc[dn][2 * rr] + off_acc[gr][rr];
+                red_o[(warp * G + row) * kD + d1] = o_acc[dn][2 * rr + 1] + off_acc[gr][rr];
+            }
+            if (t4 == 0) {
+                red_m[warp * G + row] = m_run[rr];
+                red_l[warp * G + row] = l_part[rr];
+            }
+        }
+    }
+    named_barrier_sync(1, 32 * kConsumers);
+    const int d = threadIdx.x;
+    for (int row = 0; row < G; ++row) {
+        float mx = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kConsumers; ++w) mx = fmaxf(mx, red_m[w * G + row]);
+        float acc = 0.f, l = 0.f;
+        if (mx != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < kConsumers; ++w) {
+                const float c = ex2(red_m[w * G + row] - mx);
+                l += c * red_l[w * G + row];
+                acc += c * red_o[(w * G + row) * kD + d];
+            }
+        }
+        const bool alive = l > 0.f;
+        o_base[row * head_stride + d] = alive ? acc / l : 0.f;
+        if (d == 0) lse_base[row * p.n_split] = alive ? (mx * kLn2 + logf(l)) : -INFINITY;
+    }
+}
+
+template <int G, int NG>
+cudaError_t launch_g_ng(const DecodeArgs& a, cudaStream_t stream) {
+    constexpr int NS = 6;
+    constexpr int BW = (NG <= 4) ? 20 : 24;
+    constexpr int kStageBytes = 2 * kTileTok * BW * 4;
+    const int row_words = a.n_groups + a.D / 8;
+    CUtensorMap k_map, v_map;
+    const uint64_t dims[2] = {static_cast<uint64_t>(a.Hkv) * row_words,
+                              static_cast<uint64_t>(a.num_pages) * a.page_size};
+    const uint64_t strides[1] = {static_cast<uint64_t>(a.Hkv) * row_words * 4};
+    const uint32_t box[2] = {BW, kTileTok};
+    if (!encode_tiled_map(&k_map, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, a.k_cache, dims, strides, box,
+                          CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_tiled_map(&v_map, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, a.v_cache, dims, strides, box,
+                          CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    Params p;
+    p.q = static_cast<const __nv_bfloat16*>(a.q);
+    p.block_table = a.block_table;
+    p.seq_lens = a.seq_lens;
+    p.max_pages = a.max_pages;
+    p.B = a.B;
+    p.Hq = a.Hq;
+    p.Hkv = a.Hkv;
+    p.num_pages = a.num_pages;
+    p.page_size = a.page_size;
+    p.split_tokens = a.split_tokens;
+    p.max_kv_len = a.max_kv_len;
+    p.n_split = a.n_split;
+    p.row_words = row_words;
+    p.scale_log2 = a.scale * kLog2e;
+    p.o_part = a.o_part;
+    p.lse_part = a.lse_part;
+    p.status = a.dev_status;
+    // the merge scratch (4 warps x G rows x D floats) reuses the stage ring
+    const size_t ring = NS * kStageBytes;
+    const size_t red = (kConsumers * G * kD + 2 * kConsumers * G) * sizeof(float);
+    const size_t smem = (ring > red ? ring : red) + 1024;
+    auto kern = decode_int4_kernel<G, NG, NS>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    dim3 grid(a.n_split, a.Hkv, a.B);
+    kern<<<grid, kThreads, smem, stream>>>(k_map, v_map, p);
+    return cudaGetLastError();
+}
+
+template <int G>
+cudaError_t launch_g(const DecodeArgs& a, cudaStream_t stream) {
+    switch (a.n_groups) {
+        case 1: return launch_g_ng<G, 1>(a, stream);
+        case 2: return launch_g_ng<G, 2>(a, stream);
+        case 4: return launch_g_ng<G, 4>(a, stream);
+        case 8: return launch_g_ng<G, 8>(a, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_decode_int4(const DecodeArgs& a, cudaStream_t stream) {
+    switch (a.Hq / a.Hkv) {
+        case 1: return launch_g<1>(a, stream);
+        case 2: return launch_g<2>(a, stream);
+        case 4: return launch_g<4>(a, stream);
+        case 8: return launch_g<8>(a, stream);
+        case 16: return launch_g<16>(a, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace gb300

@@ -1,0 +1,439 @@
+// prefill_tc.cu - causal GQA prefill on the 5th-generation tensor cores.
+//
+// What it computes follows "causal_forward_kernel.py" (flash-attention-scratch),
+// _flash_attention_forward_gqa_kernel: Q tiles against streamed K/V tiles,
+// S = Q K^T scaled into the exp2 domain (qk_scale = softmax_scale * log2 e),
+// an online softmax (running max m, running sum l, rescale by exp2(m_old -
+// m_new)), P rounded to bf16 before O += P V, skipping of tiles above the
+// causal diagonal and masking of the diagonal tiles only, then O = acc / l
+// and a per-row LSE.  Causal alignment is bottom-right as in
+// "gpt-o3 / triton6fd1ef", _gqa_prefill_kernel (kv_allowed = min(kv_len,
+// q_idx + 1 + delta)); the LSE is the natural log with no epsilon; the
+// fully-masked-row guard is that of "splitk_kernels.py", _fwd_kernel_splitK.
+//
+// GB300 design:
+//   * GQA packing: a 128-row Q tile holds P = 128/G consecutive query
+//     positions for each of the G query heads that share one KV head, so every
+//     K/V tile brought on chip serves the whole group;
+//   * a CTA owns two such tiles (2P positions) and one KV head: the two
+//     softmax warpgroups ping-pong so the tensor core always has work;
+//   * warp roles: warps 0-3 softmax of tile 0, warps 4-7 softmax of tile 1,
+//     warp 8 TMA producer, warp 9 MMA issuer (one elected lane), warps 10-11
+//     idle; registers move from the control warpgroup to the softmax ones;
+//   * TMA (128-byte swizzle) stages Q once per work item and K/V through a
+//     two-stage ring; tcgen05.mma accumulates S (2 x 128 columns) and O
+//     (2 x 128 columns) in the 512 TMEM columns; P is written back over S in
+//     TMEM as bf16 and fed to the P.V MMA straight from TMEM;
+//   * the max is rescaled lazily (only when it grows by more than 2^8), so
+//     the O accumulator in TMEM is rarely touched by the softmax warps;
+//   * a persistent grid walks the work items longest-first in a snake order.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace gb300 {
+namespace {
+
+constexpr int kD = 128;
+constexpr int kBM = 128;          // rows per Q tile
+constexpr int kBN = 128;          // keys per KV tile
+constexpr int kThreads = 384;     // 12 warps = 3 warpgroups
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+// Registers: launched at 168 per thread (384 x 168 = 64512); the
+// producer/MMA warpgroup drops to 72 and each softmax warpgroup rises to
+// 216 (2 x 128 x 216 + 128 x 72 = 64512, the launch total).
+constexpr uint32_t kRegsSoftmax = 216;
+constexpr uint32_t kRegsControl = 72;
+constexpr int kHalf = 128 * 128;  // bytes of one 64-column half of a 128-row tile
+constexpr int kTile = 2 * kHalf;  // 32 KB: 128 rows x 128 bf16
+constexpr int kStages = 2;
+// shared memory map (offsets from a 1024-aligned base)
+constexpr int kOffQ = 0;                        // 2 tiles
+constexpr int kOffK = kOffQ + 2 * kTile;        // kStages tiles
+constexpr int kOffV = kOffK + kStages * kTile;  // kStages tiles
+constexpr int kSmemBytes = kOffV + kStages * kTile;
+// TMEM columns
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0;    // + 128 * tile
+constexpr uint32_t kColO = 256;  // + 128 * tile
+
+struct Params {
+    __nv_bfloat16* o;
+    float* lse;
+    int32_t* status;
+    int B, Hq, Hkv, q_len, kv_len, G, P, n_qb, n_items;
+    float scale_log2;
+};
+
+struct Item {
+    int b, kvh, p0, n_kv;
+};
+
+// Work item `idx` of the snake-ordered, longest-first list.
+__device__ __forceinline__ Item item_of(const Params& p, int idx) {
+    const int bh_count = p.B * p.Hkv;
+    const int qb = p.n_qb - 1 - idx / bh_count;
+    const int bh = idx % bh_count;
+    Item it;
+    it.b = bh / p.Hkv;
+    it.kvh = bh % p.Hkv;
+    it.p0 = qb * 2 * p.P;
+    const int delta = p.kv_len - p.q_len;
+    const int p_last = min(it.p0 + 2 * p.P, p.q_len) - 1;
+    const int kv_end = min(p.kv_len, p_last + delta + 1);
+    it.n_kv = kv_end > 0 ? (kv_end + kBN - 1) / kBN : 0;
+    return it;
+}
+
+// i-th item of this CTA: rounds of gridDim.x items, every other round reversed.
+__device__ __forceinline__ int cta_item(int i) {
+    const int round = i;
+    const int pos = (round & 1) ? (gridDim.x - 1 - blockIdx.x) : blockIdx.x;
+    return round * gridDim.x + pos;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap k_map,
+                      const __grid_constant__ CUtensorMap v_map, const Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align_1024(smem_raw);
+    __shared__ __align__(8) uint64_t q_full, q_empty;
+    __shared__ __align__(8) uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
+    __shared__ __align__(8) uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
+    __shared__ uint32_t tmem_base_sh;
+    __shared__ int abort_sh;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&q_full, 1);
+        mbar_init(&q_empty, 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&k_full[s], 1);
+            mbar_init(&v_full[s], 1);
+            mbar_init(&kv_empty[s], 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(&s_full[t], 1);
+            mbar_init(&p_full[t], 128);
+            mbar_init(&o_full[t], 1);
+            mbar_init(&o_empty[t], 128);
+        }
+        abort_sh = 0;
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(&tmem_base_sh, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_sh;
+
+    auto fail = [&]() {
+        flag_status(p.status, ATTN_DEV_WAIT_TIMEOUT);
+        atomicExch(&abort_sh, 1);
+    };
+    // bounded wait that also gives up once any role has given up
+    auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+        if (mbar_wait(bar, parity, &abort_sh)) return true;
+        fail();
+        return false;
+    };
+
+    if (warp < 8) {
+        regs_inc<kRegsSoftmax>();
+        // ---------------------------------------------------------- softmax warpgroups
+        const int t = warp >> 2;                       // which Q tile
+        const int r = threadIdx.x & 127;               // row of the tile == TMEM lane
+        const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const uint32_t s_addr = tmem + lane_addr + kColS + 128 * t;
+        const uint32_t o_addr = tmem + lane_addr + kColO + 128 * t;
+        const int delta = p.kv_len - p.q_len;
+        const float sl2 = p.scale_log2;
+        uint32_t kv_iter = 0, item_iter = 0;
+        bool ok = true;
+        for (int i = 0; ok; ++i) {
+            const int idx = cta_item(i);
+            if (idx >= p.n_items) break;
+            const Item it = item_of(p, idx);
+            const int head = it.kvh * p.G + r / p.P;
+            const int pos = it.p0 + t * p.P + r % p.P;
+            const bool row_real = pos < p.q_len;
+            const size_t row_id = (static_cast<size_t>(it.b) * p.Hq + head) * p.q_len + pos;
+            if (it.n_kv == 0) {
+                if (row_real) {
+                    uint4* orow = reinterpret_cast<uint4*>(p.o + row_id * kD);
+                    for (int c = 0; c < kD / 8; ++c) orow[c] = make_uint4(0, 0, 0, 0);
+                    if (p.lse != nullptr) p.lse[row_id] = -INFINITY;
+                }
+                continue;
+            }
+            const int pos_min = it.p0 + t * p.P;     // smallest position of this tile
+            const int lim_row = pos + delta;         // last visible key of this row
+            float m = -INFINITY, l = 0.f;
+            for (int j = 0; j < it.n_kv; ++j, ++kv_iter) {
+                if (!(ok = wait(&s_full[t], kv_iter & 1))) break;
+                tc_fence_after();
+                uint32_t sr[4][32];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + 32 * c, sr[c]);
+                tmem_ld_wait();
+                const int kv0 = j * kBN;
+                // causal mask only on tiles that cross this tile's diagonal
+                if (kv0 + kBN - 1 > pos_min + delta) {
+                    const int lim = lim_row - kv0;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            if (32 * c + e > lim) sr[c][e] = __float_as_uint(-INFINITY);
+                }
+                float mx = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(sr[c][e]));
+                mx *= sl2;
+                float alpha = 1.f;
+                const bool grow = mx > m + 8.f;
+                if (grow) {
+                    alpha = ex2(m - mx);   // 0 when m = -inf
+                    m = mx;
+                    l *= alpha;
+                }
+                if (j > 0 && __any_sync(0xffffffffu, grow)) {
+                    // O_t is idle here: the commit that announced S_t also covers
+                    // the P.V of the previous tile
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t orr[32];
+                        tmem_ld32(o_addr + 32 * c, orr);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
+                        tmem_st32(o_addr + 32 * c, orr);
+                    }
+                }
+                const float neg_m = (m == -INFINITY) ? 0.f : -m;
+                float lsum = 0.f;
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const int c = 2 * hh + (e >> 4), col = 2 * (e & 15);
+                        const float p0 = ex2(fmaf(__uint_as_float(sr[c][col]), sl2, neg_m));
+                        const float p1 = ex2(fmaf(__uint_as_float(sr[c][col + 1]), sl2, neg_m));
+                        lsum += p0 + p1;
+                        pk[e] = pack_bf16x2(p0, p1);
+                    }
+                    tmem_st32(s_addr + 32 * hh, pk);
+                }
+                l += lsum;
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(&p_full[t]);
+            }
+            if (!ok) break;
+            // -------------------------------------------------------------- epilogue
+            if (!(ok = wait(&o_full[t], item_iter & 1))) break;
+            tc_fence_after();
+            const bool alive = l > 0.f;
+            const float inv_l = alive ? 1.f / l : 0.f;
+            uint4* orow = reinterpret_cast<uint4*>(p.o + row_id * kD);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t orr[32];
+                tmem_ld32(o_addr + 32 * c, orr);
+                tmem_ld_wait();
+                if (row_real) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 8) {
+                        uint4 v;
+                        v.x = pack_bf16x2(__uint_as_float(orr[e]) * inv_l, __uint_as_float(orr[e + 1]) * inv_l);
+                        v.y = pack_bf16x2(__uint_as_float(orr[e + 2]) * inv_l, __uint_as_float(orr[e + 3]) * inv_l);
+                        v.z = pack_bf16x2(__uint_as_float(orr[e + 4]) * inv_l, __uint_as_float(orr[e + 5]) * inv_l);
+                        v.w = pack_bf16x2(__uint_as_float(orr[e + 6]) * inv_l, __uint_as_float(orr[e + 7]) * inv_l);
+                        orow[(32 * c + e) / 8] = v;
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&o_empty[t]);
+            if (row_real && p.lse != nullptr) p.lse[row_id] = alive ? (m * kLn2 + logf(l)) : -INFINITY;
+            ++item_iter;
+        }
+    } else {
+        regs_dec<kRegsControl>();
+        if (warp == kProducerWarp) {
+            // ------------------------------------------------------------ TMA producer
+            if (lane == 0) {
+                tma_prefetch_desc(&q_map);
+                tma_prefetch_desc(&k_map);
+                tma_prefetch_desc(&v_map);
+                uint32_t kv_iter = 0, item_iter = 0;
+                bool ok = true;
+                for (int i = 0; ok; ++i) {
+                    const int idx = cta_item(i);
+                    if (idx >= p.n_items) break;
+                    const Item it = item_of(p, idx);
+                    if (it.n_kv == 0) continue;
+                    if (item_iter > 0 && !(ok = wait(&q_empty, (item_iter - 1) & 1))) break;
+                    mbar_arrive_expect_tx(&q_full, 2 * kTile);
+                    const int head0 = it.b * p.Hq + it.kvh * p.G;
+                    for (int t = 0; t < 2; ++t)
+                        for (int h = 0; h < 2; ++h)
+                            tma_load_3d(smem + kOffQ + t * kTile + h * kHalf, &q_map, &q_full, h * 64, it.p0 + t * p.P,
+                                        head0);
+                    const int kvrow = it.b * p.Hkv + it.kvh;
+                    for (int j = 0; j < it.n_kv; ++j, ++kv_iter) {
+                        const int s = kv_iter % kStages;
+                        if (kv_iter >= kStages && !(ok = wait(&kv_empty[s], ((kv_iter / kStages) - 1) & 1))) break;
+                        mbar_arrive_expect_tx(&k_full[s], kTile);
+                        tma_load_3d(smem + kOffK + s * kTile, &k_map, &k_full[s], 0, j * kBN, kvrow);
+                        tma_load_3d(smem + kOffK + s * kTile + kHalf, &k_map, &k_full[s], 64, j * kBN, kvrow);
+                        mbar_arrive_expect_tx(&v_full[s], kTile);
+                        tma_load_3d(smem + kOffV + s * kTile, &v_map, &v_full[s], 0, j * kBN, kvrow);
+                        tma_load_3d(smem + kOffV + s * kTile + kHalf, &v_map, &v_full[s], 64, j * kBN, kvrow);
+                    }
+                    ++item_iter;
+                }
+            }
+        } else if (warp == kMmaWarp) {
+            // ------------------------------------------------------------- MMA issuer
+            if (lane == 0) {
+                constexpr uint32_t idesc_qk = idesc_bf16_f32(kBM, kBN, false);
+                constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, kD, true);
+                const uint32_t q_s = smem_u32(smem + kOffQ), k_s = smem_u32(smem + kOffK), v_s = smem_u32(smem + kOffV);
+                auto issue_s = [&](int t, int stage) {  // S_t = Q_t K^T
+                    const uint32_t qa = q_s + t * kTile, kb = k_s + stage * kTile;
+    #pragma unroll
+                    for (int kk = 0; kk < kD / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+                        umma_ss(tmem + kColS + 128 * t, sw128_desc(qa + off, 16, 1024), sw128_desc(kb + off, 16, 1024),
+                                idesc_qk, kk > 0);
+                    }
+                };
+                auto issue_pv = [&](int t, int stage, bool acc) {  // O_t (+)= P_t V
+                    const uint32_t vb = v_s + stage * kTile;
+    #pragma unroll
+                    for (int kk = 0; kk < kBN / 16; ++kk) {
+                        umma_ts(tmem + kColO + 128 * t, tmem + kColS + 128 * t + kk * 8,
+                                sw128_desc(vb + kk * 16 * 128, kHalf, 1024), idesc_pv, (acc || kk > 0) ? 1u : 0u);
+                    }
+                };
+                uint32_t kv_iter = 0, item_iter = 0;
+                bool ok = true;
+                for (int i = 0; ok; ++i) {
+                    const int idx = cta_item(i);
+                    if (idx >= p.n_items) break;
+                    const Item it = item_of(p, idx);
+                    if (it.n_kv == 0) continue;
+                    if (!(ok = wait(&q_full, item_iter & 1))) break;
+                    if (!(ok = wait(&k_full[kv_iter % kStages], (kv_iter / kStages) & 1))) break;
+                    tc_fence_after();
+                    issue_s(0, kv_iter % kStages);
+                    umma_commit(&s_full[0]);
+                    issue_s(1, kv_iter % kStages);
+                    umma_commit(&s_full[1]);
+                    for (int j = 0; j < it.n_kv && ok; ++j, ++kv_iter) {
+                        const int s = kv_iter % kStages;
+                        const bool last = (j + 1 == it.n_kv);
+                        const uint32_t nxt = kv_iter + 1;
+                        if (!(ok = wait(&v_full[s], (kv_iter / kStages) & 1))) break;
+                        for (int t = 0; t < 2; ++t) {
+                            if (!(ok = wait(&p_full[t], kv_iter & 1))) break;
+                            if (j == 0 && item_iter > 0 && !(ok = wait(&o_empty[t], (item_iter - 1) & 1))) break;
+                            tc_fence_after();
+                            issue_pv(t, s, j > 0);                    // O_t (+)= P_t V_j
+                            if (t == 1) umma_commit(&kv_empty[s]);    // K_j, V_j no longer read
+                            if (!last) {
+                                if (t == 0) {
+                                    if (!(ok = wait(&k_full[nxt % kStages], (nxt / kStages) & 1))) break;
+                                    tc_fence_after();
+                                }
+                                issue_s(t, nxt % kStages);            // S_t = Q_t K_{j+1}^T (after P_t is read)
+                                umma_commit(&s_full[t]);
+                            } else {
+                                umma_commit(&o_full[t]);
+                                if (t == 1) umma_commit(&q_empty);
+                            }
+                        }
+                    }
+                    if (!ok) break;
+                    ++item_iter;
+                }
+            }
+        }
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+}  // namespace
+
+bool prefill_tc_supported(const PrefillArgs& a) {
+    if (a.dtype != ATTN_BF16 || a.D != kD) return false;
+    const int G = a.Hq / a.Hkv;
+    if (G < 1 || G > 128 || (128 % G) != 0) return false;
+    return true;
+}
+
+cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream) {
+    const int G = a.Hq / a.Hkv;
+    const int P = kBM / G;
+    CUtensorMap q_map, k_map, v_map;
+    {
+        const uint64_t dims[3] = {kD, static_cast<uint64_t>(a.q_len), static_cast<uint64_t>(a.B) * a.Hq};
+        const uint64_t strides[2] = {kD * 2, static_cast<uint64_t>(a.q_len) * kD * 2};
+        const uint32_t box[3] = {64, static_cast<uint32_t>(P), static_cast<uint32_t>(G)};
+        if (!encode_tiled_map(&q_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.q, dims, strides, box,
+                              CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+    }
+    {
+        const uint64_t dims[3] = {kD, static_cast<uint64_t>(a.kv_len), static_cast<uint64_t>(a.B) * a.Hkv};
+        const uint64_t strides[2] = {kD * 2, static_cast<uint64_t>(a.kv_len) * kD * 2};
+        const uint32_t box[3] = {64, kBN, 1};
+        if (!encode_tiled_map(&k_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.k, dims, strides, box,
+                              CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_tiled_map(&v_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.v, dims, strides, box,
+                              CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+    }
+    Params p;
+    p.o = static_cast<__nv_bfloat16*>(a.o);
+    p.lse = a.lse;
+    p.status = a.dev_status;
+    p.B = a.B;
+    p.Hq = a.Hq;
+    p.Hkv = a.Hkv;
+    p.q_len = a.q_len;
+    p.kv_len = a.kv_len;
+    p.G = G;
+    p.P = P;
+    p.n_qb = (a.q_len + 2 * P - 1) / (2 * P);
+    p.n_items = a.B * a.Hkv * p.n_qb;
+    p.scale_log2 = a.scale * kLog2e;
+    const int sms = device_sm_count();
+    if (sms <= 0) return cudaErrorInvalidDevice;
+    const int grid = p.n_items < sms ? p.n_items : sms;
+    const size_t smem = kSmemBytes + 1024;
+    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    prefill_tc_kernel<<<grid, kThreads, smem, stream>>>(q_map, k_map, v_map, p);
+    return cudaGetLastError();
+}
+
+}  // namespace gb300

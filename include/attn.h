@@ -1,0 +1,164 @@
+/*
+ * attn.h - C ABI of the GB300 (sm_103a) causal grouped-query attention library.
+ *
+ * What the library computes (the pages it follows are named per entry point):
+ *   O = softmax(scale * Q K^T + causal mask) V, plus the per-row natural-log
+ *   log-sum-exp LSE = log(sum_j exp(scale * q_i . k_j)) over the visible keys.
+ * Query head h reads key/value head h / (Hq / Hkv) (grouped-query attention).
+ * Causal alignment is bottom-right: with delta = kv_len - q_len, key j is
+ * visible to query i iff j <= i + delta.  A query row with no visible key gets
+ * O = 0 and LSE = -inf.
+ *
+ * Conventions shared by every entry point:
+ *   - All tensor arguments are DEVICE pointers to dense, contiguous,
+ *     row-major buffers that the CALLER allocates and owns; the library never
+ *     allocates, frees or synchronises.  Pointers must be 16-byte aligned.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
+ *     NULL means the legacy default stream).  A returned ATTN_OK means the
+ *     work was validated and enqueued, not that it has finished.
+ *   - Argument errors are detected on the host before anything is enqueued
+ *     and returned as ATTN_ERR_INVALID_ARG / ATTN_ERR_UNSUPPORTED /
+ *     ATTN_ERR_WORKSPACE; a failed launch returns ATTN_ERR_CUDA.
+ *   - Errors only the device can see (a block-table entry outside the page
+ *     pool, a sequence longer than its block table, a bounded wait that ran
+ *     out) are OR-ed as ATTN_DEV_* bits into the optional int32 device word
+ *     `dev_status` (may be NULL).  The kernel skips the offending access and
+ *     never traps; the caller reads the word after synchronising.
+ */
+#ifndef GB300_ATTN_H
+#define GB300_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = -1,   /* null pointer, non-positive size, Hq % Hkv != 0, ... */
+    ATTN_ERR_UNSUPPORTED = -2,   /* valid but not implemented (head dim, dtype, group count) */
+    ATTN_ERR_WORKSPACE = -3,     /* workspace missing or smaller than attn_decode_workspace_bytes */
+    ATTN_ERR_CUDA = -4,          /* a CUDA runtime/driver call or a launch failed */
+    ATTN_ERR_DEVICE_FAULT = -5   /* reserved for callers that translate dev_status */
+} attn_status_t;
+
+typedef enum {
+    ATTN_F32 = 0,
+    ATTN_BF16 = 1,
+    ATTN_F16 = 2,
+    ATTN_INT4_PACKED = 3         /* int32 words, see attn_decode_paged_splitk */
+} attn_dtype_t;
+
+/* Bits OR-ed into *dev_status by a kernel. */
+#define ATTN_DEV_PAGE_OUT_OF_RANGE 0x1  /* block_table entry < 0 or >= num_pages */
+#define ATTN_DEV_SEQ_TOO_LONG      0x2  /* seq_lens[b] > max_kv_len or > max_pages_per_seq * page_size */
+#define ATTN_DEV_WAIT_TIMEOUT      0x4  /* a bounded mbarrier wait gave up */
+
+/*
+ * attn_prefill_fwd - causal GQA prefill.
+ *
+ * Follows "causal_forward_kernel.py" (flash-attention-scratch),
+ * _flash_attention_forward_gqa_kernel and its wrapper flash_attention_forward
+ * (tiled online-softmax forward, GQA head map, O in the input dtype, an LSE
+ * row per query), with the bottom-right alignment of "gpt-o3 / triton6fd1ef",
+ * _gqa_prefill_kernel (kv_allowed = min(kv_len, q_idx + 1 + delta)).
+ *
+ *   q    [B, Hq,  q_len,  D]  dtype            (read)
+ *   k    [B, Hkv, kv_len, D]  dtype            (read)
+ *   v    [B, Hkv, kv_len, D]  dtype            (read)
+ *   o    [B, Hq,  q_len,  D]  dtype            (written)
+ *   lse  [B, Hq,  q_len]      float32, natural log (written; may be NULL)
+ *   dtype   ATTN_BF16 (tensor-core path; D = 128 needs Hq/Hkv to divide 128,
+ *           other shapes use the CUDA-core path) or ATTN_F32 (exact fp32
+ *           CUDA-core path, no TF32).
+ *   D       64 or 128.
+ *   scale   softmax scale; pass 1/sqrt(D) for the usual attention.
+ *   Requires Hq % Hkv == 0, all sizes > 0.
+ */
+attn_status_t attn_prefill_fwd(const void* q, const void* k, const void* v,
+                               void* o, float* lse, attn_dtype_t dtype,
+                               int B, int Hq, int Hkv, int q_len, int kv_len, int D,
+                               float scale, int32_t* dev_status, void* stream);
+
+/*
+ * attn_decode_workspace_bytes - bytes of scratch attn_decode_paged_splitk needs.
+ *
+ * The workspace holds the split partials of "splitk_kernels.py",
+ * _fwd_kernel_splitK (Out_splitK / LSE_splitk), laid out as
+ *   o_part   float32 [B, Hq, S, D]   at offset 0
+ *   lse_part float32 [B, Hq, S]      right after o_part (16-byte aligned)
+ * with S = ceil(max_kv_len / split_tokens) (at least 1).  Returns 0 for
+ * invalid sizes.
+ */
+size_t attn_decode_workspace_bytes(int B, int Hq, int max_kv_len, int split_tokens, int D);
+
+/*
+ * attn_decode_paged_splitk - single-query split-K decode over a paged KV cache.
+ *
+ * Follows "splitk_kernels.py" (xformers), _fwd_kernel_splitK (split chunks,
+ * block-table indirection, per-split O already divided by its own l, natural
+ * LSE, empty split -> O = 0 / LSE = -inf) and load_dequantize_k_v_group /
+ * cast_uint32_to_half2 / dequantize (int4 rows); then _splitK_reduce merges.
+ *
+ *   q            [B, Hq, D] bfloat16 (one query per sequence)      (read)
+ *   k_cache,
+ *   v_cache      page pool, token-major inside a page:
+ *                  ATTN_BF16:        bfloat16 [num_pages, page_size, Hkv, D]
+ *                  ATTN_INT4_PACKED: int32    [num_pages, page_size, Hkv, n_groups + D/8]
+ *                int4 row: n_groups coefficient words (fp16 scale in the low
+ *                16 bits, fp16 offset in the high 16 bits), then D/8 code
+ *                words group by group; nibble j (bits 4j..4j+3) of word w of
+ *                a group is element 8w+j of that group; value =
+ *                scale * code + offset.                            (read)
+ *   block_table  int32 [B, max_pages_per_seq]; entry p of sequence b is the
+ *                pool page holding its tokens [p*page_size, (p+1)*page_size).
+ *                Entries past the sequence's last page are never read.  (read)
+ *   seq_lens     int32 [B], 0 <= seq_lens[b] <= max_kv_len  (device)  (read)
+ *   n_groups     1, 2, 4 or 8 for ATTN_INT4_PACKED; ignored for ATTN_BF16.
+ *   D            128.  Hq / Hkv in {1, 2, 4, 8, 16}.
+ *   page_size    a multiple of 64.  split_tokens: a multiple of 64.
+ *   workspace    >= attn_decode_workspace_bytes(B, Hq, max_kv_len, split_tokens, D)
+ *                bytes of device memory owned by the caller; it receives the
+ *                split partials in the layout documented above.
+ *   o            [B, Hq, D] bfloat16 (written), lse [B, Hq] float32 (written,
+ *                may be NULL).  If o is NULL only the partials are produced
+ *                (for callers that merge across devices themselves).
+ * Split s of sequence b covers tokens [s*split_tokens, min((s+1)*split_tokens, len_b)).
+ */
+attn_status_t attn_decode_paged_splitk(const void* q, const void* k_cache, const void* v_cache,
+                                       const int32_t* block_table, int max_pages_per_seq,
+                                       const int32_t* seq_lens, attn_dtype_t kv_dtype, int n_groups,
+                                       int B, int Hq, int Hkv, int D, int num_pages, int page_size,
+                                       int split_tokens, int max_kv_len, float scale,
+                                       void* workspace, size_t workspace_bytes,
+                                       void* o, float* lse, int32_t* dev_status, void* stream);
+
+/*
+ * attn_lse_merge - LSE-weighted merge of split partials.
+ *
+ * Follows "splitk_kernels.py", _splitK_reduce: per row n,
+ *   M = max_s lse_part[n, s];  w_s = exp(lse_part[n, s] - M);
+ *   o[n] = sum_s w_s o_part[n, s] / sum_s w_s;  lse[n] = M + log(sum_s w_s);
+ *   a row whose partial LSEs are all -inf gets o = 0, lse = -inf.
+ *
+ *   o_part   float32 [N, S, D]  (read)      lse_part float32 [N, S] (read)
+ *   o        [N, D] in o_dtype (ATTN_F32 or ATTN_BF16) (written)
+ *   lse      float32 [N] (written; may be NULL)
+ *   D <= 1024 and a multiple of 4;  S >= 1.
+ */
+attn_status_t attn_lse_merge(const float* o_part, const float* lse_part, int N, int S, int D,
+                             void* o, float* lse, attn_dtype_t o_dtype, void* stream);
+
+/* Static, human-readable name of a status code. */
+const char* attn_status_string(attn_status_t status);
+
+/* ABI version of this header (major * 100 + minor). */
+int attn_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GB300_ATTN_H */

@@ -1,0 +1,122 @@
+"""The C-ABI library loads, exports every entry point include/attn.h declares,
+and rejects bad arguments on the host before touching a GPU (none here)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "attn.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    import __graft_entry__
+    __graft_entry__.build()
+    import causal_gqa_flashattention_attn_gb300 as attn
+    return attn.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("attn_prefill_fwd", "attn_decode_paged_splitk", "attn_lse_merge", "attn_decode_workspace_bytes",
+              "attn_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    import causal_gqa_flashattention_attn_gb300 as attn
+    for name in declared_functions():
+        assert hasattr(L, name), name
+        assert name in attn.EXPORTED
+    assert L.attn_abi_version() == 100
+
+
+def test_status_strings(L):
+    import causal_gqa_flashattention_attn_gb300 as attn
+    assert attn.attn_status_string(0) == "ok"
+    assert "invalid" in attn.attn_status_string(-1)
+    assert "unsupported" in attn.attn_status_string(-2)
+    assert "workspace" in attn.attn_status_string(-3)
+
+
+FAKE = ctypes.c_void_p(0x10000)   # aligned, never dereferenced: validation fails first
+
+
+def _prefill(L, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=None, dtype=1, B=1, Hq=4, Hkv=2, q_len=8, kv_len=8, D=128,
+             scale=0.1, status=None, stream=None)
+    a.update(kw)
+    return L.attn_prefill_fwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["dtype"], a["B"], a["Hq"], a["Hkv"],
+                              a["q_len"], a["kv_len"], a["D"], a["scale"], a["status"], a["stream"])
+
+
+def test_prefill_host_validation(L):
+    assert _prefill(L, q=None) == -1
+    assert _prefill(L, Hq=6, Hkv=4) == -1                # Hq % Hkv != 0
+    assert _prefill(L, B=0) == -1
+    assert _prefill(L, kv_len=-3) == -1
+    assert _prefill(L, scale=float("nan")) == -1
+    assert _prefill(L, o=ctypes.c_void_p(0x10004)) == -1  # misaligned
+    assert _prefill(L, D=96) == -2                       # unsupported head dim
+    assert _prefill(L, dtype=2) == -2                    # fp16 not implemented
+    assert _prefill(L, dtype=3) == -2
+
+
+def _decode(L, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, table=FAKE, max_pages=4, lens=FAKE, kv_dtype=1, ng=1, B=2, Hq=32, Hkv=8,
+             D=128, num_pages=8, page_size=256, split=2048, max_len=1024, scale=0.1, ws=FAKE, ws_bytes=1 << 30,
+             o=FAKE, lse=None, status=None, stream=None)
+    a.update(kw)
+    return L.attn_decode_paged_splitk(a["q"], a["k"], a["v"], a["table"], a["max_pages"], a["lens"], a["kv_dtype"],
+                                      a["ng"], a["B"], a["Hq"], a["Hkv"], a["D"], a["num_pages"], a["page_size"],
+                                      a["split"], a["max_len"], a["scale"], a["ws"], a["ws_bytes"], a["o"],
+                                      a["lse"], a["status"], a["stream"])
+
+
+def test_decode_host_validation(L):
+    assert _decode(L, table=None) == -1
+    assert _decode(L, Hq=12, Hkv=8) == -1
+    assert _decode(L, num_pages=0) == -1
+    assert _decode(L, D=64) == -2
+    assert _decode(L, Hq=24, Hkv=8) == -2               # group of 3
+    assert _decode(L, page_size=100) == -2
+    assert _decode(L, split=1000) == -2
+    assert _decode(L, kv_dtype=0) == -2                 # fp32 cache not implemented
+    assert _decode(L, kv_dtype=3, ng=3) == -2           # N_GROUPS must be 1, 2, 4 or 8
+    assert _decode(L, ws=None) == -3
+    assert _decode(L, ws_bytes=16) == -3
+
+
+def test_workspace_bytes(L):
+    import causal_gqa_flashattention_attn_gb300 as attn
+    # [B, Hq, S, D] + [B, Hq, S] floats, each rounded to 16 bytes; S = ceil(32768 / 2048) = 16
+    assert attn.attn_decode_workspace_bytes(64, 32, 32768, 2048, 128) == 64 * 32 * 16 * 128 * 4 + 64 * 32 * 16 * 4
+    assert attn.attn_decode_workspace_bytes(1, 1, 0, 64, 128) == 128 * 4 + 16   # at least one split
+    assert attn.attn_decode_workspace_bytes(0, 1, 10, 64, 128) == 0
+
+
+def test_merge_host_validation(L):
+    assert L.attn_lse_merge(None, FAKE, 4, 2, 128, FAKE, None, 0, None) == -1
+    assert L.attn_lse_merge(FAKE, FAKE, 4, 0, 128, FAKE, None, 0, None) == -1
+    assert L.attn_lse_merge(FAKE, FAKE, 4, 2, 130, FAKE, None, 0, None) == -1
+    assert L.attn_lse_merge(FAKE, FAKE, 4, 2, 2048, FAKE, None, 0, None) == -2
+    assert L.attn_lse_merge(FAKE, FAKE, 4, 2, 128, FAKE, None, 2, None) == -2
+
+
+def test_product_path_has_no_cpu_fallback():
+    """The binding must not import the oracle or reach a CPU implementation."""
+    pkg = os.path.join(ROOT, "causal_gqa_flashattention_attn_gb300")
+    for f in os.listdir(pkg):
+        if f.endswith(".py"):
+            src = open(os.path.join(pkg, f)).read()
+            assert "import oracle" not in src and "from oracle" not in src

@@ -1,0 +1,36 @@
+"""LSE merge kernel against the oracle's merge (through the C ABI)."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from parity import check_lse, check_o, gpu_or_skip
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("n,s,d", [(1, 1, 128), (37, 5, 128), (300, 16, 128), (64, 3, 64), (9, 40, 1024), (5, 2, 4)])
+def test_merge_fp32_matches_oracle(n, s, d):
+    dev = gpu_or_skip()
+    import causal_gqa_flashattention_attn_gb300 as attn
+    o_part, lse_part = synth.merge_inputs(n, s, d, seed=n * 7 + s)
+    o, lse = attn.attn_lse_merge(o_part.to(dev), lse_part.to(dev), o_dtype=torch.float32)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = oracle.lse_merge(o_part.double().numpy(), lse_part.double().numpy())
+    np.testing.assert_allclose(o.cpu().double().numpy(), o_ref, rtol=1e-5, atol=1e-5)
+    check_lse(lse, lse_ref, fp32=True)
+    # the all-empty first row
+    assert np.all(o[0].cpu().numpy() == 0) and lse[0].item() == float("-inf")
+
+
+def test_merge_bf16_output():
+    dev = gpu_or_skip()
+    import causal_gqa_flashattention_attn_gb300 as attn
+    o_part, lse_part = synth.merge_inputs(128, 8, 128, seed=3)
+    o, lse = attn.attn_lse_merge(o_part.to(dev), lse_part.to(dev), o_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = oracle.lse_merge(o_part.double().numpy(), lse_part.double().numpy())
+    check_o(o, o_ref)
+    check_lse(lse, lse_ref)

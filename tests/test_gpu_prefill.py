@@ -1,0 +1,122 @@
+"""Causal GQA prefill (tensor-core and CUDA-core paths) against the oracle,
+through the C ABI."""
+
+from dataclasses import replace
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from parity import check_lse, check_o, gpu_or_skip
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(shape, seed=0):
+    dev = gpu_or_skip()
+    import causal_gqa_flashattention_attn_gb300 as attn
+    q, k, v = synth.prefill_inputs(shape, seed=seed)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    o, lse = attn.attn_prefill_fwd(q.to(dev), k.to(dev), v.to(dev), dev_status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0, status.item()
+    return (q, k, v), o, lse
+
+
+def _np(t):
+    return t.double().numpy()
+
+
+def test_tiny_fp32_workload_matches_oracle_to_1e4():
+    """The fp32 workload: B=1, Hq=4, Hkv=2, q_len=kv_len=128, D=64."""
+    (q, k, v), o, lse = _run(synth.TINY_PREFILL_FP32)
+    o_ref, lse_ref = oracle.prefill(_np(q), _np(k), _np(v))
+    check_o(o, o_ref, fp32=True)
+    check_lse(lse, lse_ref, fp32=True)
+
+
+@pytest.mark.parametrize("hq,hkv,lq,lk", [(8, 4, 100, 100), (6, 3, 70, 200), (2, 2, 300, 40)])
+def test_fp32_other_shapes(hq, hkv, lq, lk):
+    shape = replace(synth.TINY_PREFILL_FP32, B=2, Hq=hq, Hkv=hkv, q_len=lq, kv_len=lk)
+    (q, k, v), o, lse = _run(shape, seed=lq)
+    o_ref, lse_ref = oracle.prefill(_np(q), _np(k), _np(v))
+    check_o(o, o_ref, fp32=True)
+    check_lse(lse, lse_ref, fp32=True)
+
+
+BF16_CASES = [
+    # (B, Hq, Hkv, q_len, kv_len): several tiles and a ragged tail each
+    (2, 8, 1, 200, 328),    # G = 8, delta = 128
+    (1, 8, 2, 300, 300),    # G = 4, square
+    (1, 4, 4, 257, 400),    # G = 1 (plain multi-head)
+    (2, 4, 2, 130, 130),    # G = 2
+    (1, 16, 1, 100, 612),   # G = 16
+    (1, 32, 1, 40, 1000),   # G = 32
+    (1, 8, 1, 1, 333),      # a single query row
+    (1, 8, 2, 260, 120),    # q_len > kv_len: the first rows see no key
+    (3, 8, 8, 64, 64),      # G = 1, short
+]
+
+
+@pytest.mark.parametrize("bsz,hq,hkv,lq,lk", BF16_CASES)
+def test_bf16_tensor_core_path_matches_oracle(bsz, hq, hkv, lq, lk):
+    shape = replace(synth.LLAMA_GQA_PREFILL, B=bsz, Hq=hq, Hkv=hkv, q_len=lq, kv_len=lk)
+    (q, k, v), o, lse = _run(shape, seed=lq + lk)
+    o_ref, lse_ref = oracle.prefill(_np(q), _np(k), _np(v))
+    check_o(o, o_ref)
+    check_lse(lse, lse_ref)
+
+
+def test_bf16_sharp_softmax_k_scaled():
+    """K x 2 (as in the batched workload) sharpens the softmax and exercises the
+    lazy rescaling of the running max."""
+    shape = replace(synth.BATCHED_SQUARE_PREFILL, B=1, Hq=8, Hkv=2, q_len=520, kv_len=520)
+    (q, k, v), o, lse = _run(shape, seed=4)
+    o_ref, lse_ref = oracle.prefill(_np(q), _np(k), _np(v))
+    check_o(o, o_ref)
+    check_lse(lse, lse_ref)
+
+
+def test_bf16_head_dim_64_cuda_core_path():
+    shape = replace(synth.LLAMA_GQA_PREFILL, B=1, Hq=4, Hkv=2, q_len=150, kv_len=200, D=64)
+    (q, k, v), o, lse = _run(shape, seed=1)
+    o_ref, lse_ref = oracle.prefill(_np(q), _np(k), _np(v))
+    check_o(o, o_ref)
+    check_lse(lse, lse_ref)
+
+
+def test_bf16_group_of_three_cuda_core_path():
+    shape = replace(synth.LLAMA_GQA_PREFILL, B=1, Hq=6, Hkv=2, q_len=90, kv_len=150)
+    (q, k, v), o, lse = _run(shape, seed=2)
+    o_ref, lse_ref = oracle.prefill(_np(q), _np(k), _np(v))
+    check_o(o, o_ref)
+    check_lse(lse, lse_ref)
+
+
+def _sampled_rows(shape, n_heads, rows_per_head, seed):
+    """Full-size workload in the benchmark's launch configuration; the oracle
+    computes sampled rows (first, last, around multiples of the tile sizes and
+    random ones) of sampled heads one by one."""
+    (q, k, v), o, lse = _run(shape, seed=0)
+    rng = np.random.default_rng(seed)
+    o_np = o.float().cpu().double().numpy()
+    lse_np = lse.cpu().double().numpy()
+    assert np.isfinite(o_np).all() and np.isfinite(lse_np).all()
+    fixed = [0, 1, 15, 16, 31, 32, 127, 128, 255, shape.q_len - 1]
+    for _ in range(n_heads):
+        b = int(rng.integers(shape.B))
+        h = int(rng.integers(shape.Hq))
+        rows = sorted(set(fixed + rng.integers(0, shape.q_len, rows_per_head).tolist()))
+        o_ref, lse_ref = oracle.prefill_rows(_np(q[b:b + 1]), _np(k[b:b + 1]), _np(v[b:b + 1]), 0, h, rows)
+        check_o(torch.from_numpy(o_np[b, h, rows]), o_ref, what=f"O[b={b},h={h}]")
+        check_lse(torch.from_numpy(lse_np[b, h, rows]), lse_ref, what=f"LSE[b={b},h={h}]")
+
+
+def test_full_size_llama_gqa_prefill_sampled():
+    _sampled_rows(synth.LLAMA_GQA_PREFILL, n_heads=6, rows_per_head=24, seed=1)
+
+
+def test_full_size_batched_square_prefill_sampled():
+    _sampled_rows(synth.BATCHED_SQUARE_PREFILL, n_heads=4, rows_per_head=16, seed=2)
