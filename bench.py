@@ -108,7 +108,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
                                           "-lms", "200", "-i", str(gpu_id)], stdout=subprocess.PIPE,
-                                         stderr=subprocess.DEVNULL, text=True)
+                                         stderr=subprocess.PIPE, text=True)
         except OSError:
             self.proc = None
 
@@ -117,10 +117,10 @@ class ClockSampler:
             return None
         self.proc.terminate()
         try:
-            out, _ = self.proc.communicate(timeout=5)
+            out, err = self.proc.communicate(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-            out, _ = self.proc.communicate()
+            out, err = self.proc.communicate()
         sms, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in out.splitlines():
@@ -136,7 +136,7 @@ class ClockSampler:
                 if val.lower() == "active":
                     reasons.add(n)
         if not sms:
-            return None
+            return {"error": (err or out or "no samples").strip()[:200]}
         sms.sort()
         return {"sm_mhz": sms[len(sms) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sms)}
 
@@ -248,10 +248,18 @@ def run_ours(args, rank, world, dist):
     for _ in range(args.warmup):
         step(new_events())
     torch.cuda.synchronize(dev)
+    # nvidia-smi samples every 200 ms, far longer than K steps take: the
+    # sampler covers a loaded window of untimed steps (about args.clock_window
+    # seconds) that ends with the timed region itself
+    sampler = ClockSampler(gpu_id_for_smi(torch, dev)) if rank == 0 else None
+    t_end = time.perf_counter() + args.clock_window
+    while time.perf_counter() < t_end:
+        for _ in range(8):
+            step(new_events())
+        torch.cuda.synchronize(dev)
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize(dev)
-    sampler = ClockSampler(gpu_id_for_smi(torch, dev)) if rank == 0 else None
     region0 = torch.cuda.Event(enable_timing=True)
     region1 = torch.cuda.Event(enable_timing=True)
     evs = [new_events() for _ in range(args.steps)]
@@ -433,6 +441,40 @@ def run_reference(args, rank):
             "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def run_profile(args):
+    """One kernel on its workload, `args.warmup + args.steps` launches, for an
+    ncu capture of that kernel (`-k` and `-s/-c` pick the launches)."""
+    from dataclasses import replace
+
+    import torch
+
+    import causal_gqa_flashattention_attn_gb300 as attn
+    import synth
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    attn.lib()
+    n = args.warmup + args.steps
+    if args.profile.startswith("prefill"):
+        shape = synth.LLAMA_GQA_PREFILL if args.profile == "prefill" else synth.BATCHED_SQUARE_PREFILL
+        q, k, v = (t.to(dev) for t in synth.prefill_inputs(shape, seed=0))
+        for _ in range(n):
+            attn.attn_prefill_fwd(q, k, v)
+    else:
+        shape = synth.PAGED_DECODE_BF16 if args.profile == "decode_bf16" else synth.PAGED_DECODE_INT4
+        if args.decode_batch:
+            shape = replace(shape, B=args.decode_batch)
+        inp = synth.decode_inputs(shape, seed=0)
+        t = {kk: vv.to(dev) for kk, vv in inp.items() if torch.is_tensor(vv)}
+        ws = torch.empty(attn.attn_decode_workspace_bytes(shape.B, shape.Hq, shape.len_hi, shape.split_tokens,
+                                                          shape.D), dtype=torch.uint8, device=dev)
+        for _ in range(n):
+            attn.attn_decode_paged_splitk(t["q"], t["k_cache"], t["v_cache"], t["block_table"], t["seq_lens"],
+                                          shape.split_tokens, shape.len_hi, n_groups=shape.n_groups, workspace=ws,
+                                          write_output=False)
+    torch.cuda.synchronize(dev)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -441,6 +483,11 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clock-window", type=float, default=2.0,
+                    help="seconds of loaded, untimed steps sampled by nvidia-smi before the timed region")
+    ap.add_argument("--profile", choices=["prefill", "prefill_batched", "decode_bf16", "decode_int4"],
+                    help="run only one kernel on its workload (for ncu captures); prints no JSON line")
+    ap.add_argument("--decode-batch", type=int, default=0, help="with --profile: shrink the decode batch")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -448,6 +495,9 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     dist = None
+    if args.profile:
+        run_profile(args)
+        return
     if args.impl == "reference":
         line = run_reference(args, rank)
     else:
