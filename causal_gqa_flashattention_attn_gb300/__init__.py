@@ -11,6 +11,7 @@ Entry points (names as in the C ABI):
   attn_prefill_fwd          causal GQA prefill -> (O, LSE)
   attn_decode_workspace_bytes
   attn_decode_paged_splitk  single-query split-K decode over a paged cache
+  attn_decode_paged_splitk_static  the same decode with no workspace argument
   attn_lse_merge            LSE-weighted merge of split partials
   attn_status_string
 """
@@ -32,7 +33,8 @@ ATTN_DEV_SEQ_TOO_LONG = 0x2
 ATTN_DEV_WAIT_TIMEOUT = 0x4
 
 EXPORTED = ("attn_prefill_fwd", "attn_decode_workspace_bytes", "attn_decode_paged_splitk",
-            "attn_lse_merge", "attn_status_string", "attn_abi_version")
+            "attn_decode_paged_splitk_static", "attn_lse_merge", "attn_status_string", "attn_abi_version")
+ATTN_DECODE_STATIC_SCRATCH_BYTES = 32 << 20
 
 _lib = None
 
@@ -60,6 +62,9 @@ def lib():
     L.attn_decode_paged_splitk.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, i32, i32, i32,
                                            i32, f32, vp, sz, vp, vp, vp, vp]
     L.attn_decode_paged_splitk.restype = i32
+    L.attn_decode_paged_splitk_static.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, i32,
+                                                  i32, i32, i32, f32, vp, vp, vp, vp]
+    L.attn_decode_paged_splitk_static.restype = i32
     L.attn_lse_merge.argtypes = [vp, vp, i32, i32, i32, vp, vp, i32, vp]
     L.attn_lse_merge.restype = i32
     L.attn_status_string.argtypes = [i32]
@@ -157,6 +162,33 @@ def attn_decode_paged_splitk(q, k_cache, v_cache, block_table, seq_lens, split_t
         workspace.numel() * workspace.element_size(), _ptr(o), _ptr(lse), _ptr(dev_status), _stream_ptr(stream))
     _check("attn_decode_paged_splitk", st)
     return o, lse, workspace
+
+
+def attn_decode_paged_splitk_static(q, k_cache, v_cache, block_table, seq_lens, split_tokens, max_kv_len,
+                                    scale=None, n_groups=1, o=None, lse=None, dev_status=None, stream=None):
+    """The same decode for callers that cannot allocate device memory: no
+    workspace argument, the split partials go to a fixed array inside the
+    library (at most ATTN_DECODE_STATIC_SCRATCH_BYTES).  Calls share that
+    array, so calls that overlap on the GPU race; the first call on a device
+    looks up the array's address and should come before any stream capture.
+    Returns ``(o, lse)``; ``o`` and ``lse`` are allocated here (by torch, on
+    the Python side) only when not given."""
+    _need_cuda(q, k_cache, v_cache, block_table, seq_lens, o, lse, dev_status)
+    bsz, hq, d = q.shape
+    num_pages, page_size, hkv = k_cache.shape[0], k_cache.shape[1], k_cache.shape[2]
+    kv_dtype = ATTN_INT4_PACKED if k_cache.dtype == torch.int32 else _DT.get(k_cache.dtype, -1)
+    if o is None:
+        o = torch.empty(bsz, hq, d, dtype=q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty(bsz, hq, dtype=torch.float32, device=q.device)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    st = lib().attn_decode_paged_splitk_static(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1], _ptr(seq_lens), kv_dtype,
+        n_groups, bsz, hq, hkv, d, num_pages, page_size, split_tokens, max_kv_len, float(scale), _ptr(o), _ptr(lse),
+        _ptr(dev_status), _stream_ptr(stream))
+    _check("attn_decode_paged_splitk_static", st)
+    return o, lse
 
 
 def decode_partials_view(workspace, B, Hq, max_kv_len, split_tokens, D):

@@ -136,6 +136,42 @@ attn_status_t attn_decode_paged_splitk(const void* q, const void* k_cache, const
                                        void* o, float* lse, int32_t* dev_status, void* stream);
 
 /*
+ * attn_decode_paged_splitk_static - attn_decode_paged_splitk without a workspace.
+ *
+ * The pages have no counterpart of this entry point.  It serves callers that
+ * cannot allocate device memory on the call path: plugin or callback
+ * interfaces that hand over only input and output buffers, and serving loops
+ * that forbid cudaMalloc once running (an allocation can synchronise the
+ * device and can fail under memory pressure mid-request).  It computes
+ * exactly what attn_decode_paged_splitk computes, with the same arguments
+ * minus the workspace, and allocates nothing: the split partials go to one
+ * fixed array of ATTN_DECODE_STATIC_SCRATCH_BYTES bytes of device memory that
+ * belongs to the library image and stays reserved on every GPU that loads the
+ * library until the process exits.
+ *
+ *   - o is required (the partials are not visible to the caller); lse may be NULL.
+ *   - Returns ATTN_ERR_WORKSPACE when
+ *     attn_decode_workspace_bytes(B, Hq, max_kv_len, split_tokens, D) exceeds
+ *     ATTN_DECODE_STATIC_SCRATCH_BYTES; all other checks and errors are those
+ *     of attn_decode_paged_splitk.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.  ATTN_ERR_CUDA if the lookup fails.
+ *   - All calls share the one array, which keeps the last call's contents
+ *     (nothing in it needs to start at zero: every partial is written before
+ *     it is read).  Calls whose work overlaps on the GPU (different streams or
+ *     host threads) race with each other and must be serialised by the caller.
+ */
+#define ATTN_DECODE_STATIC_SCRATCH_BYTES ((size_t)32 << 20)
+
+attn_status_t attn_decode_paged_splitk_static(const void* q, const void* k_cache, const void* v_cache,
+                                              const int32_t* block_table, int max_pages_per_seq,
+                                              const int32_t* seq_lens, attn_dtype_t kv_dtype, int n_groups,
+                                              int B, int Hq, int Hkv, int D, int num_pages, int page_size,
+                                              int split_tokens, int max_kv_len, float scale,
+                                              void* o, float* lse, int32_t* dev_status, void* stream);
+
+/*
  * attn_lse_merge - LSE-weighted merge of split partials.
  *
  * Follows "splitk_kernels.py", _splitK_reduce: per row n,
