@@ -325,6 +325,9 @@ cudaError_t launch_bf16(const DecodeArgs& a, cudaStream_t stream) {
     auto kern = decode_bf16_kernel<G, NS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
+    // two CTAs per SM: ask for the largest shared-memory carveout
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
     dim3 grid(a.n_split, a.Hkv, a.B);
     kern<<<grid, kThreads, smem, stream>>>(k_map, v_map, p);
     return cudaGetLastError();

@@ -67,7 +67,7 @@ __device__ __forceinline__ void k_word_of(int t, int ks, int& word, int& j0) {
 }
 
 template <int G, int NG, int NS>
-__global__ void __launch_bounds__(kThreads) decode_int4_kernel(const __grid_constant__ CUtensorMap k_map,
+__global__ void __launch_bounds__(kThreads, (G > 8) ? 1 : 3) decode_int4_kernel(const __grid_constant__ CUtensorMap k_map,
                                                                const __grid_constant__ CUtensorMap v_map,
                                                                const Params p) {
     constexpr bool kTwoRows = (G > 8);
@@ -182,15 +182,26 @@ __global__ void __launch_bounds__(kThreads) decode_int4_kernel(const __grid_cons
             }
         }
     }
-    float o_acc[16][4];
+    constexpr int kRows = kTwoRows ? 2 : 1;
+    constexpr int MT = E / 16;                 // 16-row m-tiles of O^T per group
+    // O^T accumulators: [head tile of 8][m-tile of 16 head-dim rows][fragment]
+    float o_acc[kRows][8][4];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) o_acc[i][0] = o_acc[i][1] = o_acc[i][2] = o_acc[i][3] = 0.f;
-    float sp[NG][2], off_acc[NG][2];
+    for (int h = 0; h < kRows; ++h)
 #pragma unroll
-    for (int gr = 0; gr < NG; ++gr) sp[gr][0] = sp[gr][1] = off_acc[gr][0] = off_acc[gr][1] = 0.f;
+        for (int i = 0; i < 8; ++i) o_acc[h][i][0] = o_acc[h][i][1] = o_acc[h][i][2] = o_acc[h][i][3] = 0.f;
+    // running sums of bf16(p * scale_g) and of p * offset_g, per group and row
+    float2 sp2[NG][kRows], off2[NG][kRows];
+#pragma unroll
+    for (int gr = 0; gr < NG; ++gr)
+#pragma unroll
+        for (int rr = 0; rr < kRows; ++rr) sp2[gr][rr] = off2[gr][rr] = make_float2(0.f, 0.f);
     float m_run[2] = {-INFINITY, -INFINITY};
     float l_part[2] = {0.f, 0.f};
     const float sl2 = p.scale_log2;
+    // this warp's fp32 coefficient table for its 16 tokens of the current tile:
+    // [0] K scale, [1] K offset - 128 * K scale, [2] V scale, [3] V offset; [kind][group][token]
+    float* cf = reinterpret_cast<float*>(smem + NS * kStageBytes) + warp * (4 * NG * 16);
 
     for (int t = 0; t < n_tiles; ++t) {
         const int slot = t % NS;
@@ -204,44 +215,56 @@ __global__ void __launch_bounds__(kThreads) decode_int4_kernel(const __grid_cons
         if (n_valid > 0) {
             const uint32_t* kt = reinterpret_cast<const uint32_t*>(smem + slot * kStageBytes) + woff;
             const uint32_t* vt = reinterpret_cast<const uint32_t*>(smem + slot * kStageBytes + kTileBytes) + woff;
-            // tokens this lane's accumulator entries refer to (relative to the warp's 16)
-            const int tk[4] = {2 * t4, 2 * t4 + 1, 8 + 2 * t4, 9 + 2 * t4};
-            // ---- scores in code space
-            float s[2][4];
+            // ---- coefficient words -> fp32, once per (token, group); rows past the
+            // end of the sequence may hold any bits and get weight 0
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+            for (int i = lane; i < 2 * 16 * NG; i += 32) {
+                const int kv = i / (16 * NG), rem = i % (16 * NG);
+                const int tok = rem / NG, gr = rem % NG;
+                const uint32_t cw = (kv == 0 ? kt : vt)[(warp * 16 + tok) * BW + gr];
+                const bool ok = tok < n_valid;
+                const float sc = ok ? lo_half(cw) : 0.f, of = ok ? hi_half(cw) : 0.f;
+                cf[((2 * kv) * NG + gr) * 16 + tok] = sc;
+                cf[((2 * kv + 1) * NG + gr) * 16 + tok] = kv == 0 ? fmaf(-128.f, sc, of) : of;
+            }
+            __syncwarp();
+            // ---- scores in code space: per group T_g = sum_d q (128 + c), then
+            //      s += scale_g * T_g + (offset_g - 128 scale_g) * Qsum_g
+            float2 s2[2][kRows];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int rr = 0; rr < kRows; ++rr) s2[nt][rr] = make_float2(0.f, 0.f);
 #pragma unroll
             for (int gr = 0; gr < NG; ++gr) {
-                float acc[2][4];
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt) {
-                    acc[nt][0] = acc[nt][1] = -128.f * qsum[gr][0];
-                    acc[nt][2] = acc[nt][3] = -128.f * qsum[gr][1];
-                }
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
+                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
                     const uint32_t* krow = kt + (warp * 16 + nt * 8 + g) * BW + NG + gr * (E / 8);
 #pragma unroll
                     for (int ks = 0; ks < KS; ++ks) {
                         int word, j0;
                         k_word_of<NG>(t4, ks, word, j0);
                         const uint32_t w = krow[word];
-                        mma_bf16_16816(acc[nt], qa[gr][ks][0], qa[gr][ks][1], qa[gr][ks][2], qa[gr][ks][3],
+                        mma_bf16_16816(acc, qa[gr][ks][0], qa[gr][ks][1], qa[gr][ks][2], qa[gr][ks][3],
                                        nib_pair(w, j0), nib_pair(w, j0 + 1));
                     }
-                }
-                // affine map of group gr for this lane's four tokens
+                    const float2 scp = *reinterpret_cast<const float2*>(cf + (0 * NG + gr) * 16 + nt * 8 + 2 * t4);
+                    const float2 c2p = *reinterpret_cast<const float2*>(cf + (1 * NG + gr) * 16 + nt * 8 + 2 * t4);
 #pragma unroll
-                for (int e4 = 0; e4 < 4; ++e4) {
-                    const int nt = e4 >> 1, e = e4 & 1;
-                    const uint32_t cw = kt[(warp * 16 + tk[e4]) * BW + gr];
-                    const float sc = lo_half(cw), of = hi_half(cw);
-                    s[nt][e] += sc * acc[nt][e] + of * qsum[gr][0];
-                    if (kTwoRows) s[nt][e + 2] += sc * acc[nt][e + 2] + of * qsum[gr][1];
+                    for (int rr = 0; rr < kRows; ++rr) {
+                        s2[nt][rr] = __ffma2_rn(scp, make_float2(acc[2 * rr], acc[2 * rr + 1]), s2[nt][rr]);
+                        s2[nt][rr] = __ffma2_rn(c2p, make_float2(qsum[gr][rr], qsum[gr][rr]), s2[nt][rr]);
+                    }
                 }
             }
+            float s[2][4];
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
+                s[nt][0] = s2[nt][0].x;
+                s[nt][1] = s2[nt][0].y;
+                s[nt][2] = kTwoRows ? s2[nt][kRows - 1].x : 0.f;
+                s[nt][3] = kTwoRows ? s2[nt][kRows - 1].y : 0.f;
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int tok = nt * 8 + 2 * t4 + (e & 1);
@@ -249,11 +272,11 @@ __global__ void __launch_bounds__(kThreads) decode_int4_kernel(const __grid_cons
                 }
             }
             // ---- online softmax (same as the bf16 path)
-            float pv[2][4];   // [row][token slot e4]
+            float pv[2][4];   // [row][token slot: 2t, 2t+1, 2t+8, 2t+9]
             bool need_rescale = false;
             float alpha[2] = {1.f, 1.f};
 #pragma unroll
-            for (int rr = 0; rr < (kTwoRows ? 2 : 1); ++rr) {
+            for (int rr = 0; rr < kRows; ++rr) {
                 float mx = fmaxf(fmaxf(s[0][2 * rr], s[0][2 * rr + 1]), fmaxf(s[1][2 * rr], s[1][2 * rr + 1]));
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
@@ -270,49 +293,50 @@ __global__ void __launch_bounds__(kThreads) decode_int4_kernel(const __grid_cons
                 l_part[rr] = l_part[rr] * alpha[rr] + ((pv[rr][0] + pv[rr][1]) + (pv[rr][2] + pv[rr][3]));
             }
             if (__any_sync(0xffffffffu, need_rescale)) {
+                // O^T columns are heads 8h + 2t and 8h + 2t + 1; their alphas live
+                // in the lanes that hold those heads' score rows
 #pragma unroll
-                for (int dn = 0; dn < 16; ++dn) {
-                    o_acc[dn][0] *= alpha[0];
-                    o_acc[dn][1] *= alpha[0];
-                    o_acc[dn][2] *= alpha[1];
-                    o_acc[dn][3] *= alpha[1];
+                for (int h = 0; h < kRows; ++h) {
+                    const float a0 = __shfl_sync(0xffffffffu, alpha[h], 8 * t4);
+                    const float a1 = __shfl_sync(0xffffffffu, alpha[h], 8 * t4 + 4);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        o_acc[h][i][0] *= a0;
+                        o_acc[h][i][1] *= a1;
+                        o_acc[h][i][2] *= a0;
+                        o_acc[h][i][3] *= a1;
+                    }
                 }
 #pragma unroll
-                for (int gr = 0; gr < NG; ++gr) {
-                    sp[gr][0] *= alpha[0];
-                    sp[gr][1] *= alpha[1];
-                    off_acc[gr][0] *= alpha[0];
-                    off_acc[gr][1] *= alpha[1];
-                }
+                for (int gr = 0; gr < NG; ++gr)
+#pragma unroll
+                    for (int rr = 0; rr < kRows; ++rr) {
+                        const float2 a2 = make_float2(alpha[rr], alpha[rr]);
+                        sp2[gr][rr] = __fmul2_rn(sp2[gr][rr], a2);
+                        off2[gr][rr] = __fmul2_rn(off2[gr][rr], a2);
+                    }
             }
-            // ---- O += (P * scale_g) (128 + codes), group by group
+            // ---- O^T += (128 + codes)^T (P * scale_g)^T, group by group: M = 16
+            //      head-dim rows, N = 8 heads, K = 16 tokens
 #pragma unroll
             for (int gr = 0; gr < NG; ++gr) {
-                float sc[4], of[4];
+                const float2 scA = *reinterpret_cast<const float2*>(cf + (2 * NG + gr) * 16 + 2 * t4);
+                const float2 scC = *reinterpret_cast<const float2*>(cf + (2 * NG + gr) * 16 + 8 + 2 * t4);
+                const float2 ofA = *reinterpret_cast<const float2*>(cf + (3 * NG + gr) * 16 + 2 * t4);
+                const float2 ofC = *reinterpret_cast<const float2*>(cf + (3 * NG + gr) * 16 + 8 + 2 * t4);
+                uint32_t pa[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-                for (int e4 = 0; e4 < 4; ++e4) {
-                    // rows past the end of the sequence may hold any bits: weight 0 there
-                    const bool ok = tk[e4] < n_valid;
-                    const uint32_t cw = vt[(warp * 16 + tk[e4]) * BW + gr];
-                    sc[e4] = ok ? lo_half(cw) : 0.f;
-                    of[e4] = ok ? hi_half(cw) : 0.f;
-                }
-                uint32_t pa[4];
-#pragma unroll
-                for (int rr = 0; rr < 2; ++rr) {
-                    if (rr == 1 && !kTwoRows) {
-                        pa[1] = pa[3] = 0u;
-                        break;
-                    }
-                    const __nv_bfloat162 lo2 = __floats2bfloat162_rn(pv[rr][0] * sc[0], pv[rr][1] * sc[1]);
-                    const __nv_bfloat162 hi2 = __floats2bfloat162_rn(pv[rr][2] * sc[2], pv[rr][3] * sc[3]);
+                for (int rr = 0; rr < kRows; ++rr) {
+                    const float2 pA = make_float2(pv[rr][0], pv[rr][1]), pC = make_float2(pv[rr][2], pv[rr][3]);
+                    const __nv_bfloat162 lo2 = __float22bfloat162_rn(__fmul2_rn(pA, scA));
+                    const __nv_bfloat162 hi2 = __float22bfloat162_rn(__fmul2_rn(pC, scC));
                     pa[rr] = *reinterpret_cast<const uint32_t*>(&lo2);
                     pa[rr + 2] = *reinterpret_cast<const uint32_t*>(&hi2);
-                    const float2 lf = __bfloat1622float2(lo2), hf = __bfloat1622float2(hi2);
-                    sp[gr][rr] += (lf.x + lf.y) + (hf.x + hf.y);
-                    off_acc[gr][rr] += pv[rr][0] * of[0] + pv[rr][1] * of[1] + pv[rr][2] * of[2] + pv[rr][3] * of[3];
+                    sp2[gr][rr] = __fadd2_rn(sp2[gr][rr], __fadd2_rn(__bfloat1622float2(lo2), __bfloat1622float2(hi2)));
+                    off2[gr][rr] = __ffma2_rn(pC, ofC, __ffma2_rn(pA, ofA, off2[gr][rr]));
                 }
-                // B operand: this lane's column c = g owns elements [g*EPT, g*EPT + EPT) of the group.
+                // A operand (codes): lane row g supplies elements g*EPT + q of the
+                // group, q = 2*mt (m-tile row g) and 2*mt + 1 (m-tile row g + 8)
                 const uint32_t* v_a = vt + (warp * 16 + 2 * t4) * BW + NG + gr * (E / 8);      // token 2t
                 const uint32_t* v_c = vt + (warp * 16 + 8 + 2 * t4) * BW + NG + gr * (E / 8);  // token 2t+8
 #pragma unroll
@@ -325,10 +349,13 @@ __global__ void __launch_bounds__(kThreads) decode_int4_kernel(const __grid_cons
                     const uint32_t xc = __byte_perm(v_c[word], v_c[word + BW], sel);  // tokens 2t+8, 2t+9
                     const int q0 = nib & 3;
 #pragma unroll
-                    for (int jj = 0; jj < (EPT < 4 ? EPT : 4); ++jj) {
-                        const int dn = gr * (E / 8) + j + jj;   // n-tile index across D
-                        mma_bf16_16816(o_acc[dn], pa[0], pa[1], pa[2], pa[3], nib_pair(xa, q0 + jj),
-                                       nib_pair(xc, q0 + jj));
+                    for (int jj = 0; jj < (EPT < 4 ? EPT : 4); jj += 2) {
+                        const int mt = gr * MT + (j + jj) / 2;
+                        const uint32_t a0 = nib_pair(xa, q0 + jj), a1 = nib_pair(xa, q0 + jj + 1);
+                        const uint32_t a2 = nib_pair(xc, q0 + jj), a3 = nib_pair(xc, q0 + jj + 1);
+#pragma unroll
+                        for (int h = 0; h < kRows; ++h)
+                            mma_bf16_16816(o_acc[h][mt], a0, a1, a2, a3, pa[h], pa[h + 2]);
                     }
                 }
             }
@@ -338,16 +365,21 @@ __global__ void __launch_bounds__(kThreads) decode_int4_kernel(const __grid_cons
     }
 
     // ------------------------------------------- corrections and warp merge
+    float corr_g[NG][2];   // OFF_g - 128 SP_g, summed over the four lanes of a row
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
         l_part[rr] += __shfl_xor_sync(0xffffffffu, l_part[rr], 1);
         l_part[rr] += __shfl_xor_sync(0xffffffffu, l_part[rr], 2);
 #pragma unroll
         for (int gr = 0; gr < NG; ++gr) {
-            float corr = off_acc[gr][rr] - 128.f * sp[gr][rr];
+            float corr = 0.f;
+            if (rr < kRows) {
+                const float2 sp = sp2[gr][rr < kRows ? rr : 0], of = off2[gr][rr < kRows ? rr : 0];
+                corr = (of.x + of.y) - 128.f * (sp.x + sp.y);
+            }
             corr += __shfl_xor_sync(0xffffffffu, corr, 1);
             corr += __shfl_xor_sync(0xffffffffu, corr, 2);
-            off_acc[gr][rr] = corr;
+            corr_g[gr][rr] = corr;
         }
     }
     named_barrier_sync(1, 32 * kConsumers);
@@ -357,19 +389,31 @@ __global__ void __launch_bounds__(kThreads) decode_int4_kernel(const __grid_cons
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
         const int row = g + rr * 8;
-        if (row < G) {
+        if (row < G && t4 == 0) {
+            red_m[warp * G + row] = m_run[rr];
+            red_l[warp * G + row] = l_part[rr];
+        }
+    }
+    // O^T fragments: rows are head-dim elements, columns heads 8h + 2t, 8h + 2t + 1
 #pragma unroll
-            for (int dn = 0; dn < 16; ++dn) {
-                const int gr = dn / (E / 8), j = dn % (E / 8);
-                // column 2t -> element (2t)*EPT + j of group gr; column 2t+1 -> (2t+1)*EPT + j
-                const int d0 = gr * E + (2 * t4) * EPT + j;
-                const int d1 = gr * E + (2 * t4 + 1) * EPT + j;
-                red_o[(warp * G + row) * kD + d0] = o_acc[dn][2 * rr] + off_acc[gr][rr];
-                red_o[(warp * G + row) * kD + d1] = o_acc[dn][2 * rr + 1] + off_acc[gr][rr];
-            }
-            if (t4 == 0) {
-                red_m[warp * G + row] = m_run[rr];
-                red_l[warp * G + row] = l_part[rr];
+    for (int h = 0; h < kRows; ++h) {
+#pragma unroll
+        for (int gr = 0; gr < NG; ++gr) {
+            const float c0 = __shfl_sync(0xffffffffu, corr_g[gr][h], 8 * t4);
+            const float c1 = __shfl_sync(0xffffffffu, corr_g[gr][h], 8 * t4 + 4);
+            const int head0 = 8 * h + 2 * t4, head1 = head0 + 1;
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+                const float* f = o_acc[h][gr * MT + mt];
+                const int d_lo = gr * E + g * EPT + 2 * mt, d_hi = d_lo + 1;   // m-tile rows g, g + 8
+                if (head0 < G) {
+                    red_o[(warp * G + head0) * kD + d_lo] = f[0] + c0;
+                    red_o[(warp * G + head0) * kD + d_hi] = f[2] + c0;
+                }
+                if (head1 < G) {
+                    red_o[(warp * G + head1) * kD + d_lo] = f[1] + c1;
+                    red_o[(warp * G + head1) * kD + d_hi] = f[3] + c1;
+                }
             }
         }
     }
@@ -429,11 +473,14 @@ cudaError_t launch_g_ng(const DecodeArgs& a, cudaStream_t stream) {
     p.lse_part = a.lse_part;
     p.status = a.dev_status;
     // the merge scratch (4 warps x G rows x D floats) reuses the stage ring
-    const size_t ring = NS * kStageBytes;
+    const size_t ring = NS * kStageBytes + kConsumers * 4 * NG * 16 * sizeof(float);
     const size_t red = (kConsumers * G * kD + 2 * kConsumers * G) * sizeof(float);
     const size_t smem = (ring > red ? ring : red) + 1024;
     auto kern = decode_int4_kernel<G, NG, NS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    // two CTAs per SM: ask for the largest shared-memory carveout
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     dim3 grid(a.n_split, a.Hkv, a.B);
     kern<<<grid, kThreads, smem, stream>>>(k_map, v_map, p);

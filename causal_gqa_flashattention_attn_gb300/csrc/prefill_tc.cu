@@ -192,12 +192,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int e = 0; e < 32; ++e)
                             if (32 * c + e > lim) sr[c][e] = __float_as_uint(-INFINITY);
                 }
-                float mx = -INFINITY;
+                // row max: four independent chains of 3-input max
+                float mc[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
+                for (int e = 0; e < 32; e += 2)
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(sr[c][e]));
-                mx *= sl2;
+                    for (int c = 0; c < 4; ++c)
+                        mc[c] = max3f(mc[c], __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
+                float mx = max3f(mc[0], mc[1], fmaxf(mc[2], mc[3])) * sl2;
                 float alpha = 1.f;
                 const bool grow = mx > m + 8.f;
                 if (grow) {
@@ -219,21 +221,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 const float neg_m = (m == -INFINITY) ? 0.f : -m;
-                float lsum = 0.f;
+                // p = 2^(s * scale * log2 e - m): packed pair FMAs, MUFU ex2,
+                // four independent pair-sum chains, bf16x2 packing into TMEM
+                const float2 scl2 = make_float2(sl2, sl2), nm2 = make_float2(neg_m, neg_m);
+                float2 ls[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                make_float2(0.f, 0.f)};
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     uint32_t pk[32];
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
                         const int c = 2 * hh + (e >> 4), col = 2 * (e & 15);
-                        const float p0 = ex2(fmaf(__uint_as_float(sr[c][col]), sl2, neg_m));
-                        const float p1 = ex2(fmaf(__uint_as_float(sr[c][col + 1]), sl2, neg_m));
-                        lsum += p0 + p1;
-                        pk[e] = pack_bf16x2(p0, p1);
+                        const float2 y = __ffma2_rn(
+                            make_float2(__uint_as_float(sr[c][col]), __uint_as_float(sr[c][col + 1])), scl2, nm2);
+                        const float2 pp = make_float2(ex2(y.x), ex2(y.y));
+                        ls[e & 3] = __fadd2_rn(ls[e & 3], pp);
+                        pk[e] = pack_bf16x2(pp.x, pp.y);
                     }
                     tmem_st32(s_addr + 32 * hh, pk);
                 }
-                l += lsum;
+                const float2 l01 = __fadd2_rn(ls[0], ls[1]), l23 = __fadd2_rn(ls[2], ls[3]);
+                l += (l01.x + l01.y) + (l23.x + l23.y);
                 tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(&p_full[t]);
@@ -340,6 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     umma_commit(&s_full[0]);
                     issue_s(1, kv_iter % kStages);
                     umma_commit(&s_full[1]);
+                    if (it.n_kv == 1) umma_commit(&q_empty);  // Q no longer read: the producer may refill it
                     for (int j = 0; j < it.n_kv && ok; ++j, ++kv_iter) {
                         const int s = kv_iter % kStages;
                         const bool last = (j + 1 == it.n_kv);
@@ -358,9 +367,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 }
                                 issue_s(t, nxt % kStages);            // S_t = Q_t K_{j+1}^T (after P_t is read)
                                 umma_commit(&s_full[t]);
+                                if (t == 1 && j + 2 == it.n_kv) umma_commit(&q_empty);  // last S read Q
                             } else {
                                 umma_commit(&o_full[t]);
-                                if (t == 1) umma_commit(&q_empty);
                             }
                         }
                     }

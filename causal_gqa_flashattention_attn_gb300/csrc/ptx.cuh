@@ -135,6 +135,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Three-input maximum (one instruction on sm_100+).
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // Hardware base-2 exponential (MUFU.EX2), flush-to-zero; ex2(-inf) = +0.
 __device__ __forceinline__ float ex2(float x) {
     float y;
