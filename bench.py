@@ -91,9 +91,23 @@ def load_traffic():
     return out
 
 
-def aggregate(per_rank_ms, world):
-    """Whole-job timing: the slowest rank's time for each kernel."""
-    return {k: max(v[k] for v in per_rank_ms) for k in per_rank_ms[0]}
+def max_over_ranks(values, dist, device=None):
+    """Whole-job timing: element-wise maximum of `values` (a list of floats,
+    one per timed quantity) over all ranks of the process group `dist`
+    (torch.distributed, any backend); `values` unchanged when dist is None."""
+    if dist is None:
+        return list(values)
+    import torch
+    t = torch.tensor(values, dtype=torch.float64)
+    if device is not None:
+        t = t.to(device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.cpu().tolist()
+
+
+def job_throughput(work_per_rank, world, ms):
+    """Units processed by all ranks divided by the slowest rank's time (per second)."""
+    return world * work_per_rank / (ms * 1e-3)
 
 
 # ------------------------------------------------------------------- clocks
@@ -277,11 +291,8 @@ def run_ours(args, rank, world, dist):
     ms = {kn: sum(e[kn][0].elapsed_time(e[kn][1]) for e in evs) / args.steps for kn in kernels}
     region_ms = region0.elapsed_time(region1) / args.steps
     if dist is not None:
-        import torch.distributed as tdist
-        vals = torch.tensor([ms[kn] for kn in kernels] + [region_ms], dtype=torch.float64)
-        vals = vals.to(dev) if tdist.get_backend() == "nccl" else vals
-        tdist.all_reduce(vals, op=tdist.ReduceOp.MAX)
-        vals = vals.cpu().tolist()
+        vals = max_over_ranks([ms[kn] for kn in kernels] + [region_ms], dist,
+                              device=dev if dist.get_backend() == "nccl" else None)
         ms = dict(zip(kernels, vals[:-1]))
         region_ms = vals[-1]
 
@@ -312,6 +323,8 @@ def run_ours(args, rank, world, dist):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1) / args.steps
+    if dist is not None:
+        e2e_ms = max_over_ranks([e2e_ms], dist, device=dev if dist.get_backend() == "nccl" else None)[0]
     h2d = sum(t.numel() * t.element_size() for t in (q, k, v))
     d2h = o.numel() * o.element_size() + lse.numel() * lse.element_size()
 
@@ -322,7 +335,7 @@ def run_ours(args, rank, world, dist):
     peaks, peak_src = load_peaks()
     traffic = load_traffic()
     flops = prefill_flops(pf)
-    tflops = world * flops / (ms["prefill"] * 1e-3) / 1e12
+    tflops = job_throughput(flops, world, ms["prefill"]) / 1e12
     rep = {}
     rep["prefill"] = dict(bound="tensor", achieved=flops / (ms["prefill"] * 1e-3) / 1e12,
                           peak=peaks["bf16_tflops"], unit="TFLOP/s", work=flops, src="prefill_tc.cu",
