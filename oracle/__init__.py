@@ -30,5 +30,6 @@ from .attention import (  # noqa: F401
     decode_split_partials,
     decode_unsplit,
     lse_merge,
+    lse_merge_bwd,
     decode,
 )

@@ -336,3 +336,34 @@ def decode(q, k_cache, v_cache, block_table, seq_lens, page_size, split_tokens, 
                                              page_size, split_tokens, scale, kv_format,
                                              n_groups, max_kv_len, batches)
     return lse_merge(o_part, lse_part)
+
+
+# --------------------------------------------------------------------------
+# Gradient of the merge (splitk_kernels.py: _splitK_reduce_varargs_backward)
+# --------------------------------------------------------------------------
+
+def lse_merge_bwd(o_part, lse_part, d_o, d_lse=None):
+    """Gradients of :func:`lse_merge` with respect to its inputs.
+
+    For each row with merged ``O`` and ``LSE`` (recomputed here by
+    :func:`lse_merge`) and incoming gradients ``dO [..., D]``, ``dLSE [...]``:
+
+    1. ``w_s = exp(LSE_s - LSE)``, the weight of split ``s`` in the merge;
+    2. ``dO_s = w_s * dO``;
+    3. ``dLSE_s = w_s * dLSE + sum_d (O_s - O)_d * w_s * dO_d``.
+
+    A split with ``LSE_s = -inf`` (weight 0), and every split of a row whose
+    merged LSE is ``-inf``, gets zero gradients.  Returns ``(d_o_part,
+    d_lse_part)`` shaped like ``o_part`` and ``lse_part``.
+    """
+    o_part = np.asarray(o_part, dtype=np.float64)
+    lse_part = np.asarray(lse_part, dtype=np.float64)
+    d_o = np.asarray(d_o, dtype=np.float64)
+    d_lse = np.zeros(lse_part.shape[:-1]) if d_lse is None else np.asarray(d_lse, dtype=np.float64)
+    o, lse = lse_merge(o_part, lse_part)
+    alive = np.isfinite(lse)[..., None] & np.isfinite(lse_part)
+    w = np.where(alive, np.exp(np.where(alive, lse_part - np.where(np.isfinite(lse), lse, 0.0)[..., None], 0.0)),
+                 0.0)                                                          # [..., S]
+    d_o_part = w[..., None] * d_o[..., None, :]                                # [..., S, D]
+    d_lse_part = w * d_lse[..., None] + w * ((o_part - o[..., None, :]) * d_o[..., None, :]).sum(axis=-1)
+    return d_o_part, d_lse_part

@@ -455,3 +455,60 @@ def test_planted_wrong_gqa_map_is_caught(monkeypatch):
     ref = torch.nn.functional.scaled_dot_product_attention(qt, kr, vr, attn_mask=mask).numpy()
     np.testing.assert_allclose(o, ref, rtol=1e-12, atol=1e-12)
     assert not np.allclose(o_bad, ref)
+
+
+# ------------------------------------------------------------ merge backward
+
+def test_merge_bwd_matches_finite_differences_of_the_merge():
+    """Central differences of the (pinned) forward merge, in fp64."""
+    rng = np.random.default_rng(21)
+    n, s, d = 3, 4, 5
+    o_part = rng.standard_normal((n, s, d))
+    lse_part = rng.standard_normal((n, s)) * 2
+    lse_part[1, 2] = -np.inf
+    d_o = rng.standard_normal((n, d))
+    d_lse = rng.standard_normal(n)
+    g_o, g_l = oracle.lse_merge_bwd(o_part, lse_part, d_o, d_lse)
+
+    def loss(op, lp):
+        o, lse = oracle.lse_merge(op, lp)
+        return float((o * d_o).sum() + (lse * d_lse).sum())
+    h = 1e-6
+    for idx in [(0, 0, 0), (1, 3, 4), (2, 1, 2), (1, 2, 0)]:
+        op1, op2 = o_part.copy(), o_part.copy()
+        op1[idx] += h
+        op2[idx] -= h
+        fd = (loss(op1, lse_part) - loss(op2, lse_part)) / (2 * h)
+        assert abs(fd - g_o[idx]) < 1e-7
+    for idx in [(0, 0), (0, 3), (2, 1), (1, 1)]:
+        lp1, lp2 = lse_part.copy(), lse_part.copy()
+        lp1[idx] += h
+        lp2[idx] -= h
+        fd = (loss(o_part, lp1) - loss(o_part, lp2)) / (2 * h)
+        assert abs(fd - g_l[idx]) < 1e-7
+    # the empty split carries no gradient
+    assert g_l[1, 2] == 0 and np.all(g_o[1, 2] == 0)
+
+
+def test_merge_bwd_matches_torch_autograd():
+    rng = np.random.default_rng(22)
+    o_part = torch.from_numpy(rng.standard_normal((6, 3, 8))).requires_grad_(True)
+    lse_part = torch.from_numpy(rng.standard_normal((6, 3)) * 3).requires_grad_(True)
+    lse = torch.logsumexp(lse_part, dim=-1)
+    o = (torch.softmax(lse_part, dim=-1)[..., None] * o_part).sum(dim=1)
+    d_o = torch.from_numpy(rng.standard_normal((6, 8)))
+    d_lse = torch.from_numpy(rng.standard_normal(6))
+    ((o * d_o).sum() + (lse * d_lse).sum()).backward()
+    g_o, g_l = oracle.lse_merge_bwd(o_part.detach().numpy(), lse_part.detach().numpy(), d_o.numpy(), d_lse.numpy())
+    np.testing.assert_allclose(g_o, o_part.grad.numpy(), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(g_l, lse_part.grad.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_merge_bwd_all_empty_row_and_missing_dlse():
+    o_part = np.ones((2, 2, 3))
+    lse_part = np.array([[-np.inf, -np.inf], [0.0, 0.0]])
+    g_o, g_l = oracle.lse_merge_bwd(o_part, lse_part, np.ones((2, 3)))
+    assert np.all(g_o[0] == 0) and np.all(g_l[0] == 0)
+    # two equal splits: each weight 1/2; O_s == O so the dLSE term vanishes
+    np.testing.assert_allclose(g_o[1], 0.5)
+    np.testing.assert_allclose(g_l[1], 0.0)
