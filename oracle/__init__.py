@@ -32,4 +32,6 @@ from .attention import (  # noqa: F401
     lse_merge,
     lse_merge_bwd,
     decode,
+    decode_mq_split_partials,
+    decode_mq,
 )

@@ -367,3 +367,59 @@ def lse_merge_bwd(o_part, lse_part, d_o, d_lse=None):
     d_o_part = w[..., None] * d_o[..., None, :]                                # [..., S, D]
     d_lse_part = w * d_lse[..., None] + w * ((o_part - o[..., None, :]) * d_o[..., None, :]).sum(axis=-1)
     return d_o_part, d_lse_part
+
+
+# --------------------------------------------------------------------------
+# Causal multi-query decode (splitk_kernels.py: _fwd_kernel_splitK with
+# IS_CAUSAL and NUM_QUERIES_CAUSAL, "Why does the masking condition below work
+# as a causal mask?")
+# --------------------------------------------------------------------------
+
+def decode_mq_split_partials(q, k_cache, v_cache, block_table, seq_lens, page_size, split_tokens, scale=None,
+                             kv_format="dense", n_groups=1, max_kv_len=None, batches=None):
+    """Split partials of decode with ``q_len`` queries per sequence.
+
+    ``q [B, Hq, q_len, D]``.  Query ``i`` of sequence ``b`` sees cached token
+    ``t`` iff ``t <= len_b - q_len + i`` (bottom-right alignment, the queries
+    being the last ``q_len`` positions).  Returns ``o_part [B, Hq, q_len, S,
+    D]`` and ``lse_part [B, Hq, q_len, S]``; a split in which a query sees no
+    token gives ``O_s = 0``, ``LSE_s = -inf``.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    bsz, hq, nq, d = q.shape
+    hkv = k_cache.shape[2]
+    if hq % hkv != 0:
+        raise ValueError("Hq must be a multiple of Hkv")
+    group = hq // hkv
+    scale = _default_scale(d) if scale is None else float(scale)
+    lens = [int(x) for x in np.asarray(seq_lens).reshape(-1)]
+    if max_kv_len is None:
+        max_kv_len = max(lens) if lens else 0
+    n_split = num_splits(max_kv_len, split_tokens)
+    o_part = np.zeros((bsz, hq, nq, n_split, d))
+    lse_part = np.full((bsz, hq, nq, n_split), NEG_INF)
+    for b in (range(bsz) if batches is None else batches):
+        for s in range(n_split):
+            lo = s * split_tokens
+            hi = min(lo + split_tokens, lens[b])
+            if hi <= lo:
+                continue
+            k_rows = _kv_rows(k_cache, block_table, b, lo, hi, page_size, kv_format, d, n_groups)
+            v_rows = _kv_rows(v_cache, block_table, b, lo, hi, page_size, kv_format, d, n_groups)
+            k_rep = np.repeat(k_rows, group, axis=1)
+            v_rep = np.repeat(v_rows, group, axis=1)
+            t = np.arange(lo, hi)
+            mask = t[None, :] <= (lens[b] - nq + np.arange(nq))[:, None]      # [q_len, n]
+            for h in range(hq):
+                o, lse = attend(q[b, h], k_rep[:, h], v_rep[:, h], mask, scale)
+                o_part[b, h, :, s] = o
+                lse_part[b, h, :, s] = lse
+    return o_part, lse_part
+
+
+def decode_mq(q, k_cache, v_cache, block_table, seq_lens, page_size, split_tokens, scale=None,
+              kv_format="dense", n_groups=1, max_kv_len=None, batches=None):
+    """Causal multi-query decode: the per-split partials merged by :func:`lse_merge`."""
+    o_part, lse_part = decode_mq_split_partials(q, k_cache, v_cache, block_table, seq_lens, page_size,
+                                                split_tokens, scale, kv_format, n_groups, max_kv_len, batches)
+    return lse_merge(o_part, lse_part)

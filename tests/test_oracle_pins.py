@@ -512,3 +512,35 @@ def test_merge_bwd_all_empty_row_and_missing_dlse():
     # two equal splits: each weight 1/2; O_s == O so the dLSE term vanishes
     np.testing.assert_allclose(g_o[1], 0.5)
     np.testing.assert_allclose(g_l[1], 0.0)
+
+
+# ----------------------------------------------------- multi-query decode
+
+def test_multi_query_decode_equals_prefill_over_the_gathered_sequence():
+    """q_len queries against a paged cache of len tokens are the last q_len
+    rows of a causal prefill with kv_len = len (bottom-right alignment);
+    checked with the scalar brute force on the gathered rows."""
+    lens = [9, 3, 16]
+    ps, d, nq = 4, 8, 3
+    qd, kc, vc, table = _decode_case(31, lens, page_size=ps, d=d)
+    rng = np.random.default_rng(32)
+    q = rng.standard_normal((len(lens), 4, nq, d))
+    for split in (4, 5, 100):
+        o, lse = oracle.decode_mq(q, kc, vc, table, lens, ps, split, scale=0.4)
+        for b, n in enumerate(lens):
+            kk = oracle.gather_paged_rows(kc, table, b, 0, n, ps).transpose(1, 0, 2)[None]   # [1, Hkv, n, D]
+            vv = oracle.gather_paged_rows(vc, table, b, 0, n, ps).transpose(1, 0, 2)[None]
+            ob, lb = _brute_prefill(q[b][None], kk, vv, 0.4)
+            np.testing.assert_allclose(o[b], ob[0], rtol=1e-12, atol=1e-12)
+            fin = np.isfinite(lb[0])
+            np.testing.assert_allclose(lse[b][fin], lb[0][fin], rtol=1e-12, atol=1e-12)
+            assert np.array_equal(np.isinf(lse[b]), np.isinf(lb[0]))
+
+
+def test_multi_query_decode_with_one_query_is_single_query_decode():
+    lens = [7, 12]
+    qd, kc, vc, table = _decode_case(33, lens, page_size=4, d=8)
+    o1, l1 = oracle.decode(qd, kc, vc, table, lens, 4, 5)
+    o2, l2 = oracle.decode_mq(qd[:, :, None, :], kc, vc, table, lens, 4, 5)
+    np.testing.assert_array_equal(o2[:, :, 0], o1)
+    np.testing.assert_array_equal(l2[:, :, 0], l1)
