@@ -238,7 +238,21 @@ def run_ours(args, rank, world, dist):
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
 
-    kernels = ["prefill", "prefill_batched", "decode_bf16", "merge_bf16", "decode_int4", "merge_int4"]
+    kernels = ["prefill", "prefill_batched", "decode_bf16", "merge_bf16", "decode_int4", "merge_int4", "merge_bwd",
+               "decode_mq"]
+    # causal multi-query decode (4 draft queries per sequence) over the bf16 paged cache
+    mq_n = 4
+    gmq = torch.Generator().manual_seed(seed + 11)
+    mq_q = torch.randn(d16.B, d16.Hq, mq_n, d16.D, generator=gmq).to(torch.bfloat16).to(dev)
+    mq_ws = torch.empty(attn.attn_decode_workspace_bytes(d16.B, d16.Hq * mq_n, d16.len_hi, d16.split_tokens, d16.D),
+                        dtype=torch.uint8, device=dev)
+    # merge backward on the bf16 decode's split partials, with seeded upstream gradients
+    mbw = dec["decode_bf16"]
+    gmb = torch.Generator().manual_seed(seed + 7)
+    mb_do = torch.randn(mbw["o"].shape, generator=gmb).to(dev)
+    mb_dlse = torch.randn(mbw["lse"].shape, generator=gmb).to(dev)
+    mb_go = torch.empty_like(mbw["o_part"])
+    mb_gl = torch.empty_like(mbw["lse_part"])
     launches_per_step = len(kernels)
 
     def step(ev):
@@ -263,6 +277,18 @@ def run_ours(args, rank, world, dist):
             ev[mname][0].record(stream)
             attn.attn_lse_merge(d["o_part"], d["lse_part"], o=d["o"], lse=d["lse"], stream=stream)
             ev[mname][1].record(stream)
+        flush.fill_(1.0)
+        ev["merge_bwd"][0].record(stream)
+        attn.attn_lse_merge_bwd(mbw["o_part"], mbw["lse_part"], mb_do, mb_dlse, d_o_part=mb_go, d_lse_part=mb_gl,
+                                stream=stream)
+        ev["merge_bwd"][1].record(stream)
+        t16 = dec["decode_bf16"]["t"]
+        flush.fill_(1.0)
+        ev["decode_mq"][0].record(stream)
+        attn.attn_decode_paged_splitk_mq(mq_q, t16["k_cache"], t16["v_cache"], t16["block_table"], t16["seq_lens"],
+                                         d16.split_tokens, d16.len_hi, workspace=mq_ws, dev_status=status,
+                                         stream=stream, write_output=False)
+        ev["decode_mq"][1].record(stream)
 
     def new_events():
         return {kn: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for kn in kernels}
@@ -364,6 +390,14 @@ def run_ours(args, rank, world, dist):
         mb = n_rows * s_max * (d["shape"].D + 1) * 4 + n_rows * (d["shape"].D * 2 + 4)
         rep[mname] = dict(bound="hbm", achieved=mb / (ms[mname] * 1e-3) / 1e9, peak=peaks["hbm_gbs"], unit="GB/s",
                           work=mb, src="merge.cu", kernel="lse_merge_kernel")
+    n_rows, s_max, dd = mbw["o_part"].shape
+    # algorithmic bytes: partials read once, gradients in, gradient partials out
+    mbb = n_rows * s_max * (dd + 1) * 4 * 2 + n_rows * (dd + 1) * 4
+    rep["merge_bwd"] = dict(bound="hbm", achieved=mbb / (ms["merge_bwd"] * 1e-3) / 1e9, peak=peaks["hbm_gbs"],
+                            unit="GB/s", work=mbb, src="merge.cu", kernel="lse_merge_bwd_kernel")
+    mqb = dec["decode_bf16"]["bytes"]["kernel"] + mq_q.numel() * 2 - d16.B * d16.Hq * d16.D * 2
+    rep["decode_mq"] = dict(bound="hbm", achieved=mqb / (ms["decode_mq"] * 1e-3) / 1e9, peak=peaks["hbm_gbs"],
+                            unit="GB/s", work=mqb, src="decode.cu", kernel="decode_bf16_kernel (q_len 4)")
     kernels_out = []
     for kn in kernels:
         r = rep[kn]

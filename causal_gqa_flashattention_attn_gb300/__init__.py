@@ -11,8 +11,10 @@ Entry points (names as in the C ABI):
   attn_prefill_fwd          causal GQA prefill -> (O, LSE)
   attn_decode_workspace_bytes
   attn_decode_paged_splitk  single-query split-K decode over a paged cache
+  attn_decode_paged_splitk_mq      causal multi-query decode (q_len <= 16 per sequence)
   attn_decode_paged_splitk_static  the same decode with no workspace argument
   attn_lse_merge            LSE-weighted merge of split partials
+  attn_lse_merge_bwd        its gradient
   attn_status_string
 """
 
@@ -32,8 +34,9 @@ ATTN_DEV_PAGE_OUT_OF_RANGE = 0x1
 ATTN_DEV_SEQ_TOO_LONG = 0x2
 ATTN_DEV_WAIT_TIMEOUT = 0x4
 
-EXPORTED = ("attn_prefill_fwd", "attn_decode_workspace_bytes", "attn_decode_paged_splitk",
-            "attn_decode_paged_splitk_static", "attn_lse_merge", "attn_status_string", "attn_abi_version")
+EXPORTED = ("attn_prefill_fwd", "attn_decode_workspace_bytes", "attn_decode_paged_splitk", "attn_decode_paged_splitk_mq",
+            "attn_decode_paged_splitk_static", "attn_lse_merge", "attn_lse_merge_bwd", "attn_status_string",
+            "attn_abi_version")
 ATTN_DECODE_STATIC_SCRATCH_BYTES = 32 << 20
 
 _lib = None
@@ -62,11 +65,16 @@ def lib():
     L.attn_decode_paged_splitk.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, i32, i32, i32,
                                            i32, f32, vp, sz, vp, vp, vp, vp]
     L.attn_decode_paged_splitk.restype = i32
+    L.attn_decode_paged_splitk_mq.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, i32, i32, i32,
+                                              i32, i32, f32, vp, sz, vp, vp, vp, vp]
+    L.attn_decode_paged_splitk_mq.restype = i32
     L.attn_decode_paged_splitk_static.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, i32,
                                                   i32, i32, i32, f32, vp, vp, vp, vp]
     L.attn_decode_paged_splitk_static.restype = i32
     L.attn_lse_merge.argtypes = [vp, vp, i32, i32, i32, vp, vp, i32, vp]
     L.attn_lse_merge.restype = i32
+    L.attn_lse_merge_bwd.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp, vp, vp]
+    L.attn_lse_merge_bwd.restype = i32
     L.attn_status_string.argtypes = [i32]
     L.attn_status_string.restype = ctypes.c_char_p
     L.attn_abi_version.argtypes = []
@@ -164,6 +172,37 @@ def attn_decode_paged_splitk(q, k_cache, v_cache, block_table, seq_lens, split_t
     return o, lse, workspace
 
 
+def attn_decode_paged_splitk_mq(q, k_cache, v_cache, block_table, seq_lens, split_tokens, max_kv_len, scale=None,
+                                n_groups=1, workspace=None, o=None, lse=None, dev_status=None, stream=None,
+                                write_output=True):
+    """Causal multi-query decode: ``q [B, Hq, q_len, D]``; query i of sequence
+    b sees tokens ``t <= len_b - q_len + i``.  Returns ``(o [B, Hq, q_len, D],
+    lse [B, Hq, q_len], workspace)``."""
+    _need_cuda(q, k_cache, v_cache, block_table, seq_lens, workspace, o, lse, dev_status)
+    bsz, hq, nq, d = q.shape
+    num_pages, page_size, hkv = k_cache.shape[0], k_cache.shape[1], k_cache.shape[2]
+    kv_dtype = ATTN_INT4_PACKED if k_cache.dtype == torch.int32 else _DT.get(k_cache.dtype, -1)
+    need = attn_decode_workspace_bytes(bsz, hq * nq, max_kv_len, split_tokens, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    if write_output:
+        if o is None:
+            o = torch.empty(bsz, hq, nq, d, dtype=q.dtype, device=q.device)
+        if lse is None:
+            lse = torch.empty(bsz, hq, nq, dtype=torch.float32, device=q.device)
+    else:
+        o = lse = None
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    st = lib().attn_decode_paged_splitk_mq(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1], _ptr(seq_lens), kv_dtype,
+        n_groups, bsz, hq, hkv, nq, d, num_pages, page_size, split_tokens, max_kv_len, float(scale),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(o), _ptr(lse), _ptr(dev_status),
+        _stream_ptr(stream))
+    _check("attn_decode_paged_splitk_mq", st)
+    return o, lse, workspace
+
+
 def attn_decode_paged_splitk_static(q, k_cache, v_cache, block_table, seq_lens, split_tokens, max_kv_len,
                                     scale=None, n_groups=1, o=None, lse=None, dev_status=None, stream=None):
     """The same decode for callers that cannot allocate device memory: no
@@ -216,3 +255,18 @@ def attn_lse_merge(o_part, lse_part, o=None, lse=None, o_dtype=torch.float32, st
                               _stream_ptr(stream))
     _check("attn_lse_merge", st)
     return o, lse
+
+
+def attn_lse_merge_bwd(o_part, lse_part, d_o, d_lse=None, d_o_part=None, d_lse_part=None, stream=None):
+    """Gradient of the merge: ``(d_o_part [N, S, D], d_lse_part [N, S])`` from
+    the partials and the gradients ``d_o [N, D]``, ``d_lse [N]`` (float32)."""
+    _need_cuda(o_part, lse_part, d_o, d_lse, d_o_part, d_lse_part)
+    n, s, d = o_part.shape
+    if d_o_part is None:
+        d_o_part = torch.empty_like(o_part)
+    if d_lse_part is None:
+        d_lse_part = torch.empty_like(lse_part)
+    st = lib().attn_lse_merge_bwd(_ptr(o_part), _ptr(lse_part), _ptr(d_o), _ptr(d_lse), n, s, d, _ptr(d_o_part),
+                                  _ptr(d_lse_part), _stream_ptr(stream))
+    _check("attn_lse_merge_bwd", st)
+    return d_o_part, d_lse_part

@@ -79,6 +79,57 @@ size_t round16(size_t x) { return (x + 15) & ~static_cast<size_t>(15); }
 
 }  // namespace
 
+namespace {
+
+// Shared by the single- and multi-query decode entry points.
+attn_status_t decode_impl(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                          int max_pages_per_seq, const int32_t* seq_lens, attn_dtype_t kv_dtype, int n_groups, int B,
+                          int Hq, int Hkv, int q_len, int D, int num_pages, int page_size, int split_tokens,
+                          int max_kv_len, float scale, void* workspace, size_t workspace_bytes, void* o, float* lse,
+                          int32_t* dev_status, void* stream) {
+    if (q == nullptr || k_cache == nullptr || v_cache == nullptr || block_table == nullptr || seq_lens == nullptr)
+        return ATTN_ERR_INVALID_ARG;
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || num_pages <= 0 || page_size <= 0 || split_tokens <= 0 ||
+        max_kv_len < 0 || max_pages_per_seq <= 0 || q_len <= 0)
+        return ATTN_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0 || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || (o != nullptr && !aligned16(o)))
+        return ATTN_ERR_INVALID_ARG;
+    if (D != 128) return ATTN_ERR_UNSUPPORTED;
+    const int G = Hq / Hkv;
+    if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return ATTN_ERR_UNSUPPORTED;
+    if (q_len > 16) return ATTN_ERR_UNSUPPORTED;
+    if (page_size % 64 != 0 || split_tokens % 64 != 0) return ATTN_ERR_UNSUPPORTED;
+    if (static_cast<long long>(num_pages) * page_size >= (1LL << 31)) return ATTN_ERR_UNSUPPORTED;
+    int fmt = 0;
+    if (kv_dtype == ATTN_BF16) {
+        fmt = 0;
+    } else if (kv_dtype == ATTN_INT4_PACKED) {
+        fmt = 1;
+        if (n_groups != 1 && n_groups != 2 && n_groups != 4 && n_groups != 8) return ATTN_ERR_UNSUPPORTED;
+        if ((static_cast<long long>(Hkv) * (n_groups + D / 8)) % 4 != 0) return ATTN_ERR_UNSUPPORTED;
+    } else {
+        return ATTN_ERR_UNSUPPORTED;
+    }
+    const int rows_q = Hq * q_len;   // output rows per sequence
+    const size_t need = attn_decode_workspace_bytes(B, rows_q, max_kv_len, split_tokens, D);
+    if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return ATTN_ERR_WORKSPACE;
+    const int S = split_count(max_kv_len, split_tokens);
+    const size_t rows = static_cast<size_t>(B) * rows_q;
+    float* o_part = static_cast<float*>(workspace);
+    float* lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + round16(rows * S * D * sizeof(float)));
+    DecodeArgs a{q,         k_cache,   v_cache,      block_table, max_pages_per_seq, seq_lens, fmt, n_groups,
+                 B,         Hq,        Hkv,          D,           num_pages,         page_size, split_tokens,
+                 max_kv_len, S,        scale,        q_len,       o_part,            lse_part,  dev_status};
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_decode(a, s);
+    if (e != cudaSuccess) return ATTN_ERR_CUDA;
+    if (o != nullptr) e = launch_merge(o_part, lse_part, static_cast<int>(rows), S, D, o, lse, ATTN_BF16, s);
+    return from_cuda(e);
+}
+
+}  // namespace
+
 extern "C" {
 
 const char* attn_status_string(attn_status_t status) {
@@ -126,42 +177,21 @@ attn_status_t attn_decode_paged_splitk(const void* q, const void* k_cache, const
                                        int Hq, int Hkv, int D, int num_pages, int page_size, int split_tokens,
                                        int max_kv_len, float scale, void* workspace, size_t workspace_bytes,
                                        void* o, float* lse, int32_t* dev_status, void* stream) {
-    if (q == nullptr || k_cache == nullptr || v_cache == nullptr || block_table == nullptr || seq_lens == nullptr)
-        return ATTN_ERR_INVALID_ARG;
-    if (B <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || num_pages <= 0 || page_size <= 0 || split_tokens <= 0 ||
-        max_kv_len < 0 || max_pages_per_seq <= 0)
-        return ATTN_ERR_INVALID_ARG;
-    if (Hq % Hkv != 0 || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || (o != nullptr && !aligned16(o)))
-        return ATTN_ERR_INVALID_ARG;
-    if (D != 128) return ATTN_ERR_UNSUPPORTED;
-    const int G = Hq / Hkv;
-    if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return ATTN_ERR_UNSUPPORTED;
-    if (page_size % 64 != 0 || split_tokens % 64 != 0) return ATTN_ERR_UNSUPPORTED;
-    if (static_cast<long long>(num_pages) * page_size >= (1LL << 31)) return ATTN_ERR_UNSUPPORTED;
-    int fmt = 0;
-    if (kv_dtype == ATTN_BF16) {
-        fmt = 0;
-    } else if (kv_dtype == ATTN_INT4_PACKED) {
-        fmt = 1;
-        if (n_groups != 1 && n_groups != 2 && n_groups != 4 && n_groups != 8) return ATTN_ERR_UNSUPPORTED;
-        if ((static_cast<long long>(Hkv) * (n_groups + D / 8)) % 4 != 0) return ATTN_ERR_UNSUPPORTED;
-    } else {
-        return ATTN_ERR_UNSUPPORTED;
-    }
-    const size_t need = attn_decode_workspace_bytes(B, Hq, max_kv_len, split_tokens, D);
-    if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return ATTN_ERR_WORKSPACE;
-    const int S = split_count(max_kv_len, split_tokens);
-    const size_t rows = static_cast<size_t>(B) * Hq;
-    float* o_part = static_cast<float*>(workspace);
-    float* lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + round16(rows * S * D * sizeof(float)));
-    DecodeArgs a{q,        k_cache, v_cache, block_table, max_pages_per_seq, seq_lens, fmt, n_groups, B, Hq, Hkv,
-                 D,        num_pages, page_size, split_tokens, max_kv_len, S, scale, o_part, lse_part, dev_status};
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = launch_decode(a, s);
-    if (e != cudaSuccess) return ATTN_ERR_CUDA;
-    if (o != nullptr) e = launch_merge(o_part, lse_part, static_cast<int>(rows), S, D, o, lse, ATTN_BF16, s);
-    return from_cuda(e);
+    return decode_impl(q, k_cache, v_cache, block_table, max_pages_per_seq, seq_lens, kv_dtype, n_groups, B, Hq,
+                       Hkv, 1, D, num_pages, page_size, split_tokens, max_kv_len, scale, workspace, workspace_bytes,
+                       o, lse, dev_status, stream);
+}
+
+attn_status_t attn_decode_paged_splitk_mq(const void* q, const void* k_cache, const void* v_cache,
+                                          const int32_t* block_table, int max_pages_per_seq,
+                                          const int32_t* seq_lens, attn_dtype_t kv_dtype, int n_groups, int B,
+                                          int Hq, int Hkv, int q_len, int D, int num_pages, int page_size,
+                                          int split_tokens, int max_kv_len, float scale, void* workspace,
+                                          size_t workspace_bytes, void* o, float* lse, int32_t* dev_status,
+                                          void* stream) {
+    return decode_impl(q, k_cache, v_cache, block_table, max_pages_per_seq, seq_lens, kv_dtype, n_groups, B, Hq,
+                       Hkv, q_len, D, num_pages, page_size, split_tokens, max_kv_len, scale, workspace,
+                       workspace_bytes, o, lse, dev_status, stream);
 }
 
 attn_status_t attn_lse_merge(const float* o_part, const float* lse_part, int N, int S, int D, void* o, float* lse,
@@ -172,6 +202,17 @@ attn_status_t attn_lse_merge(const float* o_part, const float* lse_part, int N, 
     if (o_dtype != ATTN_F32 && o_dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
     if (!aligned16(o_part) || !aligned16(o)) return ATTN_ERR_INVALID_ARG;
     return from_cuda(launch_merge(o_part, lse_part, N, S, D, o, lse, o_dtype, static_cast<cudaStream_t>(stream)));
+}
+
+attn_status_t attn_lse_merge_bwd(const float* o_part, const float* lse_part, const float* d_o, const float* d_lse,
+                                 int N, int S, int D, float* d_o_part, float* d_lse_part, void* stream) {
+    if (o_part == nullptr || lse_part == nullptr || d_o == nullptr || d_o_part == nullptr || d_lse_part == nullptr)
+        return ATTN_ERR_INVALID_ARG;
+    if (N < 0 || S < 1 || D < 4 || D % 4 != 0) return ATTN_ERR_INVALID_ARG;
+    if (D > 1024) return ATTN_ERR_UNSUPPORTED;
+    if (!aligned16(o_part) || !aligned16(d_o) || !aligned16(d_o_part)) return ATTN_ERR_INVALID_ARG;
+    return from_cuda(launch_merge_bwd(o_part, lse_part, d_o, d_lse, N, S, D, d_o_part, d_lse_part,
+                                      static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -49,14 +49,18 @@ struct DecodeArgs {
     int n_groups;
     int B, Hq, Hkv, D, num_pages, page_size, split_tokens, max_kv_len, n_split;
     float scale;
+    int q_len;   // queries per sequence (causal multi-query decode when > 1)
     float* o_part;
     float* lse_part;
     int32_t* dev_status;
 };
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+int rows_per_cta(const DecodeArgs& a);
 
 cudaError_t launch_merge(const float* o_part, const float* lse_part, int N, int S, int D, void* o,
                          float* lse, int o_dtype, cudaStream_t stream);
+cudaError_t launch_merge_bwd(const float* o_part, const float* lse_part, const float* d_o, const float* d_lse, int N,
+                             int S, int D, float* d_o_part, float* d_lse_part, cudaStream_t stream);
 
 struct PrefillArgs {
     const void* q;

@@ -9,7 +9,10 @@
 //
 // GB300 design (not the pages' design):
 //   * one CTA per (split, kv head, sequence) serves all G = Hq/Hkv query heads
-//     of the group, so each K/V byte is read from HBM exactly once;
+//     of the group, so each K/V byte is read from HBM exactly once; with
+//     q_len > 1 queries per sequence (causal multi-query decode, the
+//     NUM_QUERIES_CAUSAL mode of _fwd_kernel_splitK) a CTA serves up to 16
+//     (query, head) rows and query i sees the tokens t <= len - q_len + i;
 //   * a producer warp streams 64-token K/V tiles with TMA (128-byte swizzle)
 //     through a ring of shared-memory stages, guided by the block table;
 //   * four consumer warps each take 16 tokens of a tile and compute the G
@@ -38,6 +41,7 @@ struct Params {
     const int32_t* block_table;
     const int32_t* seq_lens;
     int max_pages, B, Hq, Hkv, num_pages, page_size, split_tokens, max_kv_len, n_split;
+    int G, nq, rpg, n_rg;   // heads per kv head, queries per sequence, rows per CTA, row groups
     float scale_log2;
     float* o_part;    // [B, Hq, S, D]
     float* lse_part;  // [B, Hq, S]
@@ -50,23 +54,29 @@ __device__ __forceinline__ uint32_t tile_off(int r, int c) {
     return (c >> 3) * kHalfBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4);
 }
 
-template <int G, int NS>
+// Row r of a CTA is the (query i, head h) pair rg * rpg + r = i * G + h.
+
+template <int R, int NS>
 __global__ void __launch_bounds__(kThreads) decode_bf16_kernel(const __grid_constant__ CUtensorMap k_map,
                                                                const __grid_constant__ CUtensorMap v_map,
                                                                const Params p) {
-    static_assert(G == 1 || G == 2 || G == 4 || G == 8 || G == 16, "group size");
-    constexpr bool kTwoRows = (G > 8);  // rows g+8 of the m16 fragment hold real heads
+    static_assert(R == 1 || R == 2 || R == 4 || R == 8 || R == 16, "rows per CTA");
+    constexpr bool kTwoRows = (R > 8);  // rows g+8 of the m16 fragment are real
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align_1024(smem_raw);
     __shared__ __align__(8) uint64_t full_bar[NS];
     __shared__ __align__(8) uint64_t empty_bar[NS];
     __shared__ int s_abort;
 
-    const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+    const int split = blockIdx.x, kvh = blockIdx.y / p.n_rg, rg = blockIdx.y % p.n_rg, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const size_t head_stride = static_cast<size_t>(p.n_split) * kD;
-    float* o_base = p.o_part + ((static_cast<size_t>(b) * p.Hq + kvh * G) * p.n_split + split) * kD;
-    float* lse_base = p.lse_part + (static_cast<size_t>(b) * p.Hq + kvh * G) * p.n_split + split;
+    const int first_row = rg * p.rpg;
+    const int n_rows = min(p.rpg, p.G * p.nq - first_row);
+    // output row of CTA row r: ((b * Hq + kvh * G + h) * nq + i), with first_row + r = i * G + h
+    auto out_row = [&](int r) -> size_t {
+        const int rr = first_row + r, i = rr / p.G, h = rr % p.G;
+        return (static_cast<size_t>(b) * p.Hq + kvh * p.G + h) * p.nq + i;
+    };
 
     int len = p.seq_lens[b];
     const int cap = min(p.max_kv_len, p.max_pages * p.page_size);
@@ -77,8 +87,9 @@ __global__ void __launch_bounds__(kThreads) decode_bf16_kernel(const __grid_cons
     const int lo = split * p.split_tokens;
     const int hi = min(lo + p.split_tokens, len);
     if (lo >= hi) {  // empty split: O = 0, LSE = -inf
-        for (int i = threadIdx.x; i < G * kD; i += kThreads) o_base[(i / kD) * head_stride + (i % kD)] = 0.f;
-        if (threadIdx.x < G) lse_base[threadIdx.x * p.n_split] = -INFINITY;
+        for (int i = threadIdx.x; i < n_rows * kD; i += kThreads)
+            p.o_part[(out_row(i / kD) * p.n_split + split) * kD + (i % kD)] = 0.f;
+        if (threadIdx.x < n_rows) p.lse_part[out_row(threadIdx.x) * p.n_split + split] = -INFINITY;
         return;
     }
     const int n_tiles = (hi - lo + kTileTok - 1) / kTileTok;
@@ -127,18 +138,23 @@ __global__ void __launch_bounds__(kThreads) decode_bf16_kernel(const __grid_cons
 
     // -------------------------------------------------------------------- consumers
     const int g = lane >> 2, t4 = lane & 3;
-    // Q fragments (A operand, rows = heads of the group, zero past G).
+    // Q fragments (A operand, rows = (query, head) pairs, zero past the valid rows),
+    // and each row's last visible token (bottom-right causal, len - q_len + i)
     uint32_t qa[8][4];
+    int lim[2];
     {
-        const __nv_bfloat16* qh = p.q + (static_cast<size_t>(b) * p.Hq + kvh * G) * kD;
+        const bool ok0 = g < n_rows, ok1 = kTwoRows && g + 8 < n_rows;
+        const __nv_bfloat16* q0 = p.q + out_row(ok0 ? g : 0) * kD;
+        const __nv_bfloat16* q1 = p.q + out_row(ok1 ? g + 8 : 0) * kD;
+        lim[0] = ok0 ? len - p.nq + (first_row + g) / p.G : -1;
+        lim[1] = ok1 ? len - p.nq + (first_row + g + 8) / p.G : -1;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
             const int d0 = kk * 16 + 2 * t4;
-            qa[kk][0] = g < G ? *reinterpret_cast<const uint32_t*>(qh + g * kD + d0) : 0u;
-            qa[kk][2] = g < G ? *reinterpret_cast<const uint32_t*>(qh + g * kD + d0 + 8) : 0u;
-            qa[kk][1] = (kTwoRows && g + 8 < G) ? *reinterpret_cast<const uint32_t*>(qh + (g + 8) * kD + d0) : 0u;
-            qa[kk][3] =
-                (kTwoRows && g + 8 < G) ? *reinterpret_cast<const uint32_t*>(qh + (g + 8) * kD + d0 + 8) : 0u;
+            qa[kk][0] = ok0 ? *reinterpret_cast<const uint32_t*>(q0 + d0) : 0u;
+            qa[kk][2] = ok0 ? *reinterpret_cast<const uint32_t*>(q0 + d0 + 8) : 0u;
+            qa[kk][1] = ok1 ? *reinterpret_cast<const uint32_t*>(q1 + d0) : 0u;
+            qa[kk][3] = ok1 ? *reinterpret_cast<const uint32_t*>(q1 + d0 + 8) : 0u;
         }
     }
     float o_acc[16][4];
@@ -183,13 +199,13 @@ __global__ void __launch_bounds__(kThreads) decode_bf16_kernel(const __grid_cons
                     mma_bf16_16816(s[1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b2, b3);
                 }
             }
-            // mask tokens past the end, scale to the log2 domain
+            // mask tokens past the end and past each row's causal limit, scale to the log2 domain
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int tok = nt * 8 + 2 * t4 + (e & 1);
-                    s[nt][e] = tok < n_valid ? s[nt][e] * sl2 : -INFINITY;
+                    s[nt][e] = (tok < n_valid && tok0 + tok <= lim[e >> 1]) ? s[nt][e] * sl2 : -INFINITY;
                 }
             }
             // online softmax per row (row g: e = 0,1; row g+8: e = 2,3)
@@ -202,6 +218,7 @@ __global__ void __launch_bounds__(kThreads) decode_bf16_kernel(const __grid_cons
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
                 // lazy rescale: keep a stale max unless the new one exceeds it by 2^8
+                // (a row that sees none of these 16 tokens keeps mx = -inf and p = 0)
                 if (mx > m_run[rr] + 8.f) {
                     alpha[rr] = ex2(m_run[rr] - mx);  // 0 when m_run = -inf
                     m_run[rr] = mx;
@@ -251,47 +268,48 @@ __global__ void __launch_bounds__(kThreads) decode_bf16_kernel(const __grid_cons
         l_part[rr] += __shfl_xor_sync(0xffffffffu, l_part[rr], 2);
     }
     named_barrier_sync(1, 32 * kConsumers);  // every consumer is done with the stages
-    float* red_o = reinterpret_cast<float*>(smem);                 // [warp][G][kD]
-    float* red_m = red_o + kConsumers * G * kD;                    // [warp][G]
-    float* red_l = red_m + kConsumers * G;                         // [warp][G]
+    float* red_o = reinterpret_cast<float*>(smem);                 // [warp][R][kD]
+    float* red_m = red_o + kConsumers * R * kD;                    // [warp][R]
+    float* red_l = red_m + kConsumers * R;                         // [warp][R]
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
         const int row = g + rr * 8;
-        if (row < G) {
+        if (row < n_rows) {
 #pragma unroll
             for (int dn = 0; dn < 16; ++dn) {
                 const int d = dn * 8 + 2 * t4;
-                red_o[(warp * G + row) * kD + d] = o_acc[dn][2 * rr];
-                red_o[(warp * G + row) * kD + d + 1] = o_acc[dn][2 * rr + 1];
+                red_o[(warp * R + row) * kD + d] = o_acc[dn][2 * rr];
+                red_o[(warp * R + row) * kD + d + 1] = o_acc[dn][2 * rr + 1];
             }
             if (t4 == 0) {
-                red_m[warp * G + row] = m_run[rr];
-                red_l[warp * G + row] = l_part[rr];
+                red_m[warp * R + row] = m_run[rr];
+                red_l[warp * R + row] = l_part[rr];
             }
         }
     }
     named_barrier_sync(1, 32 * kConsumers);
     const int d = threadIdx.x;  // 0..127
-    for (int row = 0; row < G; ++row) {
+    for (int row = 0; row < n_rows; ++row) {
         float mx = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kConsumers; ++w) mx = fmaxf(mx, red_m[w * G + row]);
+        for (int w = 0; w < kConsumers; ++w) mx = fmaxf(mx, red_m[w * R + row]);
         float acc = 0.f, l = 0.f;
         if (mx != -INFINITY) {
 #pragma unroll
             for (int w = 0; w < kConsumers; ++w) {
-                const float c = ex2(red_m[w * G + row] - mx);
-                l += c * red_l[w * G + row];
-                acc += c * red_o[(w * G + row) * kD + d];
+                const float c = ex2(red_m[w * R + row] - mx);
+                l += c * red_l[w * R + row];
+                acc += c * red_o[(w * R + row) * kD + d];
             }
         }
         const bool alive = l > 0.f;
-        o_base[row * head_stride + d] = alive ? acc / l : 0.f;
-        if (d == 0) lse_base[row * p.n_split] = alive ? (mx * kLn2 + logf(l)) : -INFINITY;
+        const size_t orow = out_row(row) * p.n_split + split;
+        p.o_part[orow * kD + d] = alive ? acc / l : 0.f;
+        if (d == 0) p.lse_part[orow] = alive ? (mx * kLn2 + logf(l)) : -INFINITY;
     }
 }
 
-template <int G>
+template <int R>
 cudaError_t launch_bf16(const DecodeArgs& a, cudaStream_t stream) {
     constexpr int NS = 3;
     CUtensorMap k_map, v_map;
@@ -317,18 +335,22 @@ cudaError_t launch_bf16(const DecodeArgs& a, cudaStream_t stream) {
     p.split_tokens = a.split_tokens;
     p.max_kv_len = a.max_kv_len;
     p.n_split = a.n_split;
+    p.G = a.Hq / a.Hkv;
+    p.nq = a.q_len;
+    p.rpg = R;
+    p.n_rg = (p.G * p.nq + R - 1) / R;
     p.scale_log2 = a.scale * kLog2e;
     p.o_part = a.o_part;
     p.lse_part = a.lse_part;
     p.status = a.dev_status;
     const size_t smem = NS * kStageBytes + 1024;
-    auto kern = decode_bf16_kernel<G, NS>;
+    auto kern = decode_bf16_kernel<R, NS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     // two CTAs per SM: ask for the largest shared-memory carveout
     e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
-    dim3 grid(a.n_split, a.Hkv, a.B);
+    dim3 grid(a.n_split, a.Hkv * p.n_rg, a.B);
     kern<<<grid, kThreads, smem, stream>>>(k_map, v_map, p);
     return cudaGetLastError();
 }
@@ -337,9 +359,17 @@ cudaError_t launch_bf16(const DecodeArgs& a, cudaStream_t stream) {
 
 cudaError_t launch_decode_int4(const DecodeArgs& a, cudaStream_t stream);
 
+// Rows per CTA: the (query, head) pairs of one KV head, at most 16.
+int rows_per_cta(const DecodeArgs& a) {
+    const int rows = (a.Hq / a.Hkv) * a.q_len;
+    int r = 1;
+    while (r < rows && r < 16) r *= 2;
+    return r;
+}
+
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     if (a.kv_format == 1) return launch_decode_int4(a, stream);
-    switch (a.Hq / a.Hkv) {
+    switch (rows_per_cta(a)) {
         case 1: return launch_bf16<1>(a, stream);
         case 2: return launch_bf16<2>(a, stream);
         case 4: return launch_bf16<4>(a, stream);

@@ -37,6 +37,7 @@ struct Params {
     const int32_t* seq_lens;
     int max_pages, B, Hq, Hkv, num_pages, page_size, split_tokens, max_kv_len, n_split;
     int row_words;   // n_groups + D/8
+    int G, nq, rpg, n_rg;   // heads per kv head, queries per sequence, rows per CTA, row groups
     float scale_log2;
     float* o_part;
     float* lse_part;
@@ -66,11 +67,13 @@ __device__ __forceinline__ void k_word_of(int t, int ks, int& word, int& j0) {
     }
 }
 
-template <int G, int NG, int NS>
-__global__ void __launch_bounds__(kThreads, (G > 8) ? 1 : 3) decode_int4_kernel(const __grid_constant__ CUtensorMap k_map,
+// Row r of a CTA is the (query i, head h) pair rg * rpg + r = i * G + h; with
+// one query per sequence the rows are the G heads of the KV group.
+template <int R, int NG, int NS>
+__global__ void __launch_bounds__(kThreads, (R > 8) ? 1 : 3) decode_int4_kernel(const __grid_constant__ CUtensorMap k_map,
                                                                const __grid_constant__ CUtensorMap v_map,
                                                                const Params p) {
-    constexpr bool kTwoRows = (G > 8);
+    constexpr bool kTwoRows = (R > 8);
     constexpr int E = kD / NG;                 // elements per group
     constexpr int KS = E / 16;                 // k-steps per group
     constexpr int EPT = E / 8;                 // V elements per lane column per group
@@ -83,11 +86,14 @@ __global__ void __launch_bounds__(kThreads, (G > 8) ? 1 : 3) decode_int4_kernel(
     __shared__ __align__(8) uint64_t empty_bar[NS];
     __shared__ int s_abort;
 
-    const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+    const int split = blockIdx.x, kvh = blockIdx.y / p.n_rg, rg = blockIdx.y % p.n_rg, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const size_t head_stride = static_cast<size_t>(p.n_split) * kD;
-    float* o_base = p.o_part + ((static_cast<size_t>(b) * p.Hq + kvh * G) * p.n_split + split) * kD;
-    float* lse_base = p.lse_part + (static_cast<size_t>(b) * p.Hq + kvh * G) * p.n_split + split;
+    const int first_row = rg * p.rpg;
+    const int n_rows = min(p.rpg, p.G * p.nq - first_row);
+    auto out_row = [&](int r) -> size_t {
+        const int rr = first_row + r, i = rr / p.G, h = rr % p.G;
+        return (static_cast<size_t>(b) * p.Hq + kvh * p.G + h) * p.nq + i;
+    };
 
     int len = p.seq_lens[b];
     const int cap = min(p.max_kv_len, p.max_pages * p.page_size);
@@ -98,8 +104,9 @@ __global__ void __launch_bounds__(kThreads, (G > 8) ? 1 : 3) decode_int4_kernel(
     const int lo = split * p.split_tokens;
     const int hi = min(lo + p.split_tokens, len);
     if (lo >= hi) {
-        for (int i = threadIdx.x; i < G * kD; i += kThreads) o_base[(i / kD) * head_stride + (i % kD)] = 0.f;
-        if (threadIdx.x < G) lse_base[threadIdx.x * p.n_split] = -INFINITY;
+        for (int i = threadIdx.x; i < n_rows * kD; i += kThreads)
+            p.o_part[(out_row(i / kD) * p.n_split + split) * kD + (i % kD)] = 0.f;
+        if (threadIdx.x < n_rows) p.lse_part[out_row(threadIdx.x) * p.n_split + split] = -INFINITY;
         return;
     }
     const int n_tiles = (hi - lo + kTileTok - 1) / kTileTok;
@@ -150,17 +157,19 @@ __global__ void __launch_bounds__(kThreads, (G > 8) ? 1 : 3) decode_int4_kernel(
     // Q fragments in the nibble order of the K operand, and per-group sums of q.
     uint32_t qa[NG][KS][4];
     float qsum[NG][2];
+    int lim[2];   // each row's last visible token (bottom-right causal: len - q_len + i)
     {
-        const __nv_bfloat16* qh = p.q + (static_cast<size_t>(b) * p.Hq + kvh * G) * kD;
 #pragma unroll
         for (int rr = 0; rr < 2; ++rr) {
             const int row = g + 8 * rr;
-            const bool real = (rr == 0 || kTwoRows) && row < G;
+            const bool real = (rr == 0 || kTwoRows) && row < n_rows;
+            const __nv_bfloat16* qrow = p.q + out_row(real ? row : 0) * kD;
+            lim[rr] = real ? len - p.nq + (first_row + row) / p.G : -1;
 #pragma unroll
             for (int gr = 0; gr < NG; ++gr) {
                 float qs = 0.f;
                 if (real) {
-                    for (int e = 0; e < E; ++e) qs += __bfloat162float(qh[row * kD + gr * E + e]);
+                    for (int e = 0; e < E; ++e) qs += __bfloat162float(qrow[gr * E + e]);
                 }
                 qsum[gr][rr] = qs;
 #pragma unroll
@@ -170,7 +179,7 @@ __global__ void __launch_bounds__(kThreads, (G > 8) ? 1 : 3) decode_int4_kernel(
                     const int e0 = gr * E + 8 * word + j0;  // element of nibble j0
                     uint32_t lo_pair = 0u, hi_pair = 0u;
                     if (real) {
-                        const __nv_bfloat16* qr = qh + row * kD;
+                        const __nv_bfloat16* qr = qrow;
                         __nv_bfloat162 a = __halves2bfloat162(qr[e0], qr[e0 + 4]);
                         __nv_bfloat162 c = __halves2bfloat162(qr[e0 + 1], qr[e0 + 5]);
                         lo_pair = *reinterpret_cast<uint32_t*>(&a);
@@ -268,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, (G > 8) ? 1 : 3) decode_int4_kernel(
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int tok = nt * 8 + 2 * t4 + (e & 1);
-                    s[nt][e] = tok < n_valid ? s[nt][e] * sl2 : -INFINITY;
+                    s[nt][e] = (tok < n_valid && tok0 + tok <= lim[e >> 1]) ? s[nt][e] * sl2 : -INFINITY;
                 }
             }
             // ---- online softmax (same as the bf16 path)
@@ -384,14 +393,14 @@ __global__ void __launch_bounds__(kThreads, (G > 8) ? 1 : 3) decode_int4_kernel(
     }
     named_barrier_sync(1, 32 * kConsumers);
     float* red_o = reinterpret_cast<float*>(smem);
-    float* red_m = red_o + kConsumers * G * kD;
-    float* red_l = red_m + kConsumers * G;
+    float* red_m = red_o + kConsumers * R * kD;
+    float* red_l = red_m + kConsumers * R;
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
         const int row = g + rr * 8;
-        if (row < G && t4 == 0) {
-            red_m[warp * G + row] = m_run[rr];
-            red_l[warp * G + row] = l_part[rr];
+        if (row < n_rows && t4 == 0) {
+            red_m[warp * R + row] = m_run[rr];
+            red_l[warp * R + row] = l_part[rr];
         }
     }
     // O^T fragments: rows are head-dim elements, columns heads 8h + 2t, 8h + 2t + 1
@@ -406,39 +415,40 @@ __global__ void __launch_bounds__(kThreads, (G > 8) ? 1 : 3) decode_int4_kernel(
             for (int mt = 0; mt < MT; ++mt) {
                 const float* f = o_acc[h][gr * MT + mt];
                 const int d_lo = gr * E + g * EPT + 2 * mt, d_hi = d_lo + 1;   // m-tile rows g, g + 8
-                if (head0 < G) {
-                    red_o[(warp * G + head0) * kD + d_lo] = f[0] + c0;
-                    red_o[(warp * G + head0) * kD + d_hi] = f[2] + c0;
+                if (head0 < n_rows) {
+                    red_o[(warp * R + head0) * kD + d_lo] = f[0] + c0;
+                    red_o[(warp * R + head0) * kD + d_hi] = f[2] + c0;
                 }
-                if (head1 < G) {
-                    red_o[(warp * G + head1) * kD + d_lo] = f[1] + c1;
-                    red_o[(warp * G + head1) * kD + d_hi] = f[3] + c1;
+                if (head1 < n_rows) {
+                    red_o[(warp * R + head1) * kD + d_lo] = f[1] + c1;
+                    red_o[(warp * R + head1) * kD + d_hi] = f[3] + c1;
                 }
             }
         }
     }
     named_barrier_sync(1, 32 * kConsumers);
     const int d = threadIdx.x;
-    for (int row = 0; row < G; ++row) {
+    for (int row = 0; row < n_rows; ++row) {
         float mx = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kConsumers; ++w) mx = fmaxf(mx, red_m[w * G + row]);
+        for (int w = 0; w < kConsumers; ++w) mx = fmaxf(mx, red_m[w * R + row]);
         float acc = 0.f, l = 0.f;
         if (mx != -INFINITY) {
 #pragma unroll
             for (int w = 0; w < kConsumers; ++w) {
-                const float c = ex2(red_m[w * G + row] - mx);
-                l += c * red_l[w * G + row];
-                acc += c * red_o[(w * G + row) * kD + d];
+                const float c = ex2(red_m[w * R + row] - mx);
+                l += c * red_l[w * R + row];
+                acc += c * red_o[(w * R + row) * kD + d];
             }
         }
         const bool alive = l > 0.f;
-        o_base[row * head_stride + d] = alive ? acc / l : 0.f;
-        if (d == 0) lse_base[row * p.n_split] = alive ? (mx * kLn2 + logf(l)) : -INFINITY;
+        const size_t orow = out_row(row) * p.n_split + split;
+        p.o_part[orow * kD + d] = alive ? acc / l : 0.f;
+        if (d == 0) p.lse_part[orow] = alive ? (mx * kLn2 + logf(l)) : -INFINITY;
     }
 }
 
-template <int G, int NG>
+template <int R, int NG>
 cudaError_t launch_g_ng(const DecodeArgs& a, cudaStream_t stream) {
     constexpr int NS = 6;
     constexpr int BW = (NG <= 4) ? 20 : 24;
@@ -468,32 +478,36 @@ cudaError_t launch_g_ng(const DecodeArgs& a, cudaStream_t stream) {
     p.max_kv_len = a.max_kv_len;
     p.n_split = a.n_split;
     p.row_words = row_words;
+    p.G = a.Hq / a.Hkv;
+    p.nq = a.q_len;
+    p.rpg = R;
+    p.n_rg = (p.G * p.nq + R - 1) / R;
     p.scale_log2 = a.scale * kLog2e;
     p.o_part = a.o_part;
     p.lse_part = a.lse_part;
     p.status = a.dev_status;
-    // the merge scratch (4 warps x G rows x D floats) reuses the stage ring
+    // the merge scratch (4 warps x R rows x D floats) reuses the stage ring
     const size_t ring = NS * kStageBytes + kConsumers * 4 * NG * 16 * sizeof(float);
-    const size_t red = (kConsumers * G * kD + 2 * kConsumers * G) * sizeof(float);
+    const size_t red = (kConsumers * R * kD + 2 * kConsumers * R) * sizeof(float);
     const size_t smem = (ring > red ? ring : red) + 1024;
-    auto kern = decode_int4_kernel<G, NG, NS>;
+    auto kern = decode_int4_kernel<R, NG, NS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     // two CTAs per SM: ask for the largest shared-memory carveout
     e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
-    dim3 grid(a.n_split, a.Hkv, a.B);
+    dim3 grid(a.n_split, a.Hkv * p.n_rg, a.B);
     kern<<<grid, kThreads, smem, stream>>>(k_map, v_map, p);
     return cudaGetLastError();
 }
 
-template <int G>
+template <int R>
 cudaError_t launch_g(const DecodeArgs& a, cudaStream_t stream) {
     switch (a.n_groups) {
-        case 1: return launch_g_ng<G, 1>(a, stream);
-        case 2: return launch_g_ng<G, 2>(a, stream);
-        case 4: return launch_g_ng<G, 4>(a, stream);
-        case 8: return launch_g_ng<G, 8>(a, stream);
+        case 1: return launch_g_ng<R, 1>(a, stream);
+        case 2: return launch_g_ng<R, 2>(a, stream);
+        case 4: return launch_g_ng<R, 4>(a, stream);
+        case 8: return launch_g_ng<R, 8>(a, stream);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -501,7 +515,7 @@ cudaError_t launch_g(const DecodeArgs& a, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_decode_int4(const DecodeArgs& a, cudaStream_t stream) {
-    switch (a.Hq / a.Hkv) {
+    switch (rows_per_cta(a)) {
         case 1: return launch_g<1>(a, stream);
         case 2: return launch_g<2>(a, stream);
         case 4: return launch_g<4>(a, stream);

@@ -136,6 +136,31 @@ attn_status_t attn_decode_paged_splitk(const void* q, const void* k_cache, const
                                        void* o, float* lse, int32_t* dev_status, void* stream);
 
 /*
+ * attn_decode_paged_splitk_mq - causal multi-query split-K decode.
+ *
+ * Follows "splitk_kernels.py", _fwd_kernel_splitK with IS_CAUSAL and
+ * NUM_QUERIES_CAUSAL (the comment "Why does the masking condition below work
+ * as a causal mask?"): the q_len queries of a sequence are its last q_len
+ * positions, so query i (0-based) sees cached tokens t <= len_b - q_len + i
+ * (bottom-right alignment).  A split in which a query sees nothing yields
+ * O_s = 0, LSE_s = -inf for that query.  Used for speculative decoding.
+ *
+ * Arguments as attn_decode_paged_splitk, except:
+ *   q       [B, Hq, q_len, D] bfloat16;   1 <= q_len <= 16
+ *   o       [B, Hq, q_len, D] bfloat16 (or NULL: partials only);  lse [B, Hq, q_len] fp32
+ *   workspace >= attn_decode_workspace_bytes(B, Hq * q_len, max_kv_len, split_tokens, D);
+ *           it receives o_part [B, Hq, q_len, S, D] and lse_part [B, Hq, q_len, S].
+ * With q_len = 1 this is exactly attn_decode_paged_splitk.
+ */
+attn_status_t attn_decode_paged_splitk_mq(const void* q, const void* k_cache, const void* v_cache,
+                                          const int32_t* block_table, int max_pages_per_seq,
+                                          const int32_t* seq_lens, attn_dtype_t kv_dtype, int n_groups,
+                                          int B, int Hq, int Hkv, int q_len, int D, int num_pages,
+                                          int page_size, int split_tokens, int max_kv_len, float scale,
+                                          void* workspace, size_t workspace_bytes,
+                                          void* o, float* lse, int32_t* dev_status, void* stream);
+
+/*
  * attn_decode_paged_splitk_static - attn_decode_paged_splitk without a workspace.
  *
  * The pages have no counterpart of this entry point.  It serves callers that
@@ -186,6 +211,25 @@ attn_status_t attn_decode_paged_splitk_static(const void* q, const void* k_cache
  */
 attn_status_t attn_lse_merge(const float* o_part, const float* lse_part, int N, int S, int D,
                              void* o, float* lse, attn_dtype_t o_dtype, void* stream);
+
+/*
+ * attn_lse_merge_bwd - gradient of attn_lse_merge.
+ *
+ * Follows "splitk_kernels.py", _splitK_reduce_varargs_backward: with the
+ * merged O and LSE of each row and w_s = exp(lse_part[n, s] - LSE[n]),
+ *   d_o_part[n, s]   = w_s * d_o[n]
+ *   d_lse_part[n, s] = w_s * d_lse[n] + sum_d (o_part[n, s, d] - O[n, d]) * w_s * d_o[n, d].
+ * O and LSE are recomputed from the partials in fp32.  Splits with LSE -inf,
+ * and every split of a row whose partials are all -inf, get zero gradients.
+ *
+ *   o_part float32 [N, S, D], lse_part float32 [N, S]            (read)
+ *   d_o    float32 [N, D], d_lse float32 [N] (may be NULL = 0)   (read)
+ *   d_o_part float32 [N, S, D], d_lse_part float32 [N, S]        (written)
+ *   D <= 1024 and a multiple of 4;  S >= 1.
+ */
+attn_status_t attn_lse_merge_bwd(const float* o_part, const float* lse_part, const float* d_o,
+                                 const float* d_lse, int N, int S, int D,
+                                 float* d_o_part, float* d_lse_part, void* stream);
 
 /* Static, human-readable name of a status code. */
 const char* attn_status_string(attn_status_t status);

@@ -113,6 +113,12 @@ def test_merge_host_validation(L):
     assert L.attn_lse_merge(FAKE, FAKE, 4, 2, 128, FAKE, None, 2, None) == -2
 
 
+def test_merge_bwd_host_validation(L):
+    assert L.attn_lse_merge_bwd(None, FAKE, FAKE, None, 4, 2, 128, FAKE, FAKE, None) == -1
+    assert L.attn_lse_merge_bwd(FAKE, FAKE, FAKE, None, 4, 0, 128, FAKE, FAKE, None) == -1
+    assert L.attn_lse_merge_bwd(FAKE, FAKE, FAKE, None, 4, 2, 2048, FAKE, FAKE, None) == -2
+
+
 def test_product_path_has_no_cpu_fallback():
     """The binding must not import the oracle or reach a CPU implementation."""
     pkg = os.path.join(ROOT, "causal_gqa_flashattention_attn_gb300")

@@ -34,3 +34,27 @@ def test_merge_bf16_output():
     o_ref, lse_ref = oracle.lse_merge(o_part.double().numpy(), lse_part.double().numpy())
     check_o(o, o_ref)
     check_lse(lse, lse_ref)
+
+
+@pytest.mark.parametrize("n,s,d", [(1, 1, 128), (37, 5, 128), (300, 16, 128), (9, 40, 1024), (5, 2, 4)])
+def test_merge_bwd_matches_oracle(n, s, d):
+    """Gradient of the merge ("splitk_kernels.py", _splitK_reduce_varargs_backward)."""
+    dev = gpu_or_skip()
+    import causal_gqa_flashattention_attn_gb300 as attn
+    o_part, lse_part = synth.merge_inputs(n, s, d, seed=n + 3 * s)
+    g = torch.Generator().manual_seed(n * 11 + d)
+    d_o = torch.randn(n, d, generator=g)
+    d_lse = torch.randn(n, generator=g)
+    go, gl = attn.attn_lse_merge_bwd(o_part.to(dev), lse_part.to(dev), d_o.to(dev), d_lse.to(dev))
+    torch.cuda.synchronize()
+    ro, rl = oracle.lse_merge_bwd(o_part.double().numpy(), lse_part.double().numpy(), d_o.double().numpy(),
+                                  d_lse.double().numpy())
+    np.testing.assert_allclose(go.cpu().double().numpy(), ro, rtol=1e-5, atol=1e-5)
+    np.testing.assert_allclose(gl.cpu().double().numpy(), rl, rtol=1e-5, atol=1e-4)
+    # the all-empty first row gets zero gradients
+    assert torch.all(go[0] == 0) and torch.all(gl[0] == 0)
+    # without d_lse
+    go2, gl2 = attn.attn_lse_merge_bwd(o_part.to(dev), lse_part.to(dev), d_o.to(dev), None)
+    torch.cuda.synchronize()
+    ro2, rl2 = oracle.lse_merge_bwd(o_part.double().numpy(), lse_part.double().numpy(), d_o.double().numpy())
+    np.testing.assert_allclose(gl2.cpu().double().numpy(), rl2, rtol=1e-5, atol=1e-4)
