@@ -24,6 +24,8 @@ from .attention import (  # noqa: F401
     unpack_coef_word,
     dequant_int4_row,
     dequant_int4_rows,
+    fp8_e4m3_value,
+    dequant_fp8_rows,
     paged_row_index,
     gather_paged_rows,
     num_splits,

@@ -197,6 +197,39 @@ def dequant_int4_rows(words, d, n_groups):
 
 
 # --------------------------------------------------------------------------
+# fp8 row format (splitk_kernels.py: FP8_QUANTIZED in _fwd_kernel_splitK,
+# the K/V_fp8_scale_shift tensors, dequantize with PACKED_PER_VAL == 4)
+# --------------------------------------------------------------------------
+
+def fp8_e4m3_value(byte):
+    """Value of one float8 e4m3 byte (1 sign bit, 4 exponent bits with bias 7,
+    3 mantissa bits, no infinities; exponent 15 with mantissa 7 is NaN)."""
+    b = int(byte) & 0xFF
+    sign = -1.0 if b >> 7 else 1.0
+    e = (b >> 3) & 0xF
+    m = b & 7
+    if e == 15 and m == 7:
+        return float("nan")
+    if e == 0:
+        return sign * m * 2.0 ** -9             # subnormal: m/8 * 2^(1-7)
+    return sign * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+
+
+_FP8_TABLE = np.array([fp8_e4m3_value(b) for b in range(256)])
+
+
+def dequant_fp8_rows(codes, scale_shift):
+    """Rows of e4m3 bytes ``codes [..., D]`` with one coefficient word per row
+    ``scale_shift [...]`` (fp16 scale in the low 16 bits, fp16 shift in the
+    high 16 bits): value = decoded byte * scale + shift, in float64."""
+    c = np.asarray(codes).astype(np.int64) & 0xFF
+    w = np.asarray(scale_shift).astype(np.int64) & 0xFFFFFFFF
+    scale = fp16_from_bits(w & 0xFFFF)[..., None]
+    shift = fp16_from_bits(w >> 16)[..., None]
+    return _FP8_TABLE[c] * scale + shift
+
+
+# --------------------------------------------------------------------------
 # Paged split-K decode (splitk_kernels.py: _fwd_kernel_splitK)
 # --------------------------------------------------------------------------
 
@@ -219,12 +252,15 @@ def gather_paged_rows(cache, block_table, b, t_lo, t_hi, page_size):
     return np.stack(out)
 
 
-def _kv_rows(cache, block_table, b, lo, hi, page_size, kv_format, d, n_groups):
+def _kv_rows(cache, block_table, b, lo, hi, page_size, kv_format, d, n_groups, scale_shift=None):
     rows = gather_paged_rows(cache, block_table, b, lo, hi, page_size)
     if kv_format == "int4":
         return dequant_int4_rows(rows, d, n_groups)
+    if kv_format == "fp8":
+        words = gather_paged_rows(scale_shift, block_table, b, lo, hi, page_size)   # [n, Hkv]
+        return dequant_fp8_rows(rows, words)
     if kv_format != "dense":
-        raise ValueError("kv_format must be 'dense' or 'int4'")
+        raise ValueError("kv_format must be 'dense', 'int4' or 'fp8'")
     return rows.astype(np.float64)
 
 
@@ -235,11 +271,13 @@ def num_splits(max_kv_len, split_tokens):
 
 def decode_split_partials(q, k_cache, v_cache, block_table, seq_lens, page_size,
                           split_tokens, scale=None, kv_format="dense", n_groups=1,
-                          max_kv_len=None, batches=None):
+                          max_kv_len=None, batches=None, k_scale_shift=None, v_scale_shift=None):
     """Per-split partial results of single-query decode.
 
-    ``q [B, Hq, D]``; caches ``[num_pages, page_size, Hkv, D]`` (dense values)
-    or ``[num_pages, page_size, Hkv, n_groups + D/8]`` (int4 words).
+    ``q [B, Hq, D]``; caches ``[num_pages, page_size, Hkv, D]`` (dense values
+    or fp8 e4m3 bytes, the latter with ``k/v_scale_shift [num_pages,
+    page_size, Hkv]`` words) or ``[num_pages, page_size, Hkv, n_groups + D/8]``
+    (int4 words).
     Split ``s`` of sequence ``b`` covers tokens
     ``[s*split_tokens, min((s+1)*split_tokens, len_b))``; with one query per
     sequence every cached token is visible.  An empty split gives ``O_s = 0``
@@ -267,8 +305,8 @@ def decode_split_partials(q, k_cache, v_cache, block_table, seq_lens, page_size,
             hi = min(lo + split_tokens, lens[b])
             if hi <= lo:
                 continue
-            k_rows = _kv_rows(k_cache, block_table, b, lo, hi, page_size, kv_format, d, n_groups)
-            v_rows = _kv_rows(v_cache, block_table, b, lo, hi, page_size, kv_format, d, n_groups)
+            k_rows = _kv_rows(k_cache, block_table, b, lo, hi, page_size, kv_format, d, n_groups, k_scale_shift)
+            v_rows = _kv_rows(v_cache, block_table, b, lo, hi, page_size, kv_format, d, n_groups, v_scale_shift)
             k_rep = np.repeat(k_rows, group, axis=1)          # [n, Hq, D]
             v_rep = np.repeat(v_rows, group, axis=1)
             every = np.ones((1, hi - lo), dtype=bool)
@@ -330,11 +368,12 @@ def lse_merge(o_part, lse_part):
 
 
 def decode(q, k_cache, v_cache, block_table, seq_lens, page_size, split_tokens, scale=None,
-           kv_format="dense", n_groups=1, max_kv_len=None, batches=None):
+           kv_format="dense", n_groups=1, max_kv_len=None, batches=None, k_scale_shift=None,
+           v_scale_shift=None):
     """Split-K decode: the per-split partials merged by :func:`lse_merge`."""
     o_part, lse_part = decode_split_partials(q, k_cache, v_cache, block_table, seq_lens,
                                              page_size, split_tokens, scale, kv_format,
-                                             n_groups, max_kv_len, batches)
+                                             n_groups, max_kv_len, batches, k_scale_shift, v_scale_shift)
     return lse_merge(o_part, lse_part)
 
 
@@ -376,7 +415,8 @@ def lse_merge_bwd(o_part, lse_part, d_o, d_lse=None):
 # --------------------------------------------------------------------------
 
 def decode_mq_split_partials(q, k_cache, v_cache, block_table, seq_lens, page_size, split_tokens, scale=None,
-                             kv_format="dense", n_groups=1, max_kv_len=None, batches=None):
+                             kv_format="dense", n_groups=1, max_kv_len=None, batches=None, k_scale_shift=None,
+                             v_scale_shift=None):
     """Split partials of decode with ``q_len`` queries per sequence.
 
     ``q [B, Hq, q_len, D]``.  Query ``i`` of sequence ``b`` sees cached token
@@ -404,8 +444,8 @@ def decode_mq_split_partials(q, k_cache, v_cache, block_table, seq_lens, page_si
             hi = min(lo + split_tokens, lens[b])
             if hi <= lo:
                 continue
-            k_rows = _kv_rows(k_cache, block_table, b, lo, hi, page_size, kv_format, d, n_groups)
-            v_rows = _kv_rows(v_cache, block_table, b, lo, hi, page_size, kv_format, d, n_groups)
+            k_rows = _kv_rows(k_cache, block_table, b, lo, hi, page_size, kv_format, d, n_groups, k_scale_shift)
+            v_rows = _kv_rows(v_cache, block_table, b, lo, hi, page_size, kv_format, d, n_groups, v_scale_shift)
             k_rep = np.repeat(k_rows, group, axis=1)
             v_rep = np.repeat(v_rows, group, axis=1)
             t = np.arange(lo, hi)
@@ -418,8 +458,10 @@ def decode_mq_split_partials(q, k_cache, v_cache, block_table, seq_lens, page_si
 
 
 def decode_mq(q, k_cache, v_cache, block_table, seq_lens, page_size, split_tokens, scale=None,
-              kv_format="dense", n_groups=1, max_kv_len=None, batches=None):
+              kv_format="dense", n_groups=1, max_kv_len=None, batches=None, k_scale_shift=None,
+              v_scale_shift=None):
     """Causal multi-query decode: the per-split partials merged by :func:`lse_merge`."""
     o_part, lse_part = decode_mq_split_partials(q, k_cache, v_cache, block_table, seq_lens, page_size,
-                                                split_tokens, scale, kv_format, n_groups, max_kv_len, batches)
+                                                split_tokens, scale, kv_format, n_groups, max_kv_len, batches,
+                                                k_scale_shift, v_scale_shift)
     return lse_merge(o_part, lse_part)

@@ -38,7 +38,7 @@ class DecodeShape:
     len_hi: int
     page_size: int
     split_tokens: int
-    kv_format: str = "dense"        # "dense" (bf16) or "int4"
+    kv_format: str = "dense"        # "dense" (bf16), "int4" or "fp8"
     n_groups: int = 1
     extra: dict = field(default_factory=dict)
 
@@ -52,6 +52,9 @@ BATCHED_SQUARE_PREFILL = PrefillShape("batched square causal GQA prefill, K x2",
 PAGED_DECODE_BF16 = DecodeShape("paged split-K decode bf16", 64, 32, 8, 128, 512, 32768, 256, 2048)
 PAGED_DECODE_INT4 = DecodeShape("int4 paged split-K decode", 16, 32, 8, 128, 16384, 16384, 256, 2048,
                                 kv_format="int4", n_groups=4)
+# fp8 row-wise cache on the int4 workload's shape (an extension of the method, not one of its five workloads)
+PAGED_DECODE_FP8 = DecodeShape("fp8 paged split-K decode", 16, 32, 8, 128, 16384, 16384, 256, 2048,
+                               kv_format="fp8")
 
 WORKLOADS = {
     "tiny_prefill_fp32": TINY_PREFILL_FP32,
@@ -120,7 +123,11 @@ def decode_inputs(shape, seed=0, lens=None, pages_per_draw=64):
          dense: N(0, 1) rounded to bf16, layout ``[pages, page_size, Hkv, D]``;
          int4: codes ~ U{0..15}, then scales ~ U[0.01, 0.1] and offsets
          ~ N(0, 0.1), both rounded to fp16, packed by :func:`pack_int4_rows`
-         into ``[pages, page_size, Hkv, n_groups + D/8]`` int32.
+         into ``[pages, page_size, Hkv, n_groups + D/8]`` int32;
+         fp8: values ~ N(0, 16) rounded to float8 e4m3 (bytes
+         ``[pages, page_size, Hkv, D]``), then scales ~ U[0.1, 0.5] and shifts
+         ~ N(0, 0.1) rounded to fp16 and packed one word per row (scale low,
+         shift high) into ``k/v_scale_shift [pages, page_size, Hkv]``.
     Block-table entries past a sequence's last page are -1.
     """
     g = generator(seed)
@@ -148,6 +155,14 @@ def decode_inputs(shape, seed=0, lens=None, pages_per_draw=64):
             n = min(pages_per_draw, n_pages - start)
             if shape.kv_format == "dense":
                 chunks.append(torch.randn(n, ps, shape.Hkv, shape.D, generator=g).to(torch.bfloat16))
+            elif shape.kv_format == "fp8":
+                x = torch.randn(n, ps, shape.Hkv, shape.D, generator=g) * 4.0
+                codes = x.to(torch.float8_e4m3fn).view(torch.uint8)
+                scales = torch.rand(n, ps, shape.Hkv, generator=g) * 0.4 + 0.1
+                shifts = torch.randn(n, ps, shape.Hkv, generator=g) * 0.1
+                words = _fp16_bits(scales).to(torch.int64) | (_fp16_bits(shifts).to(torch.int64) << 16)
+                words = torch.where(words >= 2 ** 31, words - 2 ** 32, words).to(torch.int32)
+                chunks.append((codes, words))
             elif shape.kv_format == "int4":
                 codes = torch.randint(0, 16, (n, ps, shape.Hkv, shape.D), generator=g, dtype=torch.uint8)
                 scales = torch.rand(n, ps, shape.Hkv, shape.n_groups, generator=g) * 0.09 + 0.01
@@ -155,11 +170,16 @@ def decode_inputs(shape, seed=0, lens=None, pages_per_draw=64):
                 chunks.append(pack_int4_rows(codes, _fp16_bits(scales), _fp16_bits(offsets), shape.n_groups))
             else:
                 raise ValueError(shape.kv_format)
-        return torch.cat(chunks, dim=0)
+        if shape.kv_format == "fp8":
+            return torch.cat([c for c, _ in chunks], dim=0), torch.cat([w for _, w in chunks], dim=0)
+        return torch.cat(chunks, dim=0), None
 
-    k_cache = pool()
-    v_cache = pool()
-    return {
+    k_cache, k_scale_shift = pool()
+    v_cache, v_scale_shift = pool()
+    extra = {}
+    if shape.kv_format == "fp8":
+        extra = {"k_scale_shift": k_scale_shift, "v_scale_shift": v_scale_shift}
+    return {**extra,
         "q": q,
         "k_cache": k_cache,
         "v_cache": v_cache,

@@ -544,3 +544,49 @@ def test_multi_query_decode_with_one_query_is_single_query_decode():
     o2, l2 = oracle.decode_mq(qd[:, :, None, :], kc, vc, table, lens, 4, 5)
     np.testing.assert_array_equal(o2[:, :, 0], o1)
     np.testing.assert_array_equal(l2[:, :, 0], l1)
+
+
+# ------------------------------------------------------------------- fp8
+
+def test_golden_fp8_e4m3(golden):
+    g = golden("fp8_e4m3.txt")
+    vals = [oracle.fp8_e4m3_value(int(x, 16)) for x in g["bytes"]]
+    np.testing.assert_array_equal(vals, _f(g["values"]))
+    row = oracle.dequant_fp8_rows(np.array([[int(x, 16) for x in g["row_bytes"]]]),
+                                  np.array([int(g["row_word"][0], 16)]))
+    np.testing.assert_array_equal(row[0], _f(g["row_values"]))
+
+
+def test_fp8_decoder_matches_torch_float8_e4m3fn():
+    """Every byte against torch's float8_e4m3fn (a library decoder)."""
+    b = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = b.view(torch.float8_e4m3fn).double().numpy()
+    ours = np.array([oracle.fp8_e4m3_value(x) for x in range(256)])
+    nan = np.isnan(ref)
+    assert np.array_equal(nan, np.isnan(ours)) and nan.sum() == 2    # 0x7F and 0xFF
+    np.testing.assert_array_equal(ours[~nan], ref[~nan])
+
+
+def test_fp8_decode_equals_dense_decode_on_dequantised_rows():
+    lens = [9, 14]
+    ps, d = 4, 8
+    rng = np.random.default_rng(41)
+    n_pages = sum(-(-n // ps) for n in lens)
+    table = np.array([[0, 1, 2, -1], [3, 4, 5, 6]])
+    codes_k = rng.integers(0, 256, size=(n_pages, ps, 2, d))
+    codes_v = rng.integers(0, 256, size=(n_pages, ps, 2, d))
+    codes_k[(codes_k & 0x7F) == 0x7F] = 0       # no NaN bytes
+    codes_v[(codes_v & 0x7F) == 0x7F] = 0
+    def words():
+        sc = np.float16(rng.uniform(0.1, 0.5, size=(n_pages, ps, 2))).view(np.uint16).astype(np.int64)
+        sh = np.float16(rng.normal(0, 0.1, size=(n_pages, ps, 2))).view(np.uint16).astype(np.int64)
+        return sc | (sh << 16)
+    wk, wv = words(), words()
+    q = rng.standard_normal((2, 4, d))
+    o, lse = oracle.decode(q, codes_k, codes_v, table, lens, ps, 5, kv_format="fp8", k_scale_shift=wk,
+                           v_scale_shift=wv)
+    kd = oracle.dequant_fp8_rows(codes_k, wk)
+    vd = oracle.dequant_fp8_rows(codes_v, wv)
+    o2, lse2 = oracle.decode(q, kd, vd, table, lens, ps, 5)
+    np.testing.assert_allclose(o, o2, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(lse, lse2, rtol=1e-13, atol=1e-13)
