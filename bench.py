@@ -54,7 +54,12 @@ def decode_bytes(shape, lens):
     """Algorithmic bytes of one decode: every cached K and V row once, Q, the
     block-table entries and lengths read; O and LSE written.  The split
     partials (kernel-to-kernel scratch) are not counted."""
-    row = shape.D * 2 if shape.kv_format == "dense" else (shape.n_groups + shape.D // 8) * 4
+    if shape.kv_format == "dense":
+        row = shape.D * 2
+    elif shape.kv_format == "fp8":
+        row = shape.D + 4        # e4m3 bytes + the row's scale/shift word
+    else:
+        row = (shape.n_groups + shape.D // 8) * 4
     kv = sum(lens) * shape.Hkv * row * 2
     pages = sum(-(-n // shape.page_size) for n in lens)
     q = shape.B * shape.Hq * shape.D * 2
@@ -239,7 +244,15 @@ def run_ours(args, rank, world, dist):
     status = torch.zeros(1, dtype=torch.int32, device=dev)
 
     kernels = ["prefill", "prefill_batched", "decode_bf16", "merge_bf16", "decode_int4", "merge_int4", "merge_bwd",
-               "decode_mq"]
+               "decode_mq", "decode_fp8"]
+    # fp8 e4m3 row-wise cache on the int4 workload's shape
+    d8 = synth.PAGED_DECODE_FP8
+    inp8 = synth.decode_inputs(d8, seed=seed)
+    t8 = {kk: vv.to(dev) for kk, vv in inp8.items() if torch.is_tensor(vv)}
+    ws8 = torch.empty(attn.attn_decode_workspace_bytes(d8.B, d8.Hq, d8.len_hi, d8.split_tokens, d8.D),
+                      dtype=torch.uint8, device=dev)
+    lens8 = inp8["lens"]
+    del inp8
     # causal multi-query decode (4 draft queries per sequence) over the bf16 paged cache
     mq_n = 4
     gmq = torch.Generator().manual_seed(seed + 11)
@@ -289,6 +302,13 @@ def run_ours(args, rank, world, dist):
                                          d16.split_tokens, d16.len_hi, workspace=mq_ws, dev_status=status,
                                          stream=stream, write_output=False)
         ev["decode_mq"][1].record(stream)
+        flush.fill_(1.0)
+        ev["decode_fp8"][0].record(stream)
+        attn.attn_decode_paged_splitk_fp8(t8["q"], t8["k_cache"], t8["v_cache"], t8["k_scale_shift"],
+                                          t8["v_scale_shift"], t8["block_table"], t8["seq_lens"], d8.split_tokens,
+                                          d8.len_hi, workspace=ws8, dev_status=status, stream=stream,
+                                          write_output=False)
+        ev["decode_fp8"][1].record(stream)
 
     def new_events():
         return {kn: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for kn in kernels}
@@ -398,6 +418,9 @@ def run_ours(args, rank, world, dist):
     mqb = dec["decode_bf16"]["bytes"]["kernel"] + mq_q.numel() * 2 - d16.B * d16.Hq * d16.D * 2
     rep["decode_mq"] = dict(bound="hbm", achieved=mqb / (ms["decode_mq"] * 1e-3) / 1e9, peak=peaks["hbm_gbs"],
                             unit="GB/s", work=mqb, src="decode.cu", kernel="decode_bf16_kernel (q_len 4)")
+    fp8b = decode_bytes(d8, lens8)["kernel"]
+    rep["decode_fp8"] = dict(bound="hbm", achieved=fp8b / (ms["decode_fp8"] * 1e-3) / 1e9, peak=peaks["hbm_gbs"],
+                             unit="GB/s", work=fp8b, src="decode_fp8.cu", kernel="decode_fp8_kernel")
     kernels_out = []
     for kn in kernels:
         r = rep[kn]

@@ -12,6 +12,7 @@ Entry points (names as in the C ABI):
   attn_decode_workspace_bytes
   attn_decode_paged_splitk  single-query split-K decode over a paged cache
   attn_decode_paged_splitk_mq      causal multi-query decode (q_len <= 16 per sequence)
+  attn_decode_paged_splitk_fp8     the same over an fp8 e4m3 row-wise cache
   attn_decode_paged_splitk_static  the same decode with no workspace argument
   attn_lse_merge            LSE-weighted merge of split partials
   attn_lse_merge_bwd        its gradient
@@ -29,12 +30,13 @@ LIB_PATH = os.path.join(HERE, "libattn.so")
 
 # status and dtype codes of include/attn.h
 ATTN_OK = 0
-ATTN_F32, ATTN_BF16, ATTN_F16, ATTN_INT4_PACKED = 0, 1, 2, 3
+ATTN_F32, ATTN_BF16, ATTN_F16, ATTN_INT4_PACKED, ATTN_FP8_E4M3 = 0, 1, 2, 3, 4
 ATTN_DEV_PAGE_OUT_OF_RANGE = 0x1
 ATTN_DEV_SEQ_TOO_LONG = 0x2
 ATTN_DEV_WAIT_TIMEOUT = 0x4
 
 EXPORTED = ("attn_prefill_fwd", "attn_decode_workspace_bytes", "attn_decode_paged_splitk", "attn_decode_paged_splitk_mq",
+            "attn_decode_paged_splitk_fp8",
             "attn_decode_paged_splitk_static", "attn_lse_merge", "attn_lse_merge_bwd", "attn_status_string",
             "attn_abi_version")
 ATTN_DECODE_STATIC_SCRATCH_BYTES = 32 << 20
@@ -68,6 +70,9 @@ def lib():
     L.attn_decode_paged_splitk_mq.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, i32, i32, i32,
                                               i32, i32, f32, vp, sz, vp, vp, vp, vp]
     L.attn_decode_paged_splitk_mq.restype = i32
+    L.attn_decode_paged_splitk_fp8.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, i32,
+                                               i32, i32, f32, vp, sz, vp, vp, vp, vp]
+    L.attn_decode_paged_splitk_fp8.restype = i32
     L.attn_decode_paged_splitk_static.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, i32,
                                                   i32, i32, i32, f32, vp, vp, vp, vp]
     L.attn_decode_paged_splitk_static.restype = i32
@@ -200,6 +205,39 @@ def attn_decode_paged_splitk_mq(q, k_cache, v_cache, block_table, seq_lens, spli
         _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(o), _ptr(lse), _ptr(dev_status),
         _stream_ptr(stream))
     _check("attn_decode_paged_splitk_mq", st)
+    return o, lse, workspace
+
+
+def attn_decode_paged_splitk_fp8(q, k_cache, v_cache, k_scale_shift, v_scale_shift, block_table, seq_lens,
+                                 split_tokens, max_kv_len, scale=None, workspace=None, o=None, lse=None,
+                                 dev_status=None, stream=None, write_output=True):
+    """Decode over an fp8 e4m3 cache: ``k/v_cache`` uint8 ``[num_pages,
+    page_size, Hkv, D]``, ``k/v_scale_shift`` int32 ``[num_pages, page_size,
+    Hkv]``; ``q [B, Hq, D]`` (single query) or ``[B, Hq, q_len, D]``."""
+    _need_cuda(q, k_cache, v_cache, k_scale_shift, v_scale_shift, block_table, seq_lens, workspace, o, lse,
+               dev_status)
+    single = q.dim() == 3
+    q4 = q[:, :, None, :] if single else q
+    bsz, hq, nq, d = q4.shape
+    num_pages, page_size, hkv = k_cache.shape[0], k_cache.shape[1], k_cache.shape[2]
+    need = attn_decode_workspace_bytes(bsz, hq * nq, max_kv_len, split_tokens, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    if write_output:
+        if o is None:
+            o = torch.empty(q.shape, dtype=q.dtype, device=q.device)
+        if lse is None:
+            lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+    else:
+        o = lse = None
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    st = lib().attn_decode_paged_splitk_fp8(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale_shift), _ptr(v_scale_shift), _ptr(block_table),
+        block_table.shape[1], _ptr(seq_lens), bsz, hq, hkv, nq, d, num_pages, page_size, split_tokens, max_kv_len,
+        float(scale), _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(o), _ptr(lse),
+        _ptr(dev_status), _stream_ptr(stream))
+    _check("attn_decode_paged_splitk_fp8", st)
     return o, lse, workspace
 
 

@@ -86,7 +86,8 @@ attn_status_t decode_impl(const void* q, const void* k_cache, const void* v_cach
                           int max_pages_per_seq, const int32_t* seq_lens, attn_dtype_t kv_dtype, int n_groups, int B,
                           int Hq, int Hkv, int q_len, int D, int num_pages, int page_size, int split_tokens,
                           int max_kv_len, float scale, void* workspace, size_t workspace_bytes, void* o, float* lse,
-                          int32_t* dev_status, void* stream) {
+                          int32_t* dev_status, void* stream, const void* k_scale_shift = nullptr,
+                          const void* v_scale_shift = nullptr) {
     if (q == nullptr || k_cache == nullptr || v_cache == nullptr || block_table == nullptr || seq_lens == nullptr)
         return ATTN_ERR_INVALID_ARG;
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || num_pages <= 0 || page_size <= 0 || split_tokens <= 0 ||
@@ -108,6 +109,11 @@ attn_status_t decode_impl(const void* q, const void* k_cache, const void* v_cach
         fmt = 1;
         if (n_groups != 1 && n_groups != 2 && n_groups != 4 && n_groups != 8) return ATTN_ERR_UNSUPPORTED;
         if ((static_cast<long long>(Hkv) * (n_groups + D / 8)) % 4 != 0) return ATTN_ERR_UNSUPPORTED;
+    } else if (kv_dtype == ATTN_FP8_E4M3) {
+        fmt = 2;
+        if (k_scale_shift == nullptr || v_scale_shift == nullptr) return ATTN_ERR_INVALID_ARG;
+        if (!aligned16(k_scale_shift) || !aligned16(v_scale_shift)) return ATTN_ERR_INVALID_ARG;
+        if (Hkv % 4 != 0) return ATTN_ERR_UNSUPPORTED;
     } else {
         return ATTN_ERR_UNSUPPORTED;
     }
@@ -122,7 +128,7 @@ attn_status_t decode_impl(const void* q, const void* k_cache, const void* v_cach
                  B,         Hq,        Hkv,          D,           num_pages,         page_size, split_tokens,
                  max_kv_len, S,        scale,        q_len,       o_part,            lse_part,  dev_status};
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = launch_decode(a, s);
+    cudaError_t e = (fmt == 2) ? launch_decode_fp8(a, k_scale_shift, v_scale_shift, s) : launch_decode(a, s);
     if (e != cudaSuccess) return ATTN_ERR_CUDA;
     if (o != nullptr) e = launch_merge(o_part, lse_part, static_cast<int>(rows), S, D, o, lse, ATTN_BF16, s);
     return from_cuda(e);
@@ -192,6 +198,18 @@ attn_status_t attn_decode_paged_splitk_mq(const void* q, const void* k_cache, co
     return decode_impl(q, k_cache, v_cache, block_table, max_pages_per_seq, seq_lens, kv_dtype, n_groups, B, Hq,
                        Hkv, q_len, D, num_pages, page_size, split_tokens, max_kv_len, scale, workspace,
                        workspace_bytes, o, lse, dev_status, stream);
+}
+
+attn_status_t attn_decode_paged_splitk_fp8(const void* q, const void* k_cache, const void* v_cache,
+                                           const int32_t* k_scale_shift, const int32_t* v_scale_shift,
+                                           const int32_t* block_table, int max_pages_per_seq,
+                                           const int32_t* seq_lens, int B, int Hq, int Hkv, int q_len, int D,
+                                           int num_pages, int page_size, int split_tokens, int max_kv_len,
+                                           float scale, void* workspace, size_t workspace_bytes, void* o,
+                                           float* lse, int32_t* dev_status, void* stream) {
+    return decode_impl(q, k_cache, v_cache, block_table, max_pages_per_seq, seq_lens, ATTN_FP8_E4M3, 1, B, Hq, Hkv,
+                       q_len, D, num_pages, page_size, split_tokens, max_kv_len, scale, workspace, workspace_bytes,
+                       o, lse, dev_status, stream, k_scale_shift, v_scale_shift);
 }
 
 attn_status_t attn_lse_merge(const float* o_part, const float* lse_part, int N, int S, int D, void* o, float* lse,

@@ -55,6 +55,8 @@ struct DecodeArgs {
     int32_t* dev_status;
 };
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+cudaError_t launch_decode_fp8(const DecodeArgs& a, const void* k_scale_shift, const void* v_scale_shift,
+                              cudaStream_t stream);
 int rows_per_cta(const DecodeArgs& a);
 
 cudaError_t launch_merge(const float* o_part, const float* lse_part, int N, int S, int D, void* o,

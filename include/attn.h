@@ -48,7 +48,8 @@ typedef enum {
     ATTN_F32 = 0,
     ATTN_BF16 = 1,
     ATTN_F16 = 2,
-    ATTN_INT4_PACKED = 3         /* int32 words, see attn_decode_paged_splitk */
+    ATTN_INT4_PACKED = 3,        /* int32 words, see attn_decode_paged_splitk */
+    ATTN_FP8_E4M3 = 4            /* e4m3 bytes + a scale/shift word per row, see attn_decode_paged_splitk_fp8 */
 } attn_dtype_t;
 
 /* Bits OR-ed into *dev_status by a kernel. */
@@ -159,6 +160,32 @@ attn_status_t attn_decode_paged_splitk_mq(const void* q, const void* k_cache, co
                                           int page_size, int split_tokens, int max_kv_len, float scale,
                                           void* workspace, size_t workspace_bytes,
                                           void* o, float* lse, int32_t* dev_status, void* stream);
+
+/*
+ * attn_decode_paged_splitk_fp8 - split-K decode over an fp8 (e4m3) row-wise
+ * quantised paged KV cache, single- or multi-query.
+ *
+ * Follows "splitk_kernels.py", _fwd_kernel_splitK with FP8_QUANTIZED (row-wise
+ * only), the K_fp8_scale_shift / V_fp8_scale_shift tensors,
+ * cast_uint32_to_half2 and dequantize: value = e4m3(byte) * scale + shift.
+ *
+ *   k_cache, v_cache          uint8 [num_pages, page_size, Hkv, D], e4m3 bytes
+ *   k_scale_shift, v_scale_shift
+ *                             int32 [num_pages, page_size, Hkv]: fp16 scale in
+ *                             the low 16 bits, fp16 shift in the high 16 bits
+ *   q                         [B, Hq, q_len, D] bfloat16, 1 <= q_len <= 16
+ *                             (converted to fp16 on chip: |q| < 65504)
+ *   Hkv                       a multiple of 4.
+ * Every other argument, the workspace and the causal rule for q_len > 1 are
+ * those of attn_decode_paged_splitk_mq; o [B, Hq, q_len, D] bfloat16.
+ */
+attn_status_t attn_decode_paged_splitk_fp8(const void* q, const void* k_cache, const void* v_cache,
+                                           const int32_t* k_scale_shift, const int32_t* v_scale_shift,
+                                           const int32_t* block_table, int max_pages_per_seq,
+                                           const int32_t* seq_lens, int B, int Hq, int Hkv, int q_len, int D,
+                                           int num_pages, int page_size, int split_tokens, int max_kv_len,
+                                           float scale, void* workspace, size_t workspace_bytes,
+                                           void* o, float* lse, int32_t* dev_status, void* stream);
 
 /*
  * attn_decode_paged_splitk_static - attn_decode_paged_splitk without a workspace.
