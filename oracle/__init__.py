@@ -36,4 +36,5 @@ from .attention import (  # noqa: F401
     decode,
     decode_mq_split_partials,
     decode_mq,
+    prefill_paged_varlen,
 )

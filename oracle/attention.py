@@ -465,3 +465,58 @@ def decode_mq(q, k_cache, v_cache, block_table, seq_lens, page_size, split_token
                                                 split_tokens, scale, kv_format, n_groups, max_kv_len, batches,
                                                 k_scale_shift, v_scale_shift)
     return lse_merge(o_part, lse_part)
+
+
+# --------------------------------------------------------------------------
+# Ragged (varlen) prefill over a paged KV cache ("gpt-o3 / triton6fd1ef",
+# run: CSR qo_indptr / kv_indptr / kv_indices, one query head group per KV
+# head, bottom-right causal per sequence)
+# --------------------------------------------------------------------------
+
+def prefill_paged_varlen(q, k_cache, v_cache, qo_indptr, kv_indptr, kv_indices, page_size=1,
+                         kv_last_page_len=None, scale=None):
+    """Causal GQA prefill of a ragged batch against a paged KV cache.
+
+    ``q [total_q, Hq, D]``; sequence ``b`` owns query rows
+    ``[qo_indptr[b], qo_indptr[b+1])`` and the pages
+    ``kv_indices[kv_indptr[b] : kv_indptr[b+1]]`` of the pool
+    ``k_cache, v_cache [num_pages, page_size, Hkv, D]``.  Its KV length is
+    ``(n_pages - 1) * page_size + kv_last_page_len[b]`` (every page full when
+    ``kv_last_page_len`` is None).  Each sequence is the dense causal GQA
+    prefill of :func:`attend` with ``delta = kv_len - q_len``.  Returns
+    ``o [total_q, Hq, D]`` and ``lse [total_q, Hq]``.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    total_q, hq, d = q.shape
+    hkv = k_cache.shape[2]
+    if hq % hkv != 0:
+        raise ValueError("Hq must be a multiple of Hkv")
+    group = hq // hkv
+    scale = _default_scale(d) if scale is None else float(scale)
+    qo = [int(x) for x in np.asarray(qo_indptr)]
+    kvp = [int(x) for x in np.asarray(kv_indptr)]
+    idx = [int(x) for x in np.asarray(kv_indices)]
+    o = np.zeros((total_q, hq, d))
+    lse = np.full((total_q, hq), NEG_INF)
+    for b in range(len(qo) - 1):
+        q_len = qo[b + 1] - qo[b]
+        pages = idx[kvp[b]:kvp[b + 1]]
+        last = page_size if kv_last_page_len is None else int(np.asarray(kv_last_page_len)[b])
+        kv_len = (len(pages) - 1) * page_size + last if pages else 0
+        if q_len == 0:
+            continue
+        rows_k, rows_v = [], []
+        for t in range(kv_len):
+            page = pages[t // page_size]
+            rows_k.append(np.asarray(k_cache[page, t % page_size], dtype=np.float64))
+            rows_v.append(np.asarray(v_cache[page, t % page_size], dtype=np.float64))
+        kk = np.stack(rows_k) if rows_k else np.zeros((0, hkv, d))
+        vv = np.stack(rows_v) if rows_v else np.zeros((0, hkv, d))
+        k_rep = np.repeat(kk, group, axis=1)
+        v_rep = np.repeat(vv, group, axis=1)
+        mask = visible_mask(q_len, kv_len)
+        for h in range(hq):
+            ob, lb = attend(q[qo[b]:qo[b + 1], h], k_rep[:, h], v_rep[:, h], mask, scale)
+            o[qo[b]:qo[b + 1], h] = ob
+            lse[qo[b]:qo[b + 1], h] = lb
+    return o, lse

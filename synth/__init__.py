@@ -205,3 +205,68 @@ def merge_inputs(n_rows, n_splits, d, seed=0, p_empty=0.25):
     lse_part = torch.where(empty, torch.full_like(lse_part, float("-inf")), lse_part)
     o_part = torch.where(empty[..., None], torch.zeros_like(o_part), o_part)
     return o_part, lse_part
+
+
+@dataclass(frozen=True)
+class VarlenShape:
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    D: int
+    q_lo: int
+    q_hi: int
+    prefix_lo: int     # cached tokens before the new queries
+    prefix_hi: int
+    page_size: int = 1
+
+
+# A ragged prefill batch over a token-granular paged cache, the layout of the
+# FlashInfer-style GQA prefill (32 query heads, 4 KV heads, head dim 128,
+# page size 1).  The page gives no batch sizes; these are chosen for the
+# benchmark: 8 sequences, 256-2048 new tokens each on top of 0-2048 cached.
+VARLEN_PAGED_PREFILL = VarlenShape("ragged paged GQA prefill, page size 1", 8, 32, 4, 128, 256, 2048, 0, 2048)
+
+
+def varlen_inputs(shape, seed=0, q_lens=None, kv_lens=None):
+    """Inputs of one ragged prefill over a paged cache.
+
+    Draw order (one CPU generator): new-token counts ``q_len_b`` ~
+    U{q_lo..q_hi} and cached-prefix lengths ~ U{prefix_lo..prefix_hi} (both
+    skipped when given; ``kv_len_b = q_len_b + prefix_b``); a permutation of the
+    page pool (exactly ``sum_b ceil(kv_len_b / page_size)`` pages, sequence b
+    taking the next ones in order); ``q [total_q, Hq, D]`` ~ N(0, 1) as bf16;
+    the K pool then the V pool ``[pages, page_size, Hkv, D]`` ~ N(0, 1) as bf16.
+    Returns CSR ``qo_indptr``, ``kv_indptr`` (pages) and ``kv_indices`` plus
+    ``kv_last_page_len``, all int32.
+    """
+    g = generator(seed)
+    if q_lens is None:
+        q_lens = torch.randint(shape.q_lo, shape.q_hi + 1, (shape.B,), generator=g).tolist()
+    if kv_lens is None:
+        pre = torch.randint(shape.prefix_lo, shape.prefix_hi + 1, (len(q_lens),), generator=g).tolist()
+        kv_lens = [a + b for a, b in zip(q_lens, pre)]
+    q_lens = [int(x) for x in q_lens]
+    kv_lens = [int(x) for x in kv_lens]
+    ps = shape.page_size
+    n_pages_b = [-(-n // ps) for n in kv_lens]
+    n_pages = max(1, sum(n_pages_b))
+    perm = torch.randperm(n_pages, generator=g).to(torch.int32)
+    qo = [0]
+    for n in q_lens:
+        qo.append(qo[-1] + n)
+    kvp = [0]
+    for n in n_pages_b:
+        kvp.append(kvp[-1] + n)
+    q = torch.randn(qo[-1], shape.Hq, shape.D, generator=g).to(torch.bfloat16)
+    k_cache = torch.randn(n_pages, ps, shape.Hkv, shape.D, generator=g).to(torch.bfloat16)
+    v_cache = torch.randn(n_pages, ps, shape.Hkv, shape.D, generator=g).to(torch.bfloat16)
+    last = [n - (p - 1) * ps if p > 0 else 0 for n, p in zip(kv_lens, n_pages_b)]
+    return {
+        "q": q, "k_cache": k_cache, "v_cache": v_cache,
+        "qo_indptr": torch.tensor(qo, dtype=torch.int32),
+        "kv_indptr": torch.tensor(kvp, dtype=torch.int32),
+        "kv_indices": perm[:kvp[-1]].clone() if kvp[-1] > 0 else torch.zeros(1, dtype=torch.int32),
+        "kv_last_page_len": torch.tensor(last, dtype=torch.int32),
+        "q_lens": q_lens, "kv_lens": kv_lens, "n_pages": n_pages,
+    }

@@ -590,3 +590,28 @@ def test_fp8_decode_equals_dense_decode_on_dequantised_rows():
     o2, lse2 = oracle.decode(q, kd, vd, table, lens, ps, 5)
     np.testing.assert_allclose(o, o2, rtol=1e-13, atol=1e-13)
     np.testing.assert_allclose(lse, lse2, rtol=1e-13, atol=1e-13)
+
+
+# ------------------------------------------------------- varlen paged prefill
+
+@pytest.mark.parametrize("page_size", [1, 3])
+def test_varlen_paged_prefill_equals_dense_prefill_per_sequence(page_size):
+    """Each sequence of the ragged batch is the (pinned) dense causal prefill
+    of its own Q against its gathered K/V (bottom-right, delta = kv - q)."""
+    from synth import VarlenShape, varlen_inputs
+    shape = VarlenShape("t", 3, 4, 2, 8, 1, 1, 0, 0, page_size=page_size)
+    inp = varlen_inputs(shape, seed=3, q_lens=[5, 1, 7], kv_lens=[9, 4, 7])
+    o, lse = oracle.prefill_paged_varlen(inp["q"].double().numpy(), inp["k_cache"].double().numpy(),
+                                         inp["v_cache"].double().numpy(), inp["qo_indptr"].numpy(),
+                                         inp["kv_indptr"].numpy(), inp["kv_indices"].numpy(), page_size,
+                                         inp["kv_last_page_len"].numpy(), scale=0.3)
+    qo, kvp, idx = inp["qo_indptr"].tolist(), inp["kv_indptr"].tolist(), inp["kv_indices"].tolist()
+    for b in range(3):
+        ql, kl = inp["q_lens"][b], inp["kv_lens"][b]
+        pages = idx[kvp[b]:kvp[b + 1]]
+        kk = np.stack([inp["k_cache"][pages[t // page_size], t % page_size].double().numpy() for t in range(kl)])
+        vv = np.stack([inp["v_cache"][pages[t // page_size], t % page_size].double().numpy() for t in range(kl)])
+        qb = inp["q"][qo[b]:qo[b + 1]].double().numpy().transpose(1, 0, 2)[None]     # [1, Hq, q, D]
+        ob, lb = _brute_prefill(qb, kk.transpose(1, 0, 2)[None], vv.transpose(1, 0, 2)[None], 0.3)
+        np.testing.assert_allclose(o[qo[b]:qo[b + 1]], ob[0].transpose(1, 0, 2), rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(lse[qo[b]:qo[b + 1]], lb[0].T, rtol=1e-12, atol=1e-12)
