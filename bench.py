@@ -244,7 +244,14 @@ def run_ours(args, rank, world, dist):
     status = torch.zeros(1, dtype=torch.int32, device=dev)
 
     kernels = ["prefill", "prefill_batched", "decode_bf16", "merge_bf16", "decode_int4", "merge_int4", "merge_bwd",
-               "decode_mq", "decode_fp8"]
+               "decode_mq", "decode_fp8", "prefill_varlen"]
+    # ragged prefill over a page-size-1 cache (8 sequences)
+    vl = synth.VARLEN_PAGED_PREFILL
+    inpv = synth.varlen_inputs(vl, seed=seed)
+    tv = {kk: vv.to(dev) for kk, vv in inpv.items() if torch.is_tensor(vv)}
+    vl_flops = sum(2 * vl.Hq * vl.D * visible_pairs(ql, kl) * 2 for ql, kl in zip(inpv["q_lens"], inpv["kv_lens"]))
+    vo = torch.empty_like(tv["q"])
+    vlse = torch.empty(tv["q"].shape[0], vl.Hq, dtype=torch.float32, device=dev)
     # fp8 e4m3 row-wise cache on the int4 workload's shape
     d8 = synth.PAGED_DECODE_FP8
     inp8 = synth.decode_inputs(d8, seed=seed)
@@ -309,6 +316,12 @@ def run_ours(args, rank, world, dist):
                                           d8.len_hi, workspace=ws8, dev_status=status, stream=stream,
                                           write_output=False)
         ev["decode_fp8"][1].record(stream)
+        flush.fill_(1.0)
+        ev["prefill_varlen"][0].record(stream)
+        attn.attn_prefill_paged_varlen(tv["q"], tv["k_cache"], tv["v_cache"], tv["qo_indptr"], tv["kv_indptr"],
+                                       tv["kv_indices"], tv["kv_last_page_len"], o=vo, lse=vlse, dev_status=status,
+                                       stream=stream)
+        ev["prefill_varlen"][1].record(stream)
 
     def new_events():
         return {kn: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for kn in kernels}
@@ -421,6 +434,9 @@ def run_ours(args, rank, world, dist):
     fp8b = decode_bytes(d8, lens8)["kernel"]
     rep["decode_fp8"] = dict(bound="hbm", achieved=fp8b / (ms["decode_fp8"] * 1e-3) / 1e9, peak=peaks["hbm_gbs"],
                              unit="GB/s", work=fp8b, src="decode_fp8.cu", kernel="decode_fp8_kernel")
+    rep["prefill_varlen"] = dict(bound="tensor", achieved=vl_flops / (ms["prefill_varlen"] * 1e-3) / 1e12,
+                                 peak=peaks["bf16_tflops"], unit="TFLOP/s", work=vl_flops, src="prefill_tc.cu",
+                                 kernel="prefill_tc_kernel (ragged, paged)")
     kernels_out = []
     for kn in kernels:
         r = rep[kn]

@@ -9,6 +9,7 @@ has not been built.
 
 Entry points (names as in the C ABI):
   attn_prefill_fwd          causal GQA prefill -> (O, LSE)
+  attn_prefill_paged_varlen ragged causal GQA prefill over a paged KV cache
   attn_decode_workspace_bytes
   attn_decode_paged_splitk  single-query split-K decode over a paged cache
   attn_decode_paged_splitk_mq      causal multi-query decode (q_len <= 16 per sequence)
@@ -35,7 +36,7 @@ ATTN_DEV_PAGE_OUT_OF_RANGE = 0x1
 ATTN_DEV_SEQ_TOO_LONG = 0x2
 ATTN_DEV_WAIT_TIMEOUT = 0x4
 
-EXPORTED = ("attn_prefill_fwd", "attn_decode_workspace_bytes", "attn_decode_paged_splitk", "attn_decode_paged_splitk_mq",
+EXPORTED = ("attn_prefill_fwd", "attn_prefill_paged_varlen", "attn_decode_workspace_bytes", "attn_decode_paged_splitk", "attn_decode_paged_splitk_mq",
             "attn_decode_paged_splitk_fp8",
             "attn_decode_paged_splitk_static", "attn_lse_merge", "attn_lse_merge_bwd", "attn_status_string",
             "attn_abi_version")
@@ -62,6 +63,9 @@ def lib():
     vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     L.attn_prefill_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32, vp, vp]
     L.attn_prefill_fwd.restype = i32
+    L.attn_prefill_paged_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
+                                            f32, vp, vp]
+    L.attn_prefill_paged_varlen.restype = i32
     L.attn_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
     L.attn_decode_workspace_bytes.restype = sz
     L.attn_decode_paged_splitk.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, i32, i32, i32,
@@ -135,6 +139,30 @@ def attn_prefill_fwd(q, k, v, o=None, lse=None, scale=None, dev_status=None, str
     st = lib().attn_prefill_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _DT.get(q.dtype, -1), bsz, hq,
                                 hkv, q_len, kv_len, d, float(scale), _ptr(dev_status), _stream_ptr(stream))
     _check("attn_prefill_fwd", st)
+    return o, lse
+
+
+def attn_prefill_paged_varlen(q, k_cache, v_cache, qo_indptr, kv_indptr, kv_indices, kv_last_page_len=None,
+                              o=None, lse=None, scale=None, dev_status=None, stream=None):
+    """Ragged causal GQA prefill over a paged cache: ``q [total_q, Hq, D]``,
+    caches ``[num_pages, page_size, Hkv, D]`` (bf16), CSR ``qo_indptr``,
+    ``kv_indptr`` (pages), ``kv_indices`` and optional ``kv_last_page_len``
+    (int32, on the device).  Returns ``(o [total_q, Hq, D], lse [total_q, Hq])``."""
+    _need_cuda(q, k_cache, v_cache, qo_indptr, kv_indptr, kv_indices, kv_last_page_len, o, lse, dev_status)
+    total_q, hq, d = q.shape
+    num_pages, page_size, hkv = k_cache.shape[0], k_cache.shape[1], k_cache.shape[2]
+    bsz = qo_indptr.numel() - 1
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(total_q, hq, dtype=torch.float32, device=q.device)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    st = lib().attn_prefill_paged_varlen(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(qo_indptr), _ptr(kv_indptr),
+                                         _ptr(kv_indices), _ptr(kv_last_page_len), _ptr(o), _ptr(lse), bsz, hq, hkv,
+                                         d, total_q, num_pages, page_size, float(scale), _ptr(dev_status),
+                                         _stream_ptr(stream))
+    _check("attn_prefill_paged_varlen", st)
     return o, lse
 
 

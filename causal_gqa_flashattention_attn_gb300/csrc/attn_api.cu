@@ -212,6 +212,29 @@ attn_status_t attn_decode_paged_splitk_fp8(const void* q, const void* k_cache, c
                        o, lse, dev_status, stream, k_scale_shift, v_scale_shift);
 }
 
+attn_status_t attn_prefill_paged_varlen(const void* q, const void* k_cache, const void* v_cache,
+                                        const int32_t* qo_indptr, const int32_t* kv_indptr,
+                                        const int32_t* kv_indices, const int32_t* kv_last_page_len, void* o,
+                                        float* lse, int B, int Hq, int Hkv, int D, int total_q, int num_pages,
+                                        int page_size, float scale, int32_t* dev_status, void* stream) {
+    if (q == nullptr || k_cache == nullptr || v_cache == nullptr || qo_indptr == nullptr || kv_indptr == nullptr ||
+        kv_indices == nullptr || o == nullptr)
+        return ATTN_ERR_INVALID_ARG;
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || total_q < 0 || num_pages <= 0 || page_size <= 0)
+        return ATTN_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0 || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o)) return ATTN_ERR_INVALID_ARG;
+    if (D != 128) return ATTN_ERR_UNSUPPORTED;
+    const int G = Hq / Hkv;
+    if (G > 128 || 128 % G != 0) return ATTN_ERR_UNSUPPORTED;
+    if (B > varlen_max_seqs()) return ATTN_ERR_UNSUPPORTED;
+    if (static_cast<long long>(num_pages) * page_size >= (1LL << 31) - 1) return ATTN_ERR_UNSUPPORTED;
+    if (total_q == 0) return ATTN_OK;
+    VarlenArgs a{q, k_cache, v_cache, qo_indptr, kv_indptr, kv_indices, kv_last_page_len, o, lse,
+                 B, Hq,      Hkv,     D,         total_q,   num_pages, page_size, scale,      dev_status};
+    return from_cuda(launch_prefill_varlen_tc(a, static_cast<cudaStream_t>(stream)));
+}
+
 attn_status_t attn_lse_merge(const float* o_part, const float* lse_part, int N, int S, int D, void* o, float* lse,
                              attn_dtype_t o_dtype, void* stream) {
     if (o_part == nullptr || lse_part == nullptr || o == nullptr) return ATTN_ERR_INVALID_ARG;

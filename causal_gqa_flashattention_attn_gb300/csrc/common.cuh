@@ -79,4 +79,21 @@ cudaError_t launch_prefill_simt(const PrefillArgs& a, cudaStream_t stream);
 bool prefill_tc_supported(const PrefillArgs& a);
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream);
 
+struct VarlenArgs {
+    const void* q;          // [total_q, Hq, D] bf16
+    const void* k_cache;    // [num_pages, page_size, Hkv, D] bf16
+    const void* v_cache;
+    const int32_t* qo_indptr;
+    const int32_t* kv_indptr;
+    const int32_t* kv_indices;
+    const int32_t* kv_last_page_len;   // may be NULL
+    void* o;                // [total_q, Hq, D] bf16
+    float* lse;             // [total_q, Hq]
+    int B, Hq, Hkv, D, total_q, num_pages, page_size;
+    float scale;
+    int32_t* dev_status;
+};
+int varlen_max_seqs();
+cudaError_t launch_prefill_varlen_tc(const VarlenArgs& a, cudaStream_t stream);
+
 }  // namespace gb300

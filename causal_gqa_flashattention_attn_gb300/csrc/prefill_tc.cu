@@ -65,11 +65,20 @@ struct Params {
     int32_t* status;
     int B, Hq, Hkv, q_len, kv_len, G, P, n_qb, n_items;
     float scale_log2;
+    // ragged batch over a paged cache (varlen mode only)
+    const int32_t* qo_indptr;   // [B+1]
+    const int32_t* kv_indptr;   // [B+1], in pages
+    const int32_t* kv_indices;  // pool page of each listed page
+    const int32_t* kv_last;     // [B] tokens in the last page (NULL: full pages)
+    int page_size, pool_rows;
 };
 
 struct Item {
     int b, kvh, p0, n_kv;
+    int q_start, q_len, delta, kv_len, kv_base;   // per-sequence extent (varlen: ragged)
 };
+
+constexpr int kMaxVarlenSeqs = 2048;   // sequences per ragged batch (prefix table in shared memory)
 
 // Work item `idx` of the snake-ordered, longest-first list.
 __device__ __forceinline__ Item item_of(const Params& p, int idx) {
@@ -80,9 +89,41 @@ __device__ __forceinline__ Item item_of(const Params& p, int idx) {
     it.b = bh / p.Hkv;
     it.kvh = bh % p.Hkv;
     it.p0 = qb * 2 * p.P;
-    const int delta = p.kv_len - p.q_len;
+    it.q_start = 0;
+    it.q_len = p.q_len;
+    it.kv_len = p.kv_len;
+    it.kv_base = 0;
+    it.delta = p.kv_len - p.q_len;
     const int p_last = min(it.p0 + 2 * p.P, p.q_len) - 1;
-    const int kv_end = min(p.kv_len, p_last + delta + 1);
+    const int kv_end = min(p.kv_len, p_last + it.delta + 1);
+    it.n_kv = kv_end > 0 ? (kv_end + kBN - 1) / kBN : 0;
+    return it;
+}
+
+// Ragged batch: item `idx` of sequence-major order, within a sequence the
+// furthest query block (longest KV range) first.  `prefix[b]` counts the
+// items of sequences before b.
+__device__ __forceinline__ Item item_of_varlen(const Params& p, const int* prefix, int idx) {
+    int lo = 0, hi = p.B;   // last b with prefix[b] <= idx
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (prefix[mid] <= idx) lo = mid; else hi = mid;
+    }
+    Item it;
+    it.b = lo;
+    it.q_start = p.qo_indptr[lo];
+    it.q_len = p.qo_indptr[lo + 1] - it.q_start;
+    it.kv_base = p.kv_indptr[lo];
+    const int n_pages = p.kv_indptr[lo + 1] - it.kv_base;
+    const int last = (p.kv_last != nullptr) ? p.kv_last[lo] : p.page_size;
+    it.kv_len = n_pages > 0 ? (n_pages - 1) * p.page_size + last : 0;
+    it.delta = it.kv_len - it.q_len;
+    const int local = idx - prefix[lo];
+    const int n_qb = (it.q_len + 2 * p.P - 1) / (2 * p.P);
+    it.kvh = local % p.Hkv;
+    it.p0 = (n_qb - 1 - local / p.Hkv) * 2 * p.P;
+    const int p_last = min(it.p0 + 2 * p.P, it.q_len) - 1;
+    const int kv_end = min(it.kv_len, p_last + it.delta + 1);
     it.n_kv = kv_end > 0 ? (kv_end + kBN - 1) / kBN : 0;
     return it;
 }
@@ -94,11 +135,16 @@ __device__ __forceinline__ int cta_item(int i) {
     return round * gridDim.x + pos;
 }
 
+// kVarlen: Q is ragged [total_q, Hq, D] (tile rows ordered position-major,
+// r = pos * G + head) and K/V come from a paged pool through the page list,
+// gathered four rows at a time by TMA (tile::gather4).
+template <bool kVarlen>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap k_map,
                       const __grid_constant__ CUtensorMap v_map, const Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align_1024(smem_raw);
+    __shared__ int prefix[kVarlen ? kMaxVarlenSeqs + 1 : 1];
     __shared__ __align__(8) uint64_t q_full, q_empty;
     __shared__ __align__(8) uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
     __shared__ __align__(8) uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
@@ -128,10 +174,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(&tmem_base_sh, kTmemCols);
         tmem_relinquish();
     }
+    int n_items = p.n_items;
+    if constexpr (kVarlen) {
+        // prefix[b] = items of the sequences before b (warp 0, chunked scan)
+        if (warp == 0) {
+            const int per = (p.B + 31) / 32;
+            const int b0 = min(lane * per, p.B), b1 = min(b0 + per, p.B);
+            int sum = 0;
+            for (int b = b0; b < b1; ++b) {
+                const int ql = p.qo_indptr[b + 1] - p.qo_indptr[b];
+                sum += ((ql + 2 * p.P - 1) / (2 * p.P)) * p.Hkv;
+            }
+            int incl = sum;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += v;
+            }
+            int run = incl - sum;
+            for (int b = b0; b < b1; ++b) {
+                prefix[b] = run;
+                const int ql = p.qo_indptr[b + 1] - p.qo_indptr[b];
+                run += ((ql + 2 * p.P - 1) / (2 * p.P)) * p.Hkv;
+            }
+            if (lane == 31) prefix[p.B] = incl;
+        }
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base_sh;
+    if constexpr (kVarlen) n_items = prefix[p.B];
+    auto get_item = [&](int idx) -> Item {
+        if constexpr (kVarlen) return item_of_varlen(p, prefix, idx);
+        else return item_of(p, idx);
+    };
 
     auto fail = [&]() {
         flag_status(p.status, ATTN_DEV_WAIT_TIMEOUT);
@@ -152,18 +229,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const uint32_t s_addr = tmem + lane_addr + kColS + 128 * t;
         const uint32_t o_addr = tmem + lane_addr + kColO + 128 * t;
-        const int delta = p.kv_len - p.q_len;
         const float sl2 = p.scale_log2;
         uint32_t kv_iter = 0, item_iter = 0;
         bool ok = true;
         for (int i = 0; ok; ++i) {
             const int idx = cta_item(i);
-            if (idx >= p.n_items) break;
-            const Item it = item_of(p, idx);
-            const int head = it.kvh * p.G + r / p.P;
-            const int pos = it.p0 + t * p.P + r % p.P;
-            const bool row_real = pos < p.q_len;
-            const size_t row_id = (static_cast<size_t>(it.b) * p.Hq + head) * p.q_len + pos;
+            if (idx >= n_items) break;
+            const Item it = get_item(idx);
+            const int delta = it.delta;
+            // tile row -> (query position, head): head-major rows for the dense
+            // layout, position-major rows for the ragged [total_q, Hq, D] layout
+            const int head = it.kvh * p.G + (kVarlen ? r % p.G : r / p.P);
+            const int pos = it.p0 + t * p.P + (kVarlen ? r / p.G : r % p.P);
+            const bool row_real = pos < it.q_len;
+            const size_t row_id = kVarlen ? (static_cast<size_t>(it.q_start) + pos) * p.Hq + head
+                                          : (static_cast<size_t>(it.b) * p.Hq + head) * p.q_len + pos;
             if (it.n_kv == 0) {
                 if (row_real) {
                     uint4* orow = reinterpret_cast<uint4*>(p.o + row_id * kD);
@@ -277,7 +357,71 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         regs_dec<kRegsControl>();
-        if (warp == kProducerWarp) {
+        if (warp == kProducerWarp && kVarlen) {
+            // --------------------------------------- TMA producer, ragged batch over a paged pool
+            // Lane i gathers KV rows 4i .. 4i+3 of each 128-token tile (tile::gather4,
+            // one 64-column half per instruction); tokens past the sequence map to a
+            // row past the pool, which TMA fills with zeros.
+            if (lane == 0) {
+                tma_prefetch_desc(&q_map);
+                tma_prefetch_desc(&k_map);
+                tma_prefetch_desc(&v_map);
+            }
+            uint32_t kv_iter = 0, item_iter = 0;
+            bool ok = true;
+            for (int i = 0; ok; ++i) {
+                const int idx = cta_item(i);
+                if (idx >= n_items) break;
+                const Item it = get_item(idx);
+                if (it.n_kv == 0) continue;
+                if (lane == 0) {
+                    if (item_iter > 0) ok = wait(&q_empty, (item_iter - 1) & 1);
+                    if (ok) {
+                        mbar_arrive_expect_tx(&q_full, 2 * kTile);
+                        for (int t = 0; t < 2; ++t)
+                            for (int h = 0; h < 2; ++h)
+                                tma_load_3d(smem + kOffQ + t * kTile + h * kHalf, &q_map, &q_full, h * 64,
+                                            it.kvh * p.G, it.q_start + it.p0 + t * p.P);
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                if (!ok) break;
+                for (int j = 0; j < it.n_kv; ++j, ++kv_iter) {
+                    const int s = kv_iter % kStages;
+                    if (lane == 0) {
+                        if (kv_iter >= kStages) ok = wait(&kv_empty[s], ((kv_iter / kStages) - 1) & 1);
+                        if (ok) {
+                            mbar_arrive_expect_tx(&k_full[s], kTile);
+                            mbar_arrive_expect_tx(&v_full[s], kTile);
+                        }
+                    }
+                    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                    if (!ok) break;
+                    int rows[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int tok = j * kBN + 4 * lane + e;
+                        rows[e] = p.pool_rows;   // past the pool: zero fill
+                        if (tok < it.kv_len) {
+                            const int page = p.kv_indices[it.kv_base + tok / p.page_size];
+                            if (page >= 0 && static_cast<long long>(page) * p.page_size < p.pool_rows)
+                                rows[e] = page * p.page_size + tok % p.page_size;
+                            else
+                                flag_status(p.status, ATTN_DEV_PAGE_OUT_OF_RANGE);
+                        }
+                    }
+                    const int x0 = it.kvh * kD;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        tma_gather4(smem + kOffK + s * kTile + h * kHalf + lane * 512, &k_map, &k_full[s], x0 + 64 * h,
+                                    rows[0], rows[1], rows[2], rows[3]);
+                        tma_gather4(smem + kOffV + s * kTile + h * kHalf + lane * 512, &v_map, &v_full[s], x0 + 64 * h,
+                                    rows[0], rows[1], rows[2], rows[3]);
+                    }
+                }
+                ++item_iter;
+            }
+        } else if (warp == kProducerWarp) {
             // ------------------------------------------------------------ TMA producer
             if (lane == 0) {
                 tma_prefetch_desc(&q_map);
@@ -287,8 +431,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bool ok = true;
                 for (int i = 0; ok; ++i) {
                     const int idx = cta_item(i);
-                    if (idx >= p.n_items) break;
-                    const Item it = item_of(p, idx);
+                    if (idx >= n_items) break;
+                    const Item it = get_item(idx);
                     if (it.n_kv == 0) continue;
                     if (item_iter > 0 && !(ok = wait(&q_empty, (item_iter - 1) & 1))) break;
                     mbar_arrive_expect_tx(&q_full, 2 * kTile);
@@ -338,8 +482,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bool ok = true;
                 for (int i = 0; ok; ++i) {
                     const int idx = cta_item(i);
-                    if (idx >= p.n_items) break;
-                    const Item it = item_of(p, idx);
+                    if (idx >= n_items) break;
+                    const Item it = get_item(idx);
                     if (it.n_kv == 0) continue;
                     if (!(ok = wait(&q_full, item_iter & 1))) break;
                     if (!(ok = wait(&k_full[kv_iter % kStages], (kv_iter / kStages) & 1))) break;
@@ -434,14 +578,72 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream) {
     p.n_qb = (a.q_len + 2 * P - 1) / (2 * P);
     p.n_items = a.B * a.Hkv * p.n_qb;
     p.scale_log2 = a.scale * kLog2e;
+    p.qo_indptr = p.kv_indptr = p.kv_indices = p.kv_last = nullptr;
+    p.page_size = p.pool_rows = 0;
     const int sms = device_sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
     const int grid = p.n_items < sms ? p.n_items : sms;
     const size_t smem = kSmemBytes + 1024;
-    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    prefill_tc_kernel<<<grid, kThreads, smem, stream>>>(q_map, k_map, v_map, p);
+    prefill_tc_kernel<false><<<grid, kThreads, smem, stream>>>(q_map, k_map, v_map, p);
+    return cudaGetLastError();
+}
+
+int varlen_max_seqs() { return kMaxVarlenSeqs; }
+
+cudaError_t launch_prefill_varlen_tc(const VarlenArgs& a, cudaStream_t stream) {
+    const int G = a.Hq / a.Hkv;
+    const int P = kBM / G;
+    CUtensorMap q_map, k_map, v_map;
+    {
+        // ragged Q [total_q, Hq, D]: box {64 dims, G heads, P positions} -> rows pos * G + head
+        const uint64_t dims[3] = {kD, static_cast<uint64_t>(a.Hq), static_cast<uint64_t>(a.total_q)};
+        const uint64_t strides[2] = {kD * 2, static_cast<uint64_t>(a.Hq) * kD * 2};
+        const uint32_t box[3] = {64, static_cast<uint32_t>(G), static_cast<uint32_t>(P)};
+        if (!encode_tiled_map(&q_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.q, dims, strides, box,
+                              CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+    }
+    {
+        // the pool as rows of Hkv * D; a one-row box of 64 dims for tile::gather4
+        const uint64_t rows = static_cast<uint64_t>(a.num_pages) * a.page_size;
+        const uint64_t dims[2] = {static_cast<uint64_t>(a.Hkv) * kD, rows};
+        const uint64_t strides[1] = {static_cast<uint64_t>(a.Hkv) * kD * 2};
+        const uint32_t box[2] = {64, 1};
+        if (!encode_tiled_map(&k_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.k_cache, dims, strides, box,
+                              CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_tiled_map(&v_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.v_cache, dims, strides, box,
+                              CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+    }
+    Params p;
+    p.o = static_cast<__nv_bfloat16*>(a.o);
+    p.lse = a.lse;
+    p.status = a.dev_status;
+    p.B = a.B;
+    p.Hq = a.Hq;
+    p.Hkv = a.Hkv;
+    p.q_len = p.kv_len = 0;
+    p.G = G;
+    p.P = P;
+    p.n_qb = 0;
+    p.n_items = 0;   // counted on the device from qo_indptr
+    p.scale_log2 = a.scale * kLog2e;
+    p.qo_indptr = a.qo_indptr;
+    p.kv_indptr = a.kv_indptr;
+    p.kv_indices = a.kv_indices;
+    p.kv_last = a.kv_last_page_len;
+    p.page_size = a.page_size;
+    p.pool_rows = a.num_pages * a.page_size;
+    const int sms = device_sm_count();
+    if (sms <= 0) return cudaErrorInvalidDevice;
+    const size_t smem = kSmemBytes + 1024;
+    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    prefill_tc_kernel<true><<<sms, kThreads, smem, stream>>>(q_map, k_map, v_map, p);
     return cudaGetLastError();
 }
 

@@ -104,6 +104,18 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* desc, ui
         : "memory");
 }
 
+// Four rows (row0..row3) of a 2D tensor, one box-width strip each, into four
+// consecutive box rows of shared memory (the map's box is one row high).
+__device__ __forceinline__ void tma_gather4(void* smem_dst, const void* desc, uint64_t* bar, int col, int row0,
+                                            int row1, int row2, int row3) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(desc)), "r"(smem_u32(bar)), "r"(col), "r"(row0), "r"(row1), "r"(row2),
+        "r"(row3)
+        : "memory");
+}
+
 // ------------------------------------------------------- warp-level MMA (sm_80+)
 
 __device__ __forceinline__ void ldmatrix_x4(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3,

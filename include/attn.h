@@ -96,6 +96,36 @@ attn_status_t attn_prefill_fwd(const void* q, const void* k, const void* v,
 size_t attn_decode_workspace_bytes(int B, int Hq, int max_kv_len, int split_tokens, int D);
 
 /*
+ * attn_prefill_paged_varlen - causal GQA prefill of a ragged batch over a
+ * paged KV cache, in one launch.
+ *
+ * Follows "gpt-o3 / triton6fd1ef", run and _gqa_prefill_kernel: CSR
+ * qo_indptr / kv_indptr / kv_indices, kv_head = q_head / (Hq / Hkv), and per
+ * sequence bottom-right causal alignment (delta = kv_len - q_len).  The
+ * sequences' extents are read on the device; nothing is synchronised.
+ *
+ *   q            [total_q, Hq, D] bfloat16; sequence b owns rows
+ *                [qo_indptr[b], qo_indptr[b+1])                      (read)
+ *   k_cache,
+ *   v_cache      bfloat16 [num_pages, page_size, Hkv, D] (any page_size >= 1) (read)
+ *   qo_indptr    int32 [B+1]; kv_indptr int32 [B+1], in pages;
+ *   kv_indices   int32 [kv_indptr[B]], the pool page of each listed page;
+ *   kv_last_page_len  int32 [B], tokens in each sequence's last page
+ *                (NULL: every page full); kv_len_b = (pages_b - 1) *
+ *                page_size + last_b                                  (read, device)
+ *   o            [total_q, Hq, D] bfloat16; lse [total_q, Hq] fp32 (written; lse may be NULL)
+ *   D = 128, Hq / Hkv dividing 128, B <= 2048.
+ * A page id outside [0, num_pages) sets ATTN_DEV_PAGE_OUT_OF_RANGE and is
+ * read as zeros.
+ */
+attn_status_t attn_prefill_paged_varlen(const void* q, const void* k_cache, const void* v_cache,
+                                        const int32_t* qo_indptr, const int32_t* kv_indptr,
+                                        const int32_t* kv_indices, const int32_t* kv_last_page_len,
+                                        void* o, float* lse, int B, int Hq, int Hkv, int D, int total_q,
+                                        int num_pages, int page_size, float scale,
+                                        int32_t* dev_status, void* stream);
+
+/*
  * attn_decode_paged_splitk - single-query split-K decode over a paged KV cache.
  *
  * Follows "splitk_kernels.py" (xformers), _fwd_kernel_splitK (split chunks,

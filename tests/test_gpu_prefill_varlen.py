@@ -1,0 +1,66 @@
+"""Ragged (varlen) causal GQA prefill over a paged KV cache ("gpt-o3 /
+triton6fd1ef", run) against the oracle, through the C ABI."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from parity import check_lse, check_o, gpu_or_skip
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    # (Hq, Hkv, page_size, q_lens, kv_lens)
+    (32, 4, 1, [300, 1, 129, 64], [700, 1, 129, 1000]),     # G = 8, the page's head layout
+    (32, 4, 1, [200, 77], [200, 77]),                        # no cached prefix
+    (16, 4, 16, [150, 33, 300], [400, 40, 300]),             # G = 4, page size 16, partial last pages
+    (8, 8, 1, [260, 5], [300, 5]),                           # G = 1
+    (32, 2, 256, [100, 500], [1000, 700]),                   # G = 16, large pages
+    (32, 4, 1, [90, 10], [40, 10]),                          # q_len > kv_len: early rows see nothing
+]
+
+
+@pytest.mark.parametrize("hq,hkv,ps,q_lens,kv_lens", CASES)
+def test_varlen_paged_prefill_matches_oracle(hq, hkv, ps, q_lens, kv_lens):
+    dev = gpu_or_skip()
+    import causal_gqa_flashattention_attn_gb300 as attn
+    shape = synth.VarlenShape("t", len(q_lens), hq, hkv, 128, 1, 1, 0, 0, page_size=ps)
+    inp = synth.varlen_inputs(shape, seed=len(q_lens) + ps, q_lens=q_lens, kv_lens=kv_lens)
+    t = {k: v.to(dev) for k, v in inp.items() if torch.is_tensor(v)}
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    o, lse = attn.attn_prefill_paged_varlen(t["q"], t["k_cache"], t["v_cache"], t["qo_indptr"], t["kv_indptr"],
+                                            t["kv_indices"], t["kv_last_page_len"], dev_status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    o_ref, lse_ref = oracle.prefill_paged_varlen(inp["q"].double().numpy(), inp["k_cache"].double().numpy(),
+                                                 inp["v_cache"].double().numpy(), inp["qo_indptr"].numpy(),
+                                                 inp["kv_indptr"].numpy(), inp["kv_indices"].numpy(), ps,
+                                                 inp["kv_last_page_len"].numpy())
+    check_o(o, o_ref)
+    check_lse(lse, lse_ref)
+
+
+def test_varlen_bench_workload_sampled():
+    """The benchmark's ragged batch (8 sequences, page size 1); the oracle
+    checks two whole sequences."""
+    dev = gpu_or_skip()
+    import causal_gqa_flashattention_attn_gb300 as attn
+    shape = synth.VARLEN_PAGED_PREFILL
+    inp = synth.varlen_inputs(shape, seed=0)
+    t = {k: v.to(dev) for k, v in inp.items() if torch.is_tensor(v)}
+    o, lse = attn.attn_prefill_paged_varlen(t["q"], t["k_cache"], t["v_cache"], t["qo_indptr"], t["kv_indptr"],
+                                            t["kv_indices"], t["kv_last_page_len"])
+    torch.cuda.synchronize()
+    qo = inp["qo_indptr"].tolist()
+    for b in (0, shape.B - 1):
+        sub_qo = np.array([0, qo[b + 1] - qo[b]])
+        kvp = inp["kv_indptr"].tolist()
+        sub_kvp = np.array([0, kvp[b + 1] - kvp[b]])
+        sub_idx = inp["kv_indices"][kvp[b]:kvp[b + 1]].numpy()
+        o_ref, lse_ref = oracle.prefill_paged_varlen(inp["q"][qo[b]:qo[b + 1]].double().numpy(),
+                                                     inp["k_cache"].double().numpy(),
+                                                     inp["v_cache"].double().numpy(), sub_qo, sub_kvp, sub_idx, 1)
+        check_o(o[qo[b]:qo[b + 1]], o_ref, what=f"O seq {b}")
+        check_lse(lse[qo[b]:qo[b + 1]], lse_ref, what=f"LSE seq {b}")
