@@ -557,13 +557,20 @@ def run_profile(args):
     torch.cuda.set_device(dev)
     attn.lib()
     n = args.warmup + args.steps
-    if args.profile.startswith("prefill"):
+    if args.profile == "prefill_varlen":
+        vl = synth.VARLEN_PAGED_PREFILL
+        t = {kk: vv.to(dev) for kk, vv in synth.varlen_inputs(vl, seed=0).items() if torch.is_tensor(vv)}
+        for _ in range(n):
+            attn.attn_prefill_paged_varlen(t["q"], t["k_cache"], t["v_cache"], t["qo_indptr"], t["kv_indptr"],
+                                           t["kv_indices"], t["kv_last_page_len"])
+    elif args.profile.startswith("prefill"):
         shape = synth.LLAMA_GQA_PREFILL if args.profile == "prefill" else synth.BATCHED_SQUARE_PREFILL
         q, k, v = (t.to(dev) for t in synth.prefill_inputs(shape, seed=0))
         for _ in range(n):
             attn.attn_prefill_fwd(q, k, v)
     else:
-        shape = synth.PAGED_DECODE_BF16 if args.profile == "decode_bf16" else synth.PAGED_DECODE_INT4
+        shape = {"decode_bf16": synth.PAGED_DECODE_BF16, "decode_int4": synth.PAGED_DECODE_INT4,
+                 "decode_fp8": synth.PAGED_DECODE_FP8}[args.profile]
         if args.decode_batch:
             shape = replace(shape, B=args.decode_batch)
         inp = synth.decode_inputs(shape, seed=0)
@@ -571,9 +578,14 @@ def run_profile(args):
         ws = torch.empty(attn.attn_decode_workspace_bytes(shape.B, shape.Hq, shape.len_hi, shape.split_tokens,
                                                           shape.D), dtype=torch.uint8, device=dev)
         for _ in range(n):
-            attn.attn_decode_paged_splitk(t["q"], t["k_cache"], t["v_cache"], t["block_table"], t["seq_lens"],
-                                          shape.split_tokens, shape.len_hi, n_groups=shape.n_groups, workspace=ws,
-                                          write_output=False)
+            if shape.kv_format == "fp8":
+                attn.attn_decode_paged_splitk_fp8(t["q"], t["k_cache"], t["v_cache"], t["k_scale_shift"],
+                                                  t["v_scale_shift"], t["block_table"], t["seq_lens"],
+                                                  shape.split_tokens, shape.len_hi, workspace=ws, write_output=False)
+            else:
+                attn.attn_decode_paged_splitk(t["q"], t["k_cache"], t["v_cache"], t["block_table"], t["seq_lens"],
+                                              shape.split_tokens, shape.len_hi, n_groups=shape.n_groups,
+                                              workspace=ws, write_output=False)
     torch.cuda.synchronize(dev)
 
 
@@ -587,7 +599,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--clock-window", type=float, default=2.0,
                     help="seconds of loaded, untimed steps sampled by nvidia-smi before the timed region")
-    ap.add_argument("--profile", choices=["prefill", "prefill_batched", "decode_bf16", "decode_int4"],
+    ap.add_argument("--profile", choices=["prefill", "prefill_batched", "prefill_varlen", "decode_bf16", "decode_int4",
+                                          "decode_fp8"],
                     help="run only one kernel on its workload (for ncu captures); prints no JSON line")
     ap.add_argument("--decode-batch", type=int, default=0, help="with --profile: shrink the decode batch")
     args = ap.parse_args()

@@ -70,6 +70,8 @@ struct Params {
     const int32_t* kv_indptr;   // [B+1], in pages
     const int32_t* kv_indices;  // pool page of each listed page
     const int32_t* kv_last;     // [B] tokens in the last page (NULL: full pages)
+    const __nv_bfloat16* k_pool;   // [pool_rows, Hkv, D]
+    const __nv_bfloat16* v_pool;
     int page_size, pool_rows;
 };
 
@@ -136,8 +138,9 @@ __device__ __forceinline__ int cta_item(int i) {
 }
 
 // kVarlen: Q is ragged [total_q, Hq, D] (tile rows ordered position-major,
-// r = pos * G + head) and K/V come from a paged pool through the page list,
-// gathered four rows at a time by TMA (tile::gather4).
+// r = pos * G + head) and K/V rows are gathered from a paged pool through the
+// page list by the producer warp with 16-byte cp.async copies into the
+// 128-byte-swizzled tile layout (TMA tile loads need contiguous rows).
 template <bool kVarlen>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap k_map,
@@ -157,8 +160,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&q_full, 1);
         mbar_init(&q_empty, 1);
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(&k_full[s], 1);
-            mbar_init(&v_full[s], 1);
+            mbar_init(&k_full[s], kVarlen ? 32 : 1);   // varlen: one cp.async arrival per producer lane
+            mbar_init(&v_full[s], kVarlen ? 32 : 1);
             mbar_init(&kv_empty[s], 1);
         }
         for (int t = 0; t < 2; ++t) {
@@ -358,15 +361,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         regs_dec<kRegsControl>();
         if (warp == kProducerWarp && kVarlen) {
-            // --------------------------------------- TMA producer, ragged batch over a paged pool
-            // Lane i gathers KV rows 4i .. 4i+3 of each 128-token tile (tile::gather4,
-            // one 64-column half per instruction); tokens past the sequence map to a
-            // row past the pool, which TMA fills with zeros.
-            if (lane == 0) {
-                tma_prefetch_desc(&q_map);
-                tma_prefetch_desc(&k_map);
-                tma_prefetch_desc(&v_map);
-            }
+            // ------------------------------------------ producer, ragged batch over a paged pool
+            // Q tiles by TMA; K/V rows gathered by the whole warp: lane i copies
+            // token rows 4i .. 4i+3 of each 128-token tile (16 x 16 bytes each),
+            // tokens past the sequence are zero-filled.
+            if (lane == 0) tma_prefetch_desc(&q_map);
+            const size_t row_elems = static_cast<size_t>(p.Hkv) * kD;
             uint32_t kv_iter = 0, item_iter = 0;
             bool ok = true;
             for (int i = 0; ok; ++i) {
@@ -386,38 +386,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                 if (!ok) break;
+                const __nv_bfloat16* kb = p.k_pool + it.kvh * kD;
+                const __nv_bfloat16* vb = p.v_pool + it.kvh * kD;
                 for (int j = 0; j < it.n_kv; ++j, ++kv_iter) {
                     const int s = kv_iter % kStages;
-                    if (lane == 0) {
-                        if (kv_iter >= kStages) ok = wait(&kv_empty[s], ((kv_iter / kStages) - 1) & 1);
-                        if (ok) {
-                            mbar_arrive_expect_tx(&k_full[s], kTile);
-                            mbar_arrive_expect_tx(&v_full[s], kTile);
-                        }
-                    }
+                    if (lane == 0 && kv_iter >= kStages) ok = wait(&kv_empty[s], ((kv_iter / kStages) - 1) & 1);
                     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                     if (!ok) break;
-                    int rows[4];
-#pragma unroll
+                    uint8_t* ks = smem + kOffK + s * kTile;
+                    uint8_t* vs = smem + kOffV + s * kTile;
+#pragma unroll 1
                     for (int e = 0; e < 4; ++e) {
-                        const int tok = j * kBN + 4 * lane + e;
-                        rows[e] = p.pool_rows;   // past the pool: zero fill
+                        const int r = 4 * lane + e;          // row of the tile
+                        const int tok = j * kBN + r;
+                        size_t row = 0;
+                        uint32_t nbytes = 0;
                         if (tok < it.kv_len) {
                             const int page = p.kv_indices[it.kv_base + tok / p.page_size];
-                            if (page >= 0 && static_cast<long long>(page) * p.page_size < p.pool_rows)
-                                rows[e] = page * p.page_size + tok % p.page_size;
-                            else
+                            if (page >= 0 && static_cast<long long>(page) * p.page_size < p.pool_rows) {
+                                row = static_cast<size_t>(page) * p.page_size + tok % p.page_size;
+                                nbytes = 16;
+                            } else {
                                 flag_status(p.status, ATTN_DEV_PAGE_OUT_OF_RANGE);
+                            }
+                        }
+                        const __nv_bfloat16* ksrc = kb + row * row_elems;
+                        const __nv_bfloat16* vsrc = vb + row * row_elems;
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) {
+                            const uint32_t off = (c >> 3) * kHalf + r * 128 + ((((c & 7) ^ (r & 7)) & 7) << 4);
+                            cp_async16(ks + off, ksrc + 8 * c, nbytes);
+                            cp_async16(vs + off, vsrc + 8 * c, nbytes);
                         }
                     }
-                    const int x0 = it.kvh * kD;
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        tma_gather4(smem + kOffK + s * kTile + h * kHalf + lane * 512, &k_map, &k_full[s], x0 + 64 * h,
-                                    rows[0], rows[1], rows[2], rows[3]);
-                        tma_gather4(smem + kOffV + s * kTile + h * kHalf + lane * 512, &v_map, &v_full[s], x0 + 64 * h,
-                                    rows[0], rows[1], rows[2], rows[3]);
-                    }
+                    cp_async_mbar_arrive(&k_full[s]);
+                    cp_async_mbar_arrive(&v_full[s]);
                 }
                 ++item_iter;
             }
@@ -487,6 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (it.n_kv == 0) continue;
                     if (!(ok = wait(&q_full, item_iter & 1))) break;
                     if (!(ok = wait(&k_full[kv_iter % kStages], (kv_iter / kStages) & 1))) break;
+                    if constexpr (kVarlen) fence_proxy_async_smem();   // cp.async writes -> tensor-core reads
                     tc_fence_after();
                     issue_s(0, kv_iter % kStages);
                     umma_commit(&s_full[0]);
@@ -498,6 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const bool last = (j + 1 == it.n_kv);
                         const uint32_t nxt = kv_iter + 1;
                         if (!(ok = wait(&v_full[s], (kv_iter / kStages) & 1))) break;
+                        if constexpr (kVarlen) fence_proxy_async_smem();
                         for (int t = 0; t < 2; ++t) {
                             if (!(ok = wait(&p_full[t], kv_iter & 1))) break;
                             if (j == 0 && item_iter > 0 && !(ok = wait(&o_empty[t], (item_iter - 1) & 1))) break;
@@ -507,6 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (!last) {
                                 if (t == 0) {
                                     if (!(ok = wait(&k_full[nxt % kStages], (nxt / kStages) & 1))) break;
+                                    if constexpr (kVarlen) fence_proxy_async_smem();
                                     tc_fence_after();
                                 }
                                 issue_s(t, nxt % kStages);            // S_t = Q_t K_{j+1}^T (after P_t is read)
@@ -579,6 +585,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream) {
     p.n_items = a.B * a.Hkv * p.n_qb;
     p.scale_log2 = a.scale * kLog2e;
     p.qo_indptr = p.kv_indptr = p.kv_indices = p.kv_last = nullptr;
+    p.k_pool = p.v_pool = nullptr;
     p.page_size = p.pool_rows = 0;
     const int sms = device_sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
@@ -596,25 +603,13 @@ int varlen_max_seqs() { return kMaxVarlenSeqs; }
 cudaError_t launch_prefill_varlen_tc(const VarlenArgs& a, cudaStream_t stream) {
     const int G = a.Hq / a.Hkv;
     const int P = kBM / G;
-    CUtensorMap q_map, k_map, v_map;
+    CUtensorMap q_map;   // K/V rows are gathered with cp.async (no tensor map)
     {
         // ragged Q [total_q, Hq, D]: box {64 dims, G heads, P positions} -> rows pos * G + head
         const uint64_t dims[3] = {kD, static_cast<uint64_t>(a.Hq), static_cast<uint64_t>(a.total_q)};
         const uint64_t strides[2] = {kD * 2, static_cast<uint64_t>(a.Hq) * kD * 2};
         const uint32_t box[3] = {64, static_cast<uint32_t>(G), static_cast<uint32_t>(P)};
         if (!encode_tiled_map(&q_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.q, dims, strides, box,
-                              CU_TENSOR_MAP_SWIZZLE_128B))
-            return cudaErrorInvalidValue;
-    }
-    {
-        // the pool as rows of Hkv * D; a one-row box of 64 dims for tile::gather4
-        const uint64_t rows = static_cast<uint64_t>(a.num_pages) * a.page_size;
-        const uint64_t dims[2] = {static_cast<uint64_t>(a.Hkv) * kD, rows};
-        const uint64_t strides[1] = {static_cast<uint64_t>(a.Hkv) * kD * 2};
-        const uint32_t box[2] = {64, 1};
-        if (!encode_tiled_map(&k_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.k_cache, dims, strides, box,
-                              CU_TENSOR_MAP_SWIZZLE_128B) ||
-            !encode_tiled_map(&v_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.v_cache, dims, strides, box,
                               CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
     }
@@ -637,13 +632,15 @@ cudaError_t launch_prefill_varlen_tc(const VarlenArgs& a, cudaStream_t stream) {
     p.kv_last = a.kv_last_page_len;
     p.page_size = a.page_size;
     p.pool_rows = a.num_pages * a.page_size;
+    p.k_pool = static_cast<const __nv_bfloat16*>(a.k_cache);
+    p.v_pool = static_cast<const __nv_bfloat16*>(a.v_cache);
     const int sms = device_sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
     const size_t smem = kSmemBytes + 1024;
     cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    prefill_tc_kernel<true><<<sms, kThreads, smem, stream>>>(q_map, k_map, v_map, p);
+    prefill_tc_kernel<true><<<sms, kThreads, smem, stream>>>(q_map, q_map, q_map, p);
     return cudaGetLastError();
 }
 

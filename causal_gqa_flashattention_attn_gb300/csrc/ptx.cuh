@@ -104,16 +104,17 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* desc, ui
         : "memory");
 }
 
-// Four rows (row0..row3) of a 2D tensor, one box-width strip each, into four
-// consecutive box rows of shared memory (the map's box is one row high).
-__device__ __forceinline__ void tma_gather4(void* smem_dst, const void* desc, uint64_t* bar, int col, int row0,
-                                            int row1, int row2, int row3) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(smem_dst)),
-        "l"(reinterpret_cast<uint64_t>(desc)), "r"(smem_u32(bar)), "r"(col), "r"(row0), "r"(row1), "r"(row2),
-        "r"(row3)
-        : "memory");
+// 16-byte global -> shared copy (zero-filled when src_bytes is 0).
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem_dst)), "l"(gsrc),
+                 "r"(src_bytes)
+                 : "memory");
+}
+
+// Arrive on an mbarrier once all of this thread's earlier cp.async copies
+// have landed (the barrier's expected count includes this arrival).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 // ------------------------------------------------------- warp-level MMA (sm_80+)
