@@ -229,6 +229,10 @@ attn_status_t attn_prefill_paged_varlen(const void* q, const void* k_cache, cons
     if (G > 128 || 128 % G != 0) return ATTN_ERR_UNSUPPORTED;
     if (B > varlen_max_seqs()) return ATTN_ERR_UNSUPPORTED;
     if (static_cast<long long>(num_pages) * page_size >= (1LL << 31) - 1) return ATTN_ERR_UNSUPPORTED;
+    // work items (query blocks x KV heads) are counted in int and a query
+    // block index is packed in 21 bits
+    if (total_q >= (1 << 22) || (static_cast<long long>(total_q) + B) * Hkv >= (1LL << 31))
+        return ATTN_ERR_UNSUPPORTED;
     if (total_q == 0) return ATTN_OK;
     VarlenArgs a{q, k_cache, v_cache, qo_indptr, kv_indptr, kv_indices, kv_last_page_len, o, lse,
                  B, Hq,      Hkv,     D,         total_q,   num_pages, page_size, scale,      dev_status};

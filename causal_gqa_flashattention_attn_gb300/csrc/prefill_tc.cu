@@ -41,6 +41,7 @@ constexpr int kBN = 128;          // keys per KV tile
 constexpr int kThreads = 384;     // 12 warps = 3 warpgroups
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
+constexpr uint32_t kNoRow = 0xffffffffu;
 // Registers: launched at 168 per thread (384 x 168 = 64512); the
 // producer/MMA warpgroup drops to 72 and each softmax warpgroup rises to
 // 216 (2 x 128 x 216 + 128 x 72 = 64512, the launch total).
@@ -81,6 +82,12 @@ struct Item {
 };
 
 constexpr int kMaxVarlenSeqs = 2048;   // sequences per ragged batch (prefix table in shared memory)
+// Ragged batches of up to kMaxOrder (sequence, query block) pairs are walked
+// longest-first through a sorted list in shared memory; larger ones in
+// sequence order.  Pair word: sequence << kPairQbBits | query block.
+constexpr int kMaxOrder = 4096;
+constexpr int kOrderBuckets = 512;      // sort keys: KV tiles, 511 and more share the top bucket
+constexpr int kPairQbBits = 21;
 
 // Work item `idx` of the snake-ordered, longest-first list.
 __device__ __forceinline__ Item item_of(const Params& p, int idx) {
@@ -102,32 +109,144 @@ __device__ __forceinline__ Item item_of(const Params& p, int idx) {
     return it;
 }
 
-// Ragged batch: item `idx` of sequence-major order, within a sequence the
-// furthest query block (longest KV range) first.  `prefix[b]` counts the
-// items of sequences before b.
-__device__ __forceinline__ Item item_of_varlen(const Params& p, const int* prefix, int idx) {
+// Ragged batch: the item of sequence b, query block qb (2P positions) and KV
+// head kvh.
+__device__ __forceinline__ Item varlen_item(const Params& p, int b, int qb, int kvh) {
+    Item it;
+    it.b = b;
+    it.q_start = p.qo_indptr[b];
+    it.q_len = p.qo_indptr[b + 1] - it.q_start;
+    it.kv_base = p.kv_indptr[b];
+    const int n_pages = p.kv_indptr[b + 1] - it.kv_base;
+    const int last = (p.kv_last != nullptr) ? p.kv_last[b] : p.page_size;
+    it.kv_len = n_pages > 0 ? (n_pages - 1) * p.page_size + last : 0;
+    it.delta = it.kv_len - it.q_len;
+    it.kvh = kvh;
+    it.p0 = qb * 2 * p.P;
+    const int p_last = min(it.p0 + 2 * p.P, it.q_len) - 1;
+    const int kv_end = min(it.kv_len, p_last + it.delta + 1);
+    it.n_kv = kv_end > 0 ? (kv_end + kBN - 1) / kBN : 0;
+    return it;
+}
+
+// Ragged batch, unsorted order: the pair word of item `idx` in
+// sequence-major order, within a sequence the furthest query block (longest
+// KV range) first.  `prefix[b]` counts the items of sequences before b.
+__device__ __forceinline__ uint32_t pair_of_varlen(const Params& p, const int* prefix, int idx) {
     int lo = 0, hi = p.B;   // last b with prefix[b] <= idx
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
         if (prefix[mid] <= idx) lo = mid; else hi = mid;
     }
-    Item it;
-    it.b = lo;
-    it.q_start = p.qo_indptr[lo];
-    it.q_len = p.qo_indptr[lo + 1] - it.q_start;
-    it.kv_base = p.kv_indptr[lo];
-    const int n_pages = p.kv_indptr[lo + 1] - it.kv_base;
-    const int last = (p.kv_last != nullptr) ? p.kv_last[lo] : p.page_size;
-    it.kv_len = n_pages > 0 ? (n_pages - 1) * p.page_size + last : 0;
-    it.delta = it.kv_len - it.q_len;
-    const int local = idx - prefix[lo];
-    const int n_qb = (it.q_len + 2 * p.P - 1) / (2 * p.P);
-    it.kvh = local % p.Hkv;
-    it.p0 = (n_qb - 1 - local / p.Hkv) * 2 * p.P;
-    const int p_last = min(it.p0 + 2 * p.P, it.q_len) - 1;
-    const int kv_end = min(it.kv_len, p_last + it.delta + 1);
-    it.n_kv = kv_end > 0 ? (kv_end + kBN - 1) / kBN : 0;
-    return it;
+    const int q_len = p.qo_indptr[lo + 1] - p.qo_indptr[lo];
+    const int n_qb = (q_len + 2 * p.P - 1) / (2 * p.P);
+    const int qb = n_qb - 1 - (idx - prefix[lo]) / p.Hkv;
+    return (static_cast<uint32_t>(lo) << kPairQbBits) | static_cast<uint32_t>(qb);
+}
+
+// Ragged batch: KV tiles of sequence b's query block qb, clamped to the
+// counting-sort range.
+__device__ __forceinline__ int varlen_pair_key(const Params& p, int q_len, int kv_len, int qb) {
+    const int p_last = min(qb * 2 * p.P + 2 * p.P, q_len) - 1;
+    const int kv_end = min(kv_len, p_last + kv_len - q_len + 1);
+    const int n_kv = kv_end > 0 ? (kv_end + kBN - 1) / kBN : 0;
+    return min(n_kv, kOrderBuckets - 1);
+}
+
+// Ragged batch: new-token and KV lengths of sequence b.
+__device__ __forceinline__ void varlen_lens(const Params& p, int b, int& q_len, int& kv_len) {
+    q_len = p.qo_indptr[b + 1] - p.qo_indptr[b];
+    const int n_pages = p.kv_indptr[b + 1] - p.kv_indptr[b];
+    const int last = (p.kv_last != nullptr) ? p.kv_last[b] : p.page_size;
+    kv_len = n_pages > 0 ? (n_pages - 1) * p.page_size + last : 0;
+}
+
+// Ragged batch (one warp): prefix[b] = work items of the sequences before b,
+// prefix[B] = all items.  One lane per sequence, 32 sequences per round.
+__device__ void varlen_prefix(const Params& p, int* prefix, int lane) {
+    int carry = 0;
+#pragma unroll 4
+    for (int b0 = 0; b0 < p.B; b0 += 32) {
+        const int b = b0 + lane;
+        int items = 0;
+        if (b < p.B) {
+            const int ql = p.qo_indptr[b + 1] - p.qo_indptr[b];
+            items = ((ql + 2 * p.P - 1) / (2 * p.P)) * p.Hkv;
+        }
+        int incl = items;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += v;
+        }
+        if (b < p.B) prefix[b] = carry + incl - items;
+        carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) prefix[p.B] = carry;
+}
+
+// Ragged batch, sorted order (one warp, identical in every CTA): the
+// (sequence, query block) pairs by decreasing KV tile count.  A counting
+// sort: histogram of the keys, exclusive scan from the largest key down,
+// then a scatter in a fixed order (rounds of 32 sequences, one lane each;
+// within a round the furthest query blocks first, ties by lane) so that
+// every CTA writes the same list.
+__device__ void varlen_sort_pairs(const Params& p, uint32_t* order, int* bucket, int lane) {
+    for (int k = lane; k < kOrderBuckets; k += 32) bucket[k] = 0;
+    __syncwarp();
+    for (int b0 = 0; b0 < p.B; b0 += 32) {
+        const int b = b0 + lane;
+        int q_len = 0, kv_len = 0;
+        if (b < p.B) varlen_lens(p, b, q_len, kv_len);
+        const int n_qb = (q_len + 2 * p.P - 1) / (2 * p.P);
+        for (int qb = 0; qb < n_qb; ++qb) atomicAdd(&bucket[varlen_pair_key(p, q_len, kv_len, qb)], 1);
+    }
+    __syncwarp();
+    constexpr int per = kOrderBuckets / 32;   // lane 0 owns the largest keys
+    int sum = 0;
+#pragma unroll
+    for (int e = 0; e < per; ++e) sum += bucket[kOrderBuckets - 1 - (per * lane + e)];
+    int incl = sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += v;
+    }
+    int run = incl - sum;
+#pragma unroll
+    for (int e = 0; e < per; ++e) {
+        const int k = kOrderBuckets - 1 - (per * lane + e);
+        const int c = bucket[k];
+        bucket[k] = run;
+        run += c;
+    }
+    __syncwarp();
+    const uint32_t below = (1u << lane) - 1u;
+    for (int b0 = 0; b0 < p.B; b0 += 32) {
+        const int b = b0 + lane;
+        int q_len = 0, kv_len = 0;
+        if (b < p.B) varlen_lens(p, b, q_len, kv_len);
+        const int n_qb = (q_len + 2 * p.P - 1) / (2 * p.P);
+        const int rounds = __reduce_max_sync(0xffffffffu, n_qb);
+        for (int k = 0; k < rounds; ++k) {
+            const bool valid = k < n_qb;
+            const int qb = n_qb - 1 - k;
+            const uint32_t act = __ballot_sync(0xffffffffu, valid);
+            int key = 0, pos = 0;
+            uint32_t grp = 0;
+            if (valid) {
+                key = varlen_pair_key(p, q_len, kv_len, qb);
+                grp = __match_any_sync(act, key);
+                pos = bucket[key] + __popc(grp & below);
+            }
+            __syncwarp();
+            if (valid) {
+                order[pos] = (static_cast<uint32_t>(b) << kPairQbBits) | static_cast<uint32_t>(qb);
+                if (lane == __ffs(grp) - 1) bucket[key] += __popc(grp);
+            }
+            __syncwarp();
+        }
+    }
 }
 
 // i-th item of this CTA: rounds of gridDim.x items, every other round reversed.
@@ -148,8 +267,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align_1024(smem_raw);
     __shared__ int prefix[kVarlen ? kMaxVarlenSeqs + 1 : 1];
+    __shared__ uint32_t order[kVarlen ? kMaxOrder : 1];  // sorted (sequence, query block) pairs
+    __shared__ int bucket[kVarlen ? kOrderBuckets : 1];
     __shared__ __align__(8) uint64_t q_full, q_empty;
-    __shared__ __align__(8) uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
+    __shared__ __align__(8) uint64_t k_full[kStages], v_full[kStages], k_empty[kStages], v_empty[kStages];
     __shared__ __align__(8) uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_sh;
@@ -160,9 +281,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&q_full, 1);
         mbar_init(&q_empty, 1);
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(&k_full[s], kVarlen ? 32 : 1);   // varlen: one cp.async arrival per producer lane
+            mbar_init(&k_full[s], kVarlen ? 32 : 1);   // ragged: one cp.async arrival per lane of the gather warp
             mbar_init(&v_full[s], kVarlen ? 32 : 1);
-            mbar_init(&kv_empty[s], 1);
+            mbar_init(&k_empty[s], 1);
+            mbar_init(&v_empty[s], 1);
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(&s_full[t], 1);
@@ -179,28 +301,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     int n_items = p.n_items;
     if constexpr (kVarlen) {
-        // prefix[b] = items of the sequences before b (warp 0, chunked scan)
         if (warp == 0) {
-            const int per = (p.B + 31) / 32;
-            const int b0 = min(lane * per, p.B), b1 = min(b0 + per, p.B);
-            int sum = 0;
-            for (int b = b0; b < b1; ++b) {
-                const int ql = p.qo_indptr[b + 1] - p.qo_indptr[b];
-                sum += ((ql + 2 * p.P - 1) / (2 * p.P)) * p.Hkv;
-            }
-            int incl = sum;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const int v = __shfl_up_sync(0xffffffffu, incl, off);
-                if (lane >= off) incl += v;
-            }
-            int run = incl - sum;
-            for (int b = b0; b < b1; ++b) {
-                prefix[b] = run;
-                const int ql = p.qo_indptr[b + 1] - p.qo_indptr[b];
-                run += ((ql + 2 * p.P - 1) / (2 * p.P)) * p.Hkv;
-            }
-            if (lane == 31) prefix[p.B] = incl;
+            varlen_prefix(p, prefix, lane);
+            __syncwarp();
+            if (prefix[p.B] / p.Hkv <= kMaxOrder) varlen_sort_pairs(p, order, bucket, lane);
         }
     }
     tc_fence_before();
@@ -208,9 +312,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = tmem_base_sh;
     if constexpr (kVarlen) n_items = prefix[p.B];
+    const bool sorted = kVarlen && n_items / p.Hkv <= kMaxOrder;
     auto get_item = [&](int idx) -> Item {
-        if constexpr (kVarlen) return item_of_varlen(p, prefix, idx);
-        else return item_of(p, idx);
+        if constexpr (kVarlen) {
+            const uint32_t pair = sorted ? order[idx / p.Hkv] : pair_of_varlen(p, prefix, idx);
+            return varlen_item(p, static_cast<int>(pair >> kPairQbBits),
+                               static_cast<int>(pair & ((1u << kPairQbBits) - 1u)), idx % p.Hkv);
+        } else {
+            return item_of(p, idx);
+        }
     };
 
     auto fail = [&]() {
@@ -362,11 +472,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         regs_dec<kRegsControl>();
         if (warp == kProducerWarp && kVarlen) {
             // ------------------------------------------ producer, ragged batch over a paged pool
-            // Q tiles by TMA; K/V rows gathered by the whole warp: lane i copies
-            // token rows 4i .. 4i+3 of each 128-token tile (16 x 16 bytes each),
-            // tokens past the sequence are zero-filled.
+            // Q tiles by TMA; K/V rows gathered by the whole warp with 16-byte
+            // cp.async copies: lane i copies token rows i, i+32, i+64, i+96 of
+            // each 128-token tile, 16 chunks per row.  Rows 32 apart share their
+            // swizzle phase, so one instruction's 32 chunks fill every bank
+            // four times over (the minimum for 512 bytes).  The pool rows of the
+            // next tile are looked up while this tile's copies are issued; K
+            // arrives on its own barrier before the V copies start; tokens past
+            // the sequence are zero-filled.  (A second gather warp was slower:
+            // its issue slots come out of the softmax warps of its SM quarter.)
             if (lane == 0) tma_prefetch_desc(&q_map);
             const size_t row_elems = static_cast<size_t>(p.Hkv) * kD;
+            const uint32_t swz = static_cast<uint32_t>(lane & 7);
             uint32_t kv_iter = 0, item_iter = 0;
             bool ok = true;
             for (int i = 0; ok; ++i) {
@@ -386,44 +503,55 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                 if (!ok) break;
-                const __nv_bfloat16* kb = p.k_pool + it.kvh * kD;
-                const __nv_bfloat16* vb = p.v_pool + it.kvh * kD;
-                for (int j = 0; j < it.n_kv; ++j, ++kv_iter) {
-                    const int s = kv_iter % kStages;
-                    if (lane == 0 && kv_iter >= kStages) ok = wait(&kv_empty[s], ((kv_iter / kStages) - 1) & 1);
-                    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-                    if (!ok) break;
-                    uint8_t* ks = smem + kOffK + s * kTile;
-                    uint8_t* vs = smem + kOffV + s * kTile;
-#pragma unroll 1
+                // pool rows of tokens i + 32e of tile j (kNoRow past the sequence)
+                auto resolve = [&](int j, uint32_t (&r4)[4]) {
+#pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const int r = 4 * lane + e;          // row of the tile
-                        const int tok = j * kBN + r;
-                        size_t row = 0;
-                        uint32_t nbytes = 0;
+                        const int tok = j * kBN + 32 * e + lane;
+                        r4[e] = kNoRow;
                         if (tok < it.kv_len) {
                             const int page = p.kv_indices[it.kv_base + tok / p.page_size];
-                            if (page >= 0 && static_cast<long long>(page) * p.page_size < p.pool_rows) {
-                                row = static_cast<size_t>(page) * p.page_size + tok % p.page_size;
-                                nbytes = 16;
-                            } else {
+                            if (page >= 0 && static_cast<long long>(page) * p.page_size < p.pool_rows)
+                                r4[e] = static_cast<uint32_t>(page) * p.page_size + tok % p.page_size;
+                            else
                                 flag_status(p.status, ATTN_DEV_PAGE_OUT_OF_RANGE);
-                            }
-                        }
-                        const __nv_bfloat16* ksrc = kb + row * row_elems;
-                        const __nv_bfloat16* vsrc = vb + row * row_elems;
-#pragma unroll
-                        for (int c = 0; c < 16; ++c) {
-                            const uint32_t off = (c >> 3) * kHalf + r * 128 + ((((c & 7) ^ (r & 7)) & 7) << 4);
-                            cp_async16(ks + off, ksrc + 8 * c, nbytes);
-                            cp_async16(vs + off, vsrc + 8 * c, nbytes);
                         }
                     }
-                    cp_async_mbar_arrive(&k_full[s]);
-                    cp_async_mbar_arrive(&v_full[s]);
+                };
+                uint32_t nxt[4];
+                resolve(0, nxt);
+                for (int j = 0; j < it.n_kv; ++j, ++kv_iter) {
+                    const int s = kv_iter % kStages;
+                    const uint32_t par = ((kv_iter / kStages) - 1) & 1;
+                    uint32_t cur[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) cur[e] = nxt[e];
+                    if (j + 1 < it.n_kv) resolve(j + 1, nxt);   // index loads overlap this tile's copies
+#pragma unroll 1
+                    for (int kv = 0; kv < 2 && ok; ++kv) {
+                        // K's stage frees once both S MMAs have read it, V's after both P.V
+                        if (lane == 0 && kv_iter >= kStages) ok = wait(kv == 0 ? &k_empty[s] : &v_empty[s], par);
+                        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                        if (!ok) break;
+                        const __nv_bfloat16* base = (kv == 0 ? p.k_pool : p.v_pool) + it.kvh * kD;
+                        uint8_t* dst = smem + (kv == 0 ? kOffK : kOffV) + s * kTile + lane * 128;
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const bool real = cur[e] != kNoRow;
+                            const __nv_bfloat16* src = base + (real ? static_cast<size_t>(cur[e]) * row_elems : 0);
+                            const uint32_t nb = real ? 16u : 0u;
+#pragma unroll
+                            for (int c = 0; c < 16; ++c)
+                                cp_async16(dst + e * 32 * 128 + (c >> 3) * kHalf + (((c & 7) ^ swz) << 4),
+                                           src + 8 * c, nb);
+                        }
+                        cp_async_mbar_arrive(kv == 0 ? &k_full[s] : &v_full[s]);
+                    }
+                    if (!ok) break;
                 }
                 ++item_iter;
             }
+            cp_async_wait_all();   // no copy may land after an early exit has released the CTA
         } else if (warp == kProducerWarp) {
             // ------------------------------------------------------------ TMA producer
             if (lane == 0) {
@@ -447,10 +575,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int kvrow = it.b * p.Hkv + it.kvh;
                     for (int j = 0; j < it.n_kv; ++j, ++kv_iter) {
                         const int s = kv_iter % kStages;
-                        if (kv_iter >= kStages && !(ok = wait(&kv_empty[s], ((kv_iter / kStages) - 1) & 1))) break;
+                        const uint32_t par = ((kv_iter / kStages) - 1) & 1;
+                        if (kv_iter >= kStages && !(ok = wait(&k_empty[s], par))) break;
                         mbar_arrive_expect_tx(&k_full[s], kTile);
                         tma_load_3d(smem + kOffK + s * kTile, &k_map, &k_full[s], 0, j * kBN, kvrow);
                         tma_load_3d(smem + kOffK + s * kTile + kHalf, &k_map, &k_full[s], 64, j * kBN, kvrow);
+                        if (kv_iter >= kStages && !(ok = wait(&v_empty[s], par))) break;
                         mbar_arrive_expect_tx(&v_full[s], kTile);
                         tma_load_3d(smem + kOffV + s * kTile, &v_map, &v_full[s], 0, j * kBN, kvrow);
                         tma_load_3d(smem + kOffV + s * kTile + kHalf, &v_map, &v_full[s], 64, j * kBN, kvrow);
@@ -496,6 +626,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     umma_commit(&s_full[0]);
                     issue_s(1, kv_iter % kStages);
                     umma_commit(&s_full[1]);
+                    umma_commit(&k_empty[kv_iter % kStages]);   // K_j no longer read
                     if (it.n_kv == 1) umma_commit(&q_empty);  // Q no longer read: the producer may refill it
                     for (int j = 0; j < it.n_kv && ok; ++j, ++kv_iter) {
                         const int s = kv_iter % kStages;
@@ -508,7 +639,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (j == 0 && item_iter > 0 && !(ok = wait(&o_empty[t], (item_iter - 1) & 1))) break;
                             tc_fence_after();
                             issue_pv(t, s, j > 0);                    // O_t (+)= P_t V_j
-                            if (t == 1) umma_commit(&kv_empty[s]);    // K_j, V_j no longer read
+                            if (t == 1) umma_commit(&v_empty[s]);     // V_j no longer read
                             if (!last) {
                                 if (t == 0) {
                                     if (!(ok = wait(&k_full[nxt % kStages], (nxt / kStages) & 1))) break;
@@ -517,6 +648,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 }
                                 issue_s(t, nxt % kStages);            // S_t = Q_t K_{j+1}^T (after P_t is read)
                                 umma_commit(&s_full[t]);
+                                if (t == 1) umma_commit(&k_empty[nxt % kStages]);   // K_{j+1} no longer read
                                 if (t == 1 && j + 2 == it.n_kv) umma_commit(&q_empty);  // last S read Q
                             } else {
                                 umma_commit(&o_full[t]);

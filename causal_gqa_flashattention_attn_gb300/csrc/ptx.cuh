@@ -111,6 +111,9 @@ __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc, uin
                  : "memory");
 }
 
+// Wait until all of this thread's cp.async copies have landed.
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // Arrive on an mbarrier once all of this thread's earlier cp.async copies
 // have landed (the barrier's expected count includes this arrival).
 __device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar) {

@@ -114,7 +114,8 @@ size_t attn_decode_workspace_bytes(int B, int Hq, int max_kv_len, int split_toke
  *                (NULL: every page full); kv_len_b = (pages_b - 1) *
  *                page_size + last_b                                  (read, device)
  *   o            [total_q, Hq, D] bfloat16; lse [total_q, Hq] fp32 (written; lse may be NULL)
- *   D = 128, Hq / Hkv dividing 128, B <= 2048.
+ *   D = 128, Hq / Hkv dividing 128, B <= 2048, total_q < 2^22 and
+ *   (total_q + B) * Hkv < 2^31 (ATTN_ERR_UNSUPPORTED otherwise).
  * A page id outside [0, num_pages) sets ATTN_DEV_PAGE_OUT_OF_RANGE and is
  * read as zeros.
  */

@@ -97,6 +97,74 @@ def test_decode_host_validation(L):
     assert _decode(L, ws_bytes=16) == -3
 
 
+def _varlen(L, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, qo=FAKE, kvp=FAKE, kvi=FAKE, last=None, o=FAKE, lse=None, B=2, Hq=32, Hkv=4,
+             D=128, total_q=100, num_pages=64, page_size=1, scale=0.1, status=None, stream=None)
+    a.update(kw)
+    return L.attn_prefill_paged_varlen(a["q"], a["k"], a["v"], a["qo"], a["kvp"], a["kvi"], a["last"], a["o"],
+                                       a["lse"], a["B"], a["Hq"], a["Hkv"], a["D"], a["total_q"], a["num_pages"],
+                                       a["page_size"], a["scale"], a["status"], a["stream"])
+
+
+def test_varlen_host_validation(L):
+    assert _varlen(L, qo=None) == -1
+    assert _varlen(L, kvi=None) == -1
+    assert _varlen(L, B=0) == -1
+    assert _varlen(L, total_q=-1) == -1
+    assert _varlen(L, page_size=0) == -1
+    assert _varlen(L, Hq=30, Hkv=4) == -1                 # Hq % Hkv != 0
+    assert _varlen(L, scale=float("inf")) == -1
+    assert _varlen(L, o=ctypes.c_void_p(0x10008)) == -1   # misaligned
+    assert _varlen(L, D=64) == -2
+    assert _varlen(L, Hq=24, Hkv=8) == -2                 # group of 3 does not divide 128
+    assert _varlen(L, B=2049) == -2                       # prefix table holds 2048 sequences
+    assert _varlen(L, total_q=1 << 22) == -2              # query block index packed in 21 bits
+    assert _varlen(L, Hq=1024, Hkv=1024, total_q=(1 << 21) + 1) == -2   # item count overflows int
+    assert _varlen(L, num_pages=1 << 30, page_size=4) == -2
+    assert _varlen(L, total_q=0) == 0                     # nothing to do, nothing launched
+
+
+def _decode_mq(L, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, table=FAKE, max_pages=4, lens=FAKE, kv_dtype=1, ng=1, B=2, Hq=32, Hkv=8,
+             q_len=4, D=128, num_pages=8, page_size=256, split=2048, max_len=1024, scale=0.1, ws=FAKE,
+             ws_bytes=1 << 30, o=FAKE, lse=None, status=None, stream=None)
+    a.update(kw)
+    return L.attn_decode_paged_splitk_mq(a["q"], a["k"], a["v"], a["table"], a["max_pages"], a["lens"],
+                                         a["kv_dtype"], a["ng"], a["B"], a["Hq"], a["Hkv"], a["q_len"], a["D"],
+                                         a["num_pages"], a["page_size"], a["split"], a["max_len"], a["scale"],
+                                         a["ws"], a["ws_bytes"], a["o"], a["lse"], a["status"], a["stream"])
+
+
+def test_decode_mq_host_validation(L):
+    assert _decode_mq(L, q_len=0) == -1
+    assert _decode_mq(L, q_len=17) == -2                 # at most 16 query rows per sequence
+    assert _decode_mq(L, Hq=12, Hkv=8) == -1
+    assert _decode_mq(L, kv_dtype=4) == -1               # fp8 needs its scale/shift tensors
+    # workspace rows scale with q_len: [B, Hq * q_len, S, D] + [B, Hq * q_len, S]
+    import causal_gqa_flashattention_attn_gb300 as attn
+    need = attn.attn_decode_workspace_bytes(2, 32 * 4, 1024, 2048, 128)
+    assert _decode_mq(L, ws_bytes=need - 16) == -3
+
+
+def _decode_fp8(L, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, ks=FAKE, vs=FAKE, table=FAKE, max_pages=4, lens=FAKE, B=2, Hq=32, Hkv=8,
+             q_len=1, D=128, num_pages=8, page_size=256, split=2048, max_len=1024, scale=0.1, ws=FAKE,
+             ws_bytes=1 << 30, o=FAKE, lse=None, status=None, stream=None)
+    a.update(kw)
+    return L.attn_decode_paged_splitk_fp8(a["q"], a["k"], a["v"], a["ks"], a["vs"], a["table"], a["max_pages"],
+                                          a["lens"], a["B"], a["Hq"], a["Hkv"], a["q_len"], a["D"],
+                                          a["num_pages"], a["page_size"], a["split"], a["max_len"], a["scale"],
+                                          a["ws"], a["ws_bytes"], a["o"], a["lse"], a["status"], a["stream"])
+
+
+def test_decode_fp8_host_validation(L):
+    assert _decode_fp8(L, ks=None) == -1
+    assert _decode_fp8(L, vs=ctypes.c_void_p(0x10004)) == -1   # misaligned scale/shift
+    assert _decode_fp8(L, Hq=8, Hkv=2) == -2                   # coefficient box needs Hkv % 4 == 0
+    assert _decode_fp8(L, page_size=32) == -2
+    assert _decode_fp8(L, ws=None) == -3
+
+
 def test_workspace_bytes(L):
     import causal_gqa_flashattention_attn_gb300 as attn
     # [B, Hq, S, D] + [B, Hq, S] floats, each rounded to 16 bytes; S = ceil(32768 / 2048) = 16

@@ -64,3 +64,58 @@ def test_varlen_bench_workload_sampled():
                                                      inp["v_cache"].double().numpy(), sub_qo, sub_kvp, sub_idx, 1)
         check_o(o[qo[b]:qo[b + 1]], o_ref, what=f"O seq {b}")
         check_lse(lse[qo[b]:qo[b + 1]], lse_ref, what=f"LSE seq {b}")
+
+
+def _run(attn, inp, dev):
+    t = {k: v.to(dev) for k, v in inp.items() if torch.is_tensor(v)}
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    o, lse = attn.attn_prefill_paged_varlen(t["q"], t["k_cache"], t["v_cache"], t["qo_indptr"], t["kv_indptr"],
+                                            t["kv_indices"], t["kv_last_page_len"], dev_status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    return o, lse
+
+
+def _check_seq(inp, o, lse, b, ps, pools):
+    qo = inp["qo_indptr"].tolist()
+    kvp = inp["kv_indptr"].tolist()
+    o_ref, lse_ref = oracle.prefill_paged_varlen(
+        inp["q"][qo[b]:qo[b + 1]].double().numpy(), pools[0], pools[1], np.array([0, qo[b + 1] - qo[b]]),
+        np.array([0, kvp[b + 1] - kvp[b]]), inp["kv_indices"][kvp[b]:kvp[b + 1]].numpy(), ps,
+        inp["kv_last_page_len"][b:b + 1].numpy())
+    check_o(o[qo[b]:qo[b + 1]], o_ref, what=f"O seq {b}")
+    check_lse(lse[qo[b]:qo[b + 1]], lse_ref, what=f"LSE seq {b}")
+
+
+def test_varlen_many_short_sequences():
+    """300 sequences of mixed short lengths: many work items share a KV tile
+    count, so the longest-first order has long runs of ties; every sequence
+    is checked."""
+    dev = gpu_or_skip()
+    import causal_gqa_flashattention_attn_gb300 as attn
+    g = torch.Generator().manual_seed(11)
+    q_lens = torch.randint(1, 100, (300,), generator=g).tolist()
+    kv_lens = [q + int(x) for q, x in zip(q_lens, torch.randint(0, 300, (300,), generator=g))]
+    shape = synth.VarlenShape("t", len(q_lens), 16, 2, 128, 1, 1, 0, 0, page_size=16)
+    inp = synth.varlen_inputs(shape, seed=5, q_lens=q_lens, kv_lens=kv_lens)
+    o, lse = _run(attn, inp, dev)
+    pools = (inp["k_cache"].double().numpy(), inp["v_cache"].double().numpy())
+    for b in range(len(q_lens)):
+        _check_seq(inp, o, lse, b, 16, pools)
+
+
+def test_varlen_over_the_sorted_list_capacity():
+    """2048 sequences of 65 new tokens (3 query blocks each at G = 8: 6144
+    pairs, more than the 4096 the sorted work list holds), so the kernel walks
+    the items in sequence order; sampled sequences are checked."""
+    dev = gpu_or_skip()
+    import causal_gqa_flashattention_attn_gb300 as attn
+    B = 2048
+    q_lens = [65] * B
+    kv_lens = [65 + (b * 7) % 40 for b in range(B)]
+    shape = synth.VarlenShape("t", B, 8, 1, 128, 1, 1, 0, 0, page_size=1)
+    inp = synth.varlen_inputs(shape, seed=6, q_lens=q_lens, kv_lens=kv_lens)
+    o, lse = _run(attn, inp, dev)
+    pools = (inp["k_cache"].double().numpy(), inp["v_cache"].double().numpy())
+    for b in list(range(0, B, 97)) + [B - 1]:
+        _check_seq(inp, o, lse, b, 1, pools)
