@@ -245,6 +245,9 @@ def run_ours(args, rank, world, dist):
 
     kernels = ["prefill", "prefill_batched", "decode_bf16", "merge_bf16", "decode_int4", "merge_int4", "merge_bwd",
                "decode_mq", "decode_fp8", "prefill_varlen"]
+    # the method's own steps (dense prefill, paged split-K decode, merge); the
+    # other legs are the widened rows (merge backward, multi-query, fp8, ragged)
+    hot = ["prefill", "prefill_batched", "decode_bf16", "merge_bf16", "decode_int4", "merge_int4"]
     # ragged prefill over a page-size-1 cache (8 sequences)
     vl = synth.VARLEN_PAGED_PREFILL
     inpv = synth.varlen_inputs(vl, seed=seed)
@@ -443,8 +446,8 @@ def run_ours(args, rank, world, dist):
         kernels_out.append({"name": kn, "kernel": r["kernel"], "ms": round(ms[kn], 5), "bound": r["bound"],
                             "achieved": round(r["achieved"], 2), "peak": r["peak"], "unit": r["unit"],
                             "frac": round(r["achieved"] / r["peak"], 4),
-                            "traffic": traffic.get(kn)})
-    dominant = max(kernels, key=lambda kn: ms[kn])
+                            "traffic": traffic.get(kn), "row": "hot path" if kn in hot else "widened"})
+    dominant = max(hot, key=lambda kn: ms[kn])
     dom = rep[dominant]
     path = {}
     for name in ("decode_bf16", "decode_int4"):
@@ -467,7 +470,8 @@ def run_ours(args, rank, world, dist):
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": round(sum(ms.values()), 5),
+        "ms_per_step": round(sum(ms[kn] for kn in hot), 5),
+        "ms_widened_rows_per_step": round(sum(ms[kn] for kn in kernels if kn not in hot), 5),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
