@@ -174,21 +174,27 @@ __global__ void __launch_bounds__(kThreads, (R > 8) ? 1 : 3) decode_fp8_kernel(
         const bool real = (rr == 0 || kTwoRows) && row < n_rows;
         const __nv_bfloat16* qrow = p.q + out_row(real ? row : 0) * kD;
         lim[rr] = real ? len - p.nq + (first_row + row) / p.G : -1;
+        // the quad's four lanes hold all D elements between them: the row sum
+        // of q is a quad reduction of the fragment values
         float qs = 0.f;
-        if (real)
-            for (int e = 0; e < kD; ++e) qs += __bfloat162float(qrow[e]);
-        qsum[rr] = qs;
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
             const int e0 = 4 * (8 * t4 + ks);
             uint32_t lo_pair = 0u, hi_pair = 0u;
             if (real) {
-                lo_pair = pack_f16x2(__bfloat162float(qrow[e0]), __bfloat162float(qrow[e0 + 1]));
-                hi_pair = pack_f16x2(__bfloat162float(qrow[e0 + 2]), __bfloat162float(qrow[e0 + 3]));
+                const uint2 x = *reinterpret_cast<const uint2*>(qrow + e0);   // elements e0 .. e0+3
+                const float2 f01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&x.x));
+                const float2 f23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&x.y));
+                lo_pair = pack_f16x2(f01.x, f01.y);
+                hi_pair = pack_f16x2(f23.x, f23.y);
+                qs += (f01.x + f01.y) + (f23.x + f23.y);
             }
             qa[ks][rr] = lo_pair;       // a0 / a1: k = 2t, 2t+1
             qa[ks][rr + 2] = hi_pair;   // a2 / a3: k = 2t+8, 2t+9
         }
+        qs += __shfl_xor_sync(0xffffffffu, qs, 1);
+        qs += __shfl_xor_sync(0xffffffffu, qs, 2);
+        qsum[rr] = qs;
     }
     if (!kTwoRows) {
 #pragma unroll

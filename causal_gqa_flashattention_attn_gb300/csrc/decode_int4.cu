@@ -154,7 +154,9 @@ __global__ void __launch_bounds__(kThreads, (R > 8) ? 1 : 3) decode_int4_kernel(
 
     // ------------------------------------------------------------ consumers
     const int g = lane >> 2, t4 = lane & 3;
-    // Q fragments in the nibble order of the K operand, and per-group sums of q.
+    // Q fragments in the nibble order of the K operand, and per-group sums of q
+    // (the four lanes of a quad hold every element of a group once between
+    // them, so a group's sum is a quad reduction of the fragment values).
     uint32_t qa[NG][KS][4];
     float qsum[NG][2];
     int lim[2];   // each row's last visible token (bottom-right causal: len - q_len + i)
@@ -168,29 +170,32 @@ __global__ void __launch_bounds__(kThreads, (R > 8) ? 1 : 3) decode_int4_kernel(
 #pragma unroll
             for (int gr = 0; gr < NG; ++gr) {
                 float qs = 0.f;
-                if (real) {
-                    for (int e = 0; e < E; ++e) qs += __bfloat162float(qrow[gr * E + e]);
-                }
-                qsum[gr][rr] = qs;
 #pragma unroll
                 for (int ks = 0; ks < KS; ++ks) {
                     int word, j0;
                     k_word_of<NG>(t4, ks, word, j0);
-                    const int e0 = gr * E + 8 * word + j0;  // element of nibble j0
+                    const int e0 = gr * E + 8 * word + j0;  // element of nibble j0 (even)
                     uint32_t lo_pair = 0u, hi_pair = 0u;
                     if (real) {
-                        const __nv_bfloat16* qr = qrow;
-                        __nv_bfloat162 a = __halves2bfloat162(qr[e0], qr[e0 + 4]);
-                        __nv_bfloat162 c = __halves2bfloat162(qr[e0 + 1], qr[e0 + 5]);
-                        lo_pair = *reinterpret_cast<uint32_t*>(&a);
-                        hi_pair = *reinterpret_cast<uint32_t*>(&c);
+                        const uint32_t x0 = *reinterpret_cast<const uint32_t*>(qrow + e0);      // e0, e0+1
+                        const uint32_t x4 = *reinterpret_cast<const uint32_t*>(qrow + e0 + 4);  // e0+4, e0+5
+                        lo_pair = __byte_perm(x0, x4, 0x5410);   // (e0, e0+4)
+                        hi_pair = __byte_perm(x0, x4, 0x7632);   // (e0+1, e0+5)
+                        const float2 fl = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&lo_pair));
+                        const float2 fh = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hi_pair));
+                        qs += (fl.x + fl.y) + (fh.x + fh.y);
                     }
                     qa[gr][ks][rr] = lo_pair;        // a0 (row g) / a1 (row g+8): k = 2t, 2t+1
                     qa[gr][ks][rr + 2] = hi_pair;    // a2 / a3: k = 2t+8, 2t+9
                 }
+                qs += __shfl_xor_sync(0xffffffffu, qs, 1);
+                qs += __shfl_xor_sync(0xffffffffu, qs, 2);
+                qsum[gr][rr] = qs;
             }
         }
     }
+    // smallest causal limit over this CTA's rows (rows are ordered by query)
+    const int lim_min = len - p.nq + first_row / p.G;
     constexpr int kRows = kTwoRows ? 2 : 1;
     constexpr int MT = E / 16;                 // 16-row m-tiles of O^T per group
     // O^T accumulators: [head tile of 8][m-tile of 16 head-dim rows][fragment]
@@ -209,7 +214,8 @@ __global__ void __launch_bounds__(kThreads, (R > 8) ? 1 : 3) decode_int4_kernel(
     float l_part[2] = {0.f, 0.f};
     const float sl2 = p.scale_log2;
     // this warp's fp32 coefficient table for its 16 tokens of the current tile:
-    // [0] K scale, [1] K offset - 128 * K scale, [2] V scale, [3] V offset; [kind][group][token]
+    // [0] K scale, [1] K offset - 128 * K scale (both times log2 e * softmax scale),
+    // [2] V scale, [3] V offset; [kind][group][token]
     float* cf = reinterpret_cast<float*>(smem + NS * kStageBytes) + warp * (4 * NG * 16);
 
     for (int t = 0; t < n_tiles; ++t) {
@@ -233,8 +239,8 @@ __global__ void __launch_bounds__(kThreads, (R > 8) ? 1 : 3) decode_int4_kernel(
                 const uint32_t cw = (kv == 0 ? kt : vt)[(warp * 16 + tok) * BW + gr];
                 const bool ok = tok < n_valid;
                 const float sc = ok ? lo_half(cw) : 0.f, of = ok ? hi_half(cw) : 0.f;
-                cf[((2 * kv) * NG + gr) * 16 + tok] = sc;
-                cf[((2 * kv + 1) * NG + gr) * 16 + tok] = kv == 0 ? fmaf(-128.f, sc, of) : of;
+                cf[((2 * kv) * NG + gr) * 16 + tok] = kv == 0 ? sc * sl2 : sc;
+                cf[((2 * kv + 1) * NG + gr) * 16 + tok] = kv == 0 ? fmaf(-128.f, sc, of) * sl2 : of;
             }
             __syncwarp();
             // ---- scores in code space: per group T_g = sum_d q (128 + c), then
@@ -267,6 +273,7 @@ __global__ void __launch_bounds__(kThreads, (R > 8) ? 1 : 3) decode_int4_kernel(
                     }
                 }
             }
+            // scores are already in the exp2 domain (the table carries log2(e) * scale)
             float s[2][4];
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
@@ -274,11 +281,16 @@ __global__ void __launch_bounds__(kThreads, (R > 8) ? 1 : 3) decode_int4_kernel(
                 s[nt][1] = s2[nt][0].y;
                 s[nt][2] = kTwoRows ? s2[nt][kRows - 1].x : 0.f;
                 s[nt][3] = kTwoRows ? s2[nt][kRows - 1].y : 0.f;
+            }
+            // mask only sub-tiles that reach past the split end or some row's causal limit
+            if (n_valid < 16 || tok0 + 15 > lim_min) {
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int tok = nt * 8 + 2 * t4 + (e & 1);
-                    s[nt][e] = (tok < n_valid && tok0 + tok <= lim[e >> 1]) ? s[nt][e] * sl2 : -INFINITY;
-                }
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int tok = nt * 8 + 2 * t4 + (e & 1);
+                        if (!(tok < n_valid && tok0 + tok <= lim[e >> 1])) s[nt][e] = -INFINITY;
+                    }
             }
             // ---- online softmax (same as the bf16 path)
             float pv[2][4];   // [row][token slot: 2t, 2t+1, 2t+8, 2t+9]
