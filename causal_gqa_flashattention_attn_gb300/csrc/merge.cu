@@ -24,6 +24,68 @@ __device__ __forceinline__ void store4(__nv_bfloat16* o, float4 v) {
     *reinterpret_cast<uint2*>(o) = u;
 }
 
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+    return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    return v;
+}
+
+constexpr int kBatch = 8;   // splits whose loads are in flight together
+
+// Weighted sum over the splits of lane chunk `d` of a row: lane j of each
+// block of 32 splits holds the weight of split s0 + j; loads of kBatch splits
+// are issued together, and splits of weight 0 (LSE = -inf) are not read.
+__device__ __forceinline__ float4 weighted_sum(const float* op, const float* lp, int S, int D, int d, float mx,
+                                               int lane) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < S; s0 += 32) {
+        const int s = s0 + lane;
+        const float l = s < S ? lp[s] : -INFINITY;
+        const float w = (l == -INFINITY) ? 0.f : expf(l - mx);
+        const int n = min(32, S - s0);
+        for (int j0 = 0; j0 < n; j0 += kBatch) {
+            float wj[kBatch];
+            float4 v[kBatch];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                wj[u] = __shfl_sync(0xffffffffu, w, (j0 + u) & 31);
+                const bool take = (j0 + u < n) && wj[u] != 0.f && d < D;
+                v[u] = take ? ld4(op + static_cast<size_t>(s0 + j0 + u) * D + d) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                acc.x = fmaf(wj[u], v[u].x, acc.x);
+                acc.y = fmaf(wj[u], v[u].y, acc.y);
+                acc.z = fmaf(wj[u], v[u].z, acc.z);
+                acc.w = fmaf(wj[u], v[u].w, acc.w);
+            }
+        }
+    }
+    return acc;
+}
+
+// max partial LSE and sum of the weights exp(LSE_s - max) of a row
+__device__ __forceinline__ void row_weights(const float* lp, int S, int lane, float& mx, float& wsum) {
+    mx = -INFINITY;
+    for (int s = lane; s < S; s += 32) mx = fmaxf(mx, lp[s]);
+    mx = warp_max(mx);
+    wsum = 0.f;
+    if (mx != -INFINITY)
+        for (int s = lane; s < S; s += 32) {
+            const float l = lp[s];
+            if (l != -INFINITY) wsum += expf(l - mx);
+        }
+    wsum = warp_sum(wsum);
+}
+
 template <typename OutT>
 __global__ void __launch_bounds__(32 * kWarps) lse_merge_kernel(const float* __restrict__ o_part,
                                                                 const float* __restrict__ lse_part, int N, int S,
@@ -32,42 +94,16 @@ __global__ void __launch_bounds__(32 * kWarps) lse_merge_kernel(const float* __r
     const int lane = threadIdx.x & 31;
     if (row >= N) return;
     const float* lp = lse_part + static_cast<size_t>(row) * S;
-    float mx = -INFINITY;
-    for (int s = lane; s < S; s += 32) mx = fmaxf(mx, lp[s]);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-
-    float4 acc[kMaxChunks];
-#pragma unroll
-    for (int c = 0; c < kMaxChunks; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-    float wsum = 0.f;
-    if (mx != -INFINITY) {
-        const float* op = o_part + static_cast<size_t>(row) * S * D;
-        for (int s = 0; s < S; ++s) {
-            const float l = lp[s];
-            if (l == -INFINITY) continue;
-            const float w = expf(l - mx);
-            wsum += w;
-#pragma unroll
-            for (int c = 0; c < kMaxChunks; ++c) {
-                const int d = 4 * (lane + 32 * c);
-                if (d < D) {
-                    const float4 v = *reinterpret_cast<const float4*>(op + static_cast<size_t>(s) * D + d);
-                    acc[c].x += w * v.x;
-                    acc[c].y += w * v.y;
-                    acc[c].z += w * v.z;
-                    acc[c].w += w * v.w;
-                }
-            }
-        }
-    }
+    const float* op = o_part + static_cast<size_t>(row) * S * D;
+    float mx, wsum;
+    row_weights(lp, S, lane, mx, wsum);
     const bool alive = mx != -INFINITY;
     const float inv = alive ? 1.f / wsum : 0.f;
     OutT* orow = o + static_cast<size_t>(row) * D;
-#pragma unroll
-    for (int c = 0; c < kMaxChunks; ++c) {
+    for (int c = 0; c < kMaxChunks && 128 * c < D; ++c) {
         const int d = 4 * (lane + 32 * c);
-        if (d < D) store4(orow + d, make_float4(acc[c].x * inv, acc[c].y * inv, acc[c].z * inv, acc[c].w * inv));
+        const float4 acc = alive ? weighted_sum(op, lp, S, D, d, mx, lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+        if (d < D) store4(orow + d, make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
     }
     if (lse != nullptr && lane == 0) lse[row] = alive ? mx + logf(wsum) : -INFINITY;
 }
@@ -76,7 +112,8 @@ __global__ void __launch_bounds__(32 * kWarps) lse_merge_kernel(const float* __r
 // with w_s = exp(LSE_s - LSE) the weight of split s,
 //   dO_s = w_s * dO,   dLSE_s = w_s * dLSE + sum_d (O_s - O)_d * w_s * dO_d.
 // The merged O and LSE are recomputed here from the partials (fp32), so the
-// caller needs to keep only the partials.  One warp per row.
+// caller needs to keep only the partials.  One warp per row; the splits go in
+// batches whose loads are in flight together.
 __global__ void __launch_bounds__(32 * kWarps) lse_merge_bwd_kernel(
     const float* __restrict__ o_part, const float* __restrict__ lse_part, const float* __restrict__ d_o,
     const float* __restrict__ d_lse, int N, int S, int D, float* __restrict__ d_o_part,
@@ -88,71 +125,56 @@ __global__ void __launch_bounds__(32 * kWarps) lse_merge_bwd_kernel(
     const float* op = o_part + static_cast<size_t>(row) * S * D;
     float* dop = d_o_part + static_cast<size_t>(row) * S * D;
     float* dlp = d_lse_part + static_cast<size_t>(row) * S;
-    float mx = -INFINITY;
-    for (int s = lane; s < S; s += 32) mx = fmaxf(mx, lp[s]);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    float mx, wsum;
+    row_weights(lp, S, lane, mx, wsum);
+    const bool alive = mx != -INFINITY;
+    const float inv = alive ? 1.f / wsum : 0.f;
     float4 o[kMaxChunks], g[kMaxChunks];
-    float wsum = 0.f;
 #pragma unroll
     for (int c = 0; c < kMaxChunks; ++c) {
-        o[c] = make_float4(0.f, 0.f, 0.f, 0.f);
         const int d = 4 * (lane + 32 * c);
-        g[c] = d < D ? *reinterpret_cast<const float4*>(d_o + static_cast<size_t>(row) * D + d)
-                     : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    const bool alive = mx != -INFINITY;
-    if (alive) {
-        for (int s = 0; s < S; ++s) {
-            const float l = lp[s];
-            if (l == -INFINITY) continue;
-            const float w = expf(l - mx);
-            wsum += w;
-#pragma unroll
-            for (int c = 0; c < kMaxChunks; ++c) {
-                const int d = 4 * (lane + 32 * c);
-                if (d < D) {
-                    const float4 v = *reinterpret_cast<const float4*>(op + static_cast<size_t>(s) * D + d);
-                    o[c].x += w * v.x;
-                    o[c].y += w * v.y;
-                    o[c].z += w * v.z;
-                    o[c].w += w * v.w;
-                }
-            }
-        }
-        const float inv = 1.f / wsum;
-#pragma unroll
-        for (int c = 0; c < kMaxChunks; ++c) {
-            o[c].x *= inv;
-            o[c].y *= inv;
-            o[c].z *= inv;
-            o[c].w *= inv;
+        g[c] = d < D ? ld4(d_o + static_cast<size_t>(row) * D + d) : make_float4(0.f, 0.f, 0.f, 0.f);
+        o[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (alive && 128 * c < D) {
+            const float4 a = weighted_sum(op, lp, S, D, d, mx, lane);
+            o[c] = make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
         }
     }
     const float lse = alive ? mx + logf(wsum) : -INFINITY;
     const float dl = (d_lse != nullptr) ? d_lse[row] : 0.f;
-    for (int s = 0; s < S; ++s) {
-        const float l = lp[s];
-        const bool live = alive && l != -INFINITY;
-        const float w = live ? expf(l - lse) : 0.f;
-        float dot = 0.f;
+    for (int s0 = 0; s0 < S; s0 += kBatch) {
+        float w[kBatch], dot[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int s = s0 + u;
+            const float l = s < S ? lp[s] : -INFINITY;
+            w[u] = (alive && l != -INFINITY) ? expf(l - lse) : 0.f;
+            dot[u] = 0.f;
+        }
 #pragma unroll
         for (int c = 0; c < kMaxChunks; ++c) {
             const int d = 4 * (lane + 32 * c);
-            if (d < D) {
-                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (live) {
-                    v = *reinterpret_cast<const float4*>(op + static_cast<size_t>(s) * D + d);
-                    dot += (v.x - o[c].x) * g[c].x + (v.y - o[c].y) * g[c].y + (v.z - o[c].z) * g[c].z +
-                           (v.w - o[c].w) * g[c].w;
-                }
-                *reinterpret_cast<float4*>(dop + static_cast<size_t>(s) * D + d) =
-                    make_float4(w * g[c].x, w * g[c].y, w * g[c].z, w * g[c].w);
+            if (128 * c >= D) break;
+            float4 v[kBatch];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const bool take = w[u] != 0.f && d < D;
+                v[u] = take ? ld4(op + static_cast<size_t>(s0 + u) * D + d) : o[c];
+            }
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                dot[u] += (v[u].x - o[c].x) * g[c].x + (v[u].y - o[c].y) * g[c].y + (v[u].z - o[c].z) * g[c].z +
+                          (v[u].w - o[c].w) * g[c].w;
+                if (s0 + u < S && d < D)
+                    *reinterpret_cast<float4*>(dop + static_cast<size_t>(s0 + u) * D + d) =
+                        make_float4(w[u] * g[c].x, w[u] * g[c].y, w[u] * g[c].z, w[u] * g[c].w);
             }
         }
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
-        if (lane == 0) dlp[s] = w * (dl + dot);
+        for (int u = 0; u < kBatch; ++u) {
+            const float t = warp_sum(dot[u]);
+            if (lane == 0 && s0 + u < S) dlp[s0 + u] = w[u] * (dl + t);
+        }
     }
 }
 
