@@ -38,8 +38,8 @@ ATTN_DEV_WAIT_TIMEOUT = 0x4
 
 EXPORTED = ("attn_prefill_fwd", "attn_prefill_paged_varlen", "attn_decode_workspace_bytes", "attn_decode_paged_splitk", "attn_decode_paged_splitk_mq",
             "attn_decode_paged_splitk_fp8",
-            "attn_decode_paged_splitk_static", "attn_lse_merge", "attn_lse_merge_bwd", "attn_status_string",
-            "attn_abi_version")
+            "attn_decode_paged_splitk_static", "attn_lse_merge", "attn_lse_merge_bwd", "attn_selftest_wait_timeout",
+            "attn_status_string", "attn_abi_version")
 ATTN_DECODE_STATIC_SCRATCH_BYTES = 32 << 20
 
 _lib = None
@@ -84,6 +84,8 @@ def lib():
     L.attn_lse_merge.restype = i32
     L.attn_lse_merge_bwd.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp, vp, vp]
     L.attn_lse_merge_bwd.restype = i32
+    L.attn_selftest_wait_timeout.argtypes = [vp, ctypes.c_uint, vp]
+    L.attn_selftest_wait_timeout.restype = i32
     L.attn_status_string.argtypes = [i32]
     L.attn_status_string.restype = ctypes.c_char_p
     L.attn_abi_version.argtypes = []
@@ -94,6 +96,16 @@ def lib():
 
 def attn_status_string(status):
     return lib().attn_status_string(int(status)).decode()
+
+
+def attn_selftest_wait_timeout(dev_status, limit_us=20000, stream=None):
+    """Run one bounded wait that nothing satisfies; ``ATTN_DEV_WAIT_TIMEOUT``
+    is OR-ed into ``dev_status`` (int32 CUDA tensor) after ``limit_us``."""
+    _need_cuda(dev_status)
+    if dev_status.dtype != torch.int32:
+        raise ValueError("dev_status must be int32")
+    _check("attn_selftest_wait_timeout",
+           lib().attn_selftest_wait_timeout(_ptr(dev_status), int(limit_us), _stream_ptr(stream)))
 
 
 def _ptr(t):

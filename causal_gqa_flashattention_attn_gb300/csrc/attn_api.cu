@@ -150,7 +150,13 @@ const char* attn_status_string(attn_status_t status) {
     }
 }
 
-int attn_abi_version(void) { return 100; }
+int attn_abi_version(void) { return 101; }
+
+attn_status_t attn_selftest_wait_timeout(int32_t* dev_status, unsigned int limit_us, void* stream) {
+    if (dev_status == nullptr || limit_us == 0 || limit_us > 1000000u) return ATTN_ERR_INVALID_ARG;
+    return from_cuda(launch_wait_timeout_selftest(dev_status, static_cast<uint64_t>(limit_us) * 1000u,
+                                                  static_cast<cudaStream_t>(stream)));
+}
 
 attn_status_t attn_prefill_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                                attn_dtype_t dtype, int B, int Hq, int Hkv, int q_len, int kv_len, int D,

@@ -59,6 +59,8 @@ cudaError_t launch_decode_fp8(const DecodeArgs& a, const void* k_scale_shift, co
                               cudaStream_t stream);
 int rows_per_cta(const DecodeArgs& a);
 
+cudaError_t launch_wait_timeout_selftest(int32_t* status, uint64_t limit_ns, cudaStream_t stream);
+
 cudaError_t launch_merge(const float* o_part, const float* lse_part, int N, int S, int D, void* o,
                          float* lse, int o_dtype, cudaStream_t stream);
 cudaError_t launch_merge_bwd(const float* o_part, const float* lse_part, const float* d_o, const float* d_lse, int N,

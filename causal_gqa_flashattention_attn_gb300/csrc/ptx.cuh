@@ -66,16 +66,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Waits for the phase with the given parity to complete.  Returns false if
-// the wait ran out, or if `abort` (a shared flag another role raises when it
-// gives up) becomes non-zero; the caller must then record the failure and stop.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const int* abort = nullptr) {
+// the wait ran out (after limit_ns of device time), or if `abort` (a shared
+// flag another role raises when it gives up) becomes non-zero; the caller
+// must then record the failure and stop.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const int* abort = nullptr,
+                                          uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     for (uint32_t i = 1; i != 0; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 63u) == 0) {
             if (abort != nullptr && *reinterpret_cast<const volatile int*>(abort) != 0) return false;
-            if (global_ns() - t0 > kWaitLimitNs) return false;
+            if (global_ns() - t0 > limit_ns) return false;
         }
     }
     return false;

@@ -289,10 +289,26 @@ attn_status_t attn_lse_merge_bwd(const float* o_part, const float* lse_part, con
                                  const float* d_lse, int N, int S, int D,
                                  float* d_o_part, float* d_lse_part, void* stream);
 
+/*
+ * attn_selftest_wait_timeout - check that a pipeline wait which is never
+ * satisfied ends with a status, not a hang.
+ *
+ * Launches one thread that waits, with the bounded mbarrier wait all the
+ * kernels above use, on a barrier nothing arrives on.  After limit_us
+ * microseconds of device time the wait gives up, ATTN_DEV_WAIT_TIMEOUT is
+ * OR-ed into *dev_status and the kernel returns; the CUDA context stays
+ * usable.  (The library's own kernels give up after 4 s.)
+ *
+ *   dev_status  int32 on the device (written; required)
+ *   limit_us    1 .. 1000000
+ * ATTN_ERR_INVALID_ARG for a NULL status word or a limit out of range.
+ */
+attn_status_t attn_selftest_wait_timeout(int32_t* dev_status, unsigned int limit_us, void* stream);
+
 /* Static, human-readable name of a status code. */
 const char* attn_status_string(attn_status_t status);
 
-/* ABI version of this header (major * 100 + minor). */
+/* ABI version of this header (major * 100 + minor); 101 added attn_selftest_wait_timeout. */
 int attn_abi_version(void);
 
 #ifdef __cplusplus

@@ -38,7 +38,7 @@ def test_library_exports_every_declared_symbol(L):
     for name in declared_functions():
         assert hasattr(L, name), name
         assert name in attn.EXPORTED
-    assert L.attn_abi_version() == 100
+    assert L.attn_abi_version() == 101
 
 
 def test_status_strings(L):
@@ -179,6 +179,12 @@ def test_merge_host_validation(L):
     assert L.attn_lse_merge(FAKE, FAKE, 4, 2, 130, FAKE, None, 0, None) == -1
     assert L.attn_lse_merge(FAKE, FAKE, 4, 2, 2048, FAKE, None, 0, None) == -2
     assert L.attn_lse_merge(FAKE, FAKE, 4, 2, 128, FAKE, None, 2, None) == -2
+
+
+def test_selftest_host_validation(L):
+    assert L.attn_selftest_wait_timeout(None, 1000, None) == -1
+    assert L.attn_selftest_wait_timeout(FAKE, 0, None) == -1
+    assert L.attn_selftest_wait_timeout(FAKE, 1000001, None) == -1
 
 
 def test_merge_bwd_host_validation(L):
