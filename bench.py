@@ -244,7 +244,7 @@ def run_ours(args, rank, world, dist):
     status = torch.zeros(1, dtype=torch.int32, device=dev)
 
     kernels = ["prefill", "prefill_batched", "decode_bf16", "merge_bf16", "decode_int4", "merge_int4", "merge_bwd",
-               "decode_mq", "decode_fp8", "prefill_varlen"]
+               "decode_mq", "decode_fp8", "prefill_varlen", "prefill_varlen_ws"]
     # the method's own steps (dense prefill, paged split-K decode, merge); the
     # other legs are the widened rows (merge backward, multi-query, fp8, ragged)
     hot = ["prefill", "prefill_batched", "decode_bf16", "merge_bf16", "decode_int4", "merge_int4"]
@@ -255,6 +255,8 @@ def run_ours(args, rank, world, dist):
     vl_flops = sum(2 * vl.Hq * vl.D * visible_pairs(ql, kl) * 2 for ql, kl in zip(inpv["q_lens"], inpv["kv_lens"]))
     vo = torch.empty_like(tv["q"])
     vlse = torch.empty(tv["q"].shape[0], vl.Hq, dtype=torch.float32, device=dev)
+    v_rows = inpv["k_cache"].shape[0] * vl.page_size
+    vws = torch.empty(attn.attn_prefill_varlen_workspace_bytes(v_rows, vl.Hkv, vl.D), dtype=torch.uint8, device=dev)
     # fp8 e4m3 row-wise cache on the int4 workload's shape
     d8 = synth.PAGED_DECODE_FP8
     inp8 = synth.decode_inputs(d8, seed=seed)
@@ -276,7 +278,7 @@ def run_ours(args, rank, world, dist):
     mb_dlse = torch.randn(mbw["lse"].shape, generator=gmb).to(dev)
     mb_go = torch.empty_like(mbw["o_part"])
     mb_gl = torch.empty_like(mbw["lse_part"])
-    launches_per_step = len(kernels)
+    launches_per_step = len(kernels) + 1   # the copied-pages ragged prefill launches two kernels
 
     def step(ev):
         flush.fill_(1.0)
@@ -325,6 +327,12 @@ def run_ours(args, rank, world, dist):
                                        tv["kv_indices"], tv["kv_last_page_len"], o=vo, lse=vlse, dev_status=status,
                                        stream=stream)
         ev["prefill_varlen"][1].record(stream)
+        flush.fill_(1.0)
+        ev["prefill_varlen_ws"][0].record(stream)   # two launches: page copy, then the prefill
+        attn.attn_prefill_paged_varlen_ws(tv["q"], tv["k_cache"], tv["v_cache"], tv["qo_indptr"], tv["kv_indptr"],
+                                          tv["kv_indices"], tv["kv_last_page_len"], max_kv_rows=v_rows,
+                                          workspace=vws, o=vo, lse=vlse, dev_status=status, stream=stream)
+        ev["prefill_varlen_ws"][1].record(stream)
 
     def new_events():
         return {kn: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for kn in kernels}
@@ -440,6 +448,9 @@ def run_ours(args, rank, world, dist):
     rep["prefill_varlen"] = dict(bound="tensor", achieved=vl_flops / (ms["prefill_varlen"] * 1e-3) / 1e12,
                                  peak=peaks["bf16_tflops"], unit="TFLOP/s", work=vl_flops, src="prefill_tc.cu",
                                  kernel="prefill_tc_kernel (ragged, paged)")
+    rep["prefill_varlen_ws"] = dict(bound="tensor", achieved=vl_flops / (ms["prefill_varlen_ws"] * 1e-3) / 1e12,
+                                    peak=peaks["bf16_tflops"], unit="TFLOP/s", work=vl_flops, src="prefill_tc.cu",
+                                    kernel="gather_pages_kernel + prefill_tc_kernel (ragged, pages copied first)")
     kernels_out = []
     for kn in kernels:
         r = rep[kn]
@@ -561,12 +572,18 @@ def run_profile(args):
     torch.cuda.set_device(dev)
     attn.lib()
     n = args.warmup + args.steps
-    if args.profile == "prefill_varlen":
+    if args.profile.startswith("prefill_varlen"):
         vl = synth.VARLEN_PAGED_PREFILL
         t = {kk: vv.to(dev) for kk, vv in synth.varlen_inputs(vl, seed=0).items() if torch.is_tensor(vv)}
+        rows = t["k_cache"].shape[0] * vl.page_size
         for _ in range(n):
-            attn.attn_prefill_paged_varlen(t["q"], t["k_cache"], t["v_cache"], t["qo_indptr"], t["kv_indptr"],
-                                           t["kv_indices"], t["kv_last_page_len"])
+            if args.profile == "prefill_varlen_ws":
+                attn.attn_prefill_paged_varlen_ws(t["q"], t["k_cache"], t["v_cache"], t["qo_indptr"],
+                                                  t["kv_indptr"], t["kv_indices"], t["kv_last_page_len"],
+                                                  max_kv_rows=rows)
+            else:
+                attn.attn_prefill_paged_varlen(t["q"], t["k_cache"], t["v_cache"], t["qo_indptr"], t["kv_indptr"],
+                                               t["kv_indices"], t["kv_last_page_len"])
     elif args.profile.startswith("prefill"):
         shape = synth.LLAMA_GQA_PREFILL if args.profile == "prefill" else synth.BATCHED_SQUARE_PREFILL
         q, k, v = (t.to(dev) for t in synth.prefill_inputs(shape, seed=0))
@@ -603,7 +620,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--clock-window", type=float, default=2.0,
                     help="seconds of loaded, untimed steps sampled by nvidia-smi before the timed region")
-    ap.add_argument("--profile", choices=["prefill", "prefill_batched", "prefill_varlen", "decode_bf16", "decode_int4",
+    ap.add_argument("--profile", choices=["prefill", "prefill_batched", "prefill_varlen", "prefill_varlen_ws", "decode_bf16", "decode_int4",
                                           "decode_fp8"],
                     help="run only one kernel on its workload (for ncu captures); prints no JSON line")
     ap.add_argument("--decode-batch", type=int, default=0, help="with --profile: shrink the decode batch")

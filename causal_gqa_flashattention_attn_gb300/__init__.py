@@ -36,7 +36,8 @@ ATTN_DEV_PAGE_OUT_OF_RANGE = 0x1
 ATTN_DEV_SEQ_TOO_LONG = 0x2
 ATTN_DEV_WAIT_TIMEOUT = 0x4
 
-EXPORTED = ("attn_prefill_fwd", "attn_prefill_paged_varlen", "attn_decode_workspace_bytes", "attn_decode_paged_splitk", "attn_decode_paged_splitk_mq",
+EXPORTED = ("attn_prefill_fwd", "attn_prefill_paged_varlen", "attn_prefill_varlen_workspace_bytes",
+            "attn_prefill_paged_varlen_ws", "attn_decode_workspace_bytes", "attn_decode_paged_splitk", "attn_decode_paged_splitk_mq",
             "attn_decode_paged_splitk_fp8",
             "attn_decode_paged_splitk_static", "attn_lse_merge", "attn_lse_merge_bwd", "attn_selftest_wait_timeout",
             "attn_status_string", "attn_abi_version")
@@ -66,6 +67,11 @@ def lib():
     L.attn_prefill_paged_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
                                             f32, vp, vp]
     L.attn_prefill_paged_varlen.restype = i32
+    L.attn_prefill_varlen_workspace_bytes.argtypes = [i32, i32, i32]
+    L.attn_prefill_varlen_workspace_bytes.restype = sz
+    L.attn_prefill_paged_varlen_ws.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
+                                               i32, f32, vp, sz, vp, vp]
+    L.attn_prefill_paged_varlen_ws.restype = i32
     L.attn_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
     L.attn_decode_workspace_bytes.restype = sz
     L.attn_decode_paged_splitk.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, i32, i32, i32,
@@ -175,6 +181,42 @@ def attn_prefill_paged_varlen(q, k_cache, v_cache, qo_indptr, kv_indptr, kv_indi
                                          d, total_q, num_pages, page_size, float(scale), _ptr(dev_status),
                                          _stream_ptr(stream))
     _check("attn_prefill_paged_varlen", st)
+    return o, lse
+
+
+def attn_prefill_varlen_workspace_bytes(max_kv_rows, Hkv, D):
+    return int(lib().attn_prefill_varlen_workspace_bytes(int(max_kv_rows), int(Hkv), int(D)))
+
+
+def attn_prefill_paged_varlen_ws(q, k_cache, v_cache, qo_indptr, kv_indptr, kv_indices, kv_last_page_len=None,
+                                 max_kv_rows=None, workspace=None, o=None, lse=None, scale=None, dev_status=None,
+                                 stream=None):
+    """As :func:`attn_prefill_paged_varlen`, with the pages first copied into a
+    contiguous workspace (``max_kv_rows`` rows of K and of V, at least
+    ``kv_indptr[B] * page_size``; by default the pool's row count)."""
+    _need_cuda(q, k_cache, v_cache, qo_indptr, kv_indptr, kv_indices, kv_last_page_len, o, lse, dev_status,
+               workspace)
+    total_q, hq, d = q.shape
+    num_pages, page_size, hkv = k_cache.shape[0], k_cache.shape[1], k_cache.shape[2]
+    bsz = qo_indptr.numel() - 1
+    if max_kv_rows is None:
+        max_kv_rows = num_pages * page_size
+    need = attn_prefill_varlen_workspace_bytes(max_kv_rows, hkv, d)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(total_q, hq, dtype=torch.float32, device=q.device)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    st = lib().attn_prefill_paged_varlen_ws(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(qo_indptr),
+                                            _ptr(kv_indptr), _ptr(kv_indices), _ptr(kv_last_page_len), _ptr(o),
+                                            _ptr(lse), bsz, hq, hkv, d, total_q, num_pages, page_size,
+                                            int(max_kv_rows), float(scale), _ptr(workspace),
+                                            workspace.numel() * workspace.element_size(), _ptr(dev_status),
+                                            _stream_ptr(stream))
+    _check("attn_prefill_paged_varlen_ws", st)
     return o, lse
 
 

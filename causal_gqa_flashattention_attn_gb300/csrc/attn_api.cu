@@ -136,6 +136,38 @@ attn_status_t decode_impl(const void* q, const void* k_cache, const void* v_cach
 
 }  // namespace
 
+namespace {
+
+attn_status_t varlen_impl(const void* q, const void* k_cache, const void* v_cache, const int32_t* qo_indptr,
+                          const int32_t* kv_indptr, const int32_t* kv_indices, const int32_t* kv_last_page_len,
+                          void* o, float* lse, int B, int Hq, int Hkv, int D, int total_q, int num_pages,
+                          int page_size, float scale, int32_t* dev_status, void* stream, void* kv_ws,
+                          int max_kv_rows) {
+    if (q == nullptr || k_cache == nullptr || v_cache == nullptr || qo_indptr == nullptr || kv_indptr == nullptr ||
+        kv_indices == nullptr || o == nullptr)
+        return ATTN_ERR_INVALID_ARG;
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || total_q < 0 || num_pages <= 0 || page_size <= 0)
+        return ATTN_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0 || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o)) return ATTN_ERR_INVALID_ARG;
+    if (D != 128) return ATTN_ERR_UNSUPPORTED;
+    const int G = Hq / Hkv;
+    if (G > 128 || 128 % G != 0) return ATTN_ERR_UNSUPPORTED;
+    if (B > varlen_max_seqs()) return ATTN_ERR_UNSUPPORTED;
+    if (static_cast<long long>(num_pages) * page_size >= (1LL << 31) - 1) return ATTN_ERR_UNSUPPORTED;
+    // work items (query blocks x KV heads) are counted in int and a query
+    // block index is packed in 21 bits
+    if (total_q >= (1 << 22) || (static_cast<long long>(total_q) + B) * Hkv >= (1LL << 31))
+        return ATTN_ERR_UNSUPPORTED;
+    if (total_q == 0) return ATTN_OK;
+    VarlenArgs a{q,  k_cache, v_cache, qo_indptr, kv_indptr, kv_indices, kv_last_page_len, o,      lse,
+                 B,  Hq,      Hkv,     D,         total_q,   num_pages,  page_size,        scale,  dev_status,
+                 kv_ws, max_kv_rows};
+    return from_cuda(launch_prefill_varlen_tc(a, static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
 extern "C" {
 
 const char* attn_status_string(attn_status_t status) {
@@ -150,7 +182,7 @@ const char* attn_status_string(attn_status_t status) {
     }
 }
 
-int attn_abi_version(void) { return 101; }
+int attn_abi_version(void) { return 102; }
 
 attn_status_t attn_selftest_wait_timeout(int32_t* dev_status, unsigned int limit_us, void* stream) {
     if (dev_status == nullptr || limit_us == 0 || limit_us > 1000000u) return ATTN_ERR_INVALID_ARG;
@@ -223,26 +255,27 @@ attn_status_t attn_prefill_paged_varlen(const void* q, const void* k_cache, cons
                                         const int32_t* kv_indices, const int32_t* kv_last_page_len, void* o,
                                         float* lse, int B, int Hq, int Hkv, int D, int total_q, int num_pages,
                                         int page_size, float scale, int32_t* dev_status, void* stream) {
-    if (q == nullptr || k_cache == nullptr || v_cache == nullptr || qo_indptr == nullptr || kv_indptr == nullptr ||
-        kv_indices == nullptr || o == nullptr)
-        return ATTN_ERR_INVALID_ARG;
-    if (B <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || total_q < 0 || num_pages <= 0 || page_size <= 0)
-        return ATTN_ERR_INVALID_ARG;
-    if (Hq % Hkv != 0 || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o)) return ATTN_ERR_INVALID_ARG;
-    if (D != 128) return ATTN_ERR_UNSUPPORTED;
-    const int G = Hq / Hkv;
-    if (G > 128 || 128 % G != 0) return ATTN_ERR_UNSUPPORTED;
-    if (B > varlen_max_seqs()) return ATTN_ERR_UNSUPPORTED;
-    if (static_cast<long long>(num_pages) * page_size >= (1LL << 31) - 1) return ATTN_ERR_UNSUPPORTED;
-    // work items (query blocks x KV heads) are counted in int and a query
-    // block index is packed in 21 bits
-    if (total_q >= (1 << 22) || (static_cast<long long>(total_q) + B) * Hkv >= (1LL << 31))
-        return ATTN_ERR_UNSUPPORTED;
-    if (total_q == 0) return ATTN_OK;
-    VarlenArgs a{q, k_cache, v_cache, qo_indptr, kv_indptr, kv_indices, kv_last_page_len, o, lse,
-                 B, Hq,      Hkv,     D,         total_q,   num_pages, page_size, scale,      dev_status};
-    return from_cuda(launch_prefill_varlen_tc(a, static_cast<cudaStream_t>(stream)));
+    return varlen_impl(q, k_cache, v_cache, qo_indptr, kv_indptr, kv_indices, kv_last_page_len, o, lse, B, Hq, Hkv,
+                       D, total_q, num_pages, page_size, scale, dev_status, stream, nullptr, 0);
+}
+
+size_t attn_prefill_varlen_workspace_bytes(int max_kv_rows, int Hkv, int D) {
+    if (max_kv_rows <= 0 || Hkv <= 0 || D <= 0) return 0;
+    return 2 * static_cast<size_t>(max_kv_rows) * Hkv * D * 2;
+}
+
+attn_status_t attn_prefill_paged_varlen_ws(const void* q, const void* k_cache, const void* v_cache,
+                                           const int32_t* qo_indptr, const int32_t* kv_indptr,
+                                           const int32_t* kv_indices, const int32_t* kv_last_page_len, void* o,
+                                           float* lse, int B, int Hq, int Hkv, int D, int total_q, int num_pages,
+                                           int page_size, int max_kv_rows, float scale, void* workspace,
+                                           size_t workspace_bytes, int32_t* dev_status, void* stream) {
+    if (max_kv_rows <= 0) return ATTN_ERR_INVALID_ARG;
+    if (Hkv > 0 && D > 0 && static_cast<long long>(max_kv_rows) * Hkv * D >= (1LL << 40)) return ATTN_ERR_UNSUPPORTED;
+    const size_t need = attn_prefill_varlen_workspace_bytes(max_kv_rows, Hkv, D);
+    if (workspace == nullptr || !aligned16(workspace) || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
+    return varlen_impl(q, k_cache, v_cache, qo_indptr, kv_indptr, kv_indices, kv_last_page_len, o, lse, B, Hq, Hkv,
+                       D, total_q, num_pages, page_size, scale, dev_status, stream, workspace, max_kv_rows);
 }
 
 attn_status_t attn_lse_merge(const float* o_part, const float* lse_part, int N, int S, int D, void* o, float* lse,

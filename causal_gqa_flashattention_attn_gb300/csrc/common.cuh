@@ -94,6 +94,8 @@ struct VarlenArgs {
     int B, Hq, Hkv, D, total_q, num_pages, page_size;
     float scale;
     int32_t* dev_status;
+    void* kv_ws;            // NULL: gather rows inside the kernel; else contiguous K then V copy
+    int max_kv_rows;        // rows the copy holds (>= kv_indptr[B] * page_size)
 };
 int varlen_max_seqs();
 cudaError_t launch_prefill_varlen_tc(const VarlenArgs& a, cudaStream_t stream);

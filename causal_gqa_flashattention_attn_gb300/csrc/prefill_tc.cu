@@ -74,6 +74,7 @@ struct Params {
     const __nv_bfloat16* k_pool;   // [pool_rows, Hkv, D]
     const __nv_bfloat16* v_pool;
     int page_size, pool_rows;
+    int gathered;   // K/V come by TMA from a contiguous copy in page-list order
 };
 
 struct Item {
@@ -281,8 +282,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&q_full, 1);
         mbar_init(&q_empty, 1);
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(&k_full[s], kVarlen ? 32 : 1);   // ragged: one cp.async arrival per lane of the gather warp
-            mbar_init(&v_full[s], kVarlen ? 32 : 1);
+            // ragged, gathered in the kernel: one cp.async arrival per lane of the gather warp
+            const uint32_t n_arrive = (kVarlen && !p.gathered) ? 32 : 1;
+            mbar_init(&k_full[s], n_arrive);
+            mbar_init(&v_full[s], n_arrive);
             mbar_init(&k_empty[s], 1);
             mbar_init(&v_empty[s], 1);
         }
@@ -470,7 +473,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         regs_dec<kRegsControl>();
-        if (warp == kProducerWarp && kVarlen) {
+        if (warp == kProducerWarp && kVarlen && p.gathered) {
+            // ------------------------- producer, ragged batch from the contiguous copy
+            // Token t of sequence b is row kv_indptr[b] * page_size + t of the copy
+            // [rows, Hkv, D]; the tiles are TMA boxes {64, 1, 128} as in the dense
+            // layout.  Rows past a sequence's end belong to the next sequence, or
+            // are zero: the causal limit masks them.
+            if (lane == 0) {
+                tma_prefetch_desc(&q_map);
+                tma_prefetch_desc(&k_map);
+                tma_prefetch_desc(&v_map);
+                uint32_t kv_iter = 0, item_iter = 0;
+                bool ok = true;
+                for (int i = 0; ok; ++i) {
+                    const int idx = cta_item(i);
+                    if (idx >= n_items) break;
+                    const Item it = get_item(idx);
+                    if (it.n_kv == 0) continue;
+                    if (item_iter > 0 && !(ok = wait(&q_empty, (item_iter - 1) & 1))) break;
+                    mbar_arrive_expect_tx(&q_full, 2 * kTile);
+                    for (int t = 0; t < 2; ++t)
+                        for (int h = 0; h < 2; ++h)
+                            tma_load_3d(smem + kOffQ + t * kTile + h * kHalf, &q_map, &q_full, h * 64,
+                                        it.kvh * p.G, it.q_start + it.p0 + t * p.P);
+                    const int row0 = it.kv_base * p.page_size;
+                    for (int j = 0; j < it.n_kv; ++j, ++kv_iter) {
+                        const int s = kv_iter % kStages;
+                        const uint32_t par = ((kv_iter / kStages) - 1) & 1;
+                        const int row = row0 + j * kBN;
+                        if (kv_iter >= kStages && !(ok = wait(&k_empty[s], par))) break;
+                        mbar_arrive_expect_tx(&k_full[s], kTile);
+                        tma_load_3d(smem + kOffK + s * kTile, &k_map, &k_full[s], 0, it.kvh, row);
+                        tma_load_3d(smem + kOffK + s * kTile + kHalf, &k_map, &k_full[s], 64, it.kvh, row);
+                        if (kv_iter >= kStages && !(ok = wait(&v_empty[s], par))) break;
+                        mbar_arrive_expect_tx(&v_full[s], kTile);
+                        tma_load_3d(smem + kOffV + s * kTile, &v_map, &v_full[s], 0, it.kvh, row);
+                        tma_load_3d(smem + kOffV + s * kTile + kHalf, &v_map, &v_full[s], 64, it.kvh, row);
+                    }
+                    ++item_iter;
+                }
+            }
+        } else if (warp == kProducerWarp && kVarlen) {
             // ------------------------------------------ producer, ragged batch over a paged pool
             // Q tiles by TMA; K/V rows gathered by the whole warp with 16-byte
             // cp.async copies: lane i copies token rows i, i+32, i+64, i+96 of
@@ -671,6 +714,45 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// Copies the K and V rows of every listed page into contiguous buffers in
+// page-list order (row r = list entry r / page_size, offset r % page_size),
+// one warp per row, 16-byte vectors; the 128 rows after the last one are
+// zeroed so that the last tile of the last sequence reads zeros.  A page id
+// outside the pool gives zero rows and ATTN_DEV_PAGE_OUT_OF_RANGE; a list
+// longer than the copy sets ATTN_DEV_SEQ_TOO_LONG and is cut.
+__global__ void __launch_bounds__(256) gather_pages_kernel(const uint4* __restrict__ k_pool,
+                                                           const uint4* __restrict__ v_pool,
+                                                           const int32_t* __restrict__ kv_indptr,
+                                                           const int32_t* __restrict__ kv_indices, int B,
+                                                           int page_size, int num_pages, int row_vecs,
+                                                           uint4* __restrict__ k_ws, uint4* __restrict__ v_ws,
+                                                           int max_rows, int32_t* status) {
+    const long long listed = static_cast<long long>(kv_indptr[B]) * page_size;
+    if (listed > max_rows && blockIdx.x == 0 && threadIdx.x == 0) flag_status(status, ATTN_DEV_SEQ_TOO_LONG);
+    const long long rows = listed < max_rows ? listed : max_rows;
+    const long long zero_end = (rows + kBN < max_rows) ? rows + kBN : max_rows;
+    const int lane = threadIdx.x & 31;
+    const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+    for (long long r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < zero_end; r += warps) {
+        bool real = false;
+        size_t src = 0;
+        if (r < rows) {
+            const int page = kv_indices[r / page_size];
+            real = page >= 0 && page < num_pages;
+            if (!real && lane == 0) flag_status(status, ATTN_DEV_PAGE_OUT_OF_RANGE);
+            src = (static_cast<size_t>(real ? page : 0) * page_size + r % page_size) * row_vecs;
+        }
+        const size_t dst = static_cast<size_t>(r) * row_vecs;
+        for (int v = lane; v < row_vecs; v += 32) {
+            const uint4 kx = real ? k_pool[src + v] : zero;
+            const uint4 vx = real ? v_pool[src + v] : zero;
+            k_ws[dst + v] = kx;
+            v_ws[dst + v] = vx;
+        }
+    }
+}
+
 }  // namespace
 
 bool prefill_tc_supported(const PrefillArgs& a) {
@@ -719,6 +801,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream) {
     p.qo_indptr = p.kv_indptr = p.kv_indices = p.kv_last = nullptr;
     p.k_pool = p.v_pool = nullptr;
     p.page_size = p.pool_rows = 0;
+    p.gathered = 0;
     const int sms = device_sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
     const int grid = p.n_items < sms ? p.n_items : sms;
@@ -735,7 +818,7 @@ int varlen_max_seqs() { return kMaxVarlenSeqs; }
 cudaError_t launch_prefill_varlen_tc(const VarlenArgs& a, cudaStream_t stream) {
     const int G = a.Hq / a.Hkv;
     const int P = kBM / G;
-    CUtensorMap q_map;   // K/V rows are gathered with cp.async (no tensor map)
+    CUtensorMap q_map, k_map, v_map;   // K/V maps only over the contiguous copy
     {
         // ragged Q [total_q, Hq, D]: box {64 dims, G heads, P positions} -> rows pos * G + head
         const uint64_t dims[3] = {kD, static_cast<uint64_t>(a.Hq), static_cast<uint64_t>(a.total_q)};
@@ -766,13 +849,36 @@ cudaError_t launch_prefill_varlen_tc(const VarlenArgs& a, cudaStream_t stream) {
     p.pool_rows = a.num_pages * a.page_size;
     p.k_pool = static_cast<const __nv_bfloat16*>(a.k_cache);
     p.v_pool = static_cast<const __nv_bfloat16*>(a.v_cache);
+    p.gathered = a.kv_ws != nullptr;
     const int sms = device_sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
+    k_map = v_map = q_map;
+    if (p.gathered) {
+        // K copy [max_kv_rows, Hkv, D] then V copy, each viewed as [D, Hkv, rows]
+        const size_t row_bytes = static_cast<size_t>(a.Hkv) * kD * 2;
+        uint8_t* k_ws = static_cast<uint8_t*>(a.kv_ws);
+        uint8_t* v_ws = k_ws + row_bytes * static_cast<size_t>(a.max_kv_rows);
+        const uint64_t dims[3] = {kD, static_cast<uint64_t>(a.Hkv), static_cast<uint64_t>(a.max_kv_rows)};
+        const uint64_t strides[2] = {kD * 2, row_bytes};
+        const uint32_t box[3] = {64, 1, kBN};
+        if (!encode_tiled_map(&k_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, k_ws, dims, strides, box,
+                              CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_tiled_map(&v_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, v_ws, dims, strides, box,
+                              CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+        const int row_vecs = static_cast<int>(row_bytes / 16);
+        gather_pages_kernel<<<sms * 8, 256, 0, stream>>>(
+            static_cast<const uint4*>(a.k_cache), static_cast<const uint4*>(a.v_cache), a.kv_indptr, a.kv_indices,
+            a.B, a.page_size, a.num_pages, row_vecs, reinterpret_cast<uint4*>(k_ws), reinterpret_cast<uint4*>(v_ws),
+            a.max_kv_rows, a.dev_status);
+        const cudaError_t ge = cudaGetLastError();
+        if (ge != cudaSuccess) return ge;
+    }
     const size_t smem = kSmemBytes + 1024;
     cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    prefill_tc_kernel<true><<<sms, kThreads, smem, stream>>>(q_map, q_map, q_map, p);
+    prefill_tc_kernel<true><<<sms, kThreads, smem, stream>>>(q_map, k_map, v_map, p);
     return cudaGetLastError();
 }
 

@@ -127,6 +127,31 @@ attn_status_t attn_prefill_paged_varlen(const void* q, const void* k_cache, cons
                                         int32_t* dev_status, void* stream);
 
 /*
+ * attn_prefill_paged_varlen_ws - attn_prefill_paged_varlen with a workspace:
+ * the K and V rows of every listed page are first copied into contiguous
+ * buffers in page-list order (token t of sequence b is row
+ * kv_indptr[b] * page_size + t), then read by TMA tiles as in the dense
+ * prefill.  Same results; faster when pages are small (the in-kernel gather
+ * of attn_prefill_paged_varlen cannot hide the latency of page-size-1 rows).
+ *
+ *   max_kv_rows  rows the workspace holds: at least kv_indptr[B] * page_size
+ *                (a longer list sets ATTN_DEV_SEQ_TOO_LONG and is cut)
+ *   workspace    device, 16-byte aligned, attn_prefill_varlen_workspace_bytes()
+ *                bytes: the K copy [max_kv_rows, Hkv, D] bf16, then the V copy
+ *                (scratch, overwritten)
+ * Other arguments, limits and errors as attn_prefill_paged_varlen;
+ * ATTN_ERR_WORKSPACE for a missing, misaligned or short workspace.
+ */
+size_t attn_prefill_varlen_workspace_bytes(int max_kv_rows, int Hkv, int D);
+attn_status_t attn_prefill_paged_varlen_ws(const void* q, const void* k_cache, const void* v_cache,
+                                           const int32_t* qo_indptr, const int32_t* kv_indptr,
+                                           const int32_t* kv_indices, const int32_t* kv_last_page_len,
+                                           void* o, float* lse, int B, int Hq, int Hkv, int D, int total_q,
+                                           int num_pages, int page_size, int max_kv_rows, float scale,
+                                           void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                           void* stream);
+
+/*
  * attn_decode_paged_splitk - single-query split-K decode over a paged KV cache.
  *
  * Follows "splitk_kernels.py" (xformers), _fwd_kernel_splitK (split chunks,
@@ -308,7 +333,8 @@ attn_status_t attn_selftest_wait_timeout(int32_t* dev_status, unsigned int limit
 /* Static, human-readable name of a status code. */
 const char* attn_status_string(attn_status_t status);
 
-/* ABI version of this header (major * 100 + minor); 101 added attn_selftest_wait_timeout. */
+/* ABI version of this header (major * 100 + minor); 101 added attn_selftest_wait_timeout,
+ * 102 attn_prefill_paged_varlen_ws. */
 int attn_abi_version(void);
 
 #ifdef __cplusplus

@@ -38,7 +38,7 @@ def test_library_exports_every_declared_symbol(L):
     for name in declared_functions():
         assert hasattr(L, name), name
         assert name in attn.EXPORTED
-    assert L.attn_abi_version() == 101
+    assert L.attn_abi_version() == 102
 
 
 def test_status_strings(L):
@@ -122,6 +122,31 @@ def test_varlen_host_validation(L):
     assert _varlen(L, Hq=1024, Hkv=1024, total_q=(1 << 21) + 1) == -2   # item count overflows int
     assert _varlen(L, num_pages=1 << 30, page_size=4) == -2
     assert _varlen(L, total_q=0) == 0                     # nothing to do, nothing launched
+
+
+def _varlen_ws(L, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, qo=FAKE, kvp=FAKE, kvi=FAKE, last=None, o=FAKE, lse=None, B=2, Hq=32, Hkv=4,
+             D=128, total_q=100, num_pages=64, page_size=1, rows=64, scale=0.1, ws=FAKE, ws_bytes=1 << 30,
+             status=None, stream=None)
+    a.update(kw)
+    return L.attn_prefill_paged_varlen_ws(a["q"], a["k"], a["v"], a["qo"], a["kvp"], a["kvi"], a["last"], a["o"],
+                                          a["lse"], a["B"], a["Hq"], a["Hkv"], a["D"], a["total_q"],
+                                          a["num_pages"], a["page_size"], a["rows"], a["scale"], a["ws"],
+                                          a["ws_bytes"], a["status"], a["stream"])
+
+
+def test_varlen_ws_host_validation(L):
+    import causal_gqa_flashattention_attn_gb300 as attn
+    need = 2 * 64 * 4 * 128 * 2   # K and V copies of 64 rows x 4 heads x 128 dims, bf16
+    assert attn.attn_prefill_varlen_workspace_bytes(64, 4, 128) == need
+    assert attn.attn_prefill_varlen_workspace_bytes(0, 4, 128) == 0
+    assert _varlen_ws(L, rows=0) == -1
+    assert _varlen_ws(L, ws=None) == -3
+    assert _varlen_ws(L, ws_bytes=need - 1) == -3
+    assert _varlen_ws(L, ws=ctypes.c_void_p(0x10008)) == -3   # misaligned
+    assert _varlen_ws(L, qo=None) == -1                       # the shared checks still apply
+    assert _varlen_ws(L, D=64) == -2
+    assert _varlen_ws(L, total_q=0, ws_bytes=need) == 0
 
 
 def _decode_mq(L, **kw):

@@ -22,16 +22,29 @@ CASES = [
 ]
 
 
+def _entry(attn, ws):
+    """The in-kernel gather, or the entry that copies the pages into a
+    contiguous workspace first (sized to exactly the listed rows)."""
+    if not ws:
+        return attn.attn_prefill_paged_varlen
+
+    def run(q, k, v, qo, kvp, kvi, last, **kw):
+        rows = int(kvp[-1].item()) * k.shape[1]
+        return attn.attn_prefill_paged_varlen_ws(q, k, v, qo, kvp, kvi, last, max_kv_rows=max(rows, 1), **kw)
+    return run
+
+
+@pytest.mark.parametrize("ws", [False, True], ids=["gather", "workspace"])
 @pytest.mark.parametrize("hq,hkv,ps,q_lens,kv_lens", CASES)
-def test_varlen_paged_prefill_matches_oracle(hq, hkv, ps, q_lens, kv_lens):
+def test_varlen_paged_prefill_matches_oracle(hq, hkv, ps, q_lens, kv_lens, ws):
     dev = gpu_or_skip()
     import causal_gqa_flashattention_attn_gb300 as attn
     shape = synth.VarlenShape("t", len(q_lens), hq, hkv, 128, 1, 1, 0, 0, page_size=ps)
     inp = synth.varlen_inputs(shape, seed=len(q_lens) + ps, q_lens=q_lens, kv_lens=kv_lens)
     t = {k: v.to(dev) for k, v in inp.items() if torch.is_tensor(v)}
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    o, lse = attn.attn_prefill_paged_varlen(t["q"], t["k_cache"], t["v_cache"], t["qo_indptr"], t["kv_indptr"],
-                                            t["kv_indices"], t["kv_last_page_len"], dev_status=status)
+    o, lse = _entry(attn, ws)(t["q"], t["k_cache"], t["v_cache"], t["qo_indptr"], t["kv_indptr"],
+                              t["kv_indices"], t["kv_last_page_len"], dev_status=status)
     torch.cuda.synchronize()
     assert status.item() == 0
     o_ref, lse_ref = oracle.prefill_paged_varlen(inp["q"].double().numpy(), inp["k_cache"].double().numpy(),
@@ -42,7 +55,8 @@ def test_varlen_paged_prefill_matches_oracle(hq, hkv, ps, q_lens, kv_lens):
     check_lse(lse, lse_ref)
 
 
-def test_varlen_bench_workload_sampled():
+@pytest.mark.parametrize("ws", [False, True], ids=["gather", "workspace"])
+def test_varlen_bench_workload_sampled(ws):
     """The benchmark's ragged batch (8 sequences, page size 1); the oracle
     checks two whole sequences."""
     dev = gpu_or_skip()
@@ -50,8 +64,8 @@ def test_varlen_bench_workload_sampled():
     shape = synth.VARLEN_PAGED_PREFILL
     inp = synth.varlen_inputs(shape, seed=0)
     t = {k: v.to(dev) for k, v in inp.items() if torch.is_tensor(v)}
-    o, lse = attn.attn_prefill_paged_varlen(t["q"], t["k_cache"], t["v_cache"], t["qo_indptr"], t["kv_indptr"],
-                                            t["kv_indices"], t["kv_last_page_len"])
+    o, lse = _entry(attn, ws)(t["q"], t["k_cache"], t["v_cache"], t["qo_indptr"], t["kv_indptr"],
+                              t["kv_indices"], t["kv_last_page_len"])
     torch.cuda.synchronize()
     qo = inp["qo_indptr"].tolist()
     for b in (0, shape.B - 1):
@@ -66,11 +80,11 @@ def test_varlen_bench_workload_sampled():
         check_lse(lse[qo[b]:qo[b + 1]], lse_ref, what=f"LSE seq {b}")
 
 
-def _run(attn, inp, dev):
+def _run(attn, inp, dev, ws=False):
     t = {k: v.to(dev) for k, v in inp.items() if torch.is_tensor(v)}
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    o, lse = attn.attn_prefill_paged_varlen(t["q"], t["k_cache"], t["v_cache"], t["qo_indptr"], t["kv_indptr"],
-                                            t["kv_indices"], t["kv_last_page_len"], dev_status=status)
+    o, lse = _entry(attn, ws)(t["q"], t["k_cache"], t["v_cache"], t["qo_indptr"], t["kv_indptr"],
+                              t["kv_indices"], t["kv_last_page_len"], dev_status=status)
     torch.cuda.synchronize()
     assert status.item() == 0
     return o, lse
@@ -87,7 +101,8 @@ def _check_seq(inp, o, lse, b, ps, pools):
     check_lse(lse[qo[b]:qo[b + 1]], lse_ref, what=f"LSE seq {b}")
 
 
-def test_varlen_many_short_sequences():
+@pytest.mark.parametrize("ws", [False, True], ids=["gather", "workspace"])
+def test_varlen_many_short_sequences(ws):
     """300 sequences of mixed short lengths: many work items share a KV tile
     count, so the longest-first order has long runs of ties; every sequence
     is checked."""
@@ -98,7 +113,7 @@ def test_varlen_many_short_sequences():
     kv_lens = [q + int(x) for q, x in zip(q_lens, torch.randint(0, 300, (300,), generator=g))]
     shape = synth.VarlenShape("t", len(q_lens), 16, 2, 128, 1, 1, 0, 0, page_size=16)
     inp = synth.varlen_inputs(shape, seed=5, q_lens=q_lens, kv_lens=kv_lens)
-    o, lse = _run(attn, inp, dev)
+    o, lse = _run(attn, inp, dev, ws)
     pools = (inp["k_cache"].double().numpy(), inp["v_cache"].double().numpy())
     for b in range(len(q_lens)):
         _check_seq(inp, o, lse, b, 16, pools)
@@ -119,3 +134,18 @@ def test_varlen_over_the_sorted_list_capacity():
     pools = (inp["k_cache"].double().numpy(), inp["v_cache"].double().numpy())
     for b in list(range(0, B, 97)) + [B - 1]:
         _check_seq(inp, o, lse, b, 1, pools)
+
+
+def test_varlen_workspace_too_small_is_flagged():
+    """A page list longer than the workspace's rows sets
+    ATTN_DEV_SEQ_TOO_LONG (the copy is cut, nothing is written out of it)."""
+    dev = gpu_or_skip()
+    import causal_gqa_flashattention_attn_gb300 as attn
+    shape = synth.VarlenShape("t", 2, 32, 4, 128, 1, 1, 0, 0, page_size=1)
+    inp = synth.varlen_inputs(shape, seed=9, q_lens=[40, 20], kv_lens=[300, 100])
+    t = {k: v.to(dev) for k, v in inp.items() if torch.is_tensor(v)}
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    attn.attn_prefill_paged_varlen_ws(t["q"], t["k_cache"], t["v_cache"], t["qo_indptr"], t["kv_indptr"],
+                                      t["kv_indices"], t["kv_last_page_len"], max_kv_rows=256, dev_status=status)
+    torch.cuda.synchronize()
+    assert status.item() & attn.ATTN_DEV_SEQ_TOO_LONG
