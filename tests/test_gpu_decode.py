@@ -193,3 +193,16 @@ def test_full_size_paged_decode_bf16_sampled():
 
 def test_full_size_paged_decode_int4_sampled():
     _full_size(synth.PAGED_DECODE_INT4, lambda lens: [0, 5, 15])
+
+
+@pytest.mark.parametrize("fmt", ["dense", "int4"])
+def test_long_context_decode(fmt):
+    """A 128K-token sequence (64 splits of 2048 tokens, all merged) beside a
+    short one: the largest split count the tests reach."""
+    base = synth.PAGED_DECODE_BF16 if fmt == "dense" else synth.PAGED_DECODE_INT4
+    shape = replace(base, B=2, Hq=4, Hkv=1)
+    lens = [131072, 300]
+    inp, o, lse, _ = _run(shape, lens, 2048, seed=21)
+    o_ref, lse_ref = _oracle(shape, inp, 2048, max(lens))
+    check_o(o, o_ref)
+    check_lse(lse, lse_ref)

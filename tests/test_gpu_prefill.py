@@ -120,3 +120,10 @@ def test_full_size_llama_gqa_prefill_sampled():
 
 def test_full_size_batched_square_prefill_sampled():
     _sampled_rows(synth.BATCHED_SQUARE_PREFILL, n_heads=4, rows_per_head=16, seed=2)
+
+
+def test_long_kv_prefill_sampled():
+    """512 new queries against a 64K-token cache (G = 8): 512 KV tiles per
+    work item; the oracle checks sampled rows of sampled heads."""
+    shape = replace(synth.LLAMA_GQA_PREFILL, B=1, Hq=8, Hkv=1, q_len=512, kv_len=65536)
+    _sampled_rows(shape, n_heads=3, rows_per_head=8, seed=3)
