@@ -634,6 +634,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else if (warp == kMmaWarp) {
             // ------------------------------------------------------------- MMA issuer
             if (lane == 0) {
+                // tiles written by cp.async (the generic proxy) need a proxy fence
+                // before the tensor core reads them; TMA-written tiles do not
+                const bool cp_async_tiles = kVarlen && !p.gathered;
                 constexpr uint32_t idesc_qk = idesc_bf16_f32(kBM, kBN, false);
                 constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, kD, true);
                 const uint32_t q_s = smem_u32(smem + kOffQ), k_s = smem_u32(smem + kOffK), v_s = smem_u32(smem + kOffV);
@@ -663,7 +666,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (it.n_kv == 0) continue;
                     if (!(ok = wait(&q_full, item_iter & 1))) break;
                     if (!(ok = wait(&k_full[kv_iter % kStages], (kv_iter / kStages) & 1))) break;
-                    if constexpr (kVarlen) fence_proxy_async_smem();   // cp.async writes -> tensor-core reads
+                    if (cp_async_tiles) fence_proxy_async_smem();   // cp.async writes -> tensor-core reads
                     tc_fence_after();
                     issue_s(0, kv_iter % kStages);
                     umma_commit(&s_full[0]);
@@ -676,7 +679,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const bool last = (j + 1 == it.n_kv);
                         const uint32_t nxt = kv_iter + 1;
                         if (!(ok = wait(&v_full[s], (kv_iter / kStages) & 1))) break;
-                        if constexpr (kVarlen) fence_proxy_async_smem();
+                        if (cp_async_tiles) fence_proxy_async_smem();
                         for (int t = 0; t < 2; ++t) {
                             if (!(ok = wait(&p_full[t], kv_iter & 1))) break;
                             if (j == 0 && item_iter > 0 && !(ok = wait(&o_empty[t], (item_iter - 1) & 1))) break;
@@ -686,7 +689,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (!last) {
                                 if (t == 0) {
                                     if (!(ok = wait(&k_full[nxt % kStages], (nxt / kStages) & 1))) break;
-                                    if constexpr (kVarlen) fence_proxy_async_smem();
+                                    if (cp_async_tiles) fence_proxy_async_smem();
                                     tc_fence_after();
                                 }
                                 issue_s(t, nxt % kStages);            // S_t = Q_t K_{j+1}^T (after P_t is read)
