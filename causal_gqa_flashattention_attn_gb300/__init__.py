@@ -36,7 +36,7 @@ ATTN_DEV_PAGE_OUT_OF_RANGE = 0x1
 ATTN_DEV_SEQ_TOO_LONG = 0x2
 ATTN_DEV_WAIT_TIMEOUT = 0x4
 
-EXPORTED = ("attn_prefill_fwd", "attn_prefill_paged_varlen", "attn_prefill_varlen_workspace_bytes",
+EXPORTED = ("attn_prefill_fwd", "attn_prefill_host_workspace_bytes", "attn_prefill_fwd_host", "attn_prefill_paged_varlen", "attn_prefill_varlen_workspace_bytes",
             "attn_prefill_paged_varlen_ws", "attn_decode_workspace_bytes", "attn_decode_paged_splitk", "attn_decode_paged_splitk_mq",
             "attn_decode_paged_splitk_fp8",
             "attn_decode_paged_splitk_static", "attn_lse_merge", "attn_lse_merge_bwd", "attn_selftest_wait_timeout",
@@ -64,6 +64,10 @@ def lib():
     vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     L.attn_prefill_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32, vp, vp]
     L.attn_prefill_fwd.restype = i32
+    L.attn_prefill_host_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32, i32]
+    L.attn_prefill_host_workspace_bytes.restype = sz
+    L.attn_prefill_fwd_host.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32, vp, sz, vp, vp]
+    L.attn_prefill_fwd_host.restype = i32
     L.attn_prefill_paged_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
                                             f32, vp, vp]
     L.attn_prefill_paged_varlen.restype = i32
@@ -157,6 +161,33 @@ def attn_prefill_fwd(q, k, v, o=None, lse=None, scale=None, dev_status=None, str
     st = lib().attn_prefill_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _DT.get(q.dtype, -1), bsz, hq,
                                 hkv, q_len, kv_len, d, float(scale), _ptr(dev_status), _stream_ptr(stream))
     _check("attn_prefill_fwd", st)
+    return o, lse
+
+
+def attn_prefill_host_workspace_bytes(dtype, B, Hq, Hkv, q_len, kv_len, D):
+    return int(lib().attn_prefill_host_workspace_bytes(_DT.get(dtype, -1), B, Hq, Hkv, q_len, kv_len, D))
+
+
+def attn_prefill_fwd_host(q, k, v, o, lse=None, workspace=None, scale=None, dev_status=None, stream=None):
+    """:func:`attn_prefill_fwd` on CPU tensors (pinned for asynchronous
+    copies): ``q, k, v`` are copied in, ``o`` (and ``lse``) copied out, all
+    enqueued on ``stream``; synchronise the stream before reading ``o``."""
+    for t in (q, k, v, o, lse):
+        if t is not None and (t.is_cuda or not t.is_contiguous()):
+            raise ValueError("q, k, v, o, lse must be contiguous host tensors")
+    _need_cuda(workspace, dev_status)
+    bsz, hq, q_len, d = q.shape
+    hkv, kv_len = k.shape[1], k.shape[2]
+    if workspace is None:
+        need = attn_prefill_host_workspace_bytes(q.dtype, bsz, hq, hkv, q_len, kv_len, d)
+        workspace = torch.empty(need, dtype=torch.uint8, device="cuda")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    st = lib().attn_prefill_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _DT.get(q.dtype, -1), bsz, hq,
+                                     hkv, q_len, kv_len, d, float(scale), _ptr(workspace),
+                                     workspace.numel() * workspace.element_size(), _ptr(dev_status),
+                                     _stream_ptr(stream))
+    _check("attn_prefill_fwd_host", st)
     return o, lse
 
 

@@ -77,6 +77,19 @@ int split_count(int max_kv_len, int split_tokens) {
 
 size_t round16(size_t x) { return (x + 15) & ~static_cast<size_t>(15); }
 
+// Sizes, group and dtype checks of the dense prefill (pointers aside).
+attn_status_t prefill_shape_check(attn_dtype_t dtype, int B, int Hq, int Hkv, int q_len, int kv_len, int D,
+                                  float scale) {
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || q_len <= 0 || kv_len <= 0 || D <= 0) return ATTN_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+    if (dtype != ATTN_F32 && dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
+    if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+    if (static_cast<long long>(B) * Hq * q_len >= (1LL << 31) || static_cast<long long>(B) * Hkv * kv_len >= (1LL << 31))
+        return ATTN_ERR_UNSUPPORTED;
+    return ATTN_OK;
+}
+
 }  // namespace
 
 namespace {
@@ -182,7 +195,7 @@ const char* attn_status_string(attn_status_t status) {
     }
 }
 
-int attn_abi_version(void) { return 102; }
+int attn_abi_version(void) { return 103; }
 
 attn_status_t attn_selftest_wait_timeout(int32_t* dev_status, unsigned int limit_us, void* stream) {
     if (dev_status == nullptr || limit_us == 0 || limit_us > 1000000u) return ATTN_ERR_INVALID_ARG;
@@ -194,18 +207,58 @@ attn_status_t attn_prefill_fwd(const void* q, const void* k, const void* v, void
                                attn_dtype_t dtype, int B, int Hq, int Hkv, int q_len, int kv_len, int D,
                                float scale, int32_t* dev_status, void* stream) {
     if (q == nullptr || k == nullptr || v == nullptr || o == nullptr) return ATTN_ERR_INVALID_ARG;
-    if (B <= 0 || Hq <= 0 || Hkv <= 0 || q_len <= 0 || kv_len <= 0 || D <= 0) return ATTN_ERR_INVALID_ARG;
-    if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
-    if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return ATTN_ERR_INVALID_ARG;
-    if (dtype != ATTN_F32 && dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
-    if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
-    if (static_cast<long long>(B) * Hq * q_len >= (1LL << 31) || static_cast<long long>(B) * Hkv * kv_len >= (1LL << 31))
-        return ATTN_ERR_UNSUPPORTED;
+    const attn_status_t shape_ok = prefill_shape_check(dtype, B, Hq, Hkv, q_len, kv_len, D, scale);
+    if (shape_ok != ATTN_OK) return shape_ok;
     PrefillArgs a{q, k, v, o, lse, static_cast<int>(dtype), B, Hq, Hkv, q_len, kv_len, D, scale, dev_status};
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (dtype == ATTN_BF16 && prefill_tc_supported(a)) return from_cuda(launch_prefill_tc(a, s));
     return from_cuda(launch_prefill_simt(a, s));
+}
+
+size_t attn_prefill_host_workspace_bytes(attn_dtype_t dtype, int B, int Hq, int Hkv, int q_len, int kv_len,
+                                         int D) {
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || q_len <= 0 || kv_len <= 0 || D <= 0) return 0;
+    if (dtype != ATTN_F32 && dtype != ATTN_BF16) return 0;
+    const size_t elem = dtype == ATTN_F32 ? 4 : 2;
+    const size_t qb = static_cast<size_t>(B) * Hq * q_len * D * elem;
+    const size_t kvb = static_cast<size_t>(B) * Hkv * kv_len * D * elem;
+    const size_t lb = static_cast<size_t>(B) * Hq * q_len * sizeof(float);
+    return 2 * round16(qb) + 2 * round16(kvb) + round16(lb);   // Q, O, K, V, LSE
+}
+
+attn_status_t attn_prefill_fwd_host(const void* q_host, const void* k_host, const void* v_host, void* o_host,
+                                    float* lse_host, attn_dtype_t dtype, int B, int Hq, int Hkv, int q_len,
+                                    int kv_len, int D, float scale, void* workspace, size_t workspace_bytes,
+                                    int32_t* dev_status, void* stream) {
+    if (q_host == nullptr || k_host == nullptr || v_host == nullptr || o_host == nullptr) return ATTN_ERR_INVALID_ARG;
+    const attn_status_t shape_ok = prefill_shape_check(dtype, B, Hq, Hkv, q_len, kv_len, D, scale);
+    if (shape_ok != ATTN_OK) return shape_ok;   // before anything is enqueued
+    const size_t need = attn_prefill_host_workspace_bytes(dtype, B, Hq, Hkv, q_len, kv_len, D);
+    if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return ATTN_ERR_WORKSPACE;
+    const size_t elem = dtype == ATTN_F32 ? 4 : 2;
+    const size_t qb = static_cast<size_t>(B) * Hq * q_len * D * elem;
+    const size_t kvb = static_cast<size_t>(B) * Hkv * kv_len * D * elem;
+    const size_t lb = static_cast<size_t>(B) * Hq * q_len * sizeof(float);
+    char* w = static_cast<char*>(workspace);
+    void* dq = w;
+    void* dout = w + round16(qb);
+    void* dk = w + 2 * round16(qb);
+    void* dv = w + 2 * round16(qb) + round16(kvb);
+    float* dl = reinterpret_cast<float*>(w + 2 * round16(qb) + 2 * round16(kvb));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // one copy per tensor, in, then the prefill, then one copy per result, out
+    if (cudaMemcpyAsync(dq, q_host, qb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaMemcpyAsync(dk, k_host, kvb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaMemcpyAsync(dv, v_host, kvb, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    const attn_status_t st = attn_prefill_fwd(dq, dk, dv, dout, lse_host != nullptr ? dl : nullptr, dtype, B, Hq,
+                                              Hkv, q_len, kv_len, D, scale, dev_status, stream);
+    if (st != ATTN_OK) return st;
+    if (cudaMemcpyAsync(o_host, dout, qb, cudaMemcpyDeviceToHost, s) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (lse_host != nullptr && cudaMemcpyAsync(lse_host, dl, lb, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    return ATTN_OK;
 }
 
 size_t attn_decode_workspace_bytes(int B, int Hq, int max_kv_len, int split_tokens, int D) {

@@ -84,6 +84,33 @@ attn_status_t attn_prefill_fwd(const void* q, const void* k, const void* v,
                                float scale, int32_t* dev_status, void* stream);
 
 /*
+ * attn_prefill_fwd_host - attn_prefill_fwd on host buffers.
+ *
+ * Enqueues on `stream`: one host -> device copy each of q, k and v into
+ * `workspace`, the prefill of attn_prefill_fwd, and one device -> host copy
+ * each of O and (if lse_host is not NULL) LSE.  Returns once enqueued; the
+ * results are in o_host / lse_host when the stream has reached this work, and
+ * the host buffers must not be reused before then.  Page-locked host memory
+ * (cudaHostAlloc / cudaHostRegister) lets the copies run asynchronously and
+ * overlap work on other streams; with pageable memory they stall the host.
+ *
+ *   q_host, k_host, v_host, o_host, lse_host  host memory, shapes and dtype
+ *                as the device buffers of attn_prefill_fwd
+ *   workspace    device, 16-byte aligned, attn_prefill_host_workspace_bytes()
+ *                bytes (the device copies of Q, O, K, V and LSE; overwritten)
+ * Other arguments and errors as attn_prefill_fwd; ATTN_ERR_WORKSPACE for a
+ * missing, misaligned or short workspace; ATTN_ERR_CUDA if a copy cannot be
+ * enqueued.
+ */
+size_t attn_prefill_host_workspace_bytes(attn_dtype_t dtype, int B, int Hq, int Hkv, int q_len, int kv_len,
+                                         int D);
+attn_status_t attn_prefill_fwd_host(const void* q_host, const void* k_host, const void* v_host,
+                                    void* o_host, float* lse_host, attn_dtype_t dtype,
+                                    int B, int Hq, int Hkv, int q_len, int kv_len, int D, float scale,
+                                    void* workspace, size_t workspace_bytes,
+                                    int32_t* dev_status, void* stream);
+
+/*
  * attn_decode_workspace_bytes - bytes of scratch attn_decode_paged_splitk needs.
  *
  * The workspace holds the split partials of "splitk_kernels.py",
@@ -334,7 +361,7 @@ attn_status_t attn_selftest_wait_timeout(int32_t* dev_status, unsigned int limit
 const char* attn_status_string(attn_status_t status);
 
 /* ABI version of this header (major * 100 + minor); 101 added attn_selftest_wait_timeout,
- * 102 attn_prefill_paged_varlen_ws. */
+ * 102 attn_prefill_paged_varlen_ws, 103 attn_prefill_fwd_host. */
 int attn_abi_version(void);
 
 #ifdef __cplusplus

@@ -6,6 +6,7 @@ import os
 import re
 
 import pytest
+import torch
 
 from conftest import ROOT
 
@@ -38,7 +39,7 @@ def test_library_exports_every_declared_symbol(L):
     for name in declared_functions():
         assert hasattr(L, name), name
         assert name in attn.EXPORTED
-    assert L.attn_abi_version() == 102
+    assert L.attn_abi_version() == 103
 
 
 def test_status_strings(L):
@@ -70,6 +71,30 @@ def test_prefill_host_validation(L):
     assert _prefill(L, D=96) == -2                       # unsupported head dim
     assert _prefill(L, dtype=2) == -2                    # fp16 not implemented
     assert _prefill(L, dtype=3) == -2
+
+
+def test_prefill_host_buffers_validation(L):
+    import causal_gqa_flashattention_attn_gb300 as attn
+    # Q and O [1, 4, 8, 128] bf16, K and V [1, 2, 8, 128] bf16, LSE [1, 4, 8] fp32
+    need = 2 * 1 * 4 * 8 * 128 * 2 + 2 * 1 * 2 * 8 * 128 * 2 + 1 * 4 * 8 * 4
+    assert attn.attn_prefill_host_workspace_bytes(torch.bfloat16, 1, 4, 2, 8, 8, 128) == need
+    assert attn.attn_prefill_host_workspace_bytes(torch.float16, 1, 4, 2, 8, 8, 128) == 0
+
+    def call(**kw):
+        a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=None, dtype=1, B=1, Hq=4, Hkv=2, q_len=8, kv_len=8, D=128,
+                 scale=0.1, ws=FAKE, ws_bytes=need, status=None, stream=None)
+        a.update(kw)
+        return L.attn_prefill_fwd_host(a["q"], a["k"], a["v"], a["o"], a["lse"], a["dtype"], a["B"], a["Hq"],
+                                       a["Hkv"], a["q_len"], a["kv_len"], a["D"], a["scale"], a["ws"],
+                                       a["ws_bytes"], a["status"], a["stream"])
+    assert call(q=None) == -1
+    assert call(B=0) == -1
+    assert call(dtype=2) == -2
+    assert call(ws=None) == -3
+    assert call(ws_bytes=need - 1) == -3
+    assert call(ws=ctypes.c_void_p(0x10008)) == -3
+    assert call(Hq=6, Hkv=4, ws_bytes=1 << 20) == -1     # Hq % Hkv != 0, before any copy is enqueued
+    assert call(D=96, ws_bytes=1 << 20) == -2
 
 
 def _decode(L, **kw):

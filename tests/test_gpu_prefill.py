@@ -127,3 +127,21 @@ def test_long_kv_prefill_sampled():
     work item; the oracle checks sampled rows of sampled heads."""
     shape = replace(synth.LLAMA_GQA_PREFILL, B=1, Hq=8, Hkv=1, q_len=512, kv_len=65536)
     _sampled_rows(shape, n_heads=3, rows_per_head=8, seed=3)
+
+
+def test_host_buffer_entry_matches_device_entry():
+    """attn_prefill_fwd_host (host tensors in and out, copies enqueued on the
+    stream) gives exactly the device entry's O and LSE."""
+    dev = gpu_or_skip()
+    import causal_gqa_flashattention_attn_gb300 as attn
+    shape = replace(synth.LLAMA_GQA_PREFILL, B=2, Hq=8, Hkv=2, q_len=300, kv_len=700)
+    q, k, v = synth.prefill_inputs(shape, seed=4)
+    o_d, lse_d = attn.attn_prefill_fwd(q.to(dev), k.to(dev), v.to(dev))
+    hq, hk, hv = (t.pin_memory() for t in (q, k, v))
+    ho = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+    hl = torch.empty(shape.B, shape.Hq, shape.q_len, dtype=torch.float32).pin_memory()
+    stream = torch.cuda.current_stream()
+    attn.attn_prefill_fwd_host(hq, hk, hv, ho, hl, stream=stream)
+    stream.synchronize()
+    assert torch.equal(ho, o_d.cpu())
+    assert torch.equal(hl, lse_d.cpu())
