@@ -22,6 +22,8 @@ CASES = [
     (32, 4, 1, 256, 1024, [900, 40]),     # Hkv = 4 (coefficient box at offset 0 only)
     (32, 8, 4, 256, 2048, [700, 4, 2100]),   # multi-query, 16 rows
     (32, 8, 9, 256, 512, [900, 30]),         # multi-query, 36 rows in 3 groups
+    (16, 8, 1, 128, 256, [600, 129]),        # G = 2, page 128
+    (64, 4, 1, 256, 1024, [1500, 99]),       # G = 16
 ]
 
 
@@ -74,3 +76,27 @@ def test_fp8_full_size_sampled():
                                    v_scale_shift=inp["v_scale_shift"].numpy())
     check_o(o[picks], o_ref[picks])
     check_lse(lse[picks], lse_ref[picks])
+
+
+def test_fp8_split_partials_match_oracle():
+    """With no output pointer the workspace holds the per-split partials."""
+    dev = gpu_or_skip()
+    import causal_gqa_flashattention_attn_gb300 as attn
+    lens = [1000, 64, 3]
+    split = 256
+    shape = replace(synth.PAGED_DECODE_FP8, B=3, split_tokens=split)
+    inp = synth.decode_inputs(shape, seed=15, lens=lens)
+    t = {k: v.to(dev) for k, v in inp.items() if torch.is_tensor(v)}
+    o, lse, ws = attn.attn_decode_paged_splitk_fp8(t["q"], t["k_cache"], t["v_cache"], t["k_scale_shift"],
+                                                   t["v_scale_shift"], t["block_table"], t["seq_lens"], split, 1300,
+                                                   write_output=False)
+    torch.cuda.synchronize()
+    assert o is None and lse is None
+    o_part, lse_part = attn.decode_partials_view(ws, 3, shape.Hq, 1300, split, 128)
+    op_ref, lp_ref = oracle.decode_split_partials(inp["q"].double().numpy(), inp["k_cache"].numpy(),
+                                                  inp["v_cache"].numpy(), inp["block_table"].numpy(), lens,
+                                                  shape.page_size, split, kv_format="fp8", max_kv_len=1300,
+                                                  k_scale_shift=inp["k_scale_shift"].numpy(),
+                                                  v_scale_shift=inp["v_scale_shift"].numpy())
+    check_o(o_part, op_ref, what="O_s")
+    check_lse(lse_part, lp_ref, what="LSE_s")
