@@ -21,12 +21,20 @@
 //     warp 8 TMA producer, warp 9 MMA issuer (one elected lane), warps 10-11
 //     idle; registers move from the control warpgroup to the softmax ones;
 //   * TMA (128-byte swizzle) stages Q once per work item and K/V through a
-//     two-stage ring; tcgen05.mma accumulates S (2 x 128 columns) and O
-//     (2 x 128 columns) in the 512 TMEM columns; P is written back over S in
-//     TMEM as bf16 and fed to the P.V MMA straight from TMEM;
+//     two-stage ring whose K and V stages are freed separately (K once both
+//     S MMAs have read it, V after both P.V); tcgen05.mma accumulates S
+//     (2 x 128 columns) and O (2 x 128 columns) in the 512 TMEM columns; P is
+//     written back over S in TMEM as bf16 and fed to the P.V MMA from TMEM;
 //   * the max is rescaled lazily (only when it grows by more than 2^8), so
 //     the O accumulator in TMEM is rarely touched by the softmax warps;
 //   * a persistent grid walks the work items longest-first in a snake order.
+//
+// Ragged mode (kVarlen, "gpt-o3 / triton6fd1ef", run): a batch of sequences
+// with CSR extents over a paged KV cache in one launch.  Work items are
+// (sequence, query block, KV head), sorted longest-first in every CTA.  K/V
+// tiles come either from the pool, gathered row by row with cp.async by the
+// producer warp, or by TMA from a contiguous copy of the listed pages made
+// beforehand by gather_pages_kernel.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
