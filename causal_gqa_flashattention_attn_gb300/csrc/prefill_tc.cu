@@ -484,8 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (warp == kProducerWarp && kVarlen && p.gathered) {
             // ------------------------- producer, ragged batch from the contiguous copy
             // Token t of sequence b is row kv_indptr[b] * page_size + t of the copy
-            // [rows, Hkv, D]; the tiles are TMA boxes {64, 1, 128} as in the dense
-            // layout.  Rows past a sequence's end belong to the next sequence, or
+            // [rows, Hkv, D]; the tile halves are 2D TMA boxes {64, 128}.  Rows past a sequence's end belong to the next sequence, or
             // are zero: the causal limit masks them.
             if (lane == 0) {
                 tma_prefetch_desc(&q_map);
@@ -509,14 +508,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int s = kv_iter % kStages;
                         const uint32_t par = ((kv_iter / kStages) - 1) & 1;
                         const int row = row0 + j * kBN;
+                        const int x = it.kvh * kD;
                         if (kv_iter >= kStages && !(ok = wait(&k_empty[s], par))) break;
                         mbar_arrive_expect_tx(&k_full[s], kTile);
-                        tma_load_3d(smem + kOffK + s * kTile, &k_map, &k_full[s], 0, it.kvh, row);
-                        tma_load_3d(smem + kOffK + s * kTile + kHalf, &k_map, &k_full[s], 64, it.kvh, row);
+                        tma_load_2d(smem + kOffK + s * kTile, &k_map, &k_full[s], x, row);
+                        tma_load_2d(smem + kOffK + s * kTile + kHalf, &k_map, &k_full[s], x + 64, row);
                         if (kv_iter >= kStages && !(ok = wait(&v_empty[s], par))) break;
                         mbar_arrive_expect_tx(&v_full[s], kTile);
-                        tma_load_3d(smem + kOffV + s * kTile, &v_map, &v_full[s], 0, it.kvh, row);
-                        tma_load_3d(smem + kOffV + s * kTile + kHalf, &v_map, &v_full[s], 64, it.kvh, row);
+                        tma_load_2d(smem + kOffV + s * kTile, &v_map, &v_full[s], x, row);
+                        tma_load_2d(smem + kOffV + s * kTile + kHalf, &v_map, &v_full[s], x + 64, row);
                     }
                     ++item_iter;
                 }
@@ -865,16 +865,17 @@ cudaError_t launch_prefill_varlen_tc(const VarlenArgs& a, cudaStream_t stream) {
     if (sms <= 0) return cudaErrorInvalidDevice;
     k_map = v_map = q_map;
     if (p.gathered) {
-        // K copy [max_kv_rows, Hkv, D] then V copy, each viewed as [D, Hkv, rows]
+        // K copy [max_kv_rows, Hkv, D] then V copy, each viewed as the 2D
+        // [Hkv * D, rows]: a tile half is the box {64, 128} at x = kvh * D + 64 h
         const size_t row_bytes = static_cast<size_t>(a.Hkv) * kD * 2;
         uint8_t* k_ws = static_cast<uint8_t*>(a.kv_ws);
         uint8_t* v_ws = k_ws + row_bytes * static_cast<size_t>(a.max_kv_rows);
-        const uint64_t dims[3] = {kD, static_cast<uint64_t>(a.Hkv), static_cast<uint64_t>(a.max_kv_rows)};
-        const uint64_t strides[2] = {kD * 2, row_bytes};
-        const uint32_t box[3] = {64, 1, kBN};
-        if (!encode_tiled_map(&k_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, k_ws, dims, strides, box,
+        const uint64_t dims[2] = {static_cast<uint64_t>(a.Hkv) * kD, static_cast<uint64_t>(a.max_kv_rows)};
+        const uint64_t strides[1] = {row_bytes};
+        const uint32_t box[2] = {64, kBN};
+        if (!encode_tiled_map(&k_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, k_ws, dims, strides, box,
                               CU_TENSOR_MAP_SWIZZLE_128B) ||
-            !encode_tiled_map(&v_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, v_ws, dims, strides, box,
+            !encode_tiled_map(&v_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, v_ws, dims, strides, box,
                               CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
         const int row_vecs = static_cast<int>(row_bytes / 16);
