@@ -377,18 +377,21 @@ def run_ours(args, rank, world, dist):
     # ---------------------------------------------------------------- e2e
     # the same prefill through the public host-buffer call: every step copies
     # Q, K, V in from pinned host memory and O, LSE back out (all enqueued by
-    # attn_prefill_fwd_host).  Steps alternate between two streams, each with
-    # its own workspace and host outputs, so one step's copies can overlap the
-    # neighbouring step's kernel, as a serving loop would.
+    # attn_prefill_fwd_host).  Steps rotate over three streams, each with its
+    # own workspace and host outputs, so that a step's inbound copies, the
+    # previous step's kernel and the one before's outbound copies overlap, as
+    # a serving loop would (the host link, about 205 GB/s in and 190 GB/s out,
+    # bounds it; a fourth stream measured no faster).
+    n_e2e = 3
     hq_, hk_, hv_ = (t.cpu().pin_memory() for t in (q, k, v))
-    e2e_streams = [stream, torch.cuda.Stream(dev)]
+    e2e_streams = [stream] + [torch.cuda.Stream(dev) for _ in range(n_e2e - 1)]
     need_h = attn.attn_prefill_host_workspace_bytes(q.dtype, pf.B, pf.Hq, pf.Hkv, pf.q_len, pf.kv_len, pf.D)
-    e2e_ws = [torch.empty(need_h, dtype=torch.uint8, device=dev) for _ in range(2)]
-    ho = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for _ in range(2)]
-    hl = [torch.empty(lse.shape, dtype=lse.dtype).pin_memory() for _ in range(2)]
+    e2e_ws = [torch.empty(need_h, dtype=torch.uint8, device=dev) for _ in range(n_e2e)]
+    ho = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for _ in range(n_e2e)]
+    hl = [torch.empty(lse.shape, dtype=lse.dtype).pin_memory() for _ in range(n_e2e)]
 
     def e2e_step(i):
-        j = i % 2
+        j = i % n_e2e
         attn.attn_prefill_fwd_host(hq_, hk_, hv_, ho[j], hl[j], workspace=e2e_ws[j], stream=e2e_streams[j])
 
     def join(e_from, e_to):
@@ -401,10 +404,12 @@ def run_ours(args, rank, world, dist):
     torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    join(stream, e2e_streams[1])
+    for s_ in e2e_streams[1:]:
+        join(stream, s_)
     for i in range(args.steps):
         e2e_step(i)
-    join(e2e_streams[1], stream)
+    for s_ in e2e_streams[1:]:
+        join(s_, stream)
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1) / args.steps
@@ -529,7 +534,7 @@ def run_ours(args, rank, world, dist):
         "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms": round(e2e_ms, 5),
                 "what": "prefill through the C-ABI host-buffer call attn_prefill_fwd_host: pinned host Q/K/V "
-                        "copied in and O/LSE copied out every step, steps alternating over two streams"},
+                        "copied in and O/LSE copied out every step, steps rotating over three streams"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
     }
