@@ -242,6 +242,11 @@ def run_ours(args, rank, world, dist):
         del inp
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
+    # split-schedule scratch of the two prefills (zeroed once; each call leaves it zeroed)
+    pws = torch.zeros(attn.attn_prefill_workspace_bytes(torch.bfloat16, pf.B, pf.Hq, pf.Hkv, pf.q_len, pf.kv_len,
+                                                        pf.D), dtype=torch.uint8, device=dev)
+    pwsb = torch.zeros(attn.attn_prefill_workspace_bytes(torch.bfloat16, pb.B, pb.Hq, pb.Hkv, pb.q_len, pb.kv_len,
+                                                         pb.D), dtype=torch.uint8, device=dev)
 
     kernels = ["prefill", "prefill_batched", "decode_bf16", "merge_bf16", "decode_int4", "merge_int4", "merge_bwd",
                "decode_mq", "decode_fp8", "prefill_varlen", "prefill_varlen_ws"]
@@ -283,11 +288,11 @@ def run_ours(args, rank, world, dist):
     def step(ev):
         flush.fill_(1.0)
         ev["prefill"][0].record(stream)
-        attn.attn_prefill_fwd(q, k, v, o=o, lse=lse, dev_status=status, stream=stream)
+        attn.attn_prefill_fwd_ws(q, k, v, workspace=pws, o=o, lse=lse, dev_status=status, stream=stream)
         ev["prefill"][1].record(stream)
         flush.fill_(1.0)
         ev["prefill_batched"][0].record(stream)
-        attn.attn_prefill_fwd(qb, kb, vb, o=ob, lse=lseb, dev_status=status, stream=stream)
+        attn.attn_prefill_fwd_ws(qb, kb, vb, workspace=pwsb, o=ob, lse=lseb, dev_status=status, stream=stream)
         ev["prefill_batched"][1].record(stream)
         for name in ("decode_bf16", "decode_int4"):
             d = dec[name]
@@ -599,8 +604,10 @@ def run_profile(args):
     elif args.profile.startswith("prefill"):
         shape = synth.LLAMA_GQA_PREFILL if args.profile == "prefill" else synth.BATCHED_SQUARE_PREFILL
         q, k, v = (t.to(dev) for t in synth.prefill_inputs(shape, seed=0))
+        ws = torch.zeros(attn.attn_prefill_workspace_bytes(q.dtype, *q.shape[:2], k.shape[1], q.shape[2], k.shape[2],
+                                                           q.shape[3]), dtype=torch.uint8, device=dev)
         for _ in range(n):
-            attn.attn_prefill_fwd(q, k, v)
+            attn.attn_prefill_fwd_ws(q, k, v, workspace=ws)
     else:
         shape = {"decode_bf16": synth.PAGED_DECODE_BF16, "decode_int4": synth.PAGED_DECODE_INT4,
                  "decode_fp8": synth.PAGED_DECODE_FP8}[args.profile]

@@ -9,6 +9,7 @@ has not been built.
 
 Entry points (names as in the C ABI):
   attn_prefill_fwd          causal GQA prefill -> (O, LSE)
+  attn_prefill_fwd_ws       the same with scratch for the split schedule
   attn_prefill_paged_varlen ragged causal GQA prefill over a paged KV cache
   attn_decode_workspace_bytes
   attn_decode_paged_splitk  single-query split-K decode over a paged cache
@@ -36,7 +37,7 @@ ATTN_DEV_PAGE_OUT_OF_RANGE = 0x1
 ATTN_DEV_SEQ_TOO_LONG = 0x2
 ATTN_DEV_WAIT_TIMEOUT = 0x4
 
-EXPORTED = ("attn_prefill_fwd", "attn_prefill_host_workspace_bytes", "attn_prefill_fwd_host", "attn_prefill_paged_varlen", "attn_prefill_varlen_workspace_bytes",
+EXPORTED = ("attn_prefill_fwd", "attn_prefill_workspace_bytes", "attn_prefill_plan", "attn_prefill_fwd_ws", "attn_prefill_host_workspace_bytes", "attn_prefill_fwd_host", "attn_prefill_paged_varlen", "attn_prefill_varlen_workspace_bytes",
             "attn_prefill_paged_varlen_ws", "attn_decode_workspace_bytes", "attn_decode_paged_splitk", "attn_decode_paged_splitk_mq",
             "attn_decode_paged_splitk_fp8",
             "attn_decode_paged_splitk_static", "attn_lse_merge", "attn_lse_merge_bwd", "attn_selftest_wait_timeout",
@@ -64,6 +65,12 @@ def lib():
     vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     L.attn_prefill_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32, vp, vp]
     L.attn_prefill_fwd.restype = i32
+    L.attn_prefill_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32, i32]
+    L.attn_prefill_workspace_bytes.restype = sz
+    L.attn_prefill_plan.argtypes = [i32, i32, i32, i32, i32, i32, i32, ctypes.POINTER(ctypes.c_int)]
+    L.attn_prefill_plan.restype = i32
+    L.attn_prefill_fwd_ws.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32, vp, sz, vp, vp]
+    L.attn_prefill_fwd_ws.restype = i32
     L.attn_prefill_host_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32, i32]
     L.attn_prefill_host_workspace_bytes.restype = sz
     L.attn_prefill_fwd_host.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32, vp, sz, vp, vp]
@@ -161,6 +168,48 @@ def attn_prefill_fwd(q, k, v, o=None, lse=None, scale=None, dev_status=None, str
     st = lib().attn_prefill_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _DT.get(q.dtype, -1), bsz, hq,
                                 hkv, q_len, kv_len, d, float(scale), _ptr(dev_status), _stream_ptr(stream))
     _check("attn_prefill_fwd", st)
+    return o, lse
+
+
+def attn_prefill_workspace_bytes(dtype, B, Hq, Hkv, q_len, kv_len, D):
+    """Bytes of split-schedule scratch attn_prefill_fwd_ws takes (0: none used)."""
+    return int(lib().attn_prefill_workspace_bytes(_DT.get(dtype, -1), B, Hq, Hkv, q_len, kv_len, D))
+
+
+def attn_prefill_plan(dtype, B, Hq, Hkv, q_len, kv_len, D):
+    """(schedule, grid) of attn_prefill_fwd_ws on the current device:
+    schedule 1 = split, 0 = whole items, -1 = invalid sizes or no device."""
+    grid = ctypes.c_int(0)
+    sched = lib().attn_prefill_plan(_DT.get(dtype, -1), B, Hq, Hkv, q_len, kv_len, D, ctypes.byref(grid))
+    return int(sched), int(grid.value)
+
+
+def attn_prefill_fwd_ws(q, k, v, workspace=None, o=None, lse=None, scale=None, dev_status=None, stream=None,
+                        want_lse=True):
+    """attn_prefill_fwd with scratch for the split schedule.
+
+    ``workspace`` is a uint8 CUDA tensor of at least
+    attn_prefill_workspace_bytes() bytes whose leading counters are zero (a
+    zeroed tensor stays reusable: every completed call leaves them zero);
+    None allocates a zeroed one for this call.  Returns ``(o, lse)``.
+    """
+    _need_cuda(q, k, v, o, lse, dev_status, workspace)
+    bsz, hq, q_len, d = q.shape
+    hkv, kv_len = k.shape[1], k.shape[2]
+    need = attn_prefill_workspace_bytes(q.dtype, bsz, hq, hkv, q_len, kv_len, d)
+    if workspace is None and need > 0:
+        workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty(bsz, hq, q_len, dtype=torch.float32, device=q.device)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = lib().attn_prefill_fwd_ws(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _DT.get(q.dtype, -1), bsz, hq,
+                                   hkv, q_len, kv_len, d, float(scale), _ptr(workspace), ws_bytes, _ptr(dev_status),
+                                   _stream_ptr(stream))
+    _check("attn_prefill_fwd_ws", st)
     return o, lse
 
 

@@ -195,7 +195,7 @@ const char* attn_status_string(attn_status_t status) {
     }
 }
 
-int attn_abi_version(void) { return 103; }
+int attn_abi_version(void) { return 104; }
 
 attn_status_t attn_selftest_wait_timeout(int32_t* dev_status, unsigned int limit_us, void* stream) {
     if (dev_status == nullptr || limit_us == 0 || limit_us > 1000000u) return ATTN_ERR_INVALID_ARG;
@@ -206,11 +206,45 @@ attn_status_t attn_selftest_wait_timeout(int32_t* dev_status, unsigned int limit
 attn_status_t attn_prefill_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                                attn_dtype_t dtype, int B, int Hq, int Hkv, int q_len, int kv_len, int D,
                                float scale, int32_t* dev_status, void* stream) {
+    return attn_prefill_fwd_ws(q, k, v, o, lse, dtype, B, Hq, Hkv, q_len, kv_len, D, scale, nullptr, 0, dev_status,
+                               stream);
+}
+
+size_t attn_prefill_workspace_bytes(attn_dtype_t dtype, int B, int Hq, int Hkv, int q_len, int kv_len, int D) {
+    if (prefill_shape_check(dtype, B, Hq, Hkv, q_len, kv_len, D, 1.f) != ATTN_OK) return 0;
+    PrefillArgs a{nullptr, nullptr, nullptr, nullptr, nullptr, static_cast<int>(dtype), B, Hq, Hkv, q_len, kv_len,
+                  D, 1.f, nullptr, nullptr, 0};
+    if (dtype != ATTN_BF16 || !prefill_tc_supported(a)) return 0;
+    const int sms = device_sm_count();
+    return sms > 0 ? prefill_tc_workspace_bytes(a, sms) : 0;
+}
+
+int attn_prefill_plan(attn_dtype_t dtype, int B, int Hq, int Hkv, int q_len, int kv_len, int D, int* grid) {
+    if (grid != nullptr) *grid = 0;
+    if (prefill_shape_check(dtype, B, Hq, Hkv, q_len, kv_len, D, 1.f) != ATTN_OK) return -1;
+    PrefillArgs a{nullptr, nullptr, nullptr, nullptr, nullptr, static_cast<int>(dtype), B, Hq, Hkv, q_len, kv_len,
+                  D, 1.f, nullptr, nullptr, 0};
+    if (dtype != ATTN_BF16 || !prefill_tc_supported(a)) return 0;
+    const int sms = device_sm_count();
+    if (sms <= 0) return -1;
+    return prefill_tc_plan(a, sms, grid);
+}
+
+attn_status_t attn_prefill_fwd_ws(const void* q, const void* k, const void* v, void* o, float* lse,
+                                  attn_dtype_t dtype, int B, int Hq, int Hkv, int q_len, int kv_len, int D,
+                                  float scale, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                  void* stream) {
     if (q == nullptr || k == nullptr || v == nullptr || o == nullptr) return ATTN_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return ATTN_ERR_INVALID_ARG;
     const attn_status_t shape_ok = prefill_shape_check(dtype, B, Hq, Hkv, q_len, kv_len, D, scale);
     if (shape_ok != ATTN_OK) return shape_ok;
-    PrefillArgs a{q, k, v, o, lse, static_cast<int>(dtype), B, Hq, Hkv, q_len, kv_len, D, scale, dev_status};
+    if (workspace != nullptr) {
+        if (!aligned16(workspace) ||
+            workspace_bytes < attn_prefill_workspace_bytes(dtype, B, Hq, Hkv, q_len, kv_len, D))
+            return ATTN_ERR_WORKSPACE;
+    }
+    PrefillArgs a{q, k, v, o, lse, static_cast<int>(dtype), B, Hq, Hkv, q_len, kv_len, D, scale, dev_status,
+                  workspace, workspace_bytes};
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (dtype == ATTN_BF16 && prefill_tc_supported(a)) return from_cuda(launch_prefill_tc(a, s));
     return from_cuda(launch_prefill_simt(a, s));
@@ -224,7 +258,9 @@ size_t attn_prefill_host_workspace_bytes(attn_dtype_t dtype, int B, int Hq, int 
     const size_t qb = static_cast<size_t>(B) * Hq * q_len * D * elem;
     const size_t kvb = static_cast<size_t>(B) * Hkv * kv_len * D * elem;
     const size_t lb = static_cast<size_t>(B) * Hq * q_len * sizeof(float);
-    return 2 * round16(qb) + 2 * round16(kvb) + round16(lb);   // Q, O, K, V, LSE
+    // Q, O, K, V, LSE, then the split-schedule scratch
+    return 2 * round16(qb) + 2 * round16(kvb) + round16(lb) +
+           attn_prefill_workspace_bytes(dtype, B, Hq, Hkv, q_len, kv_len, D);
 }
 
 attn_status_t attn_prefill_fwd_host(const void* q_host, const void* k_host, const void* v_host, void* o_host,
@@ -246,14 +282,23 @@ attn_status_t attn_prefill_fwd_host(const void* q_host, const void* k_host, cons
     void* dk = w + 2 * round16(qb);
     void* dv = w + 2 * round16(qb) + round16(kvb);
     float* dl = reinterpret_cast<float*>(w + 2 * round16(qb) + 2 * round16(kvb));
+    char* split_ws = w + 2 * round16(qb) + 2 * round16(kvb) + round16(lb);
+    const size_t split_bytes = attn_prefill_workspace_bytes(dtype, B, Hq, Hkv, q_len, kv_len, D);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // one copy per tensor, in, then the prefill, then one copy per result, out
     if (cudaMemcpyAsync(dq, q_host, qb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
         cudaMemcpyAsync(dk, k_host, kvb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
         cudaMemcpyAsync(dv, v_host, kvb, cudaMemcpyHostToDevice, s) != cudaSuccess)
         return ATTN_ERR_CUDA;
-    const attn_status_t st = attn_prefill_fwd(dq, dk, dv, dout, lse_host != nullptr ? dl : nullptr, dtype, B, Hq,
-                                              Hkv, q_len, kv_len, D, scale, dev_status, stream);
+    if (split_bytes > 0) {
+        // this workspace is the caller's scratch: the split counters start at zero here
+        PrefillArgs a{nullptr, nullptr, nullptr, nullptr, nullptr, static_cast<int>(dtype), B, Hq, Hkv, q_len,
+                      kv_len, D, scale, nullptr, nullptr, 0};
+        if (cudaMemsetAsync(split_ws, 0, prefill_tc_counter_bytes(a), s) != cudaSuccess) return ATTN_ERR_CUDA;
+    }
+    const attn_status_t st = attn_prefill_fwd_ws(dq, dk, dv, dout, lse_host != nullptr ? dl : nullptr, dtype, B, Hq,
+                                                 Hkv, q_len, kv_len, D, scale, split_bytes > 0 ? split_ws : nullptr,
+                                                 split_bytes, dev_status, stream);
     if (st != ATTN_OK) return st;
     if (cudaMemcpyAsync(o_host, dout, qb, cudaMemcpyDeviceToHost, s) != cudaSuccess) return ATTN_ERR_CUDA;
     if (lse_host != nullptr && cudaMemcpyAsync(lse_host, dl, lb, cudaMemcpyDeviceToHost, s) != cudaSuccess)

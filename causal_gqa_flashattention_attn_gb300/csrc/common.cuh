@@ -76,10 +76,18 @@ struct PrefillArgs {
     int B, Hq, Hkv, q_len, kv_len, D;
     float scale;
     int32_t* dev_status;
+    void* ws;          // split-schedule scratch (NULL: whole items only)
+    size_t ws_bytes;
 };
 cudaError_t launch_prefill_simt(const PrefillArgs& a, cudaStream_t stream);
 bool prefill_tc_supported(const PrefillArgs& a);
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream);
+// Scratch of the split schedule on a device with `sms` SMs, and the leading
+// part of it (the counters) that must be zero when a launch starts.
+size_t prefill_tc_workspace_bytes(const PrefillArgs& a, int sms);
+size_t prefill_tc_counter_bytes(const PrefillArgs& a);
+// 1 if a launch with a workspace takes the split schedule, else 0; *grid = its CTAs.
+int prefill_tc_plan(const PrefillArgs& a, int sms, int* grid);
 
 struct VarlenArgs {
     const void* q;          // [total_q, Hq, D] bf16

@@ -37,6 +37,9 @@
 // beforehand by gather_pages_kernel.
 #include <cuda_bf16.h>
 
+#include <algorithm>
+#include <vector>
+
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -63,6 +66,10 @@ constexpr int kOffQ = 0;                        // 2 tiles
 constexpr int kOffK = kOffQ + 2 * kTile;        // kStages tiles
 constexpr int kOffV = kOffK + kStages * kTile;  // kStages tiles
 constexpr int kSmemBytes = kOffV + kStages * kTile;
+// dense layout only: a 64-column half of each softmax warpgroup's O tile,
+// staged for a TMA store (the ragged mode's static tables leave no room)
+constexpr int kOffStage = kSmemBytes;
+constexpr int kSmemDense = kOffStage + 2 * kHalf;
 // TMEM columns
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;    // + 128 * tile
@@ -83,11 +90,20 @@ struct Params {
     const __nv_bfloat16* v_pool;
     int page_size, pool_rows;
     int gathered;   // K/V come by TMA from a contiguous copy in page-list order
+    // split schedule (dense only): the (item, KV tile) steps in item order
+    // (batch, KV head, query block), cut into gridDim.x equal ranges
+    long long sk_total;   // KV tile steps of all items
+    long long sk_per_bh;  // KV tile steps of one (batch, KV head)
+    int sk_zero_qb;       // leading query blocks that see no key
+    int32_t* sk_count;    // [n_items][2 tiles][arrived, stored], zero between launches
+    float* sk_o;          // [2 * gridDim.x slots][2 tiles][32 column quads][128 rows][4]
+    float* sk_ml;         // [2 * gridDim.x slots][2 tiles][m, l][128 rows]
 };
 
 struct Item {
     int b, kvh, p0, n_kv;
     int q_start, q_len, delta, kv_len, kv_base;   // per-sequence extent (varlen: ragged)
+    int j0, j1;           // KV tiles [j0, j1) of this piece of the item
 };
 
 constexpr int kMaxVarlenSeqs = 2048;   // sequences per ragged batch (prefix table in shared memory)
@@ -98,11 +114,15 @@ constexpr int kMaxOrder = 4096;
 constexpr int kOrderBuckets = 512;      // sort keys: KV tiles, 511 and more share the top bucket
 constexpr int kPairQbBits = 21;
 
-// Work item `idx` of the snake-ordered, longest-first list.
-__device__ __forceinline__ Item item_of(const Params& p, int idx) {
-    const int bh_count = p.B * p.Hkv;
-    const int qb = p.n_qb - 1 - idx / bh_count;
-    const int bh = idx % bh_count;
+// KV tiles that query block qb (2P positions) of the dense layout sees.
+__host__ __device__ __forceinline__ int dense_qb_tiles(int q_len, int kv_len, int P, int qb) {
+    const int p_last = min(qb * 2 * P + 2 * P, q_len) - 1;
+    const int kv_end = min(kv_len, p_last + kv_len - q_len + 1);
+    return kv_end > 0 ? (kv_end + kBN - 1) / kBN : 0;
+}
+
+// The whole item of (batch * Hkv + KV head) bh and query block qb.
+__device__ __forceinline__ Item dense_item(const Params& p, int bh, int qb) {
     Item it;
     it.b = bh / p.Hkv;
     it.kvh = bh % p.Hkv;
@@ -112,10 +132,85 @@ __device__ __forceinline__ Item item_of(const Params& p, int idx) {
     it.kv_len = p.kv_len;
     it.kv_base = 0;
     it.delta = p.kv_len - p.q_len;
-    const int p_last = min(it.p0 + 2 * p.P, p.q_len) - 1;
-    const int kv_end = min(p.kv_len, p_last + it.delta + 1);
-    it.n_kv = kv_end > 0 ? (kv_end + kBN - 1) / kBN : 0;
+    it.n_kv = dense_qb_tiles(p.q_len, p.kv_len, p.P, qb);
+    it.j0 = 0;
+    it.j1 = it.n_kv;
     return it;
+}
+
+// Work item `idx` of the snake-ordered, longest-first list.
+__device__ __forceinline__ Item item_of(const Params& p, int idx) {
+    const int bh_count = p.B * p.Hkv;
+    return dense_item(p, idx % bh_count, p.n_qb - 1 - idx / bh_count);
+}
+
+// Split schedule: the CTA whose range [L0, L1) holds step L, where CTA c
+// owns [c * total / grid, (c + 1) * total / grid).
+__device__ __forceinline__ int split_cta_of(const Params& p, long long L) {
+    return static_cast<int>(((L + 1) * gridDim.x - 1) / p.sk_total);
+}
+
+// Position of a CTA's walk through the split schedule: step L of the
+// current item (bh, qb), which starts at step `start`; the range ends at L1.
+// After split_next it still describes the item of the piece it returned.
+struct SplitWalk {
+    long long L, L1, start;
+    int bh, qb;
+};
+
+// Next piece of this CTA's range: the steps of one item that fall in it.
+// Items that see no key are skipped (the softmax warps write them apart).
+__device__ __forceinline__ bool split_next(const Params& p, SplitWalk& w, Item& it) {
+    while (w.L < w.L1) {
+        const int n = dense_qb_tiles(p.q_len, p.kv_len, p.P, w.qb);
+        const long long end = w.start + n;
+        if (w.L >= end) {
+            w.start = end;
+            if (++w.qb == p.n_qb) {
+                w.qb = 0;
+                ++w.bh;
+            }
+            continue;
+        }
+        it = dense_item(p, w.bh, w.qb);
+        it.j0 = static_cast<int>(w.L - w.start);
+        const long long stop = end < w.L1 ? end : w.L1;
+        it.j1 = static_cast<int>(stop - w.start);
+        w.L = stop;
+        return true;
+    }
+    return false;
+}
+
+// Split schedule (one warp): the item holding this CTA's first step.
+// Lanes take 32 query blocks at a time and scan their tile counts.
+__device__ void split_find_start(const Params& p, long long L0, SplitWalk& w, int lane) {
+    const int bh = static_cast<int>(L0 / p.sk_per_bh);
+    const long long r = L0 - bh * p.sk_per_bh;
+    long long acc = 0;
+    w.bh = bh;
+    w.qb = 0;
+    w.start = static_cast<long long>(bh) * p.sk_per_bh;
+    for (int q0 = 0; q0 < p.n_qb; q0 += 32) {
+        const int q = q0 + lane;
+        const long long n = q < p.n_qb ? dense_qb_tiles(p.q_len, p.kv_len, p.P, q) : 0;
+        long long cum = n;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const long long v = __shfl_up_sync(0xffffffffu, cum, off);
+            if (lane >= off) cum += v;
+        }
+        const long long total = __shfl_sync(0xffffffffu, cum, 31);
+        if (acc + total > r) {
+            const int first = __ffs(__ballot_sync(0xffffffffu, acc + cum > r)) - 1;
+            const long long cum_f = __shfl_sync(0xffffffffu, cum, first);
+            const long long n_f = __shfl_sync(0xffffffffu, n, first);
+            w.qb = q0 + first;
+            w.start += acc + cum_f - n_f;
+            return;
+        }
+        acc += total;
+    }
 }
 
 // Ragged batch: the item of sequence b, query block qb (2P positions) and KV
@@ -135,6 +230,8 @@ __device__ __forceinline__ Item varlen_item(const Params& p, int b, int qb, int 
     const int p_last = min(it.p0 + 2 * p.P, it.q_len) - 1;
     const int kv_end = min(it.kv_len, p_last + it.delta + 1);
     it.n_kv = kv_end > 0 ? (kv_end + kBN - 1) / kBN : 0;
+    it.j0 = 0;
+    it.j1 = it.n_kv;
     return it;
 }
 
@@ -269,10 +366,13 @@ __device__ __forceinline__ int cta_item(int i) {
 // r = pos * G + head) and K/V rows are gathered from a paged pool through the
 // page list by the producer warp with 16-byte cp.async copies into the
 // 128-byte-swizzled tile layout (TMA tile loads need contiguous rows).
-template <bool kVarlen>
+// kSplit (dense only): the split schedule, where an item whose KV tiles are
+// cut between CTAs is finished by the piece that ends last (see the epilogue).
+template <bool kVarlen, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap k_map,
-                      const __grid_constant__ CUtensorMap v_map, const Params p) {
+                      const __grid_constant__ CUtensorMap v_map, const __grid_constant__ CUtensorMap o_map,
+                      const Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align_1024(smem_raw);
     __shared__ int prefix[kVarlen ? kMaxVarlenSeqs + 1 : 1];
@@ -283,6 +383,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ __align__(8) uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_sh;
+    __shared__ SplitWalk walk_sh[kThreads / 32];          // split schedule: each warp's position
+    __shared__ __align__(8) uint64_t sk_bar[2];           // split epilogue: a tile's 128 threads meet
+    __shared__ __align__(8) uint64_t epi_bar[2];          // O staging: a tile's 128 threads meet
+    __shared__ int sk_word[2];                            // split epilogue: arrival order / go flag
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -302,6 +406,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&p_full[t], 128);
             mbar_init(&o_full[t], 1);
             mbar_init(&o_empty[t], 128);
+            mbar_init(&sk_bar[t], 128);
+            mbar_init(&epi_bar[t], 128);
         }
         abort_sh = 0;
         fence_mbar_init();
@@ -318,6 +424,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (prefix[p.B] / p.Hkv <= kMaxOrder) varlen_sort_pairs(p, order, bucket, lane);
         }
     }
+    if constexpr (kSplit) {
+        if (warp == 0) {
+            const long long L0 = static_cast<long long>(blockIdx.x) * p.sk_total / gridDim.x;
+            SplitWalk w;
+            split_find_start(p, L0, w, lane);
+            if (lane == 0) {
+                w.L = L0;
+                w.L1 = static_cast<long long>(blockIdx.x + 1) * p.sk_total / gridDim.x;
+                for (int k = 0; k < kThreads / 32; ++k) walk_sh[k] = w;
+            }
+        }
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -331,6 +449,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                                static_cast<int>(pair & ((1u << kPairQbBits) - 1u)), idx % p.Hkv);
         } else {
             return item_of(p, idx);
+        }
+    };
+    // every role walks the same sequence of items (or, split, of item
+    // pieces); the split position lives in shared memory, one per warp, so
+    // that it holds no registers across the KV loops
+    struct Walker {
+        int i;
+    };
+    auto walk_begin = [&]() -> Walker { return Walker{0}; };
+    auto walk_next = [&](Walker& k, Item& it) -> bool {
+        if constexpr (kSplit) {
+            const unsigned act = __activemask();
+            SplitWalk w = walk_sh[warp];
+            const bool got = split_next(p, w, it);
+            __syncwarp(act);
+            if (lane == __ffs(act) - 1) walk_sh[warp] = w;
+            __syncwarp(act);
+            return got;
+        } else {
+            const int idx = cta_item(k.i++);
+            if (idx >= n_items) return false;
+            it = get_item(idx);
+            return true;
         }
     };
 
@@ -356,30 +497,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float sl2 = p.scale_log2;
         uint32_t kv_iter = 0, item_iter = 0;
         bool ok = true;
-        for (int i = 0; ok; ++i) {
-            const int idx = cta_item(i);
-            if (idx >= n_items) break;
-            const Item it = get_item(idx);
-            const int delta = it.delta;
-            // tile row -> (query position, head): head-major rows for the dense
-            // layout, position-major rows for the ragged [total_q, Hq, D] layout
+        // this thread's row of item `it`: query position, head, output row
+        auto row_of = [&](const Item& it, int& pos, size_t& row_id) {
+            // head-major rows for the dense layout, position-major rows for
+            // the ragged [total_q, Hq, D] layout
             const int head = it.kvh * p.G + (kVarlen ? r % p.G : r / p.P);
-            const int pos = it.p0 + t * p.P + (kVarlen ? r / p.G : r % p.P);
+            pos = it.p0 + t * p.P + (kVarlen ? r / p.G : r % p.P);
+            row_id = kVarlen ? (static_cast<size_t>(it.q_start) + pos) * p.Hq + head
+                             : (static_cast<size_t>(it.b) * p.Hq + head) * p.q_len + pos;
+        };
+        // a row that sees no key: O = 0, LSE = -inf
+        auto write_empty = [&](size_t row_id) {
+            uint4* orow = reinterpret_cast<uint4*>(p.o + row_id * kD);
+            for (int c = 0; c < kD / 8; ++c) orow[c] = make_uint4(0, 0, 0, 0);
+            if (p.lse != nullptr) p.lse[row_id] = -INFINITY;
+        };
+        if constexpr (kSplit) {
+            // the split walk skips the leading query blocks that see no key
+            const int zq = p.sk_zero_qb;
+            for (int k = blockIdx.x; k < p.B * p.Hkv * zq; k += gridDim.x) {
+                int pos;
+                size_t row_id;
+                row_of(dense_item(p, k / zq, k % zq), pos, row_id);
+                if (pos < p.q_len) write_empty(row_id);
+            }
+        }
+        Walker wk = walk_begin();
+        for (Item it; ok && walk_next(wk, it);) {
+            const int delta = it.delta;
+            int pos;
+            size_t row_id;
+            row_of(it, pos, row_id);
             const bool row_real = pos < it.q_len;
-            const size_t row_id = kVarlen ? (static_cast<size_t>(it.q_start) + pos) * p.Hq + head
-                                          : (static_cast<size_t>(it.b) * p.Hq + head) * p.q_len + pos;
             if (it.n_kv == 0) {
-                if (row_real) {
-                    uint4* orow = reinterpret_cast<uint4*>(p.o + row_id * kD);
-                    for (int c = 0; c < kD / 8; ++c) orow[c] = make_uint4(0, 0, 0, 0);
-                    if (p.lse != nullptr) p.lse[row_id] = -INFINITY;
-                }
+                if (row_real) write_empty(row_id);
                 continue;
             }
             const int pos_min = it.p0 + t * p.P;     // smallest position of this tile
             const int lim_row = pos + delta;         // last visible key of this row
             float m = -INFINITY, l = 0.f;
-            for (int j = 0; j < it.n_kv; ++j, ++kv_iter) {
+            bool o_live = false;   // O_t holds this piece's accumulation (after its first P.V)
+            for (int j = it.j0; j < it.j1; ++j, ++kv_iter) {
                 if (!(ok = wait(&s_full[t], kv_iter & 1))) break;
                 tc_fence_after();
                 uint32_t sr[4][32];
@@ -411,7 +569,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     m = mx;
                     l *= alpha;
                 }
-                if (j > 0 && __any_sync(0xffffffffu, grow)) {
+                if (o_live && __any_sync(0xffffffffu, grow)) {
                     // O_t is idle here: the commit that announced S_t also covers
                     // the P.V of the previous tile
 #pragma unroll
@@ -449,36 +607,203 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(&p_full[t]);
+                o_live = true;
             }
             if (!ok) break;
             // -------------------------------------------------------------- epilogue
-            if (!(ok = wait(&o_full[t], item_iter & 1))) break;
-            tc_fence_after();
-            const bool alive = l > 0.f;
-            const float inv_l = alive ? 1.f / l : 0.f;
-            uint4* orow = reinterpret_cast<uint4*>(p.o + row_id * kD);
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t orr[32];
-                tmem_ld32(o_addr + 32 * c, orr);
-                tmem_ld_wait();
-                if (row_real) {
-#pragma unroll
-                    for (int e = 0; e < 32; e += 8) {
-                        uint4 v;
-                        v.x = pack_bf16x2(__uint_as_float(orr[e]) * inv_l, __uint_as_float(orr[e + 1]) * inv_l);
-                        v.y = pack_bf16x2(__uint_as_float(orr[e + 2]) * inv_l, __uint_as_float(orr[e + 3]) * inv_l);
-                        v.z = pack_bf16x2(__uint_as_float(orr[e + 4]) * inv_l, __uint_as_float(orr[e + 5]) * inv_l);
-                        v.w = pack_bf16x2(__uint_as_float(orr[e + 6]) * inv_l, __uint_as_float(orr[e + 7]) * inv_l);
-                        orow[(32 * c + e) / 8] = v;
-                    }
+            // Split schedule, an item cut between CTAs: each piece takes an
+            // arrival ticket (while its last P.V still runs).  Every piece but
+            // the last stores its unnormalised O, m and l (fp32) in its CTA's
+            // slot; the last waits until they are stored, merges them with its
+            // own by LSE weighting, writes O and LSE and zeroes the counters.
+            // Pieces that arrived never wait, so the wait always ends.
+            int np = 1, c0 = 0, arrival = 0;
+            int32_t* ctr = nullptr;
+            // the tile's 128 threads meet (bounded wait); every cut piece meets
+            // twice, so the barrier's phases go 0, 1, 0, 1, ...
+            auto wg_sync = [&](uint32_t phase) -> bool {
+                mbar_arrive(&sk_bar[t]);
+                return wait(&sk_bar[t], phase);
+            };
+            if constexpr (kSplit) {
+                const SplitWalk w = walk_sh[warp];   // still the item of this piece
+                const long long item_end = w.start + dense_qb_tiles(p.q_len, p.kv_len, p.P, w.qb);
+                c0 = split_cta_of(p, w.start);
+                np = split_cta_of(p, item_end - 1) - c0 + 1;
+                if (np > 1) {
+                    ctr = p.sk_count + ((static_cast<size_t>(w.bh) * p.n_qb + w.qb) * 2 + t) * 2;
+                    if (r == 0) sk_word[t] = atomicAdd(ctr, 1);
+                    if (!(ok = wg_sync(0))) break;
+                    arrival = sk_word[t];
                 }
             }
-            tc_fence_before();
-            mbar_arrive(&o_empty[t]);
-            if (row_real && p.lse != nullptr) p.lse[row_id] = alive ? (m * kLn2 + logf(l)) : -INFINITY;
-            ++item_iter;
+            if (!(ok = wait(&o_full[t], item_iter & 1))) break;
+            tc_fence_after();
+            row_of(it, pos, row_id);   // recomputed: not held in registers across the KV loop
+            if (np == 1 || arrival < np - 1) {
+                // O leaves TMEM in one round trip, and the next item's P.V may
+                // overwrite it while this one is written out
+                uint32_t ov[4][32];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tmem_ld32(o_addr + 32 * c, ov[c]);
+                tmem_ld_wait();
+                tc_fence_before();
+                mbar_arrive(&o_empty[t]);
+                ++item_iter;
+                if (np == 1) {
+                    const bool alive = l > 0.f;
+                    const float inv_l = alive ? 1.f / l : 0.f;
+                    auto pack8 = [&](int c, int e) {   // columns 32 c + e .. + 7 of this row, as bf16
+                        uint4 v;
+                        v.x = pack_bf16x2(__uint_as_float(ov[c][e]) * inv_l, __uint_as_float(ov[c][e + 1]) * inv_l);
+                        v.y = pack_bf16x2(__uint_as_float(ov[c][e + 2]) * inv_l, __uint_as_float(ov[c][e + 3]) * inv_l);
+                        v.z = pack_bf16x2(__uint_as_float(ov[c][e + 4]) * inv_l, __uint_as_float(ov[c][e + 5]) * inv_l);
+                        v.w = pack_bf16x2(__uint_as_float(ov[c][e + 6]) * inv_l, __uint_as_float(ov[c][e + 7]) * inv_l);
+                        return v;
+                    };
+                    if constexpr (!kVarlen) {
+                        // Each 64-column half of the tile goes through this warpgroup's
+                        // 16 KB stage (128-byte swizzle, row r at r * 128) and leaves
+                        // by one TMA store of the box {64, P, G} its Q came in by, so
+                        // the rows reach memory as whole lines; rows past q_len are
+                        // clipped by the store.  Four meetings per item: phases 0 1 0 1.
+                        uint8_t* stage = smem + kOffStage + t * kHalf;
+                        const bool tile_real = it.p0 + t * p.P < p.q_len;
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            if (r == 0) bulk_wait_read_all();   // the stage's last store has read it
+                            mbar_arrive(&epi_bar[t]);
+                            if (!(ok = wait(&epi_bar[t], 0))) break;
+#pragma unroll
+                            for (int cc = 0; cc < 8; ++cc)
+                                *reinterpret_cast<uint4*>(stage + r * 128 + ((cc ^ (r & 7)) << 4)) =
+                                    pack8(2 * h + (cc >> 2), 8 * (cc & 3));
+                            fence_proxy_async_smem();   // generic-proxy writes -> the TMA's reads
+                            mbar_arrive(&epi_bar[t]);
+                            if (!(ok = wait(&epi_bar[t], 1))) break;
+                            if (r == 0 && tile_real) {
+                                tma_store_3d(&o_map, stage, h * 64, it.p0 + t * p.P, it.b * p.Hq + it.kvh * p.G);
+                                bulk_commit();
+                            }
+                        }
+                        if (!ok) break;
+                    } else if (row_real) {
+                        uint4* orow = reinterpret_cast<uint4*>(p.o + row_id * kD);
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+#pragma unroll
+                            for (int e = 0; e < 32; e += 8) orow[(32 * c + e) / 8] = pack8(c, e);
+                    }
+                    if (row_real && p.lse != nullptr) p.lse[row_id] = alive ? (m * kLn2 + logf(l)) : -INFINITY;
+                } else {
+                    // the item's first piece (on CTA c0) has slot 2 c0 + 1, the others 2 c
+                    const int slot = 2 * static_cast<int>(blockIdx.x) + (c0 == static_cast<int>(blockIdx.x) ? 1 : 0);
+                    float4* dst = reinterpret_cast<float4*>(p.sk_o) + (static_cast<size_t>(slot) * 2 + t) * 32 * 128;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            dst[(c * 8 + q) * 128 + r] =
+                                make_float4(__uint_as_float(ov[c][4 * q]), __uint_as_float(ov[c][4 * q + 1]),
+                                            __uint_as_float(ov[c][4 * q + 2]), __uint_as_float(ov[c][4 * q + 3]));
+                    float* ml = p.sk_ml + (static_cast<size_t>(slot) * 2 + t) * 256;
+                    ml[r] = m;
+                    ml[128 + r] = l;
+                    __threadfence();
+                    if (!(ok = wg_sync(1))) break;   // sk_word[t] is read by every thread by now
+                    if (r == 0) atomicAdd(ctr + 1, 1);
+                }
+                continue;
+            }
+            if constexpr (kSplit) {
+                // the last piece to arrive: wait until the others are stored
+                if (r == 0) {
+                    bool stored = false;
+                    const uint64_t t0 = global_ns();
+                    for (uint32_t spin = 0;; ++spin) {
+                        if (ld_acquire_gpu(ctr + 1) >= np - 1) {
+                            stored = true;
+                            break;
+                        }
+                        if ((spin & 63u) == 63u &&
+                            (global_ns() - t0 > kWaitLimitNs || *reinterpret_cast<volatile int*>(&abort_sh)))
+                            break;
+                    }
+                    if (stored) {
+                        ctr[0] = 0;
+                        ctr[1] = 0;
+                    } else {
+                        fail();
+                    }
+                    sk_word[t] = stored ? 1 : 0;
+                }
+                if (!(ok = wg_sync(1))) break;
+                if (!(ok = sk_word[t] != 0)) break;
+                // Pieces in CTA order, this CTA's own from TMEM, the others
+                // from their slots (the first piece, on CTA c0, in slot
+                // 2 c0 + 1, a later one in 2 c): the same sums whichever
+                // piece merges, so the result does not depend on timing.
+                const int self = static_cast<int>(blockIdx.x);
+                auto slot_of = [&](int c) { return static_cast<size_t>((2 * c + (c == c0 ? 1 : 0)) * 2 + t); };
+                float mm = m;
+                for (int c = c0; c < c0 + np; ++c)
+                    if (c != self) mm = fmaxf(mm, __ldcg(p.sk_ml + slot_of(c) * 256 + r));
+                const bool none = mm == -INFINITY;
+                float lsum = 0.f;
+                for (int c = c0; c < c0 + np; ++c) {
+                    const float mc = c == self ? m : __ldcg(p.sk_ml + slot_of(c) * 256 + r);
+                    const float lc = c == self ? l : __ldcg(p.sk_ml + slot_of(c) * 256 + 128 + r);
+                    lsum += none ? 0.f : lc * ex2(mc - mm);
+                }
+                const bool alive = lsum > 0.f;
+                const float inv = alive ? 1.f / lsum : 0.f;
+                uint4* orow = reinterpret_cast<uint4*>(p.o + row_id * kD);
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t orr[32];
+                    tmem_ld32(o_addr + 32 * c, orr);
+                    tmem_ld_wait();
+                    float acc[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) acc[e] = 0.f;
+                    for (int cc = c0; cc < c0 + np && !none; ++cc) {
+                        if (cc == self) {
+                            const float w = ex2(m - mm);
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) acc[e] = fmaf(w, __uint_as_float(orr[e]), acc[e]);
+                            continue;
+                        }
+                        const size_t so = slot_of(cc);
+                        const float w = ex2(__ldcg(p.sk_ml + so * 256 + r) - mm);
+                        const float4* src = reinterpret_cast<const float4*>(p.sk_o) + so * 32 * 128;
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            const float4 v = __ldcg(src + (c * 8 + q) * 128 + r);
+                            acc[4 * q] = fmaf(w, v.x, acc[4 * q]);
+                            acc[4 * q + 1] = fmaf(w, v.y, acc[4 * q + 1]);
+                            acc[4 * q + 2] = fmaf(w, v.z, acc[4 * q + 2]);
+                            acc[4 * q + 3] = fmaf(w, v.w, acc[4 * q + 3]);
+                        }
+                    }
+                    if (row_real) {
+#pragma unroll
+                        for (int e = 0; e < 32; e += 8) {
+                            uint4 v;
+                            v.x = pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
+                            v.y = pack_bf16x2(acc[e + 2] * inv, acc[e + 3] * inv);
+                            v.z = pack_bf16x2(acc[e + 4] * inv, acc[e + 5] * inv);
+                            v.w = pack_bf16x2(acc[e + 6] * inv, acc[e + 7] * inv);
+                            orow[(32 * c + e) / 8] = v;
+                        }
+                    }
+                }
+                if (row_real && p.lse != nullptr) p.lse[row_id] = alive ? (mm * kLn2 + logf(lsum)) : -INFINITY;
+                tc_fence_before();
+                mbar_arrive(&o_empty[t]);
+                ++item_iter;
+            }
         }
+        if (!kVarlen && r == 0) bulk_wait_all();   // O's TMA stores done before the CTA exits
     } else {
         regs_dec<kRegsControl>();
         if (warp == kProducerWarp && kVarlen && p.gathered) {
@@ -492,10 +817,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_prefetch_desc(&v_map);
                 uint32_t kv_iter = 0, item_iter = 0;
                 bool ok = true;
-                for (int i = 0; ok; ++i) {
-                    const int idx = cta_item(i);
-                    if (idx >= n_items) break;
-                    const Item it = get_item(idx);
+                Walker wk = walk_begin();
+                for (Item it; ok && walk_next(wk, it);) {
                     if (it.n_kv == 0) continue;
                     if (item_iter > 0 && !(ok = wait(&q_empty, (item_iter - 1) & 1))) break;
                     mbar_arrive_expect_tx(&q_full, 2 * kTile);
@@ -537,10 +860,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t swz = static_cast<uint32_t>(lane & 7);
             uint32_t kv_iter = 0, item_iter = 0;
             bool ok = true;
-            for (int i = 0; ok; ++i) {
-                const int idx = cta_item(i);
-                if (idx >= n_items) break;
-                const Item it = get_item(idx);
+            Walker wk = walk_begin();
+            for (Item it; ok && walk_next(wk, it);) {
                 if (it.n_kv == 0) continue;
                 if (lane == 0) {
                     if (item_iter > 0) ok = wait(&q_empty, (item_iter - 1) & 1);
@@ -611,10 +932,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_prefetch_desc(&v_map);
                 uint32_t kv_iter = 0, item_iter = 0;
                 bool ok = true;
-                for (int i = 0; ok; ++i) {
-                    const int idx = cta_item(i);
-                    if (idx >= n_items) break;
-                    const Item it = get_item(idx);
+                Walker wk = walk_begin();
+                for (Item it; ok && walk_next(wk, it);) {
                     if (it.n_kv == 0) continue;
                     if (item_iter > 0 && !(ok = wait(&q_empty, (item_iter - 1) & 1))) break;
                     mbar_arrive_expect_tx(&q_full, 2 * kTile);
@@ -623,8 +942,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int h = 0; h < 2; ++h)
                             tma_load_3d(smem + kOffQ + t * kTile + h * kHalf, &q_map, &q_full, h * 64, it.p0 + t * p.P,
                                         head0);
+                    {
+                        // the next item's Q into L2 now, so that its load after
+                        // this item's last S hits L2 rather than DRAM
+                        Item nx;
+                        bool has;
+                        if constexpr (kSplit) {
+                            SplitWalk w = walk_sh[warp];
+                            has = split_next(p, w, nx);
+                        } else {
+                            const int idx = cta_item(wk.i);
+                            has = idx < n_items;
+                            if (has) nx = get_item(idx);
+                        }
+                        if (has && nx.n_kv > 0)
+                            for (int t = 0; t < 2; ++t)
+                                for (int h = 0; h < 2; ++h)
+                                    tma_prefetch_l2_3d(&q_map, h * 64, nx.p0 + t * p.P, nx.b * p.Hq + nx.kvh * p.G);
+                    }
                     const int kvrow = it.b * p.Hkv + it.kvh;
-                    for (int j = 0; j < it.n_kv; ++j, ++kv_iter) {
+                    for (int j = it.j0; j < it.j1; ++j, ++kv_iter) {
                         const int s = kv_iter % kStages;
                         const uint32_t par = ((kv_iter / kStages) - 1) & 1;
                         if (kv_iter >= kStages && !(ok = wait(&k_empty[s], par))) break;
@@ -667,10 +1004,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 };
                 uint32_t kv_iter = 0, item_iter = 0;
                 bool ok = true;
-                for (int i = 0; ok; ++i) {
-                    const int idx = cta_item(i);
-                    if (idx >= n_items) break;
-                    const Item it = get_item(idx);
+                Walker wk = walk_begin();
+                for (Item it; ok && walk_next(wk, it);) {
                     if (it.n_kv == 0) continue;
                     if (!(ok = wait(&q_full, item_iter & 1))) break;
                     if (!(ok = wait(&k_full[kv_iter % kStages], (kv_iter / kStages) & 1))) break;
@@ -681,18 +1016,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     issue_s(1, kv_iter % kStages);
                     umma_commit(&s_full[1]);
                     umma_commit(&k_empty[kv_iter % kStages]);   // K_j no longer read
-                    if (it.n_kv == 1) umma_commit(&q_empty);  // Q no longer read: the producer may refill it
-                    for (int j = 0; j < it.n_kv && ok; ++j, ++kv_iter) {
+                    if (it.j1 - it.j0 == 1) umma_commit(&q_empty);  // Q no longer read: the producer may refill it
+                    for (int j = it.j0; j < it.j1 && ok; ++j, ++kv_iter) {
                         const int s = kv_iter % kStages;
-                        const bool last = (j + 1 == it.n_kv);
+                        const bool last = (j + 1 == it.j1);
                         const uint32_t nxt = kv_iter + 1;
                         if (!(ok = wait(&v_full[s], (kv_iter / kStages) & 1))) break;
                         if (cp_async_tiles) fence_proxy_async_smem();
                         for (int t = 0; t < 2; ++t) {
                             if (!(ok = wait(&p_full[t], kv_iter & 1))) break;
-                            if (j == 0 && item_iter > 0 && !(ok = wait(&o_empty[t], (item_iter - 1) & 1))) break;
+                            if (j == it.j0 && item_iter > 0 && !(ok = wait(&o_empty[t], (item_iter - 1) & 1))) break;
                             tc_fence_after();
-                            issue_pv(t, s, j > 0);                    // O_t (+)= P_t V_j
+                            issue_pv(t, s, j > it.j0);                   // O_t (+)= P_t V_j
                             if (t == 1) umma_commit(&v_empty[s]);     // V_j no longer read
                             if (!last) {
                                 if (t == 0) {
@@ -703,7 +1038,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 issue_s(t, nxt % kStages);            // S_t = Q_t K_{j+1}^T (after P_t is read)
                                 umma_commit(&s_full[t]);
                                 if (t == 1) umma_commit(&k_empty[nxt % kStages]);   // K_{j+1} no longer read
-                                if (t == 1 && j + 2 == it.n_kv) umma_commit(&q_empty);  // last S read Q
+                                if (t == 1 && j + 2 == it.j1) umma_commit(&q_empty);  // last S read Q
                             } else {
                                 umma_commit(&o_full[t]);
                             }
@@ -766,6 +1101,105 @@ __global__ void __launch_bounds__(256) gather_pages_kernel(const uint4* __restri
 
 }  // namespace
 
+namespace {
+
+// Cost model of the two schedules, in KV tile steps of one CTA (a step is
+// about 1.8 us on GB300): a piece costs its steps plus kPieceCost (Q load,
+// pipeline fill, epilogue: measured at about 2 steps), a piece of a cut item
+// kMergeCost more (its fp32 partial stored, or the others merged).  The
+// split schedule is taken only when it is expected to be kSplitGain faster.
+constexpr double kPieceCost = 2.0;
+constexpr double kMergeCost = 1.5;
+constexpr double kSplitGain = 0.9;
+
+struct SplitPlan {
+    bool split;
+    long long total, per_bh;
+    int zero_qb, grid;
+};
+
+// Chooses between whole items, longest first in snake order, and the split
+// schedule; the split one only when it is expected to finish sooner.  Few
+// items (the tail of whole items is then large) is where splitting pays.
+SplitPlan plan_schedule(int B, int Hkv, int q_len, int kv_len, int P, int n_qb, int sms, bool have_ws) {
+    SplitPlan pl{false, 0, 0, 0, 0};
+    const long long bh = static_cast<long long>(B) * Hkv;
+    if (!have_ws || bh * n_qb >= 8LL * sms) return pl;
+    std::vector<int> tiles(n_qb);
+    for (int qb = 0; qb < n_qb; ++qb) {
+        tiles[qb] = dense_qb_tiles(q_len, kv_len, P, qb);
+        pl.per_bh += tiles[qb];
+        if (tiles[qb] == 0) pl.zero_qb = qb + 1;
+    }
+    pl.total = bh * pl.per_bh;
+    if (pl.total == 0) return pl;
+    // whole items: the kernel's snake order over the longest-first list
+    const long long n_items = bh * n_qb;
+    const int grid_w = static_cast<int>(n_items < sms ? n_items : sms);
+    std::vector<double> load(grid_w, 0.0);
+    for (long long idx = 0; idx < n_items; ++idx) {
+        const long long round = idx / grid_w, k = idx % grid_w;
+        const int cta = static_cast<int>((round & 1) ? grid_w - 1 - k : k);
+        const int n = tiles[n_qb - 1 - idx / bh];
+        if (n > 0) load[cta] += n + kPieceCost;
+    }
+    const double whole = *std::max_element(load.begin(), load.end());
+    // split: equal ranges of the (item, KV tile) order
+    const int grid_s = static_cast<int>(pl.total < sms ? pl.total : sms);
+    std::vector<double> sload(grid_s, 0.0);
+    long long start = 0;
+    for (long long i = 0; i < n_items; ++i) {
+        const int n = tiles[i % n_qb];
+        if (n == 0) continue;
+        const long long end = start + n;
+        const int c0 = static_cast<int>(((start + 1) * grid_s - 1) / pl.total);
+        const int c1 = static_cast<int>((end * grid_s - 1) / pl.total);
+        for (int c = c0; c <= c1; ++c) {
+            const long long lo = std::max(start, static_cast<long long>(c) * pl.total / grid_s);
+            const long long hi = std::min(end, static_cast<long long>(c + 1) * pl.total / grid_s);
+            sload[c] += static_cast<double>(hi - lo) + kPieceCost + (c1 > c0 ? kMergeCost : 0.0);
+        }
+        start = end;
+    }
+    const double split = *std::max_element(sload.begin(), sload.end());
+    if (split < kSplitGain * whole) {
+        pl.split = true;
+        pl.grid = grid_s;
+    }
+    return pl;
+}
+
+size_t round16(size_t x) { return (x + 15) & ~static_cast<size_t>(15); }
+
+}  // namespace
+
+size_t prefill_tc_workspace_bytes(const PrefillArgs& a, int sms) {
+    const int G = a.Hq / a.Hkv;
+    const int P = kBM / G;
+    const long long n_items = static_cast<long long>(a.B) * a.Hkv * ((a.q_len + 2 * P - 1) / (2 * P));
+    const size_t counters = round16(static_cast<size_t>(n_items) * 2 * 2 * sizeof(int32_t));
+    const size_t o_part = static_cast<size_t>(2) * sms * 2 * kD * kBM * sizeof(float);
+    const size_t ml_part = static_cast<size_t>(2) * sms * 2 * 2 * kBM * sizeof(float);
+    return counters + o_part + ml_part;
+}
+
+size_t prefill_tc_counter_bytes(const PrefillArgs& a) {
+    const int G = a.Hq / a.Hkv;
+    const int P = kBM / G;
+    const long long n_items = static_cast<long long>(a.B) * a.Hkv * ((a.q_len + 2 * P - 1) / (2 * P));
+    return round16(static_cast<size_t>(n_items) * 2 * 2 * sizeof(int32_t));
+}
+
+int prefill_tc_plan(const PrefillArgs& a, int sms, int* grid) {
+    const int G = a.Hq / a.Hkv;
+    const int P = kBM / G;
+    const int n_qb = (a.q_len + 2 * P - 1) / (2 * P);
+    const SplitPlan pl = plan_schedule(a.B, a.Hkv, a.q_len, a.kv_len, P, n_qb, sms, true);
+    const long long n_items = static_cast<long long>(a.B) * a.Hkv * n_qb;
+    if (grid != nullptr) *grid = pl.split ? pl.grid : static_cast<int>(n_items < sms ? n_items : sms);
+    return pl.split ? 1 : 0;
+}
+
 bool prefill_tc_supported(const PrefillArgs& a) {
     if (a.dtype != ATTN_BF16 || a.D != kD) return false;
     const int G = a.Hq / a.Hkv;
@@ -795,6 +1229,15 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream) {
                               CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
     }
+    CUtensorMap o_map;   // O [B * Hq, q_len, D]: the Q map's geometry over the output
+    {
+        const uint64_t dims[3] = {kD, static_cast<uint64_t>(a.q_len), static_cast<uint64_t>(a.B) * a.Hq};
+        const uint64_t strides[2] = {kD * 2, static_cast<uint64_t>(a.q_len) * kD * 2};
+        const uint32_t box[3] = {64, static_cast<uint32_t>(P), static_cast<uint32_t>(G)};
+        if (!encode_tiled_map(&o_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.o, dims, strides, box,
+                              CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+    }
     Params p;
     p.o = static_cast<__nv_bfloat16*>(a.o);
     p.lse = a.lse;
@@ -815,12 +1258,30 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream) {
     p.gathered = 0;
     const int sms = device_sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
+    const SplitPlan pl = plan_schedule(a.B, a.Hkv, a.q_len, a.kv_len, P, p.n_qb, sms,
+                                       a.ws != nullptr && a.ws_bytes >= prefill_tc_workspace_bytes(a, sms));
+    p.sk_total = pl.total;
+    p.sk_per_bh = pl.per_bh;
+    p.sk_zero_qb = pl.zero_qb;
+    p.sk_count = nullptr;
+    p.sk_o = p.sk_ml = nullptr;
+    const size_t smem = kSmemDense + 1024;
+    if (pl.split) {
+        uint8_t* w = static_cast<uint8_t*>(a.ws);
+        p.sk_count = reinterpret_cast<int32_t*>(w);
+        p.sk_o = reinterpret_cast<float*>(w + prefill_tc_counter_bytes(a));
+        p.sk_ml = p.sk_o + static_cast<size_t>(2) * sms * 2 * kD * kBM;
+        cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<false, true>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        prefill_tc_kernel<false, true><<<pl.grid, kThreads, smem, stream>>>(q_map, k_map, v_map, o_map, p);
+        return cudaGetLastError();
+    }
     const int grid = p.n_items < sms ? p.n_items : sms;
-    const size_t smem = kSmemBytes + 1024;
-    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    prefill_tc_kernel<false><<<grid, kThreads, smem, stream>>>(q_map, k_map, v_map, p);
+    prefill_tc_kernel<false, false><<<grid, kThreads, smem, stream>>>(q_map, k_map, v_map, o_map, p);
     return cudaGetLastError();
 }
 
@@ -861,6 +1322,10 @@ cudaError_t launch_prefill_varlen_tc(const VarlenArgs& a, cudaStream_t stream) {
     p.k_pool = static_cast<const __nv_bfloat16*>(a.k_cache);
     p.v_pool = static_cast<const __nv_bfloat16*>(a.v_cache);
     p.gathered = a.kv_ws != nullptr;
+    p.sk_total = p.sk_per_bh = 0;
+    p.sk_zero_qb = 0;
+    p.sk_count = nullptr;
+    p.sk_o = p.sk_ml = nullptr;
     const int sms = device_sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
     k_map = v_map = q_map;
@@ -887,10 +1352,10 @@ cudaError_t launch_prefill_varlen_tc(const VarlenArgs& a, cudaStream_t stream) {
         if (ge != cudaSuccess) return ge;
     }
     const size_t smem = kSmemBytes + 1024;
-    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    prefill_tc_kernel<true><<<sms, kThreads, smem, stream>>>(q_map, k_map, v_map, p);
+    prefill_tc_kernel<true, false><<<sms, kThreads, smem, stream>>>(q_map, k_map, v_map, q_map, p);
     return cudaGetLastError();
 }
 

@@ -84,6 +84,44 @@ attn_status_t attn_prefill_fwd(const void* q, const void* k, const void* v,
                                float scale, int32_t* dev_status, void* stream);
 
 /*
+ * attn_prefill_fwd_ws - attn_prefill_fwd with scratch for a split schedule.
+ *
+ * Same operation, arguments and results as attn_prefill_fwd.  With a
+ * workspace, the bf16 tensor-core path may cut the KV range of a query block
+ * between CTAs when there are too few blocks to keep every SM busy to the
+ * end (few heads, short prompts).  Each piece keeps its own unnormalised O,
+ * running max m and sum l; the piece that finishes last combines them,
+ * O = sum_i 2^(m_i - M) O_i / sum_i 2^(m_i - M) l_i with M = max_i m_i, the
+ * LSE-weighted combination of "splitk_kernels.py", _splitK_reduce.  The host
+ * picks the schedule from the sizes alone; results agree with
+ * attn_prefill_fwd within rounding, not bit for bit.
+ *
+ *   workspace        device, 16-byte aligned, at least
+ *                    attn_prefill_workspace_bytes() bytes, or NULL (the
+ *                    whole-item schedule of attn_prefill_fwd).  Its first
+ *                    bytes are counters that must be zero when a call starts:
+ *                    zero the workspace once; every call that completes
+ *                    without a device error leaves them zero again, so
+ *                    consecutive calls on one stream can share it.  After a
+ *                    device error (dev_status != 0) zero it again.  Calls
+ *                    that may run at the same time need separate workspaces.
+ *   workspace_bytes  its size.
+ * Errors as attn_prefill_fwd; ATTN_ERR_WORKSPACE for a misaligned or short
+ * workspace.
+ */
+size_t attn_prefill_workspace_bytes(attn_dtype_t dtype, int B, int Hq, int Hkv, int q_len, int kv_len, int D);
+/* The schedule attn_prefill_fwd_ws takes on the current device: 1 split,
+ * 0 whole items (always 0 for the CUDA-core paths), -1 for invalid sizes or
+ * no device.  If grid is not NULL, *grid = the CTAs of the tensor-core launch
+ * (0 for the CUDA-core paths and on error). */
+int attn_prefill_plan(attn_dtype_t dtype, int B, int Hq, int Hkv, int q_len, int kv_len, int D, int* grid);
+attn_status_t attn_prefill_fwd_ws(const void* q, const void* k, const void* v,
+                                  void* o, float* lse, attn_dtype_t dtype,
+                                  int B, int Hq, int Hkv, int q_len, int kv_len, int D,
+                                  float scale, void* workspace, size_t workspace_bytes,
+                                  int32_t* dev_status, void* stream);
+
+/*
  * attn_prefill_fwd_host - attn_prefill_fwd on host buffers.
  *
  * Enqueues on `stream`: one host -> device copy each of q, k and v into
@@ -97,7 +135,9 @@ attn_status_t attn_prefill_fwd(const void* q, const void* k, const void* v,
  *   q_host, k_host, v_host, o_host, lse_host  host memory, shapes and dtype
  *                as the device buffers of attn_prefill_fwd
  *   workspace    device, 16-byte aligned, attn_prefill_host_workspace_bytes()
- *                bytes (the device copies of Q, O, K, V and LSE; overwritten)
+ *                bytes (the device copies of Q, O, K, V and LSE, then the
+ *                scratch of attn_prefill_fwd_ws, whose counters this call
+ *                zeroes on the stream first; overwritten)
  * Other arguments and errors as attn_prefill_fwd; ATTN_ERR_WORKSPACE for a
  * missing, misaligned or short workspace; ATTN_ERR_CUDA if a copy cannot be
  * enqueued.
@@ -361,7 +401,8 @@ attn_status_t attn_selftest_wait_timeout(int32_t* dev_status, unsigned int limit
 const char* attn_status_string(attn_status_t status);
 
 /* ABI version of this header (major * 100 + minor); 101 added attn_selftest_wait_timeout,
- * 102 attn_prefill_paged_varlen_ws, 103 attn_prefill_fwd_host. */
+ * 102 attn_prefill_paged_varlen_ws, 103 attn_prefill_fwd_host,
+ * 104 attn_prefill_fwd_ws, attn_prefill_workspace_bytes, attn_prefill_plan. */
 int attn_abi_version(void);
 
 #ifdef __cplusplus

@@ -39,7 +39,7 @@ def test_library_exports_every_declared_symbol(L):
     for name in declared_functions():
         assert hasattr(L, name), name
         assert name in attn.EXPORTED
-    assert L.attn_abi_version() == 103
+    assert L.attn_abi_version() == 104
 
 
 def test_status_strings(L):
@@ -95,6 +95,31 @@ def test_prefill_host_buffers_validation(L):
     assert call(ws=ctypes.c_void_p(0x10008)) == -3
     assert call(Hq=6, Hkv=4, ws_bytes=1 << 20) == -1     # Hq % Hkv != 0, before any copy is enqueued
     assert call(D=96, ws_bytes=1 << 20) == -2
+
+
+def test_prefill_ws_validation(L):
+    import causal_gqa_flashattention_attn_gb300 as attn
+
+    def call(**kw):
+        a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=None, dtype=1, B=1, Hq=4, Hkv=2, q_len=8, kv_len=8, D=128,
+                 scale=0.1, ws=FAKE, ws_bytes=1 << 30, status=None, stream=None)
+        a.update(kw)
+        return L.attn_prefill_fwd_ws(a["q"], a["k"], a["v"], a["o"], a["lse"], a["dtype"], a["B"], a["Hq"],
+                                     a["Hkv"], a["q_len"], a["kv_len"], a["D"], a["scale"], a["ws"], a["ws_bytes"],
+                                     a["status"], a["stream"])
+    assert call(q=None) == -1
+    assert call(o=ctypes.c_void_p(0x10004)) == -1
+    assert call(B=0) == -1
+    assert call(Hq=6, Hkv=4) == -1
+    assert call(scale=float("nan")) == -1
+    assert call(dtype=2) == -2
+    assert call(D=96) == -2
+    assert call(ws=ctypes.c_void_p(0x10008)) == -3        # misaligned workspace
+    # sizes of the split scratch and the schedule need a device; invalid sizes never do
+    assert attn.attn_prefill_plan(torch.bfloat16, 1, 4, 3, 8, 8, 128) == (-1, 0)
+    assert attn.attn_prefill_plan(torch.float32, 1, 4, 2, 8, 8, 64) == (0, 0)   # CUDA-core path: no split
+    assert attn.attn_prefill_workspace_bytes(torch.float32, 1, 4, 2, 8, 8, 64) == 0
+    assert attn.attn_prefill_workspace_bytes(torch.bfloat16, 0, 4, 2, 8, 8, 128) == 0
 
 
 def _decode(L, **kw):
