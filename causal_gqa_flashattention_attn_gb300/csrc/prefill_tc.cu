@@ -942,24 +942,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int h = 0; h < 2; ++h)
                             tma_load_3d(smem + kOffQ + t * kTile + h * kHalf, &q_map, &q_full, h * 64, it.p0 + t * p.P,
                                         head0);
-                    {
-                        // the next item's Q into L2 now, so that its load after
-                        // this item's last S hits L2 rather than DRAM
-                        Item nx;
-                        bool has;
-                        if constexpr (kSplit) {
-                            SplitWalk w = walk_sh[warp];
-                            has = split_next(p, w, nx);
-                        } else {
-                            const int idx = cta_item(wk.i);
-                            has = idx < n_items;
-                            if (has) nx = get_item(idx);
-                        }
-                        if (has && nx.n_kv > 0)
-                            for (int t = 0; t < 2; ++t)
-                                for (int h = 0; h < 2; ++h)
-                                    tma_prefetch_l2_3d(&q_map, h * 64, nx.p0 + t * p.P, nx.b * p.Hq + nx.kvh * p.G);
-                    }
                     const int kvrow = it.b * p.Hkv + it.kvh;
                     for (int j = it.j0; j < it.j1; ++j, ++kv_iter) {
                         const int s = kv_iter % kStages;

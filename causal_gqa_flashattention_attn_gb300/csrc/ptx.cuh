@@ -106,14 +106,6 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const void* desc, ui
         : "memory");
 }
 
-// Bring a tile of a tensor map into L2 (no shared-memory destination, no barrier).
-__device__ __forceinline__ void tma_prefetch_l2_3d(const void* desc, int c0, int c1, int c2) {
-    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global [%0, {%1, %2, %3}];" ::"l"(
-                     reinterpret_cast<uint64_t>(desc)),
-                 "r"(c0), "r"(c1), "r"(c2)
-                 : "memory");
-}
-
 __device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* desc, uint64_t* bar, int c0, int c1) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
