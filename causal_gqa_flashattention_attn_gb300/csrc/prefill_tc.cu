@@ -80,6 +80,7 @@ struct Params {
     float* lse;
     int32_t* status;
     int B, Hq, Hkv, q_len, kv_len, G, P, n_qb, n_items;
+    int sec_bh;   // whole items: (batch, KV head) pairs per section of the order (their K/V fits in L2)
     float scale_log2;
     // ragged batch over a paged cache (varlen mode only)
     const int32_t* qo_indptr;   // [B+1]
@@ -138,10 +139,20 @@ __device__ __forceinline__ Item dense_item(const Params& p, int bh, int qb) {
     return it;
 }
 
-// Work item `idx` of the snake-ordered, longest-first list.
+// Work item `idx` of the whole-item order: sections of sec_bh (batch, KV
+// head) pairs, whose K/V stays in L2 while the section runs; within a
+// section longest first (query blocks from the last), pairs inner.
+__host__ __device__ __forceinline__ void whole_item(int idx, int bh_count, int n_qb, int sec_bh, int& bh, int& qb) {
+    const int per_sec = sec_bh * n_qb;
+    const int sec = idx / per_sec, local = idx - sec * per_sec;
+    const int in_sec = min(sec_bh, bh_count - sec * sec_bh);   // the last section may be short
+    qb = n_qb - 1 - local / in_sec;
+    bh = sec * sec_bh + local % in_sec;
+}
 __device__ __forceinline__ Item item_of(const Params& p, int idx) {
-    const int bh_count = p.B * p.Hkv;
-    return dense_item(p, idx % bh_count, p.n_qb - 1 - idx / bh_count);
+    int bh, qb;
+    whole_item(idx, p.B * p.Hkv, p.n_qb, p.sec_bh, bh, qb);
+    return dense_item(p, bh, qb);
 }
 
 // Split schedule: the CTA whose range [L0, L1) holds step L, where CTA c
@@ -1103,7 +1114,8 @@ struct SplitPlan {
 // Chooses between whole items, longest first in snake order, and the split
 // schedule; the split one only when it is expected to finish sooner.  Few
 // items (the tail of whole items is then large) is where splitting pays.
-SplitPlan plan_schedule(int B, int Hkv, int q_len, int kv_len, int P, int n_qb, int sms, bool have_ws) {
+SplitPlan plan_schedule(int B, int Hkv, int q_len, int kv_len, int P, int n_qb, int sec_bh, int sms,
+                        bool have_ws) {
     SplitPlan pl{false, 0, 0, 0, 0};
     const long long bh = static_cast<long long>(B) * Hkv;
     if (!have_ws || bh * n_qb >= 8LL * sms) return pl;
@@ -1122,7 +1134,9 @@ SplitPlan plan_schedule(int B, int Hkv, int q_len, int kv_len, int P, int n_qb, 
     for (long long idx = 0; idx < n_items; ++idx) {
         const long long round = idx / grid_w, k = idx % grid_w;
         const int cta = static_cast<int>((round & 1) ? grid_w - 1 - k : k);
-        const int n = tiles[n_qb - 1 - idx / bh];
+        int b_h, qb;
+        whole_item(static_cast<int>(idx), static_cast<int>(bh), n_qb, sec_bh, b_h, qb);
+        const int n = tiles[qb];
         if (n > 0) load[cta] += n + kPieceCost;
     }
     const double whole = *std::max_element(load.begin(), load.end());
@@ -1153,6 +1167,24 @@ SplitPlan plan_schedule(int B, int Hkv, int q_len, int kv_len, int P, int n_qb, 
 
 size_t round16(size_t x) { return (x + 15) & ~static_cast<size_t>(15); }
 
+// (batch, KV head) pairs per section of the whole-item order.  A section's
+// K/V must fit in kSectionBytes (half of the 126 MB L2, the rest for the
+// streaming Q and O), and its items must fill whole rounds of `grid` CTAs:
+// the longest-first snake balances the CTAs only while item sizes fall from
+// round to round, and a round shared by two sections would mix the shortest
+// items of one with the longest of the next.  Without such a size, a single
+// section (all pairs, the plain longest-first order).
+constexpr double kSectionBytes = 64.0 * (1 << 20);
+int section_pairs(const PrefillArgs& a, int n_qb, int grid) {
+    const double kv_pair = 2.0 * a.kv_len * kD * 2;   // K and V of one pair, bf16
+    const int bh = a.B * a.Hkv;
+    const int most = static_cast<int>(kSectionBytes / kv_pair);
+    if (most >= bh) return bh;
+    for (int s = most; s >= 1; --s)
+        if ((static_cast<long long>(s) * n_qb) % grid == 0) return s;
+    return bh;
+}
+
 }  // namespace
 
 size_t prefill_tc_workspace_bytes(const PrefillArgs& a, int sms) {
@@ -1176,9 +1208,11 @@ int prefill_tc_plan(const PrefillArgs& a, int sms, int* grid) {
     const int G = a.Hq / a.Hkv;
     const int P = kBM / G;
     const int n_qb = (a.q_len + 2 * P - 1) / (2 * P);
-    const SplitPlan pl = plan_schedule(a.B, a.Hkv, a.q_len, a.kv_len, P, n_qb, sms, true);
     const long long n_items = static_cast<long long>(a.B) * a.Hkv * n_qb;
-    if (grid != nullptr) *grid = pl.split ? pl.grid : static_cast<int>(n_items < sms ? n_items : sms);
+    const int grid_w = static_cast<int>(n_items < sms ? n_items : sms);
+    const SplitPlan pl =
+        plan_schedule(a.B, a.Hkv, a.q_len, a.kv_len, P, n_qb, section_pairs(a, n_qb, grid_w), sms, true);
+    if (grid != nullptr) *grid = pl.split ? pl.grid : grid_w;
     return pl.split ? 1 : 0;
 }
 
@@ -1240,7 +1274,8 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream) {
     p.gathered = 0;
     const int sms = device_sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
-    const SplitPlan pl = plan_schedule(a.B, a.Hkv, a.q_len, a.kv_len, P, p.n_qb, sms,
+    p.sec_bh = section_pairs(a, p.n_qb, p.n_items < sms ? p.n_items : sms);
+    const SplitPlan pl = plan_schedule(a.B, a.Hkv, a.q_len, a.kv_len, P, p.n_qb, p.sec_bh, sms,
                                        a.ws != nullptr && a.ws_bytes >= prefill_tc_workspace_bytes(a, sms));
     p.sk_total = pl.total;
     p.sk_per_bh = pl.per_bh;
@@ -1294,6 +1329,7 @@ cudaError_t launch_prefill_varlen_tc(const VarlenArgs& a, cudaStream_t stream) {
     p.P = P;
     p.n_qb = 0;
     p.n_items = 0;   // counted on the device from qo_indptr
+    p.sec_bh = 1;
     p.scale_log2 = a.scale * kLog2e;
     p.qo_indptr = a.qo_indptr;
     p.kv_indptr = a.kv_indptr;
