@@ -36,6 +36,7 @@ ATTN_F32, ATTN_BF16, ATTN_F16, ATTN_INT4_PACKED, ATTN_FP8_E4M3 = 0, 1, 2, 3, 4
 ATTN_DEV_PAGE_OUT_OF_RANGE = 0x1
 ATTN_DEV_SEQ_TOO_LONG = 0x2
 ATTN_DEV_WAIT_TIMEOUT = 0x4
+ATTN_DEV_WORKSPACE_STATE = 0x8
 
 EXPORTED = ("attn_prefill_fwd", "attn_prefill_workspace_bytes", "attn_prefill_plan", "attn_prefill_fwd_ws", "attn_prefill_host_workspace_bytes", "attn_prefill_fwd_host", "attn_prefill_paged_varlen", "attn_prefill_varlen_workspace_bytes",
             "attn_prefill_paged_varlen_ws", "attn_decode_workspace_bytes", "attn_decode_paged_splitk", "attn_decode_paged_splitk_mq",

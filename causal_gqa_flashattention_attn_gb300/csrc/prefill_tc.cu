@@ -643,7 +643,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 np = split_cta_of(p, item_end - 1) - c0 + 1;
                 if (np > 1) {
                     ctr = p.sk_count + ((static_cast<size_t>(w.bh) * p.n_qb + w.qb) * 2 + t) * 2;
-                    if (r == 0) sk_word[t] = atomicAdd(ctr, 1);
+                    if (r == 0) {
+                        const int a = atomicAdd(ctr, 1);
+                        // a ticket past the piece count: the counters did not start at zero
+                        if (a >= np) flag_status(p.status, ATTN_DEV_WORKSPACE_STATE);
+                        sk_word[t] = a;
+                    }
                     if (!(ok = wg_sync(0))) break;
                     arrival = sk_word[t];
                 }
@@ -732,7 +737,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     bool stored = false;
                     const uint64_t t0 = global_ns();
                     for (uint32_t spin = 0;; ++spin) {
-                        if (ld_acquire_gpu(ctr + 1) >= np - 1) {
+                        const int done = ld_acquire_gpu(ctr + 1);
+                        if (done >= np - 1) {
+                            if (done > np - 1) flag_status(p.status, ATTN_DEV_WORKSPACE_STATE);
                             stored = true;
                             break;
                         }

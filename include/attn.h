@@ -56,6 +56,7 @@ typedef enum {
 #define ATTN_DEV_PAGE_OUT_OF_RANGE 0x1  /* block_table entry < 0 or >= num_pages */
 #define ATTN_DEV_SEQ_TOO_LONG      0x2  /* seq_lens[b] > max_kv_len or > max_pages_per_seq * page_size */
 #define ATTN_DEV_WAIT_TIMEOUT      0x4  /* a bounded mbarrier wait gave up */
+#define ATTN_DEV_WORKSPACE_STATE   0x8  /* attn_prefill_fwd_ws: the split counters were not zero */
 
 /*
  * attn_prefill_fwd - causal GQA prefill.
@@ -105,6 +106,8 @@ attn_status_t attn_prefill_fwd(const void* q, const void* k, const void* v,
  *                    consecutive calls on one stream can share it.  After a
  *                    device error (dev_status != 0) zero it again.  Calls
  *                    that may run at the same time need separate workspaces.
+ *                    A counter found past its range sets
+ *                    ATTN_DEV_WORKSPACE_STATE (the results are then not valid).
  *   workspace_bytes  its size.
  * Errors as attn_prefill_fwd; ATTN_ERR_WORKSPACE for a misaligned or short
  * workspace.

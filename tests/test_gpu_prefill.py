@@ -217,3 +217,29 @@ def test_host_buffer_entry_matches_device_entry():
     stream.synchronize()
     assert torch.equal(ho, o_d.cpu())
     assert torch.equal(hl, lse_d.cpu())
+
+
+def test_split_workspace_not_zeroed_is_flagged():
+    """A workspace whose counters do not start at zero (here every byte 0x7F)
+    is reported as ATTN_DEV_WORKSPACE_STATE; zeroed again, it gives correct
+    results.  Every wait in the split epilogue is bounded, and with these
+    counters they end at once."""
+    dev = gpu_or_skip()
+    import causal_gqa_flashattention_attn_gb300 as attn
+    shape = replace(synth.LLAMA_GQA_PREFILL, B=1, Hq=8, Hkv=2, q_len=160, kv_len=1100)
+    q, k, v = (t.to(dev) for t in synth.prefill_inputs(shape, seed=12))
+    assert attn.attn_prefill_plan(torch.bfloat16, 1, 8, 2, 160, 1100, 128)[0] == 1
+    ws = torch.full((attn.attn_prefill_workspace_bytes(torch.bfloat16, 1, 8, 2, 160, 1100, 128),), 0x7F,
+                    dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    attn.attn_prefill_fwd_ws(q, k, v, workspace=ws, dev_status=status)
+    torch.cuda.synchronize()
+    assert status.item() & attn.ATTN_DEV_WORKSPACE_STATE
+    ws.zero_()
+    status.zero_()
+    o, lse = attn.attn_prefill_fwd_ws(q, k, v, workspace=ws, dev_status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    o_ref, lse_ref = oracle.prefill(_np(q.cpu()), _np(k.cpu()), _np(v.cpu()))
+    check_o(o, o_ref)
+    check_lse(lse, lse_ref)
