@@ -21,6 +21,7 @@ problems, no collective on the data path); rank 0 prints one JSON line.
 """
 
 import argparse
+from dataclasses import replace
 import hashlib
 import json
 import math
@@ -76,6 +77,18 @@ def load_peaks():
         return {k: float(pk[k]) for k in FALLBACK_PEAKS}, "measured"
     except (OSError, KeyError, ValueError):
         return dict(FALLBACK_PEAKS), "fallback"
+
+
+def filled_split(shape):
+    """The int4 and fp8 decode workloads fix no split size: take the one that
+    fills the GPU with whole waves of CTAs (attn_decode_split_tokens).  The
+    bf16 workload keeps its stated 2048."""
+    import causal_gqa_flashattention_attn_gb300 as attn
+    if shape.kv_format not in ("int4", "fp8"):
+        return shape
+    s = attn.attn_decode_split_tokens(shape.kv_format, shape.B, shape.Hq, shape.Hkv, shape.len_hi,
+                                      n_groups=shape.n_groups, D=shape.D)
+    return replace(shape, split_tokens=s) if s > 0 else shape
 
 
 def load_traffic():
@@ -216,7 +229,7 @@ def run_ours(args, rank, world, dist):
 
     pf = synth.LLAMA_GQA_PREFILL
     d16 = synth.PAGED_DECODE_BF16
-    d4 = synth.PAGED_DECODE_INT4
+    d4 = filled_split(synth.PAGED_DECODE_INT4)
     seed = 1000 * rank
     q, k, v = (t.to(dev) for t in synth.prefill_inputs(pf, seed=seed))
     o = torch.empty_like(q)
@@ -263,7 +276,7 @@ def run_ours(args, rank, world, dist):
     v_rows = inpv["k_cache"].shape[0] * vl.page_size
     vws = torch.empty(attn.attn_prefill_varlen_workspace_bytes(v_rows, vl.Hkv, vl.D), dtype=torch.uint8, device=dev)
     # fp8 e4m3 row-wise cache on the int4 workload's shape
-    d8 = synth.PAGED_DECODE_FP8
+    d8 = filled_split(synth.PAGED_DECODE_FP8)
     inp8 = synth.decode_inputs(d8, seed=seed)
     t8 = {kk: vv.to(dev) for kk, vv in inp8.items() if torch.is_tensor(vv)}
     ws8 = torch.empty(attn.attn_decode_workspace_bytes(d8.B, d8.Hq, d8.len_hi, d8.split_tokens, d8.D),
@@ -578,7 +591,6 @@ def run_reference(args, rank):
 def run_profile(args):
     """One kernel on its workload, `args.warmup + args.steps` launches, for an
     ncu capture of that kernel (`-k` and `-s/-c` pick the launches)."""
-    from dataclasses import replace
 
     import torch
 
@@ -613,6 +625,7 @@ def run_profile(args):
                  "decode_fp8": synth.PAGED_DECODE_FP8}[args.profile]
         if args.decode_batch:
             shape = replace(shape, B=args.decode_batch)
+        shape = filled_split(shape)
         inp = synth.decode_inputs(shape, seed=0)
         t = {kk: vv.to(dev) for kk, vv in inp.items() if torch.is_tensor(vv)}
         ws = torch.empty(attn.attn_decode_workspace_bytes(shape.B, shape.Hq, shape.len_hi, shape.split_tokens,

@@ -39,7 +39,7 @@ ATTN_DEV_WAIT_TIMEOUT = 0x4
 ATTN_DEV_WORKSPACE_STATE = 0x8
 
 EXPORTED = ("attn_prefill_fwd", "attn_prefill_workspace_bytes", "attn_prefill_plan", "attn_prefill_fwd_ws", "attn_prefill_host_workspace_bytes", "attn_prefill_fwd_host", "attn_prefill_paged_varlen", "attn_prefill_varlen_workspace_bytes",
-            "attn_prefill_paged_varlen_ws", "attn_decode_workspace_bytes", "attn_decode_paged_splitk", "attn_decode_paged_splitk_mq",
+            "attn_prefill_paged_varlen_ws", "attn_decode_workspace_bytes", "attn_decode_split_tokens", "attn_decode_paged_splitk", "attn_decode_paged_splitk_mq",
             "attn_decode_paged_splitk_fp8",
             "attn_decode_paged_splitk_static", "attn_lse_merge", "attn_lse_merge_bwd", "attn_selftest_wait_timeout",
             "attn_status_string", "attn_abi_version")
@@ -84,6 +84,8 @@ def lib():
     L.attn_prefill_paged_varlen_ws.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
                                                i32, f32, vp, sz, vp, vp]
     L.attn_prefill_paged_varlen_ws.restype = i32
+    L.attn_decode_split_tokens.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32]
+    L.attn_decode_split_tokens.restype = i32
     L.attn_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
     L.attn_decode_workspace_bytes.restype = sz
     L.attn_decode_paged_splitk.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, i32, i32, i32,
@@ -303,6 +305,13 @@ def attn_prefill_paged_varlen_ws(q, k_cache, v_cache, qo_indptr, kv_indptr, kv_i
 
 def attn_decode_workspace_bytes(B, Hq, max_kv_len, split_tokens, D):
     return int(lib().attn_decode_workspace_bytes(B, Hq, max_kv_len, split_tokens, D))
+
+
+def attn_decode_split_tokens(kv_dtype, B, Hq, Hkv, max_kv_len, q_len=1, n_groups=4, D=128):
+    """Split size that fills the current GPU with the decode's CTAs (0: unsupported).
+    ``kv_dtype``: "bf16", "int4" or "fp8"."""
+    code = {"bf16": ATTN_BF16, "int4": ATTN_INT4_PACKED, "fp8": ATTN_FP8_E4M3}[kv_dtype]
+    return int(lib().attn_decode_split_tokens(code, n_groups, B, Hq, Hkv, q_len, max_kv_len, D))
 
 
 def attn_decode_paged_splitk(q, k_cache, v_cache, block_table, seq_lens, split_tokens, max_kv_len, scale=None,

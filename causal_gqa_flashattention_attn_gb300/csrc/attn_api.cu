@@ -195,7 +195,7 @@ const char* attn_status_string(attn_status_t status) {
     }
 }
 
-int attn_abi_version(void) { return 104; }
+int attn_abi_version(void) { return 105; }
 
 attn_status_t attn_selftest_wait_timeout(int32_t* dev_status, unsigned int limit_us, void* stream) {
     if (dev_status == nullptr || limit_us == 0 || limit_us > 1000000u) return ATTN_ERR_INVALID_ARG;
@@ -304,6 +304,55 @@ attn_status_t attn_prefill_fwd_host(const void* q_host, const void* k_host, cons
     if (lse_host != nullptr && cudaMemcpyAsync(lse_host, dl, lb, cudaMemcpyDeviceToHost, s) != cudaSuccess)
         return ATTN_ERR_CUDA;
     return ATTN_OK;
+}
+
+int attn_decode_split_tokens(attn_dtype_t kv_dtype, int n_groups, int B, int Hq, int Hkv, int q_len, int max_kv_len,
+                             int D) {
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || q_len <= 0 || q_len > 16 || max_kv_len <= 0 || D != 128) return 0;
+    if (Hq % Hkv != 0) return 0;
+    const int G = Hq / Hkv;
+    if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return 0;
+    int fmt = 0;
+    if (kv_dtype == ATTN_INT4_PACKED) {
+        if (n_groups != 1 && n_groups != 2 && n_groups != 4 && n_groups != 8) return 0;
+        fmt = 1;
+    } else if (kv_dtype == ATTN_FP8_E4M3) {
+        fmt = 2;
+    } else if (kv_dtype != ATTN_BF16) {
+        return 0;
+    }
+    DecodeArgs a{};
+    a.kv_format = fmt;
+    a.n_groups = n_groups;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.D = D;
+    a.q_len = q_len;
+    int occ = 0;
+    const cudaError_t e = (fmt == 2) ? launch_decode_fp8(a, nullptr, nullptr, nullptr, &occ)
+                                     : launch_decode(a, nullptr, &occ);
+    const int sms = device_sm_count();
+    if (e != cudaSuccess || occ <= 0 || sms <= 0) return 0;
+    const double slots = static_cast<double>(sms) * occ;
+    const int R = rows_per_cta(a);
+    const double units = static_cast<double>(B) * Hkv * ((G * q_len + R - 1) / R);
+    // fewest splits whose CTAs fill at least one wave, the last one 90 % full
+    const int tiles = (max_kv_len + 63) / 64;
+    int best = 64 * tiles;
+    double best_eff = -1.0;
+    for (int n = 1; n <= tiles; ++n) {
+        const int split = 64 * ((tiles + n - 1) / n);
+        if ((max_kv_len + split - 1) / split != n) continue;   // this split gives fewer pieces
+        const double waves = units * n / slots;
+        const double eff = waves / std::ceil(waves);
+        if (waves >= 1.0 && eff >= 0.9) return split;
+        if (eff > best_eff) {
+            best_eff = eff;
+            best = split;
+        }
+    }
+    return best;
 }
 
 size_t attn_decode_workspace_bytes(int B, int Hq, int max_kv_len, int split_tokens, int D) {

@@ -54,10 +54,23 @@ struct DecodeArgs {
     float* lse_part;
     int32_t* dev_status;
 };
-cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+// With `occ` set, a decode launcher launches nothing: it writes how many CTAs
+// of the kernel it would launch fit on one SM at once.
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream, int* occ = nullptr);
+cudaError_t launch_decode_int4(const DecodeArgs& a, cudaStream_t stream, int* occ = nullptr);
 cudaError_t launch_decode_fp8(const DecodeArgs& a, const void* k_scale_shift, const void* v_scale_shift,
-                              cudaStream_t stream);
+                              cudaStream_t stream, int* occ = nullptr);
 int rows_per_cta(const DecodeArgs& a);
+
+// CTAs of `kern` (with its shared-memory attributes set as for a launch)
+// resident on one SM at once.
+template <typename K>
+cudaError_t ctas_per_sm(K kern, int threads, size_t smem, int* occ) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+    return e == cudaSuccess ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, kern, threads, smem) : e;
+}
 
 cudaError_t launch_wait_timeout_selftest(int32_t* status, uint64_t limit_ns, cudaStream_t stream);
 

@@ -310,8 +310,11 @@ __global__ void __launch_bounds__(kThreads) decode_bf16_kernel(const __grid_cons
 }
 
 template <int R>
-cudaError_t launch_bf16(const DecodeArgs& a, cudaStream_t stream) {
+cudaError_t launch_bf16(const DecodeArgs& a, cudaStream_t stream, int* occ) {
     constexpr int NS = 3;
+    const size_t smem = NS * kStageBytes + 1024;
+    auto kern = decode_bf16_kernel<R, NS>;
+    if (occ != nullptr) return ctas_per_sm(kern, kThreads, smem, occ);
     CUtensorMap k_map, v_map;
     const uint64_t rows = static_cast<uint64_t>(a.num_pages) * a.page_size;
     const uint64_t dims[3] = {static_cast<uint64_t>(a.D), static_cast<uint64_t>(a.Hkv), rows};
@@ -343,8 +346,6 @@ cudaError_t launch_bf16(const DecodeArgs& a, cudaStream_t stream) {
     p.o_part = a.o_part;
     p.lse_part = a.lse_part;
     p.status = a.dev_status;
-    const size_t smem = NS * kStageBytes + 1024;
-    auto kern = decode_bf16_kernel<R, NS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     // two CTAs per SM: ask for the largest shared-memory carveout
@@ -357,7 +358,6 @@ cudaError_t launch_bf16(const DecodeArgs& a, cudaStream_t stream) {
 
 }  // namespace
 
-cudaError_t launch_decode_int4(const DecodeArgs& a, cudaStream_t stream);
 
 // Rows per CTA: the (query, head) pairs of one KV head, at most 16.
 int rows_per_cta(const DecodeArgs& a) {
@@ -367,14 +367,14 @@ int rows_per_cta(const DecodeArgs& a) {
     return r;
 }
 
-cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
-    if (a.kv_format == 1) return launch_decode_int4(a, stream);
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream, int* occ) {
+    if (a.kv_format == 1) return launch_decode_int4(a, stream, occ);
     switch (rows_per_cta(a)) {
-        case 1: return launch_bf16<1>(a, stream);
-        case 2: return launch_bf16<2>(a, stream);
-        case 4: return launch_bf16<4>(a, stream);
-        case 8: return launch_bf16<8>(a, stream);
-        case 16: return launch_bf16<16>(a, stream);
+        case 1: return launch_bf16<1>(a, stream, occ);
+        case 2: return launch_bf16<2>(a, stream, occ);
+        case 4: return launch_bf16<4>(a, stream, occ);
+        case 8: return launch_bf16<8>(a, stream, occ);
+        case 16: return launch_bf16<16>(a, stream, occ);
         default: return cudaErrorInvalidValue;
     }
 }

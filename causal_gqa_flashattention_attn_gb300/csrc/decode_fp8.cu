@@ -386,7 +386,12 @@ __global__ void __launch_bounds__(kThreads, (R > 8) ? 1 : 3) decode_fp8_kernel(
 }
 
 template <int R>
-cudaError_t launch_r(const DecodeArgs& a, const void* k_ss, const void* v_ss, cudaStream_t stream) {
+cudaError_t launch_r(const DecodeArgs& a, const void* k_ss, const void* v_ss, cudaStream_t stream, int* occ) {
+    const size_t ring = NS * kStageBytes;
+    const size_t red = (kConsumers * R * kD + 2 * kConsumers * R) * sizeof(float);
+    const size_t smem = (ring > red ? ring : red) + 1024;
+    auto kern = decode_fp8_kernel<R>;
+    if (occ != nullptr) return ctas_per_sm(kern, kThreads, smem, occ);
     CUtensorMap k_map, v_map, kw_map, vw_map;
     const uint64_t rows = static_cast<uint64_t>(a.num_pages) * a.page_size;
     {
@@ -430,10 +435,6 @@ cudaError_t launch_r(const DecodeArgs& a, const void* k_ss, const void* v_ss, cu
     p.o_part = a.o_part;
     p.lse_part = a.lse_part;
     p.status = a.dev_status;
-    const size_t ring = NS * kStageBytes;
-    const size_t red = (kConsumers * R * kD + 2 * kConsumers * R) * sizeof(float);
-    const size_t smem = (ring > red ? ring : red) + 1024;
-    auto kern = decode_fp8_kernel<R>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
@@ -446,13 +447,13 @@ cudaError_t launch_r(const DecodeArgs& a, const void* k_ss, const void* v_ss, cu
 }  // namespace
 
 cudaError_t launch_decode_fp8(const DecodeArgs& a, const void* k_scale_shift, const void* v_scale_shift,
-                              cudaStream_t stream) {
+                              cudaStream_t stream, int* occ) {
     switch (rows_per_cta(a)) {
-        case 1: return launch_r<1>(a, k_scale_shift, v_scale_shift, stream);
-        case 2: return launch_r<2>(a, k_scale_shift, v_scale_shift, stream);
-        case 4: return launch_r<4>(a, k_scale_shift, v_scale_shift, stream);
-        case 8: return launch_r<8>(a, k_scale_shift, v_scale_shift, stream);
-        case 16: return launch_r<16>(a, k_scale_shift, v_scale_shift, stream);
+        case 1: return launch_r<1>(a, k_scale_shift, v_scale_shift, stream, occ);
+        case 2: return launch_r<2>(a, k_scale_shift, v_scale_shift, stream, occ);
+        case 4: return launch_r<4>(a, k_scale_shift, v_scale_shift, stream, occ);
+        case 8: return launch_r<8>(a, k_scale_shift, v_scale_shift, stream, occ);
+        case 16: return launch_r<16>(a, k_scale_shift, v_scale_shift, stream, occ);
         default: return cudaErrorInvalidValue;
     }
 }

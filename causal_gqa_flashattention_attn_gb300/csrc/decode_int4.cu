@@ -461,11 +461,16 @@ __global__ void __launch_bounds__(kThreads, (R > 8) ? 1 : 3) decode_int4_kernel(
 }
 
 template <int R, int NG>
-cudaError_t launch_g_ng(const DecodeArgs& a, cudaStream_t stream) {
+cudaError_t launch_g_ng(const DecodeArgs& a, cudaStream_t stream, int* occ) {
     constexpr int NS = 6;
     constexpr int BW = (NG <= 4) ? 20 : 24;
     constexpr int kStageBytes = 2 * kTileTok * BW * 4;
     const int row_words = a.n_groups + a.D / 8;
+    const size_t ring = NS * kStageBytes + kConsumers * 4 * NG * 16 * sizeof(float);
+    const size_t red = (kConsumers * R * kD + 2 * kConsumers * R) * sizeof(float);
+    const size_t smem = (ring > red ? ring : red) + 1024;
+    auto kern = decode_int4_kernel<R, NG, NS>;
+    if (occ != nullptr) return ctas_per_sm(kern, kThreads, smem, occ);
     CUtensorMap k_map, v_map;
     const uint64_t dims[2] = {static_cast<uint64_t>(a.Hkv) * row_words,
                               static_cast<uint64_t>(a.num_pages) * a.page_size};
@@ -499,10 +504,6 @@ cudaError_t launch_g_ng(const DecodeArgs& a, cudaStream_t stream) {
     p.lse_part = a.lse_part;
     p.status = a.dev_status;
     // the merge scratch (4 warps x R rows x D floats) reuses the stage ring
-    const size_t ring = NS * kStageBytes + kConsumers * 4 * NG * 16 * sizeof(float);
-    const size_t red = (kConsumers * R * kD + 2 * kConsumers * R) * sizeof(float);
-    const size_t smem = (ring > red ? ring : red) + 1024;
-    auto kern = decode_int4_kernel<R, NG, NS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     // two CTAs per SM: ask for the largest shared-memory carveout
@@ -514,25 +515,25 @@ cudaError_t launch_g_ng(const DecodeArgs& a, cudaStream_t stream) {
 }
 
 template <int R>
-cudaError_t launch_g(const DecodeArgs& a, cudaStream_t stream) {
+cudaError_t launch_g(const DecodeArgs& a, cudaStream_t stream, int* occ) {
     switch (a.n_groups) {
-        case 1: return launch_g_ng<R, 1>(a, stream);
-        case 2: return launch_g_ng<R, 2>(a, stream);
-        case 4: return launch_g_ng<R, 4>(a, stream);
-        case 8: return launch_g_ng<R, 8>(a, stream);
+        case 1: return launch_g_ng<R, 1>(a, stream, occ);
+        case 2: return launch_g_ng<R, 2>(a, stream, occ);
+        case 4: return launch_g_ng<R, 4>(a, stream, occ);
+        case 8: return launch_g_ng<R, 8>(a, stream, occ);
         default: return cudaErrorInvalidValue;
     }
 }
 
 }  // namespace
 
-cudaError_t launch_decode_int4(const DecodeArgs& a, cudaStream_t stream) {
+cudaError_t launch_decode_int4(const DecodeArgs& a, cudaStream_t stream, int* occ) {
     switch (rows_per_cta(a)) {
-        case 1: return launch_g<1>(a, stream);
-        case 2: return launch_g<2>(a, stream);
-        case 4: return launch_g<4>(a, stream);
-        case 8: return launch_g<8>(a, stream);
-        case 16: return launch_g<16>(a, stream);
+        case 1: return launch_g<1>(a, stream, occ);
+        case 2: return launch_g<2>(a, stream, occ);
+        case 4: return launch_g<4>(a, stream, occ);
+        case 8: return launch_g<8>(a, stream, occ);
+        case 16: return launch_g<16>(a, stream, occ);
         default: return cudaErrorInvalidValue;
     }
 }

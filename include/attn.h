@@ -166,6 +166,24 @@ attn_status_t attn_prefill_fwd_host(const void* q_host, const void* k_host, cons
 size_t attn_decode_workspace_bytes(int B, int Hq, int max_kv_len, int split_tokens, int D);
 
 /*
+ * attn_decode_split_tokens - a split size for the paged decode entries that
+ * fills the current device.
+ *
+ * "splitk_kernels.py", _fwd_kernel_splitK cuts every sequence's keys into
+ * chunks of split_tokens, one program each.  Here each (chunk, KV head,
+ * sequence) is one CTA.  This returns the split_tokens (a multiple of 64) that
+ * gives the fewest chunks per sequence while the CTAs, at the number of them
+ * that fit on the device at once, come to at least one wave with the last
+ * wave at least 90 % full (else the fullest last wave found).  It counts every
+ * sequence at max_kv_len, so it suits batches of similar lengths.
+ *
+ *   kv_dtype   ATTN_BF16, ATTN_INT4_PACKED (with n_groups) or ATTN_FP8_E4M3
+ * Returns 0 for sizes the decode entries do not take, or without a device.
+ */
+int attn_decode_split_tokens(attn_dtype_t kv_dtype, int n_groups, int B, int Hq, int Hkv, int q_len, int max_kv_len,
+                             int D);
+
+/*
  * attn_prefill_paged_varlen - causal GQA prefill of a ragged batch over a
  * paged KV cache, in one launch.
  *
@@ -405,7 +423,8 @@ const char* attn_status_string(attn_status_t status);
 
 /* ABI version of this header (major * 100 + minor); 101 added attn_selftest_wait_timeout,
  * 102 attn_prefill_paged_varlen_ws, 103 attn_prefill_fwd_host,
- * 104 attn_prefill_fwd_ws, attn_prefill_workspace_bytes, attn_prefill_plan. */
+ * 104 attn_prefill_fwd_ws, attn_prefill_workspace_bytes, attn_prefill_plan,
+ * 105 attn_decode_split_tokens. */
 int attn_abi_version(void);
 
 #ifdef __cplusplus

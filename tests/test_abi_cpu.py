@@ -39,7 +39,7 @@ def test_library_exports_every_declared_symbol(L):
     for name in declared_functions():
         assert hasattr(L, name), name
         assert name in attn.EXPORTED
-    assert L.attn_abi_version() == 104
+    assert L.attn_abi_version() == 105
 
 
 def test_status_strings(L):
@@ -120,6 +120,19 @@ def test_prefill_ws_validation(L):
     assert attn.attn_prefill_plan(torch.float32, 1, 4, 2, 8, 8, 64) == (0, 0)   # CUDA-core path: no split
     assert attn.attn_prefill_workspace_bytes(torch.float32, 1, 4, 2, 8, 8, 64) == 0
     assert attn.attn_prefill_workspace_bytes(torch.bfloat16, 0, 4, 2, 8, 8, 128) == 0
+
+
+def test_decode_split_tokens_validation(L):
+    import causal_gqa_flashattention_attn_gb300 as attn
+    # sizes the decode entries do not take give 0; so does a machine without a GPU
+    assert attn.attn_decode_split_tokens("int4", 16, 32, 8, 16384, n_groups=3) == 0
+    assert attn.attn_decode_split_tokens("bf16", 16, 32, 8, 16384, q_len=17) == 0
+    assert attn.attn_decode_split_tokens("bf16", 16, 32, 8, 16384, D=64) == 0
+    assert attn.attn_decode_split_tokens("bf16", 16, 24, 8, 16384) == 0        # G = 3
+    assert attn.attn_decode_split_tokens("bf16", 0, 32, 8, 16384) == 0
+    assert L.attn_decode_split_tokens(0, 1, 16, 32, 8, 1, 16384, 128) == 0     # fp32 cache: no decode kernel
+    if not torch.cuda.is_available():
+        assert attn.attn_decode_split_tokens("bf16", 16, 32, 8, 16384) == 0
 
 
 def _decode(L, **kw):

@@ -165,10 +165,16 @@ def test_device_status_flags_bad_page_and_length():
 
 
 def _full_size(shape, sample):
-    """The full workload in the benchmark's launch configuration; the oracle
-    checks a sample of sequences (every head of each)."""
+    """The full workload in the benchmark's launch configuration (for int4 the
+    split from attn_decode_split_tokens, as the benchmark takes it); the
+    oracle checks a sample of sequences (every head of each)."""
     dev = gpu_or_skip()
     import causal_gqa_flashattention_attn_gb300 as attn
+    if shape.kv_format == "int4":
+        split = attn.attn_decode_split_tokens("int4", shape.B, shape.Hq, shape.Hkv, shape.len_hi,
+                                              n_groups=shape.n_groups)
+        assert split > 0 and split % 64 == 0
+        shape = replace(shape, split_tokens=split)
     inp = synth.decode_inputs(shape, seed=0)
     lens = inp["lens"]
     t = {k: x.to(dev) for k, x in inp.items() if torch.is_tensor(x)}
@@ -193,6 +199,22 @@ def test_full_size_paged_decode_bf16_sampled():
 
 def test_full_size_paged_decode_int4_sampled():
     _full_size(synth.PAGED_DECODE_INT4, lambda lens: [0, 5, 15])
+
+
+def test_split_tokens_fills_the_gpu():
+    """attn_decode_split_tokens on the int4 and fp8 workloads (16 sequences x
+    8 KV heads, 16384 tokens): a multiple of 64 whose CTA count is not the
+    2.25 waves of 2048-token splits, and never more pieces than tiles."""
+    gpu_or_skip()
+    import causal_gqa_flashattention_attn_gb300 as attn
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for fmt in ("int4", "fp8", "bf16"):
+        split = attn.attn_decode_split_tokens(fmt, 16, 32, 8, 16384, n_groups=4)
+        assert split > 0 and split % 64 == 0 and split <= 16384
+        ctas = 16 * 8 * -(-16384 // split)
+        assert ctas >= sms
+    assert attn.attn_decode_split_tokens("int4", 16, 32, 8, 16384, n_groups=3) == 0
+    assert attn.attn_decode_split_tokens("bf16", 16, 32, 8, 16384, q_len=17) == 0
 
 
 @pytest.mark.parametrize("fmt", ["dense", "int4"])

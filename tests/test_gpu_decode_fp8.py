@@ -62,6 +62,10 @@ def test_fp8_full_size_sampled():
     dev = gpu_or_skip()
     import causal_gqa_flashattention_attn_gb300 as attn
     shape = synth.PAGED_DECODE_FP8
+    # the split the benchmark takes: the one that fills the GPU
+    split = attn.attn_decode_split_tokens("fp8", shape.B, shape.Hq, shape.Hkv, shape.len_hi)
+    assert split > 0
+    shape = replace(shape, split_tokens=split)
     inp = synth.decode_inputs(shape, seed=0)
     t = {k: v.to(dev) for k, v in inp.items() if torch.is_tensor(v)}
     o, lse, _ = attn.attn_decode_paged_splitk_fp8(t["q"], t["k_cache"], t["v_cache"], t["k_scale_shift"],
