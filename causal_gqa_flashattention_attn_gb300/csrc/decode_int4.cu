@@ -8,15 +8,20 @@
 // offset.
 //
 // The dequantisation is fused into the tensor-core operands instead of being
-// materialised: a code c becomes the exact bf16 value 128 + c by OR-ing the
-// nibble into the bit pattern 0x4300 (no conversion instruction), and the
-// affine map is applied where it is cheap:
+// materialised.  Scores use bf16 "code space": a code c becomes the exact
+// bf16 value 128 + c by OR-ing the nibble (shifted to bits 0-3) into 0x4300.
+// Values use fp16 code space: a code in bits 0-3 of a 16-bit half becomes the
+// exact fp16 1024 + c by OR-ing it into 0x6400, a code in bits 4-7 the exact
+// 1024 + 16 c (both within the 10 mantissa bits), and codes in the upper byte
+// are first moved down by one byte permute, so no shifts.  With sigma_d = 16
+// for the codes taken from bits 4-7 and 1 otherwise, the affine map is
+// applied where it is cheap:
 //   s[h,t]   = sum_g scale_g(t) * (sum_{d in g} q_hd c_td)  +  sum_g offset_g(t) * Qsum_g[h]
-//              (the MMA accumulator of group g starts at -128 * Qsum_g[h])
-//   O[h,d]   = sum_t (p_ht scale_g(t)) (128 + c_td) - 128 SP_g[h] + OFF_g[h],
-//              SP_g = sum_t bf16(p_ht scale_g(t)),  OFF_g = sum_t p_ht offset_g(t)
-// so per element only one bit operation feeds the MMA; the per-group affine
-// terms cost a few FMAs per (token, head).
+//              (computed as scale * (sum q (128 + c)) + (offset - 128 scale) * Qsum)
+//   O[h,d]   = (sum_t w_ht (1024 + sigma_d c_td) - 1024 SP_g[h]) / sigma_d + OFF_g[h],
+//              w = fp16(p_ht scale_g(t)),  SP_g = sum_t w_ht,  OFF_g = sum_t p_ht offset_g(t)
+// where dividing by sigma_d is exact; the per-group affine terms cost a few
+// FMAs per (token, head).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -51,6 +56,13 @@ __device__ __forceinline__ float hi_half(uint32_t w) { return __half2float(__ush
 __device__ __forceinline__ uint32_t nib_pair(uint32_t x, int q) {
     return ((x >> (4 * q)) & 0x000F000Fu) | 0x43004300u;
 }
+
+// fp16x2 (1024 + c, 1024 + c) of the codes in bits 0-3 of each 16-bit half of x
+__device__ __forceinline__ uint32_t nib_lo(uint32_t x) { return (x & 0x000F000Fu) | 0x64006400u; }
+// fp16x2 (1024 + 16 c, 1024 + 16 c) of the codes in bits 4-7 of each half
+__device__ __forceinline__ uint32_t nib_hi(uint32_t x) { return (x & 0x00F000F0u) | 0x64006400u; }
+// the upper byte of each 16-bit half moved to its lower byte (codes 2 and 3 of the half)
+__device__ __forceinline__ uint32_t upper_bytes(uint32_t x) { return __byte_perm(x, 0u, 0x4341u); }
 
 // Coordinates of the K-side operand of group-local k-step `ks` for lane
 // quad index t: the code word (within the group) and the first nibble pair.
@@ -243,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, (R > 8) ? 1 : 3) decode_int4_kernel(
                 cf[((2 * kv + 1) * NG + gr) * 16 + tok] = kv == 0 ? fmaf(-128.f, sc, of) * sl2 : of;
             }
             __syncwarp();
-            // ---- scores in code space: per group T_g = sum_d q (128 + c), then
+            // ---- scores in bf16 code space: per group T_g = sum_d q (128 + c), then
             //      s += scale_g * T_g + (offset_g - 128 scale_g) * Qsum_g
             float2 s2[2][kRows];
 #pragma unroll
@@ -337,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, (R > 8) ? 1 : 3) decode_int4_kernel(
                         off2[gr][rr] = __fmul2_rn(off2[gr][rr], a2);
                     }
             }
-            // ---- O^T += (128 + codes)^T (P * scale_g)^T, group by group: M = 16
+            // ---- O^T += (1024 + sigma codes)^T (P * scale_g)^T, group by group: M = 16
             //      head-dim rows, N = 8 heads, K = 16 tokens
 #pragma unroll
             for (int gr = 0; gr < NG; ++gr) {
@@ -349,11 +361,11 @@ __global__ void __launch_bounds__(kThreads, (R > 8) ? 1 : 3) decode_int4_kernel(
 #pragma unroll
                 for (int rr = 0; rr < kRows; ++rr) {
                     const float2 pA = make_float2(pv[rr][0], pv[rr][1]), pC = make_float2(pv[rr][2], pv[rr][3]);
-                    const __nv_bfloat162 lo2 = __float22bfloat162_rn(__fmul2_rn(pA, scA));
-                    const __nv_bfloat162 hi2 = __float22bfloat162_rn(__fmul2_rn(pC, scC));
+                    const __half2 lo2 = __float22half2_rn(__fmul2_rn(pA, scA));
+                    const __half2 hi2 = __float22half2_rn(__fmul2_rn(pC, scC));
                     pa[rr] = *reinterpret_cast<const uint32_t*>(&lo2);
                     pa[rr + 2] = *reinterpret_cast<const uint32_t*>(&hi2);
-                    sp2[gr][rr] = __fadd2_rn(sp2[gr][rr], __fadd2_rn(__bfloat1622float2(lo2), __bfloat1622float2(hi2)));
+                    sp2[gr][rr] = __fadd2_rn(sp2[gr][rr], __fadd2_rn(__half22float2(lo2), __half22float2(hi2)));
                     off2[gr][rr] = __ffma2_rn(pC, ofC, __ffma2_rn(pA, ofA, off2[gr][rr]));
                 }
                 // A operand (codes): lane row g supplies elements g*EPT + q of the
@@ -372,11 +384,13 @@ __global__ void __launch_bounds__(kThreads, (R > 8) ? 1 : 3) decode_int4_kernel(
 #pragma unroll
                     for (int jj = 0; jj < (EPT < 4 ? EPT : 4); jj += 2) {
                         const int mt = gr * MT + (j + jj) / 2;
-                        const uint32_t a0 = nib_pair(xa, q0 + jj), a1 = nib_pair(xa, q0 + jj + 1);
-                        const uint32_t a2 = nib_pair(xc, q0 + jj), a3 = nib_pair(xc, q0 + jj + 1);
+                        // codes q0 + jj (m-tile row g) and q0 + jj + 1 (row g + 8, times 16)
+                        const bool upper = (q0 + jj) != 0;
+                        const uint32_t ya = upper ? upper_bytes(xa) : xa, yc = upper ? upper_bytes(xc) : xc;
+                        const uint32_t a0 = nib_lo(ya), a1 = nib_hi(ya), a2 = nib_lo(yc), a3 = nib_hi(yc);
 #pragma unroll
                         for (int h = 0; h < kRows; ++h)
-                            mma_bf16_16816(o_acc[h][mt], a0, a1, a2, a3, pa[h], pa[h + 2]);
+                            mma_f16_16816(o_acc[h][mt], a0, a1, a2, a3, pa[h], pa[h + 2]);
                     }
                 }
             }
@@ -386,21 +400,27 @@ __global__ void __launch_bounds__(kThreads, (R > 8) ? 1 : 3) decode_int4_kernel(
     }
 
     // ------------------------------------------- corrections and warp merge
-    float corr_g[NG][2];   // OFF_g - 128 SP_g, summed over the four lanes of a row
+    // OFF_g - 1024 SP_g (codes with sigma 1) and OFF_g - 64 SP_g (sigma 16, the
+    // accumulator then divided by 16), summed over the four lanes of a row
+    float corr_lo[NG][2], corr_hi[NG][2];
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
         l_part[rr] += __shfl_xor_sync(0xffffffffu, l_part[rr], 1);
         l_part[rr] += __shfl_xor_sync(0xffffffffu, l_part[rr], 2);
 #pragma unroll
         for (int gr = 0; gr < NG; ++gr) {
-            float corr = 0.f;
+            float off = 0.f, sp = 0.f;
             if (rr < kRows) {
-                const float2 sp = sp2[gr][rr < kRows ? rr : 0], of = off2[gr][rr < kRows ? rr : 0];
-                corr = (of.x + of.y) - 128.f * (sp.x + sp.y);
+                const float2 sp_v = sp2[gr][rr < kRows ? rr : 0], of_v = off2[gr][rr < kRows ? rr : 0];
+                off = of_v.x + of_v.y;
+                sp = sp_v.x + sp_v.y;
             }
-            corr += __shfl_xor_sync(0xffffffffu, corr, 1);
-            corr += __shfl_xor_sync(0xffffffffu, corr, 2);
-            corr_g[gr][rr] = corr;
+            off += __shfl_xor_sync(0xffffffffu, off, 1);
+            off += __shfl_xor_sync(0xffffffffu, off, 2);
+            sp += __shfl_xor_sync(0xffffffffu, sp, 1);
+            sp += __shfl_xor_sync(0xffffffffu, sp, 2);
+            corr_lo[gr][rr] = fmaf(-1024.f, sp, off);
+            corr_hi[gr][rr] = fmaf(-64.f, sp, off);
         }
     }
     named_barrier_sync(1, 32 * kConsumers);
@@ -420,20 +440,23 @@ __global__ void __launch_bounds__(kThreads, (R > 8) ? 1 : 3) decode_int4_kernel(
     for (int h = 0; h < kRows; ++h) {
 #pragma unroll
         for (int gr = 0; gr < NG; ++gr) {
-            const float c0 = __shfl_sync(0xffffffffu, corr_g[gr][h], 8 * t4);
-            const float c1 = __shfl_sync(0xffffffffu, corr_g[gr][h], 8 * t4 + 4);
+            const float c0 = __shfl_sync(0xffffffffu, corr_lo[gr][h], 8 * t4);
+            const float c1 = __shfl_sync(0xffffffffu, corr_lo[gr][h], 8 * t4 + 4);
+            const float c0h = __shfl_sync(0xffffffffu, corr_hi[gr][h], 8 * t4);
+            const float c1h = __shfl_sync(0xffffffffu, corr_hi[gr][h], 8 * t4 + 4);
             const int head0 = 8 * h + 2 * t4, head1 = head0 + 1;
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt) {
                 const float* f = o_acc[h][gr * MT + mt];
-                const int d_lo = gr * E + g * EPT + 2 * mt, d_hi = d_lo + 1;   // m-tile rows g, g + 8
+                // m-tile rows g (sigma 1) and g + 8 (sigma 16)
+                const int d_lo = gr * E + g * EPT + 2 * mt, d_hi = d_lo + 1;
                 if (head0 < n_rows) {
                     red_o[(warp * R + head0) * kD + d_lo] = f[0] + c0;
-                    red_o[(warp * R + head0) * kD + d_hi] = f[2] + c0;
+                    red_o[(warp * R + head0) * kD + d_hi] = fmaf(f[2], 0.0625f, c0h);
                 }
                 if (head1 < n_rows) {
                     red_o[(warp * R + head1) * kD + d_lo] = f[1] + c1;
-                    red_o[(warp * R + head1) * kD + d_hi] = f[3] + c1;
+                    red_o[(warp * R + head1) * kD + d_hi] = fmaf(f[3], 0.0625f, c1h);
                 }
             }
         }
