@@ -27,7 +27,14 @@
 //     written back over S in TMEM as bf16 and fed to the P.V MMA from TMEM;
 //   * the max is rescaled lazily (only when it grows by more than 2^8), so
 //     the O accumulator in TMEM is rarely touched by the softmax warps;
-//   * a persistent grid walks the work items longest-first in a snake order.
+//   * O leaves TMEM in one round trip and is released to the next item's P.V
+//     before it is written; the dense layout writes it through a 16 KB
+//     shared-memory stage per softmax warpgroup with TMA stores;
+//   * a persistent grid walks whole work items longest-first in a snake
+//     order, in sections of (batch, KV head) pairs whose K/V stays in L2;
+//   * with caller scratch, shapes with too few items to fill the GPU take
+//     a split schedule: the (item, KV tile) steps are cut into equal ranges
+//     per CTA and a cut item is merged by the piece that finishes last.
 //
 // Ragged mode (kVarlen, "gpt-o3 / triton6fd1ef", run): a batch of sequences
 // with CSR extents over a paged KV cache in one launch.  Work items are
