@@ -38,8 +38,8 @@ ATTN_DEV_SEQ_TOO_LONG = 0x2
 ATTN_DEV_WAIT_TIMEOUT = 0x4
 ATTN_DEV_WORKSPACE_STATE = 0x8
 
-EXPORTED = ("attn_prefill_fwd", "attn_prefill_workspace_bytes", "attn_prefill_plan", "attn_prefill_fwd_ws", "attn_prefill_host_workspace_bytes", "attn_prefill_fwd_host", "attn_prefill_paged_varlen", "attn_prefill_varlen_workspace_bytes",
-            "attn_prefill_paged_varlen_ws", "attn_decode_workspace_bytes", "attn_decode_split_tokens", "attn_decode_paged_splitk", "attn_decode_paged_splitk_mq",
+EXPORTED = ("attn_prefill_fwd", "attn_prefill_workspace_bytes", "attn_prefill_plan", "attn_prefill_plan_sms", "attn_prefill_fwd_ws", "attn_prefill_host_workspace_bytes", "attn_prefill_fwd_host", "attn_prefill_paged_varlen", "attn_prefill_varlen_workspace_bytes",
+            "attn_prefill_paged_varlen_ws", "attn_decode_workspace_bytes", "attn_decode_split_tokens", "attn_decode_split_tokens_for", "attn_decode_paged_splitk", "attn_decode_paged_splitk_mq",
             "attn_decode_paged_splitk_fp8",
             "attn_decode_paged_splitk_static", "attn_lse_merge", "attn_lse_merge_bwd", "attn_selftest_wait_timeout",
             "attn_status_string", "attn_abi_version")
@@ -70,6 +70,10 @@ def lib():
     L.attn_prefill_workspace_bytes.restype = sz
     L.attn_prefill_plan.argtypes = [i32, i32, i32, i32, i32, i32, i32, ctypes.POINTER(ctypes.c_int)]
     L.attn_prefill_plan.restype = i32
+    L.attn_prefill_plan_sms.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, ctypes.POINTER(ctypes.c_int)]
+    L.attn_prefill_plan_sms.restype = i32
+    L.attn_decode_split_tokens_for.argtypes = [i32, i32, i32, i32, i32, i32, i32]
+    L.attn_decode_split_tokens_for.restype = i32
     L.attn_prefill_fwd_ws.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32, vp, sz, vp, vp]
     L.attn_prefill_fwd_ws.restype = i32
     L.attn_prefill_host_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32, i32]
@@ -185,6 +189,18 @@ def attn_prefill_plan(dtype, B, Hq, Hkv, q_len, kv_len, D):
     grid = ctypes.c_int(0)
     sched = lib().attn_prefill_plan(_DT.get(dtype, -1), B, Hq, Hkv, q_len, kv_len, D, ctypes.byref(grid))
     return int(sched), int(grid.value)
+
+
+def attn_prefill_plan_sms(dtype, B, Hq, Hkv, q_len, kv_len, D, sms):
+    """(schedule, grid) of attn_prefill_fwd_ws on a device with ``sms`` SMs."""
+    grid = ctypes.c_int(0)
+    sched = lib().attn_prefill_plan_sms(_DT.get(dtype, -1), B, Hq, Hkv, q_len, kv_len, D, sms, ctypes.byref(grid))
+    return int(sched), int(grid.value)
+
+
+def attn_decode_split_tokens_for(sms, ctas_per_sm, B, Hq, Hkv, max_kv_len, q_len=1):
+    """attn_decode_split_tokens for ``sms`` SMs holding ``ctas_per_sm`` decode CTAs each."""
+    return int(lib().attn_decode_split_tokens_for(sms, ctas_per_sm, B, Hq, Hkv, q_len, max_kv_len))
 
 
 def attn_prefill_fwd_ws(q, k, v, workspace=None, o=None, lse=None, scale=None, dev_status=None, stream=None,

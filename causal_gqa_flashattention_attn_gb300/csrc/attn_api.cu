@@ -195,7 +195,7 @@ const char* attn_status_string(attn_status_t status) {
     }
 }
 
-int attn_abi_version(void) { return 105; }
+int attn_abi_version(void) { return 106; }
 
 attn_status_t attn_selftest_wait_timeout(int32_t* dev_status, unsigned int limit_us, void* stream) {
     if (dev_status == nullptr || limit_us == 0 || limit_us > 1000000u) return ATTN_ERR_INVALID_ARG;
@@ -219,15 +219,23 @@ size_t attn_prefill_workspace_bytes(attn_dtype_t dtype, int B, int Hq, int Hkv, 
     return sms > 0 ? prefill_tc_workspace_bytes(a, sms) : 0;
 }
 
+int attn_prefill_plan_sms(attn_dtype_t dtype, int B, int Hq, int Hkv, int q_len, int kv_len, int D, int sms,
+                          int* grid) {
+    if (grid != nullptr) *grid = 0;
+    if (sms <= 0 || prefill_shape_check(dtype, B, Hq, Hkv, q_len, kv_len, D, 1.f) != ATTN_OK) return -1;
+    PrefillArgs a{nullptr, nullptr, nullptr, nullptr, nullptr, static_cast<int>(dtype), B, Hq, Hkv, q_len, kv_len,
+                  D, 1.f, nullptr, nullptr, 0};
+    if (dtype != ATTN_BF16 || !prefill_tc_supported(a)) return 0;
+    return prefill_tc_plan(a, sms, grid);
+}
+
 int attn_prefill_plan(attn_dtype_t dtype, int B, int Hq, int Hkv, int q_len, int kv_len, int D, int* grid) {
     if (grid != nullptr) *grid = 0;
     if (prefill_shape_check(dtype, B, Hq, Hkv, q_len, kv_len, D, 1.f) != ATTN_OK) return -1;
     PrefillArgs a{nullptr, nullptr, nullptr, nullptr, nullptr, static_cast<int>(dtype), B, Hq, Hkv, q_len, kv_len,
                   D, 1.f, nullptr, nullptr, 0};
     if (dtype != ATTN_BF16 || !prefill_tc_supported(a)) return 0;
-    const int sms = device_sm_count();
-    if (sms <= 0) return -1;
-    return prefill_tc_plan(a, sms, grid);
+    return attn_prefill_plan_sms(dtype, B, Hq, Hkv, q_len, kv_len, D, device_sm_count(), grid);
 }
 
 attn_status_t attn_prefill_fwd_ws(const void* q, const void* k, const void* v, void* o, float* lse,
@@ -306,6 +314,35 @@ attn_status_t attn_prefill_fwd_host(const void* q_host, const void* k_host, cons
     return ATTN_OK;
 }
 
+int attn_decode_split_tokens_for(int sms, int ctas_per_sm, int B, int Hq, int Hkv, int q_len, int max_kv_len) {
+    if (sms <= 0 || ctas_per_sm <= 0 || B <= 0 || Hq <= 0 || Hkv <= 0 || q_len <= 0 || q_len > 16 || max_kv_len <= 0)
+        return 0;
+    if (Hq % Hkv != 0) return 0;
+    const int G = Hq / Hkv;
+    if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return 0;
+    // rows per CTA: the (query, head) pairs of a KV head, a power of two up to 16
+    int R = 1;
+    while (R < G * q_len && R < 16) R *= 2;
+    const double slots = static_cast<double>(sms) * ctas_per_sm;
+    const double units = static_cast<double>(B) * Hkv * ((G * q_len + R - 1) / R);
+    // fewest splits whose CTAs fill at least one wave, the last one 90 % full
+    const int tiles = (max_kv_len + 63) / 64;
+    int best = 64 * tiles;
+    double best_eff = -1.0;
+    for (int n = 1; n <= tiles; ++n) {
+        const int split = 64 * ((tiles + n - 1) / n);
+        if ((max_kv_len + split - 1) / split != n) continue;   // this split gives fewer pieces
+        const double waves = units * n / slots;
+        const double eff = waves / std::ceil(waves);
+        if (waves >= 1.0 && eff >= 0.9) return split;
+        if (eff > best_eff) {
+            best_eff = eff;
+            best = split;
+        }
+    }
+    return best;
+}
+
 int attn_decode_split_tokens(attn_dtype_t kv_dtype, int n_groups, int B, int Hq, int Hkv, int q_len, int max_kv_len,
                              int D) {
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || q_len <= 0 || q_len > 16 || max_kv_len <= 0 || D != 128) return 0;
@@ -332,27 +369,8 @@ int attn_decode_split_tokens(attn_dtype_t kv_dtype, int n_groups, int B, int Hq,
     int occ = 0;
     const cudaError_t e = (fmt == 2) ? launch_decode_fp8(a, nullptr, nullptr, nullptr, &occ)
                                      : launch_decode(a, nullptr, &occ);
-    const int sms = device_sm_count();
-    if (e != cudaSuccess || occ <= 0 || sms <= 0) return 0;
-    const double slots = static_cast<double>(sms) * occ;
-    const int R = rows_per_cta(a);
-    const double units = static_cast<double>(B) * Hkv * ((G * q_len + R - 1) / R);
-    // fewest splits whose CTAs fill at least one wave, the last one 90 % full
-    const int tiles = (max_kv_len + 63) / 64;
-    int best = 64 * tiles;
-    double best_eff = -1.0;
-    for (int n = 1; n <= tiles; ++n) {
-        const int split = 64 * ((tiles + n - 1) / n);
-        if ((max_kv_len + split - 1) / split != n) continue;   // this split gives fewer pieces
-        const double waves = units * n / slots;
-        const double eff = waves / std::ceil(waves);
-        if (waves >= 1.0 && eff >= 0.9) return split;
-        if (eff > best_eff) {
-            best_eff = eff;
-            best = split;
-        }
-    }
-    return best;
+    if (e != cudaSuccess) return 0;
+    return attn_decode_split_tokens_for(device_sm_count(), occ, B, Hq, Hkv, q_len, max_kv_len);
 }
 
 size_t attn_decode_workspace_bytes(int B, int Hq, int max_kv_len, int split_tokens, int D) {

@@ -118,6 +118,10 @@ size_t attn_prefill_workspace_bytes(attn_dtype_t dtype, int B, int Hq, int Hkv, 
  * no device.  If grid is not NULL, *grid = the CTAs of the tensor-core launch
  * (0 for the CUDA-core paths and on error). */
 int attn_prefill_plan(attn_dtype_t dtype, int B, int Hq, int Hkv, int q_len, int kv_len, int D, int* grid);
+/* The same for a device with `sms` SMs (nothing is asked of the driver), for
+ * planning ahead; -1 also for sms <= 0. */
+int attn_prefill_plan_sms(attn_dtype_t dtype, int B, int Hq, int Hkv, int q_len, int kv_len, int D, int sms,
+                          int* grid);
 attn_status_t attn_prefill_fwd_ws(const void* q, const void* k, const void* v,
                                   void* o, float* lse, attn_dtype_t dtype,
                                   int B, int Hq, int Hkv, int q_len, int kv_len, int D,
@@ -182,6 +186,10 @@ size_t attn_decode_workspace_bytes(int B, int Hq, int max_kv_len, int split_toke
  */
 int attn_decode_split_tokens(attn_dtype_t kv_dtype, int n_groups, int B, int Hq, int Hkv, int q_len, int max_kv_len,
                              int D);
+/* The same choice for `sms` SMs holding ctas_per_sm decode CTAs each
+ * (nothing is asked of the driver); 0 for sizes the decode entries do not take
+ * or a non-positive device description. */
+int attn_decode_split_tokens_for(int sms, int ctas_per_sm, int B, int Hq, int Hkv, int q_len, int max_kv_len);
 
 /*
  * attn_prefill_paged_varlen - causal GQA prefill of a ragged batch over a
@@ -424,7 +432,8 @@ const char* attn_status_string(attn_status_t status);
 /* ABI version of this header (major * 100 + minor); 101 added attn_selftest_wait_timeout,
  * 102 attn_prefill_paged_varlen_ws, 103 attn_prefill_fwd_host,
  * 104 attn_prefill_fwd_ws, attn_prefill_workspace_bytes, attn_prefill_plan,
- * 105 attn_decode_split_tokens. */
+ * 105 attn_decode_split_tokens,
+ * 106 attn_prefill_plan_sms, attn_decode_split_tokens_for. */
 int attn_abi_version(void);
 
 #ifdef __cplusplus
