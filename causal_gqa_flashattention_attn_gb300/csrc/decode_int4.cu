@@ -92,6 +92,7 @@ __global__ void __launch_bounds__(kThreads, (R > 8) ? 1 : 3) decode_int4_kernel(
     constexpr int BW = (NG <= 4) ? 20 : 24;    // words per smem row (box width)
     constexpr int kTileBytes = kTileTok * BW * 4;
     constexpr int kStageBytes = 2 * kTileBytes;
+    constexpr int kCfV = 2 * NG * 16 + 16;     // V half of a coefficient table (16 floats of bank padding)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align_1024(smem_raw);
     __shared__ __align__(8) uint64_t full_bar[NS];
@@ -225,10 +226,10 @@ __global__ void __launch_bounds__(kThreads, (R > 8) ? 1 : 3) decode_int4_kernel(
     float m_run[2] = {-INFINITY, -INFINITY};
     float l_part[2] = {0.f, 0.f};
     const float sl2 = p.scale_log2;
-    // this warp's fp32 coefficient table for its 16 tokens of the current tile:
-    // [0] K scale, [1] K offset - 128 * K scale (both times log2 e * softmax scale),
-    // [2] V scale, [3] V offset; [kind][group][token]
-    float* cf = reinterpret_cast<float*>(smem + NS * kStageBytes) + warp * (4 * NG * 16);
+    // this warp's fp32 coefficient table for its 16 tokens of the current tile,
+    // [group][token] blocks: K scale, K offset - 128 * K scale (both times
+    // log2 e * softmax scale), then at kCfV: V scale, V offset
+    float* cf = reinterpret_cast<float*>(smem + NS * kStageBytes) + warp * (2 * kCfV);
 
     for (int t = 0; t < n_tiles; ++t) {
         const int slot = t % NS;
@@ -244,15 +245,37 @@ __global__ void __launch_bounds__(kThreads, (R > 8) ? 1 : 3) decode_int4_kernel(
             const uint32_t* vt = reinterpret_cast<const uint32_t*>(smem + slot * kStageBytes + kTileBytes) + woff;
             // ---- coefficient words -> fp32, once per (token, group); rows past the
             // end of the sequence may hold any bits and get weight 0
-#pragma unroll
-            for (int i = lane; i < 2 * 16 * NG; i += 32) {
-                const int kv = i / (16 * NG), rem = i % (16 * NG);
-                const int tok = rem / NG, gr = rem % NG;
-                const uint32_t cw = (kv == 0 ? kt : vt)[(warp * 16 + tok) * BW + gr];
+            if constexpr (NG % 4 == 0) {
+                // rows of n_groups + 16 words start on 16 bytes (the box starts at
+                // this head's row): one lane per (K or V, token) takes its row's
+                // coefficient words four at a time
+                const int kv = lane >> 4, tok = lane & 15;
                 const bool ok = tok < n_valid;
-                const float sc = ok ? lo_half(cw) : 0.f, of = ok ? hi_half(cw) : 0.f;
-                cf[((2 * kv) * NG + gr) * 16 + tok] = kv == 0 ? sc * sl2 : sc;
-                cf[((2 * kv + 1) * NG + gr) * 16 + tok] = kv == 0 ? fmaf(-128.f, sc, of) * sl2 : of;
+                const uint32_t* crow = (kv == 0 ? kt : vt) + (warp * 16 + tok) * BW;
+                float* dst = cf + kv * kCfV + tok;
+#pragma unroll
+                for (int q4 = 0; q4 < NG / 4; ++q4) {
+                    const uint4 c4 = *reinterpret_cast<const uint4*>(crow + 4 * q4);
+                    const uint32_t cw[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int gr = 4 * q4 + u;
+                        const float sc = ok ? lo_half(cw[u]) : 0.f, of = ok ? hi_half(cw[u]) : 0.f;
+                        dst[gr * 16] = kv == 0 ? sc * sl2 : sc;
+                        dst[(NG + gr) * 16] = kv == 0 ? fmaf(-128.f, sc, of) * sl2 : of;
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int i = lane; i < 2 * 16 * NG; i += 32) {
+                    const int kv = i / (16 * NG), rem = i % (16 * NG);
+                    const int tok = rem / NG, gr = rem % NG;
+                    const uint32_t cw = (kv == 0 ? kt : vt)[(warp * 16 + tok) * BW + gr];
+                    const bool ok = tok < n_valid;
+                    const float sc = ok ? lo_half(cw) : 0.f, of = ok ? hi_half(cw) : 0.f;
+                    cf[kv * kCfV + gr * 16 + tok] = kv == 0 ? sc * sl2 : sc;
+                    cf[kv * kCfV + (NG + gr) * 16 + tok] = kv == 0 ? fmaf(-128.f, sc, of) * sl2 : of;
+                }
             }
             __syncwarp();
             // ---- scores in bf16 code space: per group T_g = sum_d q (128 + c), then
@@ -353,10 +376,10 @@ __global__ void __launch_bounds__(kThreads, (R > 8) ? 1 : 3) decode_int4_kernel(
             //      head-dim rows, N = 8 heads, K = 16 tokens
 #pragma unroll
             for (int gr = 0; gr < NG; ++gr) {
-                const float2 scA = *reinterpret_cast<const float2*>(cf + (2 * NG + gr) * 16 + 2 * t4);
-                const float2 scC = *reinterpret_cast<const float2*>(cf + (2 * NG + gr) * 16 + 8 + 2 * t4);
-                const float2 ofA = *reinterpret_cast<const float2*>(cf + (3 * NG + gr) * 16 + 2 * t4);
-                const float2 ofC = *reinterpret_cast<const float2*>(cf + (3 * NG + gr) * 16 + 8 + 2 * t4);
+                const float2 scA = *reinterpret_cast<const float2*>(cf + kCfV + gr * 16 + 2 * t4);
+                const float2 scC = *reinterpret_cast<const float2*>(cf + kCfV + gr * 16 + 8 + 2 * t4);
+                const float2 ofA = *reinterpret_cast<const float2*>(cf + kCfV + (NG + gr) * 16 + 2 * t4);
+                const float2 ofC = *reinterpret_cast<const float2*>(cf + kCfV + (NG + gr) * 16 + 8 + 2 * t4);
                 uint32_t pa[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
                 for (int rr = 0; rr < kRows; ++rr) {
@@ -489,7 +512,7 @@ cudaError_t launch_g_ng(const DecodeArgs& a, cudaStream_t stream, int* occ) {
     constexpr int BW = (NG <= 4) ? 20 : 24;
     constexpr int kStageBytes = 2 * kTileTok * BW * 4;
     const int row_words = a.n_groups + a.D / 8;
-    const size_t ring = NS * kStageBytes + kConsumers * 4 * NG * 16 * sizeof(float);
+    const size_t ring = NS * kStageBytes + kConsumers * (4 * NG * 16 + 32) * sizeof(float);
     const size_t red = (kConsumers * R * kD + 2 * kConsumers * R) * sizeof(float);
     const size_t smem = (ring > red ? ring : red) + 1024;
     auto kern = decode_int4_kernel<R, NG, NS>;
