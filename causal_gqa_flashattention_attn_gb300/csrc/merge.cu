@@ -4,7 +4,8 @@
 // maximum partial LSE M, weights w_s = exp(LSE_s - M), O = sum w_s O_s / sum w_s,
 // LSE = M + log(sum w_s); a row whose partial LSEs are all -inf gives O = 0
 // and LSE = -inf.  One warp per row, lanes across D in float4 chunks; splits
-// with LSE = -inf are skipped without reading their O.
+// with LSE = -inf add nothing, whatever bits their O holds (rows of up to 16
+// splits and D <= 128 load every partial at once, the rest skip reading them).
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -39,6 +40,7 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 constexpr int kBatch = 8;   // splits whose loads are in flight together
+constexpr int kFastSplits = 16;   // rows of at most this many splits load everything at once
 
 // Weighted sum over the splits of lane chunk `d` of a row: lane j of each
 // block of 32 splits holds the weight of split s0 + j; loads of kBatch splits
@@ -95,11 +97,40 @@ __global__ void __launch_bounds__(32 * kWarps) lse_merge_kernel(const float* __r
     if (row >= N) return;
     const float* lp = lse_part + static_cast<size_t>(row) * S;
     const float* op = o_part + static_cast<size_t>(row) * S * D;
+    OutT* orow = o + static_cast<size_t>(row) * D;
+    if (S <= kFastSplits && D <= 128) {
+        // the row's partial LSEs (one per lane) and all its partial-O chunks are
+        // loaded together; the same weights, sums and order as the general path
+        const int d = 4 * lane;
+        const float l = lane < S ? lp[lane] : -INFINITY;
+        float4 v[kFastSplits];
+#pragma unroll
+        for (int u = 0; u < kFastSplits; ++u)
+            v[u] = (u < S && d < D) ? ld4(op + static_cast<size_t>(u) * D + d) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float mx = warp_max(l);
+        const bool alive = mx != -INFINITY;
+        const float w = (l == -INFINITY) ? 0.f : expf(l - mx);
+        const float wsum = warp_sum(w);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int u = 0; u < kFastSplits; ++u) {
+            const float wu = __shfl_sync(0xffffffffu, w, u);
+            if (wu != 0.f) {   // splits of weight 0 may hold any bits
+                acc.x = fmaf(wu, v[u].x, acc.x);
+                acc.y = fmaf(wu, v[u].y, acc.y);
+                acc.z = fmaf(wu, v[u].z, acc.z);
+                acc.w = fmaf(wu, v[u].w, acc.w);
+            }
+        }
+        const float inv = alive ? 1.f / wsum : 0.f;
+        if (d < D) store4(orow + d, make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
+        if (lse != nullptr && lane == 0) lse[row] = alive ? mx + logf(wsum) : -INFINITY;
+        return;
+    }
     float mx, wsum;
     row_weights(lp, S, lane, mx, wsum);
     const bool alive = mx != -INFINITY;
     const float inv = alive ? 1.f / wsum : 0.f;
-    OutT* orow = o + static_cast<size_t>(row) * D;
     for (int c = 0; c < kMaxChunks && 128 * c < D; ++c) {
         const int d = 4 * (lane + 32 * c);
         const float4 acc = alive ? weighted_sum(op, lp, S, D, d, mx, lane) : make_float4(0.f, 0.f, 0.f, 0.f);

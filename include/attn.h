@@ -381,7 +381,8 @@ attn_status_t attn_decode_paged_splitk_static(const void* q, const void* k_cache
  * Follows "splitk_kernels.py", _splitK_reduce: per row n,
  *   M = max_s lse_part[n, s];  w_s = exp(lse_part[n, s] - M);
  *   o[n] = sum_s w_s o_part[n, s] / sum_s w_s;  lse[n] = M + log(sum_s w_s);
- *   a row whose partial LSEs are all -inf gets o = 0, lse = -inf.
+ *   a row whose partial LSEs are all -inf gets o = 0, lse = -inf; the o_part
+ *   entries of a split whose LSE is -inf add nothing, whatever they hold.
  *
  *   o_part   float32 [N, S, D]  (read)      lse_part float32 [N, S] (read)
  *   o        [N, D] in o_dtype (ATTN_F32 or ATTN_BF16) (written)
