@@ -50,7 +50,9 @@ def visible_mask(q_len, kv_len, rows=None):
 
 
 def attend(q, k, v, mask, scale):
-    """Masked softmax attention of one head, materialised in full.
+    """Masked softmax attention of one head, materialised in full: what the
+    blockwise online-softmax loop of ``causal_forward_kernel.py``
+    (``_flash_attention_forward_gqa_kernel``) computes, written directly.
 
     ``q [M, D]``, ``k [N, D]``, ``v [N, Dv]``, ``mask`` bool ``[M, N]``.
     Returns ``o [M, Dv]`` and the natural-log ``lse [M]``:
@@ -202,7 +204,8 @@ def dequant_int4_rows(words, d, n_groups):
 # --------------------------------------------------------------------------
 
 def fp8_e4m3_value(byte):
-    """Value of one float8 e4m3 byte (1 sign bit, 4 exponent bits with bias 7,
+    """Value of one float8 e4m3 byte, the encoding ``splitk_kernels.py``'s
+    ``dequantize`` bitcasts fp8 codes to (1 sign bit, 4 exponent bits with bias 7,
     3 mantissa bits, no infinities; exponent 15 with mantissa 7 is NaN)."""
     b = int(byte) & 0xFF
     sign = -1.0 if b >> 7 else 1.0
@@ -219,7 +222,9 @@ _FP8_TABLE = np.array([fp8_e4m3_value(b) for b in range(256)])
 
 
 def dequant_fp8_rows(codes, scale_shift):
-    """Rows of e4m3 bytes ``codes [..., D]`` with one coefficient word per row
+    """Row-wise fp8 dequantisation (``splitk_kernels.py``, ``_fwd_kernel_splitK``
+    with a separate scale/shift tensor, and ``dequantize``).
+    Rows of e4m3 bytes ``codes [..., D]`` with one coefficient word per row
     ``scale_shift [...]`` (fp16 scale in the low 16 bits, fp16 shift in the
     high 16 bits): value = decoded byte * scale + shift, in float64."""
     c = np.asarray(codes).astype(np.int64) & 0xFF
@@ -265,7 +270,9 @@ def _kv_rows(cache, block_table, b, lo, hi, page_size, kv_format, d, n_groups, s
 
 
 def num_splits(max_kv_len, split_tokens):
-    """Number of split-K chunks for the longest sequence (at least one)."""
+    """Number of split-K chunks for the longest sequence (at least one); chunk
+    ``s`` starts at ``s * split_tokens``, as ``chunk_lo = splitk_idx *
+    BLOCK_N_PER_SPLIT`` in ``splitk_kernels.py``'s ``_fwd_kernel_splitK``."""
     return max(1, -(-int(max_kv_len) // int(split_tokens)))
 
 
@@ -319,7 +326,9 @@ def decode_split_partials(q, k_cache, v_cache, block_table, seq_lens, page_size,
 
 def decode_unsplit(q, k_cache, v_cache, block_table, seq_lens, page_size, scale=None,
                    kv_format="dense", n_groups=1, batches=None):
-    """Single-query decode over each whole sequence in one piece (no split)."""
+    """Single-query decode over each whole sequence in one piece (no split):
+    the result every split of ``splitk_kernels.py``'s ``_fwd_kernel_splitK``
+    followed by ``_splitK_reduce`` must reproduce."""
     q = np.asarray(q, dtype=np.float64)
     bsz, hq, d = q.shape
     hkv = k_cache.shape[2]
@@ -345,7 +354,8 @@ def decode_unsplit(q, k_cache, v_cache, block_table, seq_lens, page_size, scale=
 # --------------------------------------------------------------------------
 
 def lse_merge(o_part, lse_part):
-    """Merge split partials ``o_part [..., S, D]``, ``lse_part [..., S]``.
+    """Merge split partials ``o_part [..., S, D]``, ``lse_part [..., S]``
+    (``splitk_kernels.py``, ``_splitK_reduce``).
 
     ``M = max_s LSE_s``; ``w_s = exp(LSE_s - M)``;
     ``O = sum_s w_s O_s / sum_s w_s``; ``LSE = M + log(sum_s w_s)``;
@@ -382,7 +392,8 @@ def decode(q, k_cache, v_cache, block_table, seq_lens, page_size, split_tokens, 
 # --------------------------------------------------------------------------
 
 def lse_merge_bwd(o_part, lse_part, d_o, d_lse=None):
-    """Gradients of :func:`lse_merge` with respect to its inputs.
+    """Gradients of :func:`lse_merge` with respect to its inputs
+    (``splitk_kernels.py``, ``_splitK_reduce_varargs_backward``).
 
     For each row with merged ``O`` and ``LSE`` (recomputed here by
     :func:`lse_merge`) and incoming gradients ``dO [..., D]``, ``dLSE [...]``:
@@ -417,7 +428,9 @@ def lse_merge_bwd(o_part, lse_part, d_o, d_lse=None):
 def decode_mq_split_partials(q, k_cache, v_cache, block_table, seq_lens, page_size, split_tokens, scale=None,
                              kv_format="dense", n_groups=1, max_kv_len=None, batches=None, k_scale_shift=None,
                              v_scale_shift=None):
-    """Split partials of decode with ``q_len`` queries per sequence.
+    """Split partials of decode with ``q_len`` queries per sequence
+    (``splitk_kernels.py``, ``_fwd_kernel_splitK``, its causal mask for several
+    queries per sequence).
 
     ``q [B, Hq, q_len, D]``.  Query ``i`` of sequence ``b`` sees cached token
     ``t`` iff ``t <= len_b - q_len + i`` (bottom-right alignment, the queries
