@@ -271,8 +271,9 @@ def _kv_rows(cache, block_table, b, lo, hi, page_size, kv_format, d, n_groups, s
 
 def num_splits(max_kv_len, split_tokens):
     """Number of split-K chunks for the longest sequence (at least one); chunk
-    ``s`` starts at ``s * split_tokens``, as ``chunk_lo = splitk_idx *
-    BLOCK_N_PER_SPLIT`` in ``splitk_kernels.py``'s ``_fwd_kernel_splitK``."""
+    ``s`` starts at ``s * split_tokens`` (``splitk_kernels.py``,
+    ``_fwd_kernel_splitK``: each split's key range begins at its index times
+    the per-split block size)."""
     return max(1, -(-int(max_kv_len) // int(split_tokens)))
 
 
