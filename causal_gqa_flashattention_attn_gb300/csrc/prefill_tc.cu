@@ -7,8 +7,8 @@
 // m_new)), P rounded to bf16 before O += P V, skipping of tiles above the
 // causal diagonal and masking of the diagonal tiles only, then O = acc / l
 // and a per-row LSE.  Causal alignment is bottom-right as in
-// "gpt-o3 / triton6fd1ef", _gqa_prefill_kernel (kv_allowed = min(kv_len,
-// q_idx + 1 + delta)); the LSE is the natural log with no epsilon; the
+// "gpt-o3 / triton6fd1ef", _gqa_prefill_kernel (query i sees the first
+// i + 1 + delta keys, at most kv_len of them); the LSE is the natural log with no epsilon; the
 // fully-masked-row guard is that of "splitk_kernels.py", _fwd_kernel_splitK.
 //
 // GB300 design:

@@ -65,7 +65,8 @@ typedef enum {
  * _flash_attention_forward_gqa_kernel and its wrapper flash_attention_forward
  * (tiled online-softmax forward, GQA head map, O in the input dtype, an LSE
  * row per query), with the bottom-right alignment of "gpt-o3 / triton6fd1ef",
- * _gqa_prefill_kernel (kv_allowed = min(kv_len, q_idx + 1 + delta)).
+ * _gqa_prefill_kernel: query i sees the first i + 1 + delta keys, at most
+ * kv_len of them, delta = kv_len - q_len.
  *
  *   q    [B, Hq,  q_len,  D]  dtype            (read)
  *   k    [B, Hkv, kv_len, D]  dtype            (read)
@@ -292,8 +293,8 @@ attn_status_t attn_decode_paged_splitk(const void* q, const void* k_cache, const
  * attn_decode_paged_splitk_mq - causal multi-query split-K decode.
  *
  * Follows "splitk_kernels.py", _fwd_kernel_splitK with IS_CAUSAL and
- * NUM_QUERIES_CAUSAL (the comment "Why does the masking condition below work
- * as a causal mask?"): the q_len queries of a sequence are its last q_len
+ * NUM_QUERIES_CAUSAL (the kernel's own explanation of its causal mask): the
+ * q_len queries of a sequence are its last q_len
  * positions, so query i (0-based) sees cached tokens t <= len_b - q_len + i
  * (bottom-right alignment).  A split in which a query sees nothing yields
  * O_s = 0, LSE_s = -inf for that query.  Used for speculative decoding.

@@ -5,9 +5,10 @@ Sources, by page title and section:
 
 * ``causal_forward_kernel.py`` (flash-attention-scratch),
   ``_flash_attention_forward_gqa_kernel``: the GQA head map
-  (``kv_head = q_head // (Hq // Hkv)``) and what the blockwise loop computes.
+  (query head h reads KV head h // G, G = Hq / Hkv) and what the blockwise
+  loop computes.
 * ``gpt-o3 / triton6fd1ef`` (FlashInfer-style GQA prefill), ``_gqa_prefill_kernel``,
-  "Number of KV tokens visible to this query": bottom-right causal alignment,
+  the block that counts the KV tokens each query may see: bottom-right causal alignment,
   a key j is visible to query i iff ``j < min(kv_len, i + 1 + delta)`` with
   ``delta = kv_len - q_len``.
 * ``splitk_kernels.py`` (xformers), ``_fwd_kernel_splitK``: split-K chunks,
@@ -39,7 +40,7 @@ def visible_mask(q_len, kv_len, rows=None):
     """Boolean visibility matrix ``[len(rows), kv_len]``.
 
     Bottom-right causal alignment (``gpt-o3 / triton6fd1ef``,
-    ``_gqa_prefill_kernel``, the ``kv_allowed`` computation): with
+    ``_gqa_prefill_kernel``, the count of keys each query may see): with
     ``delta = kv_len - q_len`` key ``j`` is visible to query ``i`` iff
     ``j <= i + delta`` (and ``j < kv_len``, which the range of ``j`` gives).
     """
@@ -200,7 +201,7 @@ def dequant_int4_rows(words, d, n_groups):
 
 # --------------------------------------------------------------------------
 # fp8 row format (splitk_kernels.py: FP8_QUANTIZED in _fwd_kernel_splitK,
-# the K/V_fp8_scale_shift tensors, dequantize with PACKED_PER_VAL == 4)
+# the K/V_fp8_scale_shift tensors, the fp8 branch of dequantize)
 # --------------------------------------------------------------------------
 
 def fp8_e4m3_value(byte):
@@ -241,7 +242,7 @@ def dequant_fp8_rows(codes, scale_shift):
 def paged_row_index(block_table, b, t, page_size):
     """Physical row of logical token ``t`` of sequence ``b``:
     ``block_table[b, t // page_size] * page_size + t % page_size``
-    ("Offset in integer pages" / ``physical_page_idx`` in ``_fwd_kernel_splitK``)."""
+    (the page-offset computation, ``physical_page_idx``, in ``_fwd_kernel_splitK``)."""
     return int(block_table[b][t // page_size]) * page_size + t % page_size
 
 
@@ -422,8 +423,8 @@ def lse_merge_bwd(o_part, lse_part, d_o, d_lse=None):
 
 # --------------------------------------------------------------------------
 # Causal multi-query decode (splitk_kernels.py: _fwd_kernel_splitK with
-# IS_CAUSAL and NUM_QUERIES_CAUSAL, "Why does the masking condition below work
-# as a causal mask?")
+# IS_CAUSAL and NUM_QUERIES_CAUSAL, and the kernel's own explanation of its
+# causal mask)
 # --------------------------------------------------------------------------
 
 def decode_mq_split_partials(q, k_cache, v_cache, block_table, seq_lens, page_size, split_tokens, scale=None,
