@@ -91,8 +91,8 @@ def prefill(q, k, v, scale=None):
     Returns ``o [B, Hq, q_len, D]`` and ``lse [B, Hq, q_len]`` in float64.
     K and V are expanded to Hq heads with an explicit ``np.repeat`` so that
     query head ``h`` reads key/value head ``h // (Hq // Hkv)``
-    (``causal_forward_kernel.py``, "map the current query head to its shared
-    key/value head").
+    (``causal_forward_kernel.py``, ``_flash_attention_forward_gqa_kernel``,
+    its GQA head-map block).
     """
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
