@@ -327,10 +327,12 @@ def decode_split_partials(q, k_cache, v_cache, block_table, seq_lens, page_size,
 
 
 def decode_unsplit(q, k_cache, v_cache, block_table, seq_lens, page_size, scale=None,
-                   kv_format="dense", n_groups=1, batches=None):
+                   kv_format="dense", n_groups=1, batches=None, k_scale_shift=None, v_scale_shift=None):
     """Single-query decode over each whole sequence in one piece (no split):
     the result every split of ``splitk_kernels.py``'s ``_fwd_kernel_splitK``
-    followed by ``_splitK_reduce`` must reproduce."""
+    followed by ``_splitK_reduce`` must reproduce.  Cache formats as in
+    :func:`decode_split_partials` (an fp8 cache comes with its per-row
+    ``k/v_scale_shift`` words)."""
     q = np.asarray(q, dtype=np.float64)
     bsz, hq, d = q.shape
     hkv = k_cache.shape[2]
@@ -340,8 +342,8 @@ def decode_unsplit(q, k_cache, v_cache, block_table, seq_lens, page_size, scale=
     o_out = np.zeros((bsz, hq, d))
     lse_out = np.full((bsz, hq), NEG_INF)
     for b in (range(bsz) if batches is None else batches):
-        k_rows = _kv_rows(k_cache, block_table, b, 0, lens[b], page_size, kv_format, d, n_groups)
-        v_rows = _kv_rows(v_cache, block_table, b, 0, lens[b], page_size, kv_format, d, n_groups)
+        k_rows = _kv_rows(k_cache, block_table, b, 0, lens[b], page_size, kv_format, d, n_groups, k_scale_shift)
+        v_rows = _kv_rows(v_cache, block_table, b, 0, lens[b], page_size, kv_format, d, n_groups, v_scale_shift)
         k_rep = np.repeat(k_rows, group, axis=1)
         v_rep = np.repeat(v_rows, group, axis=1)
         every = np.ones((1, lens[b]), dtype=bool)

@@ -592,6 +592,49 @@ def test_fp8_decode_equals_dense_decode_on_dequantised_rows():
     np.testing.assert_allclose(lse, lse2, rtol=1e-13, atol=1e-13)
 
 
+def test_fp8_unsplit_decode_against_brute_force_on_torch_decoded_rows():
+    """decode_unsplit over an fp8 cache equals brute-force attention over rows
+    rebuilt page by page, each byte decoded by torch's float8_e4m3fn and
+    mapped by its row's fp16 scale and shift (a decoder independent of the
+    oracle's own table)."""
+    lens = [9, 14, 1]
+    ps, d, hkv = 4, 8, 2
+    rng = np.random.default_rng(43)
+    n_pages = sum(-(-n // ps) for n in lens)
+    perm = rng.permutation(n_pages)
+    table = np.full((3, 4), -1, dtype=np.int64)
+    cur = 0
+    for b, n in enumerate(lens):
+        table[b, :-(-n // ps)] = perm[cur:cur - (-n // ps)]
+        cur += -(-n // ps)
+    codes = [rng.integers(0, 256, size=(n_pages, ps, hkv, d)) for _ in range(2)]
+    for c in codes:
+        c[(c & 0x7F) == 0x7F] = 0                 # no NaN bytes
+    words = []
+    for _ in range(2):
+        sc = np.float16(rng.uniform(0.1, 0.5, size=(n_pages, ps, hkv))).view(np.uint16).astype(np.int64)
+        sh = np.float16(rng.normal(0, 0.1, size=(n_pages, ps, hkv))).view(np.uint16).astype(np.int64)
+        words.append(sc | (sh << 16))
+    q = rng.standard_normal((3, 4, d))
+    o, lse = oracle.decode_unsplit(q, codes[0], codes[1], table, lens, ps, scale=0.4, kv_format="fp8",
+                                   k_scale_shift=words[0], v_scale_shift=words[1])
+
+    def rows(c, w, b, n):
+        out = []
+        for t in range(n):
+            pg, sl = table[b, t // ps], t % ps
+            x = torch.tensor(c[pg, sl].astype(np.uint8)).view(torch.float8_e4m3fn).double().numpy()
+            sc = np.float64(np.uint16(w[pg, sl] & 0xFFFF).view(np.float16))
+            sh = np.float64(np.uint16(w[pg, sl] >> 16).view(np.float16))
+            out.append(x * sc[:, None] + sh[:, None])
+        return np.stack(out)[None].transpose(0, 2, 1, 3)          # [1, Hkv, n, D]
+    for b, n in enumerate(lens):
+        kk, vv = rows(codes[0], words[0], b, n), rows(codes[1], words[1], b, n)
+        ob, lb = _brute_prefill(q[b][None, :, None, :], kk, vv, 0.4)
+        np.testing.assert_allclose(o[b], ob[0, :, 0], rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(lse[b], lb[0, :, 0], rtol=1e-12, atol=1e-13)
+
+
 # ------------------------------------------------------- varlen paged prefill
 
 @pytest.mark.parametrize("page_size", [1, 3])
