@@ -51,16 +51,20 @@ def prefill_flops(shape):
     return 2 * shape.B * shape.Hq * shape.D * visible_pairs(shape.q_len, shape.kv_len) * 2
 
 
+def kv_row_bytes(shape):
+    """Bytes of one cached (token, KV head) row of K (or of V)."""
+    if shape.kv_format == "dense":
+        return shape.D * 2
+    if shape.kv_format == "fp8":
+        return shape.D + 4       # e4m3 bytes + the row's scale/shift word
+    return (shape.n_groups + shape.D // 8) * 4
+
+
 def decode_bytes(shape, lens):
     """Algorithmic bytes of one decode: every cached K and V row once, Q, the
     block-table entries and lengths read; O and LSE written.  The split
     partials (kernel-to-kernel scratch) are not counted."""
-    if shape.kv_format == "dense":
-        row = shape.D * 2
-    elif shape.kv_format == "fp8":
-        row = shape.D + 4        # e4m3 bytes + the row's scale/shift word
-    else:
-        row = (shape.n_groups + shape.D // 8) * 4
+    row = kv_row_bytes(shape)
     kv = sum(lens) * shape.Hkv * row * 2
     pages = sum(-(-n // shape.page_size) for n in lens)
     q = shape.B * shape.Hq * shape.D * 2
@@ -206,6 +210,43 @@ def oracle_prefill_sample(seconds, shape):
     return per_head * heads / el / 1e12, heads, el
 
 
+def oracle_decode_sample(seconds, shape, inp):
+    """The oracle as it stands on the host cores: whole sequences of a decode
+    workload (every head, every split, merged), in order, until `seconds`
+    pass.  Each sequence's pages are first gathered into a compact pool with a
+    matching block table (outside the timed region); the oracle then walks
+    that table token by token itself.  Returns KV GB/s of algorithmic bytes."""
+    import numpy as np
+
+    import oracle
+    ps = shape.page_size
+    qn = inp["q"].double().numpy()
+    table = inp["block_table"].numpy()
+    done_bytes, done, el = 0, 0, 0.0
+    row = kv_row_bytes(shape)
+    for b, n in enumerate(inp["lens"]):
+        pages = table[b, :-(-n // ps)]
+        kc, vc = inp["k_cache"][pages], inp["v_cache"][pages]
+        if shape.kv_format == "dense":
+            kc, vc = kc.float().numpy(), vc.float().numpy()
+        else:
+            kc, vc = kc.numpy(), vc.numpy()
+        extra = {}
+        if shape.kv_format == "fp8":
+            extra = dict(k_scale_shift=inp["k_scale_shift"][pages].numpy(),
+                         v_scale_shift=inp["v_scale_shift"][pages].numpy())
+        t_b = np.arange(len(pages))[None, :]
+        t0 = time.perf_counter()
+        oracle.decode(qn[b:b + 1], kc, vc, t_b, [n], ps, shape.split_tokens, kv_format=shape.kv_format,
+                      n_groups=shape.n_groups, **extra)
+        el += time.perf_counter() - t0
+        done_bytes += n * shape.Hkv * row * 2
+        done += 1
+        if el >= seconds:
+            break
+    return done_bytes / el / 1e9, done, el
+
+
 def host_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -252,7 +293,14 @@ def run_ours(args, rank, world, dist):
                          o=torch.empty(shape.B * shape.Hq, shape.D, dtype=torch.bfloat16, device=dev),
                          lse=torch.empty(shape.B * shape.Hq, dtype=torch.float32, device=dev),
                          bytes=decode_bytes(shape, inp["lens"]))
+        if rank == 0 and not args.no_cpu_baseline:
+            dec[name]["cpu_inp"] = inp     # the oracle's decode baseline reads the same draws
         del inp
+    # the int4 decode again at the 2048-token split the workload description
+    # gives for the bf16 cache (the leg above takes the split that fills the GPU)
+    d4s = synth.PAGED_DECODE_INT4
+    ws4s = torch.empty(attn.attn_decode_workspace_bytes(d4s.B, d4s.Hq, d4s.len_hi, d4s.split_tokens, d4s.D),
+                       dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     # split-schedule scratch of the two prefills (zeroed once; each call leaves it zeroed)
@@ -261,8 +309,8 @@ def run_ours(args, rank, world, dist):
     pwsb = torch.zeros(attn.attn_prefill_workspace_bytes(torch.bfloat16, pb.B, pb.Hq, pb.Hkv, pb.q_len, pb.kv_len,
                                                          pb.D), dtype=torch.uint8, device=dev)
 
-    kernels = ["prefill", "prefill_batched", "decode_bf16", "merge_bf16", "decode_int4", "merge_int4", "merge_bwd",
-               "decode_mq", "decode_fp8", "prefill_varlen", "prefill_varlen_ws"]
+    kernels = ["prefill", "prefill_batched", "decode_bf16", "merge_bf16", "decode_int4", "merge_int4",
+               "decode_int4_split2048", "merge_bwd", "decode_mq", "decode_fp8", "prefill_varlen", "prefill_varlen_ws"]
     # the method's own steps (dense prefill, paged split-K decode, merge); the
     # other legs are the widened rows (merge backward, multi-query, fp8, ragged)
     hot = ["prefill", "prefill_batched", "decode_bf16", "merge_bf16", "decode_int4", "merge_int4"]
@@ -320,6 +368,13 @@ def run_ours(args, rank, world, dist):
             ev[mname][0].record(stream)
             attn.attn_lse_merge(d["o_part"], d["lse_part"], o=d["o"], lse=d["lse"], stream=stream)
             ev[mname][1].record(stream)
+        t4 = dec["decode_int4"]["t"]
+        flush.fill_(1.0)
+        ev["decode_int4_split2048"][0].record(stream)
+        attn.attn_decode_paged_splitk(t4["q"], t4["k_cache"], t4["v_cache"], t4["block_table"], t4["seq_lens"],
+                                      d4s.split_tokens, d4s.len_hi, n_groups=d4s.n_groups, workspace=ws4s,
+                                      dev_status=status, stream=stream, write_output=False)
+        ev["decode_int4_split2048"][1].record(stream)
         flush.fill_(1.0)
         ev["merge_bwd"][0].record(stream)
         attn.attn_lse_merge_bwd(mbw["o_part"], mbw["lse_part"], mb_do, mb_dlse, d_o_part=mb_go, d_lse_part=mb_gl,
@@ -464,6 +519,10 @@ def run_ours(args, rank, world, dist):
         mb = n_rows * s_max * (d["shape"].D + 1) * 4 + n_rows * (d["shape"].D * 2 + 4)
         rep[mname] = dict(bound="hbm", achieved=mb / (ms[mname] * 1e-3) / 1e9, peak=peaks["hbm_gbs"], unit="GB/s",
                           work=mb, src="merge.cu", kernel="lse_merge_kernel")
+    kb4 = dec["decode_int4"]["bytes"]["kernel"]
+    rep["decode_int4_split2048"] = dict(bound="hbm", achieved=kb4 / (ms["decode_int4_split2048"] * 1e-3) / 1e9,
+                                        peak=peaks["hbm_gbs"], unit="GB/s", work=kb4, src="decode_int4.cu",
+                                        kernel="decode_int4_kernel (split 2048)")
     n_rows, s_max, dd = mbw["o_part"].shape
     # algorithmic bytes: partials read once, gradients in, gradient partials out
     mbb = n_rows * s_max * (dd + 1) * 4 * 2 + n_rows * (dd + 1) * 4
@@ -487,7 +546,10 @@ def run_ours(args, rank, world, dist):
         kernels_out.append({"name": kn, "kernel": r["kernel"], "ms": round(ms[kn], 5), "bound": r["bound"],
                             "achieved": round(r["achieved"], 2), "peak": r["peak"], "unit": r["unit"],
                             "frac": round(r["achieved"] / r["peak"], 4),
-                            "traffic": traffic.get(kn), "row": "hot path" if kn in hot else "widened"})
+                            "traffic": traffic.get(kn),
+                            "row": "hot path" if kn in hot else
+                            ("hot path, split 2048 (not in ms_per_step)" if kn == "decode_int4_split2048"
+                             else "widened")})
     dominant = max(hot, key=lambda kn: ms[kn])
     dom = rep[dominant]
     path = {}
@@ -504,6 +566,12 @@ def run_ours(args, rank, world, dist):
         cpu = {"value": val, "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
                "sample": f"{heads} whole heads (all {pf.q_len} query rows x {pf.kv_len} keys) of the prefill "
                          f"workload, {el:.1f} s of numpy float64 on the host"}
+        for name in ("decode_bf16", "decode_int4"):
+            d = dec[name]
+            gbs, n_seq, el_d = oracle_decode_sample(args.cpu_seconds / 2, d["shape"], d.pop("cpu_inp"))
+            cpu[name] = {"value": gbs, "unit": "GB/s", "kind": "oracle", "cores": host_cores(),
+                         "sample": f"{n_seq} whole sequences (every head and split, merged) of the {name} "
+                                   f"workload, {el_d:.1f} s of numpy float64 on the host; KV bytes read"}
     line = {
         "metric": METRIC,
         "value": round(tflops, 3),
@@ -561,30 +629,75 @@ def run_ours(args, rank, world, dist):
 
 def run_reference(args, rank):
     """The oracle arm: the CPU oracle as it stands, timed on the host cores on
-    a bounded sample of the same prefill workload (one head per step)."""
+    bounded samples of the same workloads.  Each step runs one whole head of
+    the Llama-style prefill (the headline TFLOP/s), one whole sequence of the
+    bf16 paged decode and one of the int4 paged decode (KV GB/s, every head
+    and split of the sequence, merged)."""
     import synth
     if rank != 0:
         return None
+    import numpy as np
+
+    import oracle
     pf = synth.LLAMA_GQA_PREFILL
     per_head = 2 * pf.D * visible_pairs(pf.q_len, pf.kv_len) * 2
-    import oracle
     q, k, v = synth.prefill_inputs(pf, seed=0)
     qn, kn, vn = q[:1].double().numpy(), k[:1].double().numpy(), v[:1].double().numpy()
     rows = list(range(pf.q_len))
+    dec = {}
+    for name, shape in (("decode_bf16", synth.PAGED_DECODE_BF16), ("decode_int4", synth.PAGED_DECODE_INT4)):
+        inp = synth.decode_inputs(shape, seed=0)
+        ps = shape.page_size
+        seqs = []
+        for i in range(args.warmup + args.steps):   # the pages of each sampled sequence, in a compact pool
+            b = i % shape.B
+            n = inp["lens"][b]
+            pages = inp["block_table"][b, :-(-n // ps)].numpy()
+            kc, vc = inp["k_cache"][pages], inp["v_cache"][pages]
+            conv = (lambda x: x.float().numpy()) if shape.kv_format == "dense" else (lambda x: x.numpy())
+            seqs.append((inp["q"][b:b + 1].double().numpy(), conv(kc), conv(vc), np.arange(len(pages))[None, :], n))
+        dec[name] = dict(shape=shape, seqs=seqs, row=kv_row_bytes(shape))
+        del inp
+
+    def decode_one(name, i):
+        d = dec[name]
+        sh = d["shape"]
+        qb, kc, vc, table, n = d["seqs"][i]
+        oracle.decode(qb, kc, vc, table, [n], sh.page_size, sh.split_tokens, kv_format=sh.kv_format,
+                      n_groups=sh.n_groups)
+        return n * sh.Hkv * d["row"] * 2
+
     for i in range(args.warmup):
         oracle.prefill_rows(qn, kn, vn, 0, i % pf.Hq, rows)
-    t0 = time.perf_counter()
+        decode_one("decode_bf16", i)
+        decode_one("decode_int4", i)
+    t_pf = 0.0
+    t_dec = {"decode_bf16": 0.0, "decode_int4": 0.0}
+    kv_bytes = {"decode_bf16": 0, "decode_int4": 0}
     for i in range(args.steps):
+        t0 = time.perf_counter()
         oracle.prefill_rows(qn, kn, vn, 0, i % pf.Hq, rows)
-    el = time.perf_counter() - t0
-    val = per_head * args.steps / el / 1e12
+        t_pf += time.perf_counter() - t0
+        for name in ("decode_bf16", "decode_int4"):
+            t0 = time.perf_counter()
+            kv_bytes[name] += decode_one(name, args.warmup + i)
+            t_dec[name] += time.perf_counter() - t0
+    val = per_head * args.steps / t_pf / 1e12
+    cores = host_cores()
     sample = f"one whole head (all {pf.q_len} query rows x {pf.kv_len} keys) of the prefill workload per step"
+    decode = {name: {"value": kv_bytes[name] / t_dec[name] / 1e9, "unit": "GB/s", "kind": "oracle", "cores": cores,
+                     "sample": f"one whole sequence of the {name} workload per step (every head and split, "
+                               f"merged); KV bytes read"}
+              for name in t_dec}
+    total = t_pf + sum(t_dec.values())
     return {"impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": 1,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "prefill B1 Hq32 Hkv4 q2048 kv4096 D128 (bottom-right causal), CPU oracle"},
-            "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
-                             "sample": sample},
+            "config": {"workload": "prefill B1 Hq32 Hkv4 q2048 kv4096 D128 (bottom-right causal) + paged split-K "
+                                   "decode bf16 B64 len U[512,32768] + int4 decode B16 len16384, CPU oracle"},
+            "decode": decode,
+            "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": sample, **decode},
             "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 

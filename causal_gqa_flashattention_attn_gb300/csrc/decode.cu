@@ -67,6 +67,7 @@ __global__ void __launch_bounds__(kThreads) decode_bf16_kernel(const __grid_cons
     __shared__ __align__(8) uint64_t full_bar[NS];
     __shared__ __align__(8) uint64_t empty_bar[NS];
     __shared__ int s_abort;
+    __shared__ int s_skip[NS];   // stage holds no tile: its page id was out of range
 
     const int split = blockIdx.x, kvh = blockIdx.y / p.n_rg, rg = blockIdx.y % p.n_rg, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -121,11 +122,13 @@ __global__ void __launch_bounds__(kThreads) decode_bf16_kernel(const __grid_cons
                 const int page = table[tok / p.page_size];
                 if (page < 0 || page >= p.num_pages) {
                     flag_status(p.status, ATTN_DEV_PAGE_OUT_OF_RANGE);
+                    s_skip[slot] = 1;               // the consumers leave the page's tokens out
                     mbar_arrive(&full_bar[slot]);  // release the consumers; the tile is not loaded
                     continue;
                 }
                 const int row = page * p.page_size + tok % p.page_size;
                 uint8_t* st = smem + slot * kStageBytes;
+                s_skip[slot] = 0;
                 mbar_arrive_expect_tx(&full_bar[slot], kStageBytes);
                 tma_load_3d(st, &k_map, &full_bar[slot], 0, kvh, row);
                 tma_load_3d(st + kHalfBytes, &k_map, &full_bar[slot], 64, kvh, row);
@@ -175,7 +178,7 @@ __global__ void __launch_bounds__(kThreads) decode_bf16_kernel(const __grid_cons
         const int n_valid = min(max(hi - tok0, 0), 16);
         const uint32_t k_s = smem_u32(smem + slot * kStageBytes);
         const uint32_t v_s = k_s + kKVTileBytes;
-        if (n_valid > 0) {
+        if (n_valid > 0 && !s_skip[slot]) {
             if (n_valid < 16) {
                 // rows past the end of the sequence: zero V so 0 * garbage stays 0
                 uint8_t* vt = smem + slot * kStageBytes + kKVTileBytes;

@@ -98,6 +98,7 @@ __global__ void __launch_bounds__(kThreads, (R > 8) ? 1 : 3) decode_int4_kernel(
     __shared__ __align__(8) uint64_t full_bar[NS];
     __shared__ __align__(8) uint64_t empty_bar[NS];
     __shared__ int s_abort;
+    __shared__ int s_skip[NS];   // stage holds no tile: its page id was out of range
 
     const int split = blockIdx.x, kvh = blockIdx.y / p.n_rg, rg = blockIdx.y % p.n_rg, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -152,11 +153,13 @@ __global__ void __launch_bounds__(kThreads, (R > 8) ? 1 : 3) decode_int4_kernel(
                 const int page = table[tok / p.page_size];
                 if (page < 0 || page >= p.num_pages) {
                     flag_status(p.status, ATTN_DEV_PAGE_OUT_OF_RANGE);
-                    mbar_arrive(&full_bar[slot]);
+                    s_skip[slot] = 1;               // the consumers leave the page's tokens out
+                    mbar_arrive(&full_bar[slot]);  // release the consumers; the tile is not loaded
                     continue;
                 }
                 const int row = page * p.page_size + tok % p.page_size;
                 uint8_t* st = smem + slot * kStageBytes;
+                s_skip[slot] = 0;
                 mbar_arrive_expect_tx(&full_bar[slot], kStageBytes);
                 tma_load_2d(st, &k_map, &full_bar[slot], x0, row);
                 tma_load_2d(st + kTileBytes, &v_map, &full_bar[slot], x0, row);
@@ -240,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, (R > 8) ? 1 : 3) decode_int4_kernel(
         if (s_abort) break;
         const int tok0 = lo + t * kTileTok + warp * 16;
         const int n_valid = min(max(hi - tok0, 0), 16);
-        if (n_valid > 0) {
+        if (n_valid > 0 && !s_skip[slot]) {
             const uint32_t* kt = reinterpret_cast<const uint32_t*>(smem + slot * kStageBytes) + woff;
             const uint32_t* vt = reinterpret_cast<const uint32_t*>(smem + slot * kStageBytes + kTileBytes) + woff;
             // ---- coefficient words -> fp32, once per (token, group); rows past the

@@ -14,7 +14,9 @@
 // host-side stand-in, not device memory), so the device address is looked up
 // with cudaGetSymbolAddress once per device, with that device current, on the
 // first call made on that device.  That first call should therefore come
-// before any stream capture.  Nothing in the array has to start at zero: the
+// before any stream capture.  The address is kept per device ordinal for the
+// life of the process; a cudaDeviceReset (or a non-primary context) would
+// leave it stale, and the entry point does not support either.  Nothing in the array has to start at zero: the
 // decode kernel writes every partial (O_s and LSE_s, including empty splits)
 // before the merge reads it.  Every call shares the one array and it keeps
 // the last call's contents, so calls whose work overlaps on the GPU (on

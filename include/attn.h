@@ -280,6 +280,10 @@ attn_status_t attn_prefill_paged_varlen_ws(const void* q, const void* k_cache, c
  *                may be NULL).  If o is NULL only the partials are produced
  *                (for callers that merge across devices themselves).
  * Split s of sequence b covers tokens [s*split_tokens, min((s+1)*split_tokens, len_b)).
+ * A block-table entry outside [0, num_pages) sets ATTN_DEV_PAGE_OUT_OF_RANGE;
+ * that page is not read and its tokens are left out of their split (as if
+ * masked), so the outputs stay defined: the decode of the sequence without
+ * that page.  This holds for every decode entry (mq, fp8, static as well).
  */
 attn_status_t attn_decode_paged_splitk(const void* q, const void* k_cache, const void* v_cache,
                                        const int32_t* block_table, int max_pages_per_seq,
@@ -361,7 +365,11 @@ attn_status_t attn_decode_paged_splitk_fp8(const void* q, const void* k_cache, c
  *     of attn_decode_paged_splitk.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.  ATTN_ERR_CUDA if the lookup fails.
+ *     before any stream capture.  ATTN_ERR_CUDA if the lookup fails.  The
+ *     address is kept per device ordinal for the life of the process, so the
+ *     entry point is not for use across a cudaDeviceReset (or with a context
+ *     other than the device's primary context current): the kept address
+ *     would then be stale.
  *   - All calls share the one array, which keeps the last call's contents
  *     (nothing in it needs to start at zero: every partial is written before
  *     it is read).  Calls whose work overlaps on the GPU (different streams or

@@ -68,10 +68,12 @@ def test_fp8_full_size_sampled():
     shape = replace(shape, split_tokens=split)
     inp = synth.decode_inputs(shape, seed=0)
     t = {k: v.to(dev) for k, v in inp.items() if torch.is_tensor(v)}
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
     o, lse, _ = attn.attn_decode_paged_splitk_fp8(t["q"], t["k_cache"], t["v_cache"], t["k_scale_shift"],
                                                   t["v_scale_shift"], t["block_table"], t["seq_lens"],
-                                                  shape.split_tokens, shape.len_hi)
+                                                  shape.split_tokens, shape.len_hi, dev_status=status)
     torch.cuda.synchronize()
+    assert status.item() == 0
     picks = [0, 7, 15]
     o_ref, lse_ref = oracle.decode(inp["q"].double().numpy(), inp["k_cache"].numpy(), inp["v_cache"].numpy(),
                                    inp["block_table"].numpy(), inp["lens"], shape.page_size, shape.split_tokens,
@@ -104,3 +106,32 @@ def test_fp8_split_partials_match_oracle():
                                                   v_scale_shift=inp["v_scale_shift"].numpy())
     check_o(o_part, op_ref, what="O_s")
     check_lse(lse_part, lp_ref, what="LSE_s")
+
+
+def test_fp8_bad_page_is_flagged_and_left_out():
+    """A block-table entry outside the pool sets ATTN_DEV_PAGE_OUT_OF_RANGE and
+    its page's tokens are left out: the result is the oracle's decode of the
+    sequence with that page removed from its page list."""
+    dev = gpu_or_skip()
+    import causal_gqa_flashattention_attn_gb300 as attn
+    lens = [600, 300]
+    shape = replace(synth.PAGED_DECODE_FP8, B=2)
+    inp = synth.decode_inputs(shape, seed=3, lens=lens)
+    t = {k: v.to(dev) for k, v in inp.items() if torch.is_tensor(v)}
+    bad = t["block_table"].clone()
+    bad[0, 1] = -7
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    o, lse, _ = attn.attn_decode_paged_splitk_fp8(t["q"], t["k_cache"], t["v_cache"], t["k_scale_shift"],
+                                                  t["v_scale_shift"], bad, t["seq_lens"], 2048, 600,
+                                                  dev_status=status)
+    torch.cuda.synchronize()
+    assert status.item() & attn.ATTN_DEV_PAGE_OUT_OF_RANGE
+    table = inp["block_table"].numpy().copy()
+    table[0, 1:-1] = table[0, 2:]
+    table[0, -1] = -1
+    o_ref, lse_ref = oracle.decode(inp["q"].double().numpy(), inp["k_cache"].numpy(), inp["v_cache"].numpy(), table,
+                                   [600 - 256, 300], 256, 2048, kv_format="fp8", max_kv_len=600,
+                                   k_scale_shift=inp["k_scale_shift"].numpy(),
+                                   v_scale_shift=inp["v_scale_shift"].numpy())
+    check_o(o, o_ref)
+    check_lse(lse, lse_ref)

@@ -74,3 +74,32 @@ def test_static_entry_rejects_sizes_beyond_its_maximum():
     st = L.attn_decode_paged_splitk_static(p, p, p, p, 512, p, attn.ATTN_BF16, 1, 64, 32, 8, 128, 1, 256, 2048,
                                            1 << 17, 0.1, p, None, None, None)
     assert st == -3, attn.attn_status_string(st)
+
+
+def test_static_entry_allocates_nothing_on_a_warm_call():
+    """With its outputs given, a call after the first on the device leaves
+    both torch's allocator and the device's free memory unchanged."""
+    dev = gpu_or_skip()
+    import causal_gqa_flashattention_attn_gb300 as attn
+    shape = replace(synth.PAGED_DECODE_BF16, B=4)
+    lens = [3000, 17, 2048, 900]
+    t = _inputs(dev, shape, 5, lens)
+    o = torch.empty(shape.B, shape.Hq, shape.D, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(shape.B, shape.Hq, dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def call():
+        attn.attn_decode_paged_splitk_static(t["q"], t["k_cache"], t["v_cache"], t["block_table"], t["seq_lens"],
+                                             shape.split_tokens, max(lens), o=o, lse=lse, dev_status=status)
+        torch.cuda.synchronize()
+
+    call()                      # first call: address lookup, kernels loaded
+    first_o, first_lse = o.clone(), lse.clone()
+    torch.cuda.synchronize()
+    alloc0 = torch.cuda.memory_allocated(dev)
+    free0 = torch.cuda.mem_get_info(dev)[0]
+    call()
+    assert torch.cuda.memory_allocated(dev) == alloc0
+    assert torch.cuda.mem_get_info(dev)[0] == free0
+    assert status.item() == 0
+    assert torch.equal(o, first_o) and torch.equal(lse, first_lse)
