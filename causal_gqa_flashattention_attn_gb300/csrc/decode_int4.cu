@@ -577,6 +577,7 @@ cudaError_t launch_g(const DecodeArgs& a, cudaStream_t stream, int* occ) {
 }  // namespace
 
 cudaError_t launch_decode_int4(const DecodeArgs& a, cudaStream_t stream, int* occ) {
+    if (decode_int4_g32_supported(a)) return launch_decode_int4_g32(a, stream, occ);
     switch (rows_per_cta(a)) {
         case 1: return launch_g<1>(a, stream, occ);
         case 2: return launch_g<2>(a, stream, occ);
