@@ -39,7 +39,7 @@ ATTN_DEV_WAIT_TIMEOUT = 0x4
 ATTN_DEV_WORKSPACE_STATE = 0x8
 
 EXPORTED = ("attn_prefill_fwd", "attn_prefill_workspace_bytes", "attn_prefill_plan", "attn_prefill_plan_sms", "attn_prefill_fwd_ws", "attn_prefill_host_workspace_bytes", "attn_prefill_fwd_host", "attn_prefill_paged_varlen", "attn_prefill_varlen_workspace_bytes",
-            "attn_prefill_paged_varlen_ws", "attn_decode_workspace_bytes", "attn_decode_split_tokens", "attn_decode_split_tokens_for", "attn_decode_paged_splitk", "attn_decode_paged_splitk_mq",
+            "attn_prefill_paged_varlen_ws", "attn_decode_workspace_bytes", "attn_decode_split_tokens", "attn_decode_split_tokens_for", "attn_decode_split_tokens_balanced_for", "attn_decode_paged_splitk", "attn_decode_paged_splitk_mq",
             "attn_decode_paged_splitk_fp8",
             "attn_decode_paged_splitk_static", "attn_lse_merge", "attn_lse_merge_bwd", "attn_selftest_wait_timeout",
             "attn_status_string", "attn_abi_version")
@@ -74,6 +74,8 @@ def lib():
     L.attn_prefill_plan_sms.restype = i32
     L.attn_decode_split_tokens_for.argtypes = [i32, i32, i32, i32, i32, i32, i32]
     L.attn_decode_split_tokens_for.restype = i32
+    L.attn_decode_split_tokens_balanced_for.argtypes = [i32, i32, i32, i32]
+    L.attn_decode_split_tokens_balanced_for.restype = i32
     L.attn_prefill_fwd_ws.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32, vp, sz, vp, vp]
     L.attn_prefill_fwd_ws.restype = i32
     L.attn_prefill_host_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32, i32]
@@ -196,6 +198,11 @@ def attn_prefill_plan_sms(dtype, B, Hq, Hkv, q_len, kv_len, D, sms):
     grid = ctypes.c_int(0)
     sched = lib().attn_prefill_plan_sms(_DT.get(dtype, -1), B, Hq, Hkv, q_len, kv_len, D, sms, ctypes.byref(grid))
     return int(sched), int(grid.value)
+
+
+def attn_decode_split_tokens_balanced_for(sms, B, head_groups, max_kv_len):
+    """The split of the persistent int4 decode for a described device (no driver call)."""
+    return int(lib().attn_decode_split_tokens_balanced_for(sms, B, head_groups, max_kv_len))
 
 
 def attn_decode_split_tokens_for(sms, ctas_per_sm, B, Hq, Hkv, max_kv_len, q_len=1):

@@ -8,7 +8,9 @@
 #include <cudaTypedefs.h>
 
 #include <cmath>
+#include <algorithm>
 #include <mutex>
+#include <vector>
 
 #include "common.cuh"
 
@@ -195,7 +197,7 @@ const char* attn_status_string(attn_status_t status) {
     }
 }
 
-int attn_abi_version(void) { return 106; }
+int attn_abi_version(void) { return 107; }
 
 attn_status_t attn_selftest_wait_timeout(int32_t* dev_status, unsigned int limit_us, void* stream) {
     if (dev_status == nullptr || limit_us == 0 || limit_us > 1000000u) return ATTN_ERR_INVALID_ARG;
@@ -343,6 +345,35 @@ int attn_decode_split_tokens_for(int sms, int ctas_per_sm, int B, int Hq, int Hk
     return best;
 }
 
+int attn_decode_split_tokens_balanced_for(int sms, int B, int head_groups, int max_kv_len) {
+    if (sms <= 0 || B <= 0 || head_groups <= 0 || max_kv_len <= 0) return 0;
+    constexpr long long kUnitCost = 64;   // a unit's fixed cost, in tokens
+    const int tiles = (max_kv_len + 63) / 64;
+    int best = 0;
+    long long best_cost = -1;
+    std::vector<long long> load;
+    for (int split = 64 * tiles; split >= 64; split -= 64) {
+        const int S = (max_kv_len + split - 1) / split;
+        const long long per_group = static_cast<long long>(B) * S;
+        const long long units = per_group * head_groups;
+        const int grid = units < sms ? static_cast<int>(units) : sms;
+        // every CTA c takes units c, c + grid, ...: all of `split` tokens but the
+        // last chunk of each sequence, which is max_kv_len - (S - 1) * split long
+        load.assign(grid, 0);
+        for (int c = 0; c < grid; ++c) load[c] = ((units - c + grid - 1) / grid) * (split + kUnitCost);
+        const long long short_by = split - (max_kv_len - static_cast<long long>(S - 1) * split);
+        if (short_by > 0)
+            for (long long hg = 0; hg < head_groups; ++hg)
+                for (long long b = 0; b < B; ++b) load[(hg * per_group + (S - 1) * static_cast<long long>(B) + b) % grid] -= short_by;
+        const long long cost = *std::max_element(load.begin(), load.end());
+        if (best_cost < 0 || cost < best_cost) {   // ties keep the larger split, found first
+            best_cost = cost;
+            best = split;
+        }
+    }
+    return best;
+}
+
 int attn_decode_split_tokens(attn_dtype_t kv_dtype, int n_groups, int B, int Hq, int Hkv, int q_len, int max_kv_len,
                              int D) {
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || q_len <= 0 || q_len > 16 || max_kv_len <= 0 || D != 128) return 0;
@@ -366,6 +397,8 @@ int attn_decode_split_tokens(attn_dtype_t kv_dtype, int n_groups, int B, int Hq,
     a.Hkv = Hkv;
     a.D = D;
     a.q_len = q_len;
+    if (fmt == 1 && decode_int4_g32_shape_ok(a))
+        return attn_decode_split_tokens_balanced_for(device_sm_count(), B, Hkv / 8, max_kv_len);
     int occ = 0;
     const cudaError_t e = (fmt == 2) ? launch_decode_fp8(a, nullptr, nullptr, nullptr, &occ)
                                      : launch_decode(a, nullptr, &occ);

@@ -60,6 +60,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream, int* occ = n
 cudaError_t launch_decode_int4(const DecodeArgs& a, cudaStream_t stream, int* occ = nullptr);
 // int4 rows of four 32-element groups and at most 8 (query, head) rows per KV
 // head: the fp16-subnormal code-space kernel of decode_int4_g32.cu.
+bool decode_int4_g32_shape_ok(const DecodeArgs& a);   // shape only (no page or split size)
 bool decode_int4_g32_supported(const DecodeArgs& a);
 cudaError_t launch_decode_int4_g32(const DecodeArgs& a, cudaStream_t stream, int* occ = nullptr);
 cudaError_t launch_decode_fp8(const DecodeArgs& a, const void* k_scale_shift, const void* v_scale_shift,

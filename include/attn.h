@@ -183,6 +183,9 @@ size_t attn_decode_workspace_bytes(int B, int Hq, int max_kv_len, int split_toke
  * sequence at max_kv_len, so it suits batches of similar lengths.
  *
  *   kv_dtype   ATTN_BF16, ATTN_INT4_PACKED (with n_groups) or ATTN_FP8_E4M3
+ * The int4 decode with N_GROUPS 4, Hkv a multiple of 8 and G * q_len <= 8
+ * runs one persistent CTA per SM over work units (sequence, chunk, group of 8
+ * KV heads); for it the choice is attn_decode_split_tokens_balanced_for.
  * Returns 0 for sizes the decode entries do not take, or without a device.
  */
 int attn_decode_split_tokens(attn_dtype_t kv_dtype, int n_groups, int B, int Hq, int Hkv, int q_len, int max_kv_len,
@@ -191,6 +194,13 @@ int attn_decode_split_tokens(attn_dtype_t kv_dtype, int n_groups, int B, int Hq,
  * (nothing is asked of the driver); 0 for sizes the decode entries do not take
  * or a non-positive device description. */
 int attn_decode_split_tokens_for(int sms, int ctas_per_sm, int B, int Hq, int Hkv, int q_len, int max_kv_len);
+/* The split for a persistent decode whose `sms` CTAs walk the work units
+ * (head group, chunk, sequence) round-robin, B sequences and head_groups groups
+ * of KV heads, every sequence counted at max_kv_len: the multiple of 64 that
+ * minimises the largest per-CTA sum of unit tokens, each unit counted 64
+ * tokens longer for its fixed cost; ties go to the larger split.  0 for
+ * non-positive sizes. */
+int attn_decode_split_tokens_balanced_for(int sms, int B, int head_groups, int max_kv_len);
 
 /*
  * attn_prefill_paged_varlen - causal GQA prefill of a ragged batch over a
@@ -443,7 +453,8 @@ const char* attn_status_string(attn_status_t status);
  * 102 attn_prefill_paged_varlen_ws, 103 attn_prefill_fwd_host,
  * 104 attn_prefill_fwd_ws, attn_prefill_workspace_bytes, attn_prefill_plan,
  * 105 attn_decode_split_tokens,
- * 106 attn_prefill_plan_sms, attn_decode_split_tokens_for. */
+ * 106 attn_prefill_plan_sms, attn_decode_split_tokens_for.
+ * 107 attn_decode_split_tokens_balanced_for; bad decode pages are left out. */
 int attn_abi_version(void);
 
 #ifdef __cplusplus
