@@ -16,6 +16,7 @@ Entry points (names as in the C ABI):
   attn_decode_paged_splitk_mq      causal multi-query decode (q_len <= 16 per sequence)
   attn_decode_paged_splitk_fp8     the same over an fp8 e4m3 row-wise cache
   attn_decode_paged_splitk_static  the same decode with no workspace argument
+  attn_decode_paged_fused   the decode with the LSE merge inside the same launch
   attn_lse_merge            LSE-weighted merge of split partials
   attn_lse_merge_bwd        its gradient
   attn_status_string
@@ -40,7 +41,7 @@ ATTN_DEV_WORKSPACE_STATE = 0x8
 
 EXPORTED = ("attn_prefill_fwd", "attn_prefill_workspace_bytes", "attn_prefill_plan", "attn_prefill_plan_sms", "attn_prefill_fwd_ws", "attn_prefill_host_workspace_bytes", "attn_prefill_fwd_host", "attn_prefill_paged_varlen", "attn_prefill_varlen_workspace_bytes",
             "attn_prefill_paged_varlen_ws", "attn_decode_workspace_bytes", "attn_decode_split_tokens", "attn_decode_split_tokens_for", "attn_decode_split_tokens_balanced_for", "attn_decode_paged_splitk", "attn_decode_paged_splitk_mq",
-            "attn_decode_paged_splitk_fp8",
+            "attn_decode_paged_splitk_fp8", "attn_decode_paged_fused", "attn_decode_fused_workspace_bytes",
             "attn_decode_paged_splitk_static", "attn_lse_merge", "attn_lse_merge_bwd", "attn_selftest_wait_timeout",
             "attn_status_string", "attn_abi_version")
 ATTN_DECODE_STATIC_SCRATCH_BYTES = 32 << 20
@@ -103,6 +104,11 @@ def lib():
     L.attn_decode_paged_splitk_fp8.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, i32,
                                                i32, i32, f32, vp, sz, vp, vp, vp, vp]
     L.attn_decode_paged_splitk_fp8.restype = i32
+    L.attn_decode_fused_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32, i32]
+    L.attn_decode_fused_workspace_bytes.restype = sz
+    L.attn_decode_paged_fused.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, i32, i32,
+                                          i32, i32, i32, f32, vp, sz, vp, vp, vp, vp]
+    L.attn_decode_paged_fused.restype = i32
     L.attn_decode_paged_splitk_static.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, i32,
                                                   i32, i32, i32, f32, vp, vp, vp, vp]
     L.attn_decode_paged_splitk_static.restype = i32
@@ -433,6 +439,51 @@ def attn_decode_paged_splitk_fp8(q, k_cache, v_cache, k_scale_shift, v_scale_shi
         float(scale), _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(o), _ptr(lse),
         _ptr(dev_status), _stream_ptr(stream))
     _check("attn_decode_paged_splitk_fp8", st)
+    return o, lse, workspace
+
+
+def attn_decode_fused_workspace_bytes(B, Hq, Hkv, max_kv_len, split_tokens, D=128, q_len=1):
+    return int(lib().attn_decode_fused_workspace_bytes(B, Hq, Hkv, q_len, max_kv_len, split_tokens, D))
+
+
+def attn_decode_paged_fused(q, k_cache, v_cache, block_table, seq_lens, split_tokens, max_kv_len, scale=None,
+                            n_groups=1, k_scale_shift=None, v_scale_shift=None, workspace=None, o=None, lse=None,
+                            dev_status=None, stream=None):
+    """The paged split-K decode with the merge inside the same launch.
+
+    ``q [B, Hq, D]`` (one query per sequence) or ``[B, Hq, q_len, D]`` bf16;
+    the cache is bf16, int4 words (int32, with ``n_groups``) or fp8 e4m3 bytes
+    (uint8, with ``k/v_scale_shift``).  ``workspace`` holds the partials and the
+    arrival counters, which must be zero when a call starts (a new workspace is
+    allocated zeroed here; every completed call leaves the counters zero).
+    Returns ``(o, lse, workspace)``."""
+    _need_cuda(q, k_cache, v_cache, k_scale_shift, v_scale_shift, block_table, seq_lens, workspace, o, lse,
+               dev_status)
+    single = q.dim() == 3
+    q4 = q[:, :, None, :] if single else q
+    bsz, hq, nq, d = q4.shape
+    num_pages, page_size, hkv = k_cache.shape[0], k_cache.shape[1], k_cache.shape[2]
+    if k_cache.dtype == torch.int32:
+        kv_dtype = ATTN_INT4_PACKED
+    elif k_cache.dtype == torch.uint8:
+        kv_dtype = ATTN_FP8_E4M3
+    else:
+        kv_dtype = _DT.get(k_cache.dtype, -1)
+    need = attn_decode_fused_workspace_bytes(bsz, hq, hkv, max_kv_len, split_tokens, d, q_len=nq)
+    if workspace is None:
+        workspace = torch.zeros(max(need, 16), dtype=torch.uint8, device=q.device)
+    if o is None:
+        o = torch.empty(q.shape, dtype=q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    st = lib().attn_decode_paged_fused(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale_shift), _ptr(v_scale_shift), _ptr(block_table),
+        block_table.shape[1], _ptr(seq_lens), kv_dtype, n_groups, bsz, hq, hkv, nq, d, num_pages, page_size,
+        split_tokens, max_kv_len, float(scale), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(o), _ptr(lse), _ptr(dev_status), _stream_ptr(stream))
+    _check("attn_decode_paged_fused", st)
     return o, lse, workspace
 
 

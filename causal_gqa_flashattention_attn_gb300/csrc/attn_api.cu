@@ -102,7 +102,7 @@ attn_status_t decode_impl(const void* q, const void* k_cache, const void* v_cach
                           int Hq, int Hkv, int q_len, int D, int num_pages, int page_size, int split_tokens,
                           int max_kv_len, float scale, void* workspace, size_t workspace_bytes, void* o, float* lse,
                           int32_t* dev_status, void* stream, const void* k_scale_shift = nullptr,
-                          const void* v_scale_shift = nullptr) {
+                          const void* v_scale_shift = nullptr, bool fused = false) {
     if (q == nullptr || k_cache == nullptr || v_cache == nullptr || block_table == nullptr || seq_lens == nullptr)
         return ATTN_ERR_INVALID_ARG;
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || num_pages <= 0 || page_size <= 0 || split_tokens <= 0 ||
@@ -133,8 +133,12 @@ attn_status_t decode_impl(const void* q, const void* k_cache, const void* v_cach
         return ATTN_ERR_UNSUPPORTED;
     }
     const int rows_q = Hq * q_len;   // output rows per sequence
-    const size_t need = attn_decode_workspace_bytes(B, rows_q, max_kv_len, split_tokens, D);
+    const size_t partial_bytes = attn_decode_workspace_bytes(B, rows_q, max_kv_len, split_tokens, D);
+    const size_t need = fused ? attn_decode_fused_workspace_bytes(B, Hq, Hkv, q_len, max_kv_len, split_tokens, D)
+                              : partial_bytes;
+    if (need == 0) return ATTN_ERR_INVALID_ARG;
     if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return ATTN_ERR_WORKSPACE;
+    if (fused && o == nullptr) return ATTN_ERR_INVALID_ARG;
     const int S = split_count(max_kv_len, split_tokens);
     const size_t rows = static_cast<size_t>(B) * rows_q;
     float* o_part = static_cast<float*>(workspace);
@@ -142,10 +146,15 @@ attn_status_t decode_impl(const void* q, const void* k_cache, const void* v_cach
     DecodeArgs a{q,         k_cache,   v_cache,      block_table, max_pages_per_seq, seq_lens, fmt, n_groups,
                  B,         Hq,        Hkv,          D,           num_pages,         page_size, split_tokens,
                  max_kv_len, S,        scale,        q_len,       o_part,            lse_part,  dev_status};
+    if (fused) {
+        a.counters = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + partial_bytes);
+        a.o_final = o;
+        a.lse_final = lse;
+    }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = (fmt == 2) ? launch_decode_fp8(a, k_scale_shift, v_scale_shift, s) : launch_decode(a, s);
     if (e != cudaSuccess) return ATTN_ERR_CUDA;
-    if (o != nullptr) e = launch_merge(o_part, lse_part, static_cast<int>(rows), S, D, o, lse, ATTN_BF16, s);
+    if (o != nullptr && !fused) e = launch_merge(o_part, lse_part, static_cast<int>(rows), S, D, o, lse, ATTN_BF16, s);
     return from_cuda(e);
 }
 
@@ -197,7 +206,7 @@ const char* attn_status_string(attn_status_t status) {
     }
 }
 
-int attn_abi_version(void) { return 107; }
+int attn_abi_version(void) { return 108; }
 
 attn_status_t attn_selftest_wait_timeout(int32_t* dev_status, unsigned int limit_us, void* stream) {
     if (dev_status == nullptr || limit_us == 0 || limit_us > 1000000u) return ATTN_ERR_INVALID_ARG;
@@ -446,6 +455,26 @@ attn_status_t attn_decode_paged_splitk_fp8(const void* q, const void* k_cache, c
     return decode_impl(q, k_cache, v_cache, block_table, max_pages_per_seq, seq_lens, ATTN_FP8_E4M3, 1, B, Hq, Hkv,
                        q_len, D, num_pages, page_size, split_tokens, max_kv_len, scale, workspace, workspace_bytes,
                        o, lse, dev_status, stream, k_scale_shift, v_scale_shift);
+}
+
+size_t attn_decode_fused_workspace_bytes(int B, int Hq, int Hkv, int q_len, int max_kv_len, int split_tokens,
+                                         int D) {
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || q_len <= 0 || Hq % Hkv != 0) return 0;
+    const size_t partials = attn_decode_workspace_bytes(B, Hq * q_len, max_kv_len, split_tokens, D);
+    if (partials == 0) return 0;
+    return partials + round16(static_cast<size_t>(B) * Hkv * sizeof(int32_t));
+}
+
+attn_status_t attn_decode_paged_fused(const void* q, const void* k_cache, const void* v_cache,
+                                      const int32_t* k_scale_shift, const int32_t* v_scale_shift,
+                                      const int32_t* block_table, int max_pages_per_seq, const int32_t* seq_lens,
+                                      attn_dtype_t kv_dtype, int n_groups, int B, int Hq, int Hkv, int q_len, int D,
+                                      int num_pages, int page_size, int split_tokens, int max_kv_len, float scale,
+                                      void* workspace, size_t workspace_bytes, void* o, float* lse,
+                                      int32_t* dev_status, void* stream) {
+    return decode_impl(q, k_cache, v_cache, block_table, max_pages_per_seq, seq_lens, kv_dtype, n_groups, B, Hq, Hkv,
+                       q_len, D, num_pages, page_size, split_tokens, max_kv_len, scale, workspace, workspace_bytes, o,
+                       lse, dev_status, stream, k_scale_shift, v_scale_shift, true);
 }
 
 attn_status_t attn_prefill_paged_varlen(const void* q, const void* k_cache, const void* v_cache,

@@ -53,6 +53,11 @@ struct DecodeArgs {
     float* o_part;
     float* lse_part;
     int32_t* dev_status;
+    // fused mode (counters not NULL): the last split of each (sequence, KV head)
+    // merges its partials into o_final / lse_final inside the launch
+    int32_t* counters;   // [B * Hkv], zero when the launch starts
+    void* o_final;       // bf16 [B, Hq, q_len, D]
+    float* lse_final;    // [B, Hq, q_len] or NULL
 };
 // With `occ` set, a decode launcher launches nothing: it writes how many CTAs
 // of the kernel it would launch fit on one SM at once.

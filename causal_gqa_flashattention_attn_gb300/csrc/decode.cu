@@ -24,6 +24,7 @@
 
 #include "common.cuh"
 #include "ptx.cuh"
+#include "split_merge.cuh"
 
 namespace gb300 {
 namespace {
@@ -46,6 +47,8 @@ struct Params {
     float* o_part;    // [B, Hq, S, D]
     float* lse_part;  // [B, Hq, S]
     int32_t* status;
+    FusedOut fused;       // fused merge (counters NULL: partials only)
+    int n_arrivals;       // CTAs per (sequence, KV head): splits x row groups
 };
 
 // Byte offset of 16-byte chunk `c` (0..15 across D) of token row `r` inside a
@@ -91,6 +94,9 @@ __global__ void __launch_bounds__(kThreads) decode_bf16_kernel(const __grid_cons
         for (int i = threadIdx.x; i < n_rows * kD; i += kThreads)
             p.o_part[(out_row(i / kD) * p.n_split + split) * kD + (i % kD)] = 0.f;
         if (threadIdx.x < n_rows) p.lse_part[out_row(threadIdx.x) * p.n_split + split] = -INFINITY;
+        if (p.fused.counters != nullptr)
+            fused_tail_cta(p.fused, p.n_arrivals, p.status, p.o_part, p.lse_part, p.n_split, b, kvh, p.Hq, p.Hkv, p.G,
+                           p.nq, 2, kThreads);
         return;
     }
     const int n_tiles = (hi - lo + kTileTok - 1) / kTileTok;
@@ -310,6 +316,9 @@ __global__ void __launch_bounds__(kThreads) decode_bf16_kernel(const __grid_cons
         p.o_part[orow * kD + d] = alive ? acc / l : 0.f;
         if (d == 0) p.lse_part[orow] = alive ? (mx * kLn2 + logf(l)) : -INFINITY;
     }
+    if (p.fused.counters != nullptr)
+        fused_tail_cta(p.fused, p.n_arrivals, p.status, p.o_part, p.lse_part, p.n_split, b, kvh, p.Hq, p.Hkv, p.G,
+                       p.nq, 1, 32 * kConsumers);
 }
 
 template <int R>
@@ -349,6 +358,10 @@ cudaError_t launch_bf16(const DecodeArgs& a, cudaStream_t stream, int* occ) {
     p.o_part = a.o_part;
     p.lse_part = a.lse_part;
     p.status = a.dev_status;
+    p.fused.counters = a.counters;
+    p.fused.o = static_cast<__nv_bfloat16*>(a.o_final);
+    p.fused.lse = a.lse_final;
+    p.n_arrivals = a.n_split * p.n_rg;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     // two CTAs per SM: ask for the largest shared-memory carveout

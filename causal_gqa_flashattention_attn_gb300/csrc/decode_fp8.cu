@@ -19,6 +19,7 @@
 
 #include "common.cuh"
 #include "ptx.cuh"
+#include "split_merge.cuh"
 
 namespace gb300 {
 namespace {
@@ -42,6 +43,8 @@ struct Params {
     float* o_part;
     float* lse_part;
     int32_t* status;
+    FusedOut fused;       // fused merge (counters NULL: partials only)
+    int n_arrivals;       // CTAs per (sequence, KV head): splits x row groups
 };
 
 __device__ __forceinline__ float lo_half(uint32_t w) {
@@ -114,6 +117,9 @@ __global__ void __launch_bounds__(kThreads, (R > 8) ? 1 : 3) decode_fp8_kernel(
         for (int i = threadIdx.x; i < n_rows * kD; i += kThreads)
             p.o_part[(out_row(i / kD) * p.n_split + split) * kD + (i % kD)] = 0.f;
         if (threadIdx.x < n_rows) p.lse_part[out_row(threadIdx.x) * p.n_split + split] = -INFINITY;
+        if (p.fused.counters != nullptr)
+            fused_tail_cta(p.fused, p.n_arrivals, p.status, p.o_part, p.lse_part, p.n_split, b, kvh, p.Hq, p.Hkv, p.G,
+                           p.nq, 2, kThreads);
         return;
     }
     const int n_tiles = (hi - lo + kTileTok - 1) / kTileTok;
@@ -386,6 +392,9 @@ __global__ void __launch_bounds__(kThreads, (R > 8) ? 1 : 3) decode_fp8_kernel(
         p.o_part[orow * kD + d] = alive ? acc / l : 0.f;
         if (d == 0) p.lse_part[orow] = alive ? (mx * kLn2 + logf(l)) : -INFINITY;
     }
+    if (p.fused.counters != nullptr)
+        fused_tail_cta(p.fused, p.n_arrivals, p.status, p.o_part, p.lse_part, p.n_split, b, kvh, p.Hq, p.Hkv, p.G,
+                       p.nq, 1, 32 * kConsumers);
 }
 
 template <int R>
@@ -438,6 +447,10 @@ cudaError_t launch_r(const DecodeArgs& a, const void* k_ss, const void* v_ss, cu
     p.o_part = a.o_part;
     p.lse_part = a.lse_part;
     p.status = a.dev_status;
+    p.fused.counters = a.counters;
+    p.fused.o = static_cast<__nv_bfloat16*>(a.o_final);
+    p.fused.lse = a.lse_final;
+    p.n_arrivals = a.n_split * p.n_rg;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);

@@ -27,6 +27,7 @@
 
 #include "common.cuh"
 #include "ptx.cuh"
+#include "split_merge.cuh"
 
 namespace gb300 {
 namespace {
@@ -47,6 +48,8 @@ struct Params {
     float* o_part;
     float* lse_part;
     int32_t* status;
+    FusedOut fused;       // fused merge (counters NULL: partials only)
+    int n_arrivals;       // CTAs per (sequence, KV head): splits x row groups
 };
 
 __device__ __forceinline__ float lo_half(uint32_t w) { return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xFFFFu))); }
@@ -121,6 +124,9 @@ __global__ void __launch_bounds__(kThreads, (R > 8) ? 1 : 3) decode_int4_kernel(
         for (int i = threadIdx.x; i < n_rows * kD; i += kThreads)
             p.o_part[(out_row(i / kD) * p.n_split + split) * kD + (i % kD)] = 0.f;
         if (threadIdx.x < n_rows) p.lse_part[out_row(threadIdx.x) * p.n_split + split] = -INFINITY;
+        if (p.fused.counters != nullptr)
+            fused_tail_cta(p.fused, p.n_arrivals, p.status, p.o_part, p.lse_part, p.n_split, b, kvh, p.Hq, p.Hkv, p.G,
+                           p.nq, 2, kThreads);
         return;
     }
     const int n_tiles = (hi - lo + kTileTok - 1) / kTileTok;
@@ -507,6 +513,9 @@ __global__ void __launch_bounds__(kThreads, (R > 8) ? 1 : 3) decode_int4_kernel(
         p.o_part[orow * kD + d] = alive ? acc / l : 0.f;
         if (d == 0) p.lse_part[orow] = alive ? (mx * kLn2 + logf(l)) : -INFINITY;
     }
+    if (p.fused.counters != nullptr)
+        fused_tail_cta(p.fused, p.n_arrivals, p.status, p.o_part, p.lse_part, p.n_split, b, kvh, p.Hq, p.Hkv, p.G,
+                       p.nq, 1, 32 * kConsumers);
 }
 
 template <int R, int NG>
@@ -552,6 +561,10 @@ cudaError_t launch_g_ng(const DecodeArgs& a, cudaStream_t stream, int* occ) {
     p.o_part = a.o_part;
     p.lse_part = a.lse_part;
     p.status = a.dev_status;
+    p.fused.counters = a.counters;
+    p.fused.o = static_cast<__nv_bfloat16*>(a.o_final);
+    p.fused.lse = a.lse_final;
+    p.n_arrivals = a.n_split * p.n_rg;
     // the merge scratch (4 warps x R rows x D floats) reuses the stage ring
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;

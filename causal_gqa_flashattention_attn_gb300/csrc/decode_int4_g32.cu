@@ -44,6 +44,7 @@
 
 #include "common.cuh"
 #include "ptx.cuh"
+#include "split_merge.cuh"
 
 namespace gb300 {
 namespace {
@@ -77,6 +78,7 @@ struct Params {
     float* o_part;
     float* lse_part;
     int32_t* status;
+    FusedOut fused;          // fused merge (counters NULL: partials only)
 };
 
 // m16n8k16 fp16 MMA, fp32 accumulators (registers only, so the compiler may
@@ -451,10 +453,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_int4_g32_kernel(const __gr
             const int i = r / p.G, h = r % p.G;
             return (static_cast<size_t>(w.b) * p.Hq + kvh * p.G + h) * p.nq + i;
         };
+        // fused mode: this warp's rows of (sequence, KV head) are written; the
+        // split that arrives last merges them
+        auto fused_tail = [&]() {
+            if (p.fused.counters == nullptr) return;
+            int32_t* cnt = p.fused.counters + static_cast<size_t>(w.b) * p.Hkv + kvh;
+            if (split_arrive_warp(cnt, p.n_split, p.status, lane)) {
+                merge_head(p.o_part, p.lse_part, p.n_split, out_row(0), n_rows, p.fused, 0, 1, lane);
+                if (lane == 0) atomicExch(cnt, 0);
+            }
+        };
         if (w.n_tiles == 0) {   // empty split: O = 0, LSE = -inf
             for (int i = lane; i < n_rows * kD; i += 32)
                 p.o_part[(out_row(i / kD) * p.n_split + w.split) * kD + (i % kD)] = 0.f;
             if (lane < n_rows) p.lse_part[out_row(lane) * p.n_split + w.split] = -INFINITY;
+            fused_tail();
             continue;
         }
         // ---- the unit's queries.  B operand of the score MMA: column g is CTA row g
@@ -578,6 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_int4_g32_kernel(const __gr
                 p.lse_part[out_row(col) * p.n_split + w.split] = alive ? st.m_run[j] * kLn2 + logf(l_tot[j])
                                                                          : -INFINITY;
         }
+        fused_tail();
     }
 }
 
@@ -633,6 +647,9 @@ cudaError_t launch_decode_int4_g32(const DecodeArgs& a, cudaStream_t stream, int
     p.o_part = a.o_part;
     p.lse_part = a.lse_part;
     p.status = a.dev_status;
+    p.fused.counters = a.counters;
+    p.fused.o = static_cast<__nv_bfloat16*>(a.o_final);
+    p.fused.lse = a.lse_final;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     const int sms = device_sm_count();

@@ -355,6 +355,46 @@ attn_status_t attn_decode_paged_splitk_fp8(const void* q, const void* k_cache, c
                                            void* o, float* lse, int32_t* dev_status, void* stream);
 
 /*
+ * attn_decode_paged_fused - the paged split-K decode with the LSE merge
+ * inside the same launch.
+ *
+ * Computes what attn_decode_paged_splitk (q_len == 1), attn_decode_paged_splitk_mq
+ * (q_len > 1) or attn_decode_paged_splitk_fp8 computes, and then merges: the
+ * split of each (sequence, KV head) that finishes last reads that head's
+ * partials and writes its O and LSE ("splitk_kernels.py", _splitK_reduce:
+ * M = max_s LSE_s, w_s = exp(LSE_s - M), O = sum_s w_s O_s / sum_s w_s,
+ * LSE = M + log sum_s w_s; O = 0 and LSE = -inf when every LSE_s is -inf).
+ * No CTA waits for another: arrival is counted, and the last arrival merges.
+ *
+ *   kv_dtype       ATTN_BF16, ATTN_INT4_PACKED (with n_groups) or
+ *                  ATTN_FP8_E4M3 (with k_scale_shift / v_scale_shift, as for
+ *                  attn_decode_paged_splitk_fp8; NULL otherwise)
+ *   q              [B, Hq, q_len, D] bfloat16 (query i of a sequence sees
+ *                  tokens t <= len - q_len + i)                       (read)
+ *   workspace      >= attn_decode_fused_workspace_bytes(...) bytes: the split
+ *                  partials (layout as for attn_decode_paged_splitk with
+ *                  Hq * q_len rows per sequence), then one int32 arrival
+ *                  counter per (sequence, KV head).  The counters must be 0
+ *                  when a call starts: zero the workspace once; every call
+ *                  that completes without a device error leaves them 0
+ *                  again (so a replayed CUDA graph needs no re-zeroing).  A
+ *                  counter found past its range sets ATTN_DEV_WORKSPACE_STATE.
+ *                  Calls that share a workspace must not overlap on the GPU.
+ *   o              [B, Hq, q_len, D] bfloat16 (written, required); lse
+ *                  [B, Hq, q_len] fp32 (written, may be NULL)
+ * Other arguments, limits and errors as the entries named above.
+ */
+size_t attn_decode_fused_workspace_bytes(int B, int Hq, int Hkv, int q_len, int max_kv_len, int split_tokens,
+                                         int D);
+attn_status_t attn_decode_paged_fused(const void* q, const void* k_cache, const void* v_cache,
+                                      const int32_t* k_scale_shift, const int32_t* v_scale_shift,
+                                      const int32_t* block_table, int max_pages_per_seq, const int32_t* seq_lens,
+                                      attn_dtype_t kv_dtype, int n_groups, int B, int Hq, int Hkv, int q_len, int D,
+                                      int num_pages, int page_size, int split_tokens, int max_kv_len, float scale,
+                                      void* workspace, size_t workspace_bytes, void* o, float* lse,
+                                      int32_t* dev_status, void* stream);
+
+/*
  * attn_decode_paged_splitk_static - attn_decode_paged_splitk without a workspace.
  *
  * The pages have no counterpart of this entry point.  It serves callers that
@@ -454,7 +494,8 @@ const char* attn_status_string(attn_status_t status);
  * 104 attn_prefill_fwd_ws, attn_prefill_workspace_bytes, attn_prefill_plan,
  * 105 attn_decode_split_tokens,
  * 106 attn_prefill_plan_sms, attn_decode_split_tokens_for.
- * 107 attn_decode_split_tokens_balanced_for; bad decode pages are left out. */
+ * 107 attn_decode_split_tokens_balanced_for; bad decode pages are left out.
+ * 108 attn_decode_paged_fused, attn_decode_fused_workspace_bytes. */
 int attn_abi_version(void);
 
 #ifdef __cplusplus

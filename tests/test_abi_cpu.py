@@ -39,7 +39,7 @@ def test_library_exports_every_declared_symbol(L):
     for name in declared_functions():
         assert hasattr(L, name), name
         assert name in attn.EXPORTED
-    assert L.attn_abi_version() == 107
+    assert L.attn_abi_version() == 108
 
 
 def test_status_strings(L):
@@ -251,6 +251,37 @@ def test_decode_fp8_host_validation(L):
     assert _decode_fp8(L, Hq=8, Hkv=2) == -2                   # coefficient box needs Hkv % 4 == 0
     assert _decode_fp8(L, page_size=32) == -2
     assert _decode_fp8(L, ws=None) == -3
+
+
+def _decode_fused(L, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, ks=None, vs=None, table=FAKE, max_pages=4, lens=FAKE, kv_dtype=1, ng=1, B=2,
+             Hq=32, Hkv=8, nq=1, D=128, num_pages=8, page_size=256, split=512, max_len=1024, scale=0.1, ws=FAKE,
+             ws_bytes=1 << 30, o=FAKE, lse=None, status=None, stream=None)
+    a.update(kw)
+    return L.attn_decode_paged_fused(a["q"], a["k"], a["v"], a["ks"], a["vs"], a["table"], a["max_pages"], a["lens"],
+                                     a["kv_dtype"], a["ng"], a["B"], a["Hq"], a["Hkv"], a["nq"], a["D"],
+                                     a["num_pages"], a["page_size"], a["split"], a["max_len"], a["scale"], a["ws"],
+                                     a["ws_bytes"], a["o"], a["lse"], a["status"], a["stream"])
+
+
+def test_decode_fused_host_validation(L):
+    """The fused entry: O is required (the partials stay in the workspace), the
+    workspace must hold the partials and the counters, and the format checks
+    are those of the separate entries."""
+    import causal_gqa_flashattention_attn_gb300 as attn
+    assert _decode_fused(L, o=None) == -1
+    assert _decode_fused(L, table=None) == -1
+    assert _decode_fused(L, kv_dtype=4) == -1                    # fp8 without scale/shift words
+    assert _decode_fused(L, kv_dtype=3, ng=3) == -2
+    assert _decode_fused(L, nq=17) == -2
+    assert _decode_fused(L, ws=None) == -3
+    partial = attn.attn_decode_workspace_bytes(2, 32, 1024, 512, 128)
+    fused = attn.attn_decode_fused_workspace_bytes(2, 32, 8, 1024, 512, 128)
+    assert fused == partial + 64                                  # 2 x 8 int32 counters
+    assert attn.attn_decode_fused_workspace_bytes(2, 32, 8, 1024, 512, 128, q_len=4) == \
+        attn.attn_decode_workspace_bytes(2, 128, 1024, 512, 128) + 64
+    assert _decode_fused(L, ws_bytes=partial) == -3               # room for the partials only
+    assert attn.attn_decode_fused_workspace_bytes(2, 12, 8, 1024, 512, 128) == 0
 
 
 def test_workspace_bytes(L):

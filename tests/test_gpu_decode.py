@@ -141,8 +141,8 @@ def test_block_table_indexing_is_exact():
     assert np.array_equal(np.isneginf(lse_part.cpu().numpy()), ~live)
 
 
-@pytest.mark.parametrize("fmt", ["dense", "int4"])
-def test_device_status_flags_bad_page_and_length(fmt):
+@pytest.mark.parametrize("fmt,len0", [("dense", 600), ("int4", 600), ("int4", 1024)])
+def test_device_status_flags_bad_page_and_length(fmt, len0):
     """A block-table entry outside the pool is reported in the device status
     word and its page's tokens are left out of the split, so the result is the
     decode of the sequence without that page (finite, checked against the
@@ -150,7 +150,7 @@ def test_device_status_flags_bad_page_and_length(fmt):
     reported too."""
     dev = gpu_or_skip()
     import causal_gqa_flashattention_attn_gb300 as attn
-    lens = [600, 300]
+    lens = [len0, 300]    # 1024: the int4 kernel's split is whole stages (its pipelined loop)
     base = synth.PAGED_DECODE_BF16 if fmt == "dense" else synth.PAGED_DECODE_INT4
     shape = replace(base, B=2)
     inp = synth.decode_inputs(shape, seed=2, lens=lens)
@@ -158,7 +158,7 @@ def test_device_status_flags_bad_page_and_length(fmt):
     bad = t["block_table"].clone()
     bad[0, 1] = inp["n_pages"] + 5
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    o, lse, _ = attn.attn_decode_paged_splitk(t["q"], t["k_cache"], t["v_cache"], bad, t["seq_lens"], 2048, 600,
+    o, lse, _ = attn.attn_decode_paged_splitk(t["q"], t["k_cache"], t["v_cache"], bad, t["seq_lens"], 2048, len0,
                                               n_groups=shape.n_groups, dev_status=status)
     torch.cuda.synchronize()
     assert status.item() & attn.ATTN_DEV_PAGE_OUT_OF_RANGE
@@ -168,13 +168,13 @@ def test_device_status_flags_bad_page_and_length(fmt):
     table[0, 1:-1] = table[0, 2:]
     table[0, -1] = -1
     kc, vc = _oracle_inputs(shape, inp)
-    o_ref, lse_ref = oracle.decode(inp["q"].double().numpy(), kc, vc, table, [600 - 256, 300], 256, 2048,
-                                   kv_format=fmt, n_groups=shape.n_groups, max_kv_len=600)
+    o_ref, lse_ref = oracle.decode(inp["q"].double().numpy(), kc, vc, table, [len0 - 256, 300], 256, 2048,
+                                   kv_format=fmt, n_groups=shape.n_groups, max_kv_len=len0)
     check_o(o, o_ref)
     check_lse(lse, lse_ref)
     status.zero_()
-    attn.attn_decode_paged_splitk(t["q"], t["k_cache"], t["v_cache"], t["block_table"], t["seq_lens"], 2048, 400,
-                                  n_groups=shape.n_groups, dev_status=status)
+    attn.attn_decode_paged_splitk(t["q"], t["k_cache"], t["v_cache"], t["block_table"], t["seq_lens"], 2048,
+                                  len0 - 200, n_groups=shape.n_groups, dev_status=status)
     torch.cuda.synchronize()
     assert status.item() & attn.ATTN_DEV_SEQ_TOO_LONG
 
