@@ -319,6 +319,17 @@ def run_ours(args, rank, world, dist):
     d4s = synth.PAGED_DECODE_INT4
     ws4s = torch.empty(attn.attn_decode_workspace_bytes(d4s.B, d4s.Hq, d4s.len_hi, d4s.split_tokens, d4s.D),
                        dtype=torch.uint8, device=dev)
+    # the same two decodes through attn_decode_paged_fused (the merge inside the
+    # launch): workspaces with the arrival counters, zeroed once
+    fused = {}
+    for name in ("decode_bf16", "decode_int4"):
+        d = dec[name]
+        sh = d["shape"]
+        fused[name] = dict(ws=torch.zeros(attn.attn_decode_fused_workspace_bytes(sh.B, sh.Hq, sh.Hkv, d["max_len"],
+                                                                                 sh.split_tokens, sh.D),
+                                          dtype=torch.uint8, device=dev),
+                           o=torch.empty(sh.B, sh.Hq, sh.D, dtype=torch.bfloat16, device=dev),
+                           lse=torch.empty(sh.B, sh.Hq, dtype=torch.float32, device=dev))
     flush = L2Flush(torch, dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     # split-schedule scratch of the two prefills (zeroed once; each call leaves it zeroed)
@@ -328,7 +339,8 @@ def run_ours(args, rank, world, dist):
                                                          pb.D), dtype=torch.uint8, device=dev)
 
     kernels = ["prefill", "prefill_batched", "decode_bf16", "merge_bf16", "decode_int4", "merge_int4",
-               "decode_int4_split2048", "merge_bwd", "decode_mq", "decode_fp8", "prefill_varlen", "prefill_varlen_ws"]
+               "decode_int4_split2048", "decode_bf16_fused", "decode_int4_fused", "merge_bwd", "decode_mq",
+               "decode_fp8", "prefill_varlen", "prefill_varlen_ws"]
     # the method's own steps (dense prefill, paged split-K decode, merge); the
     # other legs are the widened rows (merge backward, multi-query, fp8, ragged)
     hot = ["prefill", "prefill_batched", "decode_bf16", "merge_bf16", "decode_int4", "merge_int4"]
@@ -386,6 +398,15 @@ def run_ours(args, rank, world, dist):
             ev[mname][0].record(stream)
             attn.attn_lse_merge(d["o_part"], d["lse_part"], o=d["o"], lse=d["lse"], stream=stream)
             ev[mname][1].record(stream)
+        for name in ("decode_bf16", "decode_int4"):
+            d, f = dec[name], fused[name]
+            sh, t = d["shape"], d["t"]
+            flush()
+            ev[name + "_fused"][0].record(stream)
+            attn.attn_decode_paged_fused(t["q"], t["k_cache"], t["v_cache"], t["block_table"], t["seq_lens"],
+                                         sh.split_tokens, d["max_len"], n_groups=sh.n_groups, workspace=f["ws"],
+                                         o=f["o"], lse=f["lse"], dev_status=status, stream=stream)
+            ev[name + "_fused"][1].record(stream)
         t4 = dec["decode_int4"]["t"]
         flush()
         ev["decode_int4_split2048"][0].record(stream)
@@ -529,8 +550,8 @@ def run_ours(args, rank, world, dist):
         d = dec[name]
         kb = d["bytes"]["kernel"]
         rep[name] = dict(bound="hbm", achieved=kb / (ms[name] * 1e-3) / 1e9, peak=peaks["hbm_gbs"], unit="GB/s",
-                         work=kb, src="decode.cu" if name == "decode_bf16" else "decode_int4.cu",
-                         kernel="decode_bf16_kernel" if name == "decode_bf16" else "decode_int4_kernel")
+                         work=kb, src="decode.cu" if name == "decode_bf16" else "decode_int4_g32.cu",
+                         kernel="decode_bf16_kernel" if name == "decode_bf16" else "decode_int4_g32_kernel")
         mname = name.replace("decode", "merge")
         n_rows = d["shape"].B * d["shape"].Hq
         s_max = d["o_part"].shape[1]
@@ -539,8 +560,15 @@ def run_ours(args, rank, world, dist):
                           work=mb, src="merge.cu", kernel="lse_merge_kernel")
     kb4 = dec["decode_int4"]["bytes"]["kernel"]
     rep["decode_int4_split2048"] = dict(bound="hbm", achieved=kb4 / (ms["decode_int4_split2048"] * 1e-3) / 1e9,
-                                        peak=peaks["hbm_gbs"], unit="GB/s", work=kb4, src="decode_int4.cu",
-                                        kernel="decode_int4_kernel (split 2048)")
+                                        peak=peaks["hbm_gbs"], unit="GB/s", work=kb4, src="decode_int4_g32.cu",
+                                        kernel="decode_int4_g32_kernel (split 2048)")
+    for name in ("decode_bf16", "decode_int4"):
+        pb_ = dec[name]["bytes"]["path"]
+        rep[name + "_fused"] = dict(bound="hbm", achieved=pb_ / (ms[name + "_fused"] * 1e-3) / 1e9,
+                                    peak=peaks["hbm_gbs"], unit="GB/s", work=pb_,
+                                    src="decode.cu" if name == "decode_bf16" else "decode_int4_g32.cu",
+                                    kernel=("decode_bf16_kernel" if name == "decode_bf16" else "decode_int4_g32_kernel")
+                                    + " (merge inside the launch)")
     n_rows, s_max, dd = mbw["o_part"].shape
     # algorithmic bytes: partials read once, gradients in, gradient partials out
     mbb = n_rows * s_max * (dd + 1) * 4 * 2 + n_rows * (dd + 1) * 4
@@ -567,7 +595,8 @@ def run_ours(args, rank, world, dist):
                             "traffic": traffic.get(kn),
                             "row": "hot path" if kn in hot else
                             ("hot path, split 2048 (not in ms_per_step)" if kn == "decode_int4_split2048"
-                             else "widened")})
+                             else "hot path, decode and merge in one launch (not in ms_per_step)"
+                             if kn.endswith("_fused") else "widened")})
     dominant = max(hot, key=lambda kn: ms[kn])
     dom = rep[dominant]
     path = {}

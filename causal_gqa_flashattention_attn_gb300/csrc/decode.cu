@@ -59,7 +59,7 @@ __device__ __forceinline__ uint32_t tile_off(int r, int c) {
 
 // Row r of a CTA is the (query i, head h) pair rg * rpg + r = i * G + h.
 
-template <int R, int NS>
+template <int R, int NS, bool kFused>
 __global__ void __launch_bounds__(kThreads) decode_bf16_kernel(const __grid_constant__ CUtensorMap k_map,
                                                                const __grid_constant__ CUtensorMap v_map,
                                                                const Params p) {
@@ -94,7 +94,7 @@ __global__ void __launch_bounds__(kThreads) decode_bf16_kernel(const __grid_cons
         for (int i = threadIdx.x; i < n_rows * kD; i += kThreads)
             p.o_part[(out_row(i / kD) * p.n_split + split) * kD + (i % kD)] = 0.f;
         if (threadIdx.x < n_rows) p.lse_part[out_row(threadIdx.x) * p.n_split + split] = -INFINITY;
-        if (p.fused.counters != nullptr)
+        if constexpr (kFused)
             fused_tail_cta(p.fused, p.n_arrivals, p.status, p.o_part, p.lse_part, p.n_split, b, kvh, p.Hq, p.Hkv, p.G,
                            p.nq, 2, kThreads);
         return;
@@ -316,7 +316,7 @@ __global__ void __launch_bounds__(kThreads) decode_bf16_kernel(const __grid_cons
         p.o_part[orow * kD + d] = alive ? acc / l : 0.f;
         if (d == 0) p.lse_part[orow] = alive ? (mx * kLn2 + logf(l)) : -INFINITY;
     }
-    if (p.fused.counters != nullptr)
+    if constexpr (kFused)
         fused_tail_cta(p.fused, p.n_arrivals, p.status, p.o_part, p.lse_part, p.n_split, b, kvh, p.Hq, p.Hkv, p.G,
                        p.nq, 1, 32 * kConsumers);
 }
@@ -325,7 +325,7 @@ template <int R>
 cudaError_t launch_bf16(const DecodeArgs& a, cudaStream_t stream, int* occ) {
     constexpr int NS = 3;
     const size_t smem = NS * kStageBytes + 1024;
-    auto kern = decode_bf16_kernel<R, NS>;
+    auto kern = a.counters != nullptr ? decode_bf16_kernel<R, NS, true> : decode_bf16_kernel<R, NS, false>;
     if (occ != nullptr) return ctas_per_sm(kern, kThreads, smem, occ);
     CUtensorMap k_map, v_map;
     const uint64_t rows = static_cast<uint64_t>(a.num_pages) * a.page_size;

@@ -83,7 +83,7 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 // 16-byte chunk c (0..7) of token row r in a 128-byte-swizzled code tile
 __device__ __forceinline__ uint32_t code_off(int r, int c) { return r * 128 + (((c ^ (r & 7)) & 7) << 4); }
 
-template <int R>
+template <int R, bool kFused>
 __global__ void __launch_bounds__(kThreads, (R > 8) ? 1 : 3) decode_fp8_kernel(
     const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
     const __grid_constant__ CUtensorMap kw_map, const __grid_constant__ CUtensorMap vw_map, const Params p) {
@@ -117,7 +117,7 @@ __global__ void __launch_bounds__(kThreads, (R > 8) ? 1 : 3) decode_fp8_kernel(
         for (int i = threadIdx.x; i < n_rows * kD; i += kThreads)
             p.o_part[(out_row(i / kD) * p.n_split + split) * kD + (i % kD)] = 0.f;
         if (threadIdx.x < n_rows) p.lse_part[out_row(threadIdx.x) * p.n_split + split] = -INFINITY;
-        if (p.fused.counters != nullptr)
+        if constexpr (kFused)
             fused_tail_cta(p.fused, p.n_arrivals, p.status, p.o_part, p.lse_part, p.n_split, b, kvh, p.Hq, p.Hkv, p.G,
                            p.nq, 2, kThreads);
         return;
@@ -392,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, (R > 8) ? 1 : 3) decode_fp8_kernel(
         p.o_part[orow * kD + d] = alive ? acc / l : 0.f;
         if (d == 0) p.lse_part[orow] = alive ? (mx * kLn2 + logf(l)) : -INFINITY;
     }
-    if (p.fused.counters != nullptr)
+    if constexpr (kFused)
         fused_tail_cta(p.fused, p.n_arrivals, p.status, p.o_part, p.lse_part, p.n_split, b, kvh, p.Hq, p.Hkv, p.G,
                        p.nq, 1, 32 * kConsumers);
 }
@@ -402,7 +402,7 @@ cudaError_t launch_r(const DecodeArgs& a, const void* k_ss, const void* v_ss, cu
     const size_t ring = NS * kStageBytes;
     const size_t red = (kConsumers * R * kD + 2 * kConsumers * R) * sizeof(float);
     const size_t smem = (ring > red ? ring : red) + 1024;
-    auto kern = decode_fp8_kernel<R>;
+    auto kern = a.counters != nullptr ? decode_fp8_kernel<R, true> : decode_fp8_kernel<R, false>;
     if (occ != nullptr) return ctas_per_sm(kern, kThreads, smem, occ);
     CUtensorMap k_map, v_map, kw_map, vw_map;
     const uint64_t rows = static_cast<uint64_t>(a.num_pages) * a.page_size;

@@ -84,7 +84,7 @@ __device__ __forceinline__ void k_word_of(int t, int ks, int& word, int& j0) {
 
 // Row r of a CTA is the (query i, head h) pair rg * rpg + r = i * G + h; with
 // one query per sequence the rows are the G heads of the KV group.
-template <int R, int NG, int NS>
+template <int R, int NG, int NS, bool kFused>
 __global__ void __launch_bounds__(kThreads, (R > 8) ? 1 : 3) decode_int4_kernel(const __grid_constant__ CUtensorMap k_map,
                                                                const __grid_constant__ CUtensorMap v_map,
                                                                const Params p) {
@@ -124,7 +124,7 @@ __global__ void __launch_bounds__(kThreads, (R > 8) ? 1 : 3) decode_int4_kernel(
         for (int i = threadIdx.x; i < n_rows * kD; i += kThreads)
             p.o_part[(out_row(i / kD) * p.n_split + split) * kD + (i % kD)] = 0.f;
         if (threadIdx.x < n_rows) p.lse_part[out_row(threadIdx.x) * p.n_split + split] = -INFINITY;
-        if (p.fused.counters != nullptr)
+        if constexpr (kFused)
             fused_tail_cta(p.fused, p.n_arrivals, p.status, p.o_part, p.lse_part, p.n_split, b, kvh, p.Hq, p.Hkv, p.G,
                            p.nq, 2, kThreads);
         return;
@@ -513,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, (R > 8) ? 1 : 3) decode_int4_kernel(
         p.o_part[orow * kD + d] = alive ? acc / l : 0.f;
         if (d == 0) p.lse_part[orow] = alive ? (mx * kLn2 + logf(l)) : -INFINITY;
     }
-    if (p.fused.counters != nullptr)
+    if constexpr (kFused)
         fused_tail_cta(p.fused, p.n_arrivals, p.status, p.o_part, p.lse_part, p.n_split, b, kvh, p.Hq, p.Hkv, p.G,
                        p.nq, 1, 32 * kConsumers);
 }
@@ -527,7 +527,7 @@ cudaError_t launch_g_ng(const DecodeArgs& a, cudaStream_t stream, int* occ) {
     const size_t ring = NS * kStageBytes + kConsumers * (4 * NG * 16 + 32) * sizeof(float);
     const size_t red = (kConsumers * R * kD + 2 * kConsumers * R) * sizeof(float);
     const size_t smem = (ring > red ? ring : red) + 1024;
-    auto kern = decode_int4_kernel<R, NG, NS>;
+    auto kern = a.counters != nullptr ? decode_int4_kernel<R, NG, NS, true> : decode_int4_kernel<R, NG, NS, false>;
     if (occ != nullptr) return ctas_per_sm(kern, kThreads, smem, occ);
     CUtensorMap k_map, v_map;
     const uint64_t dims[2] = {static_cast<uint64_t>(a.Hkv) * row_words,

@@ -347,6 +347,7 @@ __device__ __forceinline__ Unit unit_of(const Params& p, int u, bool flag) {
     return w;
 }
 
+template <bool kFused>
 __global__ void __launch_bounds__(kThreads, 1) decode_int4_g32_kernel(const __grid_constant__ CUtensorMap k_map,
                                                                       const __grid_constant__ CUtensorMap v_map,
                                                                       const Params p) {
@@ -359,6 +360,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_int4_g32_kernel(const __gr
     __shared__ __align__(8) uint64_t q_empty;
     __shared__ int s_abort;
     __shared__ int s_skip[kStages];   // the stage was not loaded: its page id was out of range
+    __shared__ __align__(8) uint64_t unit_bar;   // fused mode: the consumer warps have written a unit
+    __shared__ __align__(8) uint64_t last_bar;   // fused mode: warp 0 has counted the CTA in
+    __shared__ int s_last;                       // fused mode: this CTA's split arrived last
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_rows = p.G * p.nq;    // <= 8 (query, head) rows per KV head
@@ -371,6 +375,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_int4_g32_kernel(const __gr
         }
         mbar_init(&q_full, 1);
         mbar_init(&q_empty, kConsumers);
+        mbar_init(&unit_bar, kConsumers);
+        mbar_init(&last_bar, 1);
         s_abort = 0;
         fence_mbar_init();
     }
@@ -445,6 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_int4_g32_kernel(const __gr
     int slot = 0;
     uint32_t phase = 0;
     int n_q = 0;
+    uint32_t unit_phase = 0, last_phase = 0;
     WarpState st;
     for (int u = blockIdx.x; u < p.n_units; u += gridDim.x) {
         const Unit w = unit_of(p, u, false);
@@ -453,21 +460,45 @@ __global__ void __launch_bounds__(kThreads, 1) decode_int4_g32_kernel(const __gr
             const int i = r / p.G, h = r % p.G;
             return (static_cast<size_t>(w.b) * p.Hq + kvh * p.G + h) * p.nq + i;
         };
-        // fused mode: this warp's rows of (sequence, KV head) are written; the
-        // split that arrives last merges them
-        auto fused_tail = [&]() {
-            if (p.fused.counters == nullptr) return;
-            int32_t* cnt = p.fused.counters + static_cast<size_t>(w.b) * p.Hkv + kvh;
-            if (split_arrive_warp(cnt, p.n_split, p.status, lane)) {
-                merge_head(p.o_part, p.lse_part, p.n_split, out_row(0), n_rows, p.fused, 0, 1, lane);
-                if (lane == 0) atomicExch(cnt, 0);
+        // fused mode: the 8 warps have written their rows of the unit's (sequence,
+        // head group); the CTA counts itself in once (on the counter of the
+        // group's first KV head) and, if its split is the last to arrive, every
+        // warp merges its own head's rows.  The warps meet at bounded mbarrier
+        // waits, so a role that gave up cannot leave the others waiting.
+        auto fused_tail = [&]() -> bool {
+            if constexpr (!kFused) return true;
+            __threadfence();   // this lane's partials, before the CTA counts itself in
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&unit_bar);
+            if (!mbar_wait(&unit_bar, unit_phase, &s_abort)) return false;
+            unit_phase ^= 1u;
+            int32_t* cnt = p.fused.counters + static_cast<size_t>(w.b) * p.Hkv + w.hg * kHeads;
+            if (warp == 0 && lane == 0) {
+                __threadfence();
+                const int old = atomicAdd(cnt, 1);
+                if (old >= p.n_split) flag_status(p.status, ATTN_DEV_WORKSPACE_STATE);
+                const bool last = old == p.n_split - 1;
+                if (last) atomicExch(cnt, 0);
+                s_last = last;
+                mbar_arrive(&last_bar);
             }
+            if (!mbar_wait(&last_bar, last_phase, &s_abort)) return false;
+            last_phase ^= 1u;
+            if (volatile_load(&s_last)) {
+                __threadfence();
+                merge_head(p.o_part, p.lse_part, p.n_split, out_row(0), n_rows, p.fused, 0, 1, lane);
+            }
+            return true;
         };
         if (w.n_tiles == 0) {   // empty split: O = 0, LSE = -inf
             for (int i = lane; i < n_rows * kD; i += 32)
                 p.o_part[(out_row(i / kD) * p.n_split + w.split) * kD + (i % kD)] = 0.f;
             if (lane < n_rows) p.lse_part[out_row(lane) * p.n_split + w.split] = -INFINITY;
-            fused_tail();
+            if (!fused_tail()) {
+                flag_status(p.status, ATTN_DEV_WAIT_TIMEOUT);
+                atomicExch(&s_abort, 1);
+                break;
+            }
             continue;
         }
         // ---- the unit's queries.  B operand of the score MMA: column g is CTA row g
@@ -591,7 +622,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_int4_g32_kernel(const __gr
                 p.lse_part[out_row(col) * p.n_split + w.split] = alive ? st.m_run[j] * kLn2 + logf(l_tot[j])
                                                                          : -INFINITY;
         }
-        fused_tail();
+        if (!fused_tail()) {
+            flag_status(p.status, ATTN_DEV_WAIT_TIMEOUT);
+            atomicExch(&s_abort, 1);
+            break;
+        }
     }
 }
 
@@ -609,7 +644,7 @@ bool decode_int4_g32_supported(const DecodeArgs& a) {
 // per SM serving 8 KV heads at a time, reported as 8 (KV head, split) slots per SM.
 cudaError_t launch_decode_int4_g32(const DecodeArgs& a, cudaStream_t stream, int* occ) {
     const size_t smem = kStages * kStageBytes + kQBytes + 1024;
-    auto kern = decode_int4_g32_kernel;
+    auto kern = a.counters != nullptr ? decode_int4_g32_kernel<true> : decode_int4_g32_kernel<false>;
     if (occ != nullptr) {
         int ctas = 0;
         const cudaError_t e = ctas_per_sm(kern, kThreads, smem, &ctas);

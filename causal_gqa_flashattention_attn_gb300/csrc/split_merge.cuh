@@ -55,49 +55,88 @@ __device__ __forceinline__ bool split_arrive_warp(int32_t* counter, int expected
     return last != 0;
 }
 
-// One warp merges partial row `row` (D = 128: four elements per lane) of
-// o_part [rows][S][128] / lse_part [rows][S] into o [rows][128] (bf16) and lse
-// [rows] (may be NULL).  Partials are read through L2 (other SMs wrote them).
-__device__ __forceinline__ void merge_row_warp(const float* o_part, const float* lse_part, int S, size_t row,
-                                               __nv_bfloat16* o, float* lse, int lane) {
-    const float* lp = lse_part + row * S;
-    const float* op = o_part + row * S * 128;
-    float mx = -INFINITY;
-    for (int s = lane; s < S; s += 32) mx = fmaxf(mx, __ldcg(lp + s));
+// One warp merges up to 4 partial rows row0 + k * stride (k < nr; D = 128:
+// four elements per lane) of o_part [rows][S][128] / lse_part [rows][S] into
+// o [rows][128] (bf16) and lse [rows] (may be NULL).  Partials are read through
+// L2 (other SMs wrote them); every load of a batch of 4 splits of all the rows
+// is issued before any is used, so a merge costs a few L2 round trips, and
+// the sums run in split order as attn_lse_merge's do.  Not inlined: its
+// registers do not add to the decode loop's.
+static __device__ __noinline__ void merge_rows_warp(const float* o_part, const float* lse_part, int S, size_t row0,
+                                                    size_t stride, int nr, __nv_bfloat16* o, float* lse, int lane) {
+    constexpr int kR = 4, kB = 4;
+    float mx[kR], wsum[kR];
+    float4 acc[kR];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    const bool alive = mx != -INFINITY;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float wsum = 0.f;
-    if (alive) {
-        for (int s0 = 0; s0 < S; s0 += 32) {
-            const int s = s0 + lane;
-            const float l = s < S ? __ldcg(lp + s) : -INFINITY;
-            const float w = l == -INFINITY ? 0.f : expf(l - mx);
-            wsum += w;
-            const int n = min(32, S - s0);
-            for (int u = 0; u < n; ++u) {
-                const float wu = __shfl_sync(0xffffffffu, w, u);
-                if (wu != 0.f) {   // splits of weight 0 may hold any bits
-                    const float4 v = __ldcg(reinterpret_cast<const float4*>(op + static_cast<size_t>(s0 + u) * 128) + lane);
-                    acc.x = fmaf(wu, v.x, acc.x);
-                    acc.y = fmaf(wu, v.y, acc.y);
-                    acc.z = fmaf(wu, v.z, acc.z);
-                    acc.w = fmaf(wu, v.w, acc.w);
-                }
-            }
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
+    for (int k = 0; k < kR; ++k) {
+        mx[k] = -INFINITY;
+        wsum[k] = 0.f;
+        acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    const float inv = alive ? 1.f / wsum : 0.f;
-    const __nv_bfloat162 a = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-    const __nv_bfloat162 b = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
-    uint2 u;
-    u.x = *reinterpret_cast<const uint32_t*>(&a);
-    u.y = *reinterpret_cast<const uint32_t*>(&b);
-    *reinterpret_cast<uint2*>(o + row * 128 + 4 * lane) = u;
-    if (lse != nullptr && lane == 0) lse[row] = alive ? mx + logf(wsum) : -INFINITY;
+    // the maximum partial LSE of each row
+    for (int s0 = 0; s0 < S; s0 += 32) {
+        float l[kR];
+#pragma unroll
+        for (int k = 0; k < kR; ++k)
+            l[k] = (k < nr && s0 + lane < S) ? __ldcg(lse_part + (row0 + k * stride) * S + s0 + lane) : -INFINITY;
+#pragma unroll
+        for (int k = 0; k < kR; ++k) mx[k] = fmaxf(mx[k], l[k]);
+    }
+#pragma unroll
+    for (int k = 0; k < kR; ++k)
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) mx[k] = fmaxf(mx[k], __shfl_xor_sync(0xffffffffu, mx[k], off));
+    for (int s0 = 0; s0 < S; s0 += 32) {
+        // lane j holds the weight of split s0 + j of each row
+        float w[kR];
+#pragma unroll
+        for (int k = 0; k < kR; ++k) {
+            const float l = (k < nr && s0 + lane < S) ? __ldcg(lse_part + (row0 + k * stride) * S + s0 + lane)
+                                                      : -INFINITY;
+            w[k] = (l == -INFINITY || mx[k] == -INFINITY) ? 0.f : expf(l - mx[k]);
+            wsum[k] += w[k];
+        }
+        const int n = min(32, S - s0);
+        for (int j0 = 0; j0 < n; j0 += kB) {
+            float4 v[kR][kB];
+#pragma unroll
+            for (int u = 0; u < kB; ++u)
+#pragma unroll
+                for (int k = 0; k < kR; ++k)
+                    v[k][u] = (k < nr && j0 + u < n)
+                                  ? __ldcg(reinterpret_cast<const float4*>(
+                                               o_part + ((row0 + k * stride) * S + s0 + j0 + u) * 128) + lane)
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int u = 0; u < kB; ++u)
+#pragma unroll
+                for (int k = 0; k < kR; ++k) {
+                    const float wu = __shfl_sync(0xffffffffu, w[k], (j0 + u) & 31);
+                    if (wu != 0.f) {   // a split of weight 0 adds nothing, whatever its O holds
+                        acc[k].x = fmaf(wu, v[k][u].x, acc[k].x);
+                        acc[k].y = fmaf(wu, v[k][u].y, acc[k].y);
+                        acc[k].z = fmaf(wu, v[k][u].z, acc[k].z);
+                        acc[k].w = fmaf(wu, v[k][u].w, acc[k].w);
+                    }
+                }
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < kR; ++k) {
+        if (k >= nr) break;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) wsum[k] += __shfl_xor_sync(0xffffffffu, wsum[k], off);
+        const bool alive = mx[k] != -INFINITY;
+        const float inv = alive ? 1.f / wsum[k] : 0.f;
+        const __nv_bfloat162 a = __floats2bfloat162_rn(acc[k].x * inv, acc[k].y * inv);
+        const __nv_bfloat162 b = __floats2bfloat162_rn(acc[k].z * inv, acc[k].w * inv);
+        uint2 u;
+        u.x = *reinterpret_cast<const uint32_t*>(&a);
+        u.y = *reinterpret_cast<const uint32_t*>(&b);
+        const size_t row = row0 + k * stride;
+        *reinterpret_cast<uint2*>(o + row * 128 + 4 * lane) = u;
+        if (lse != nullptr && lane == 0) lse[row] = alive ? mx[k] + logf(wsum[k]) : -INFINITY;
+    }
 }
 
 // Fused-mode outputs of a decode launch.
@@ -108,10 +147,12 @@ struct FusedOut {
 };
 
 // Rows [row0, row0 + n_rows) of a (sequence, KV head), merged by warps
-// warp0, warp0 + n_warps, ... of the caller.
+// warp, warp + n_warps, ... of the caller, up to four rows per pass.
 __device__ __forceinline__ void merge_head(const float* o_part, const float* lse_part, int S, size_t row0, int n_rows,
                                            const FusedOut& f, int warp, int n_warps, int lane) {
-    for (int r = warp; r < n_rows; r += n_warps) merge_row_warp(o_part, lse_part, S, row0 + r, f.o, f.lse, lane);
+    for (int r = warp; r < n_rows; r += 4 * n_warps)
+        merge_rows_warp(o_part, lse_part, S, row0 + r, n_warps, min(4, (n_rows - r + n_warps - 1) / n_warps), f.o,
+                        f.lse, lane);
 }
 
 // Fused tail of a decode CTA whose `nthreads` threads (warps 0.., meeting at

@@ -5,8 +5,10 @@ C ABI, in the launch configuration the benchmark times:
   square prefill (B8 Hq32 Hkv8 q=kv=4096, K x2) through attn_prefill_fwd_ws
   with a zeroed workspace;
 * the bf16 paged decode (B64, lengths U[512, 32768], split 2048) and the int4
-  paged decode (B16, 16384 tokens, N_GROUPS 4, the split that fills the GPU)
-  through attn_decode_paged_splitk writing partials only, then attn_lse_merge;
+  paged decode (B16, 16384 tokens, N_GROUPS 4, the split attn_decode_split_tokens
+  picks) through attn_decode_paged_splitk writing partials only, then
+  attn_lse_merge; the int4 one also through attn_decode_paged_fused (the merge
+  inside the launch);
 * the fp8 decode on the int4 workload's shape, the same way.
 
 Each compares O element by element (maximum and mean absolute error over the
@@ -71,9 +73,10 @@ def test_batched_square_prefill_every_output():
     _prefill_whole(synth.BATCHED_SQUARE_PREFILL)
 
 
-def _decode_whole(shape):
-    """Partials-only decode then the merge, as the benchmark launches them;
-    the oracle decodes every sequence (all heads, all splits, merged)."""
+def _decode_whole(shape, fused=False):
+    """Partials-only decode then the merge, as the benchmark's hot path launches
+    them (fused: attn_decode_paged_fused, the merge inside the launch); the
+    oracle decodes every sequence (all heads, all splits, merged)."""
     dev = gpu_or_skip()
     import causal_gqa_flashattention_attn_gb300 as attn
     if shape.kv_format in ("int4", "fp8"):
@@ -85,27 +88,39 @@ def _decode_whole(shape):
     lens = inp["lens"]
     t = {k: x.to(dev) for k, x in inp.items() if torch.is_tensor(x)}
     max_len = shape.len_hi
-    ws = torch.empty(attn.attn_decode_workspace_bytes(shape.B, shape.Hq, max_len, shape.split_tokens, shape.D),
-                     dtype=torch.uint8, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
+    extra = {}
     if shape.kv_format == "fp8":
-        attn.attn_decode_paged_splitk_fp8(t["q"], t["k_cache"], t["v_cache"], t["k_scale_shift"],
-                                          t["v_scale_shift"], t["block_table"], t["seq_lens"], shape.split_tokens,
-                                          max_len, workspace=ws, dev_status=status, write_output=False)
+        extra = dict(k_scale_shift=t["k_scale_shift"], v_scale_shift=t["v_scale_shift"])
+    if fused:
+        ws = torch.zeros(attn.attn_decode_fused_workspace_bytes(shape.B, shape.Hq, shape.Hkv, max_len,
+                                                                shape.split_tokens, shape.D),
+                         dtype=torch.uint8, device=dev)
+        o, lse, _ = attn.attn_decode_paged_fused(t["q"], t["k_cache"], t["v_cache"], t["block_table"],
+                                                 t["seq_lens"], shape.split_tokens, max_len, n_groups=shape.n_groups,
+                                                 workspace=ws, dev_status=status, **extra)
     else:
-        attn.attn_decode_paged_splitk(t["q"], t["k_cache"], t["v_cache"], t["block_table"], t["seq_lens"],
-                                      shape.split_tokens, max_len, n_groups=shape.n_groups, workspace=ws,
-                                      dev_status=status, write_output=False)
-    o_part, lse_part = attn.decode_partials_view(ws, shape.B, shape.Hq, max_len, shape.split_tokens, shape.D)
-    o = torch.empty(shape.B * shape.Hq, shape.D, dtype=torch.bfloat16, device=dev)
-    lse = torch.empty(shape.B * shape.Hq, dtype=torch.float32, device=dev)
-    attn.attn_lse_merge(o_part.reshape(shape.B * shape.Hq, -1, shape.D), lse_part.reshape(shape.B * shape.Hq, -1),
-                        o=o, lse=lse)
+        ws = torch.empty(attn.attn_decode_workspace_bytes(shape.B, shape.Hq, max_len, shape.split_tokens, shape.D),
+                         dtype=torch.uint8, device=dev)
+        if shape.kv_format == "fp8":
+            attn.attn_decode_paged_splitk_fp8(t["q"], t["k_cache"], t["v_cache"], t["k_scale_shift"],
+                                              t["v_scale_shift"], t["block_table"], t["seq_lens"],
+                                              shape.split_tokens, max_len, workspace=ws, dev_status=status,
+                                              write_output=False)
+        else:
+            attn.attn_decode_paged_splitk(t["q"], t["k_cache"], t["v_cache"], t["block_table"], t["seq_lens"],
+                                          shape.split_tokens, max_len, n_groups=shape.n_groups, workspace=ws,
+                                          dev_status=status, write_output=False)
+        o_part, lse_part = attn.decode_partials_view(ws, shape.B, shape.Hq, max_len, shape.split_tokens, shape.D)
+        o = torch.empty(shape.B * shape.Hq, shape.D, dtype=torch.bfloat16, device=dev)
+        lse = torch.empty(shape.B * shape.Hq, dtype=torch.float32, device=dev)
+        attn.attn_lse_merge(o_part.reshape(shape.B * shape.Hq, -1, shape.D),
+                            lse_part.reshape(shape.B * shape.Hq, -1), o=o, lse=lse)
     torch.cuda.synchronize()
     assert status.item() == 0, status.item()
     o_np = o.float().cpu().numpy().reshape(shape.B, shape.Hq, shape.D)
     lse_np = lse.cpu().numpy().reshape(shape.B, shape.Hq)
-    del t, ws, o_part, lse_part
+    del t, ws
     if shape.kv_format == "dense":
         kc, vc = inp["k_cache"].float().numpy(), inp["v_cache"].float().numpy()
     else:
@@ -132,6 +147,10 @@ def test_paged_decode_bf16_every_output():
 
 def test_paged_decode_int4_every_output():
     _decode_whole(synth.PAGED_DECODE_INT4)
+
+
+def test_paged_decode_int4_fused_every_output():
+    _decode_whole(synth.PAGED_DECODE_INT4, fused=True)
 
 
 def test_paged_decode_fp8_every_output():
