@@ -75,7 +75,7 @@ def lib():
     L.attn_prefill_plan_sms.restype = i32
     L.attn_decode_split_tokens_for.argtypes = [i32, i32, i32, i32, i32, i32, i32]
     L.attn_decode_split_tokens_for.restype = i32
-    L.attn_decode_split_tokens_balanced_for.argtypes = [i32, i32, i32, i32]
+    L.attn_decode_split_tokens_balanced_for.argtypes = [i32, i32, i32, i32, i32]
     L.attn_decode_split_tokens_balanced_for.restype = i32
     L.attn_prefill_fwd_ws.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32, vp, sz, vp, vp]
     L.attn_prefill_fwd_ws.restype = i32
@@ -206,9 +206,9 @@ def attn_prefill_plan_sms(dtype, B, Hq, Hkv, q_len, kv_len, D, sms):
     return int(sched), int(grid.value)
 
 
-def attn_decode_split_tokens_balanced_for(sms, B, head_groups, max_kv_len):
+def attn_decode_split_tokens_balanced_for(sms, B, head_groups, max_kv_len, tile=32):
     """The split of the persistent int4 decode for a described device (no driver call)."""
-    return int(lib().attn_decode_split_tokens_balanced_for(sms, B, head_groups, max_kv_len))
+    return int(lib().attn_decode_split_tokens_balanced_for(sms, B, head_groups, max_kv_len, tile))
 
 
 def attn_decode_split_tokens_for(sms, ctas_per_sm, B, Hq, Hkv, max_kv_len, q_len=1):

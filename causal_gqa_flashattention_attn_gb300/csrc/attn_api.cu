@@ -115,7 +115,11 @@ attn_status_t decode_impl(const void* q, const void* k_cache, const void* v_cach
     const int G = Hq / Hkv;
     if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return ATTN_ERR_UNSUPPORTED;
     if (q_len > 16) return ATTN_ERR_UNSUPPORTED;
-    if (page_size % 64 != 0 || split_tokens % 64 != 0) return ATTN_ERR_UNSUPPORTED;
+    // the persistent int4 kernel (N_GROUPS 4, Hkv a multiple of 8, at most 8 rows
+    // per KV head) takes splits in 32-token steps, the others in 64-token steps
+    const bool int4_g32 = kv_dtype == ATTN_INT4_PACKED && n_groups == 4 && D == 128 && Hkv % 8 == 0 &&
+                          G * q_len <= 8;
+    if (page_size % 64 != 0 || split_tokens % (int4_g32 ? 32 : 64) != 0) return ATTN_ERR_UNSUPPORTED;
     if (static_cast<long long>(num_pages) * page_size >= (1LL << 31)) return ATTN_ERR_UNSUPPORTED;
     int fmt = 0;
     if (kv_dtype == ATTN_BF16) {
@@ -206,7 +210,7 @@ const char* attn_status_string(attn_status_t status) {
     }
 }
 
-int attn_abi_version(void) { return 108; }
+int attn_abi_version(void) { return 109; }
 
 attn_status_t attn_selftest_wait_timeout(int32_t* dev_status, unsigned int limit_us, void* stream) {
     if (dev_status == nullptr || limit_us == 0 || limit_us > 1000000u) return ATTN_ERR_INVALID_ARG;
@@ -354,14 +358,14 @@ int attn_decode_split_tokens_for(int sms, int ctas_per_sm, int B, int Hq, int Hk
     return best;
 }
 
-int attn_decode_split_tokens_balanced_for(int sms, int B, int head_groups, int max_kv_len) {
-    if (sms <= 0 || B <= 0 || head_groups <= 0 || max_kv_len <= 0) return 0;
+int attn_decode_split_tokens_balanced_for(int sms, int B, int head_groups, int max_kv_len, int tile) {
+    if (sms <= 0 || B <= 0 || head_groups <= 0 || max_kv_len <= 0 || (tile != 32 && tile != 64)) return 0;
     constexpr long long kUnitCost = 64;   // a unit's fixed cost, in tokens
-    const int tiles = (max_kv_len + 63) / 64;
+    const int tiles = (max_kv_len + tile - 1) / tile;
     int best = 0;
     long long best_cost = -1;
     std::vector<long long> load;
-    for (int split = 64 * tiles; split >= 64; split -= 64) {
+    for (int split = tile * tiles; split >= tile; split -= tile) {
         const int S = (max_kv_len + split - 1) / split;
         const long long per_group = static_cast<long long>(B) * S;
         const long long units = per_group * head_groups;
@@ -407,7 +411,7 @@ int attn_decode_split_tokens(attn_dtype_t kv_dtype, int n_groups, int B, int Hq,
     a.D = D;
     a.q_len = q_len;
     if (fmt == 1 && decode_int4_g32_shape_ok(a))
-        return attn_decode_split_tokens_balanced_for(device_sm_count(), B, Hkv / 8, max_kv_len);
+        return attn_decode_split_tokens_balanced_for(device_sm_count(), B, Hkv / 8, max_kv_len, 32);
     int occ = 0;
     const cudaError_t e = (fmt == 2) ? launch_decode_fp8(a, nullptr, nullptr, nullptr, &occ)
                                      : launch_decode(a, nullptr, &occ);

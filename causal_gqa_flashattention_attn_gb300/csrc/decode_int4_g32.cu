@@ -225,6 +225,28 @@ __device__ __forceinline__ void subtiles(WarpState& st, const uint8_t* kt, const
             }
         }
     }
+    // ---- the value side's shared-memory loads, issued before the softmax so
+    // their latency hides behind it (none depends on P)
+    uint4 vc_all[2][4];
+    uint32_t woff[2][4];
+    uint32_t rv[2][2][4];
+#pragma unroll
+    for (int sb = 0; sb < 2; ++sb) {
+        const uint32_t sbo = sb * 2 * kRow8;
+        const uint8_t* va = vt + lo.vc[0] + sbo;
+        const uint8_t* vb = vt + lo.vc[1] + sbo;
+        const uint8_t* vrow[4] = {va, vb, va + kRow8, vb + kRow8};
+        const int wo = 4 * (g & 3);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            vc_all[sb][i] = *reinterpret_cast<const uint4*>(vrow[i]);
+            woff[sb][i] = *reinterpret_cast<const uint32_t*>(vrow[i] + wo);
+        }
+#pragma unroll
+        for (int half = 0; half < 2; ++half)
+            ldmatrix_x4_trans(rv[sb][half][0], rv[sb][half][1], rv[sb][half][2], rv[sb][half][3],
+                              vt_s + lo.ldm[half] + sbo);
+    }
     // ---- online softmax per column; the max is reduced across the warp only
     // when some score passes the column's threshold (lazy rescale by 2^8)
     bool over = false;
@@ -269,13 +291,10 @@ __device__ __forceinline__ void subtiles(WarpState& st, const uint8_t* kt, const
         const uint32_t pt0 = movmatrix_trans(h2_bits(__floats2half2_rn(pr[0], pr[1])));
         const uint32_t pt1 = movmatrix_trans(h2_bits(__floats2half2_rn(pr[2], pr[3])));
         // V coefficient words of tokens 2t4, 2t4 + 1, 2t4 + 8, 2t4 + 9
-        const uint8_t* va = vt + lo.vc[0] + sbo;
-        const uint8_t* vb = vt + lo.vc[1] + sbo;
-        const uint8_t* vrow[4] = {va, vb, va + kRow8, vb + kRow8};
         uint4 vc[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            vc[i] = *reinterpret_cast<const uint4*>(vrow[i]);
+            vc[i] = vc_all[sb][i];
             if constexpr (kPartial) {
                 const int tok = 2 * t4 + (i & 1) + 8 * (i >> 1);
                 if (tok >= n_valid[sb]) vc[i] = make_uint4(0u, 0u, 0u, 0u);   // P is 0 there; keep 0 * x finite
@@ -284,11 +303,7 @@ __device__ __forceinline__ void subtiles(WarpState& st, const uint8_t* kt, const
         // offset term of O: A = offsets of group g (rows 0-3 are read; rows 4-7 repeat
         // groups 0-3 and are discarded) by tokens, B = P^T
         {
-            const int wo = 4 * (g & 3);
-            uint32_t w_a = *reinterpret_cast<const uint32_t*>(vrow[0] + wo);
-            uint32_t w_b = *reinterpret_cast<const uint32_t*>(vrow[1] + wo);
-            uint32_t w_c = *reinterpret_cast<const uint32_t*>(vrow[2] + wo);
-            uint32_t w_d = *reinterpret_cast<const uint32_t*>(vrow[3] + wo);
+            uint32_t w_a = woff[sb][0], w_b = woff[sb][1], w_c = woff[sb][2], w_d = woff[sb][3];
             if constexpr (kPartial) {
                 w_a = 2 * t4 < n_valid[sb] ? w_a : 0u;
                 w_b = 2 * t4 + 1 < n_valid[sb] ? w_b : 0u;
@@ -302,8 +317,7 @@ __device__ __forceinline__ void subtiles(WarpState& st, const uint8_t* kt, const
                                     {vc[2].x, vc[2].y, vc[2].z, vc[2].w}, {vc[3].x, vc[3].y, vc[3].z, vc[3].w}};
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
-            uint32_t r[4];   // (group 2h, tokens 2t4..), (2h, 2t4+8..), (2h+1, 2t4..), (2h+1, 2t4+8..); elements 4g..4g+3
-            ldmatrix_x4_trans(r[0], r[1], r[2], r[3], vt_s + lo.ldm[half] + sbo);
+            const uint32_t* r = rv[sb][half];   // (group 2h, tokens 2t4..), (2h, 2t4+8..), (2h+1, 2t4..), (2h+1, 2t4+8..)
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
                 const int c = 2 * half + u;

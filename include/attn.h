@@ -185,7 +185,8 @@ size_t attn_decode_workspace_bytes(int B, int Hq, int max_kv_len, int split_toke
  *   kv_dtype   ATTN_BF16, ATTN_INT4_PACKED (with n_groups) or ATTN_FP8_E4M3
  * The int4 decode with N_GROUPS 4, Hkv a multiple of 8 and G * q_len <= 8
  * runs one persistent CTA per SM over work units (sequence, chunk, group of 8
- * KV heads); for it the choice is attn_decode_split_tokens_balanced_for.
+ * KV heads); for it the choice is attn_decode_split_tokens_balanced_for with
+ * 32-token steps (so the returned split may be a multiple of 32 only).
  * Returns 0 for sizes the decode entries do not take, or without a device.
  */
 int attn_decode_split_tokens(attn_dtype_t kv_dtype, int n_groups, int B, int Hq, int Hkv, int q_len, int max_kv_len,
@@ -196,11 +197,11 @@ int attn_decode_split_tokens(attn_dtype_t kv_dtype, int n_groups, int B, int Hq,
 int attn_decode_split_tokens_for(int sms, int ctas_per_sm, int B, int Hq, int Hkv, int q_len, int max_kv_len);
 /* The split for a persistent decode whose `sms` CTAs walk the work units
  * (head group, chunk, sequence) round-robin, B sequences and head_groups groups
- * of KV heads, every sequence counted at max_kv_len: the multiple of 64 that
- * minimises the largest per-CTA sum of unit tokens, each unit counted 64
- * tokens longer for its fixed cost; ties go to the larger split.  0 for
- * non-positive sizes. */
-int attn_decode_split_tokens_balanced_for(int sms, int B, int head_groups, int max_kv_len);
+ * of KV heads, every sequence counted at max_kv_len: the multiple of `tile`
+ * (32 or 64) that minimises the largest per-CTA sum of unit tokens, each unit
+ * counted 64 tokens longer for its fixed cost; ties go to the larger split.
+ * 0 for non-positive sizes or another tile. */
+int attn_decode_split_tokens_balanced_for(int sms, int B, int head_groups, int max_kv_len, int tile);
 
 /*
  * attn_prefill_paged_varlen - causal GQA prefill of a ragged batch over a
@@ -282,7 +283,9 @@ attn_status_t attn_prefill_paged_varlen_ws(const void* q, const void* k_cache, c
  *   seq_lens     int32 [B], 0 <= seq_lens[b] <= max_kv_len  (device)  (read)
  *   n_groups     1, 2, 4 or 8 for ATTN_INT4_PACKED; ignored for ATTN_BF16.
  *   D            128.  Hq / Hkv in {1, 2, 4, 8, 16}.
- *   page_size    a multiple of 64.  split_tokens: a multiple of 64.
+ *   page_size    a multiple of 64.  split_tokens: a multiple of 64, or of 32
+ *                for an int4 cache with n_groups 4, Hkv a multiple of 8 and
+ *                Hq / Hkv * q_len <= 8 (the persistent int4 kernel).
  *   workspace    >= attn_decode_workspace_bytes(B, Hq, max_kv_len, split_tokens, D)
  *                bytes of device memory owned by the caller; it receives the
  *                split partials in the layout documented above.
@@ -495,7 +498,8 @@ const char* attn_status_string(attn_status_t status);
  * 105 attn_decode_split_tokens,
  * 106 attn_prefill_plan_sms, attn_decode_split_tokens_for.
  * 107 attn_decode_split_tokens_balanced_for; bad decode pages are left out.
- * 108 attn_decode_paged_fused, attn_decode_fused_workspace_bytes. */
+ * 108 attn_decode_paged_fused, attn_decode_fused_workspace_bytes.
+ * 109 32-token splits for the persistent int4 decode; the balanced split takes a tile. */
 int attn_abi_version(void);
 
 #ifdef __cplusplus

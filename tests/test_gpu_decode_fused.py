@@ -25,6 +25,7 @@ CASES = [
     ("dense", 1, 32, 8, 16, 512, [1200, 16, 300]),      # multi-query, four row groups
     ("int4", 4, 32, 8, 1, 2048, [700, 1, 2100, 64, 0]),  # the persistent kernel (8 KV heads a CTA)
     ("int4", 4, 32, 8, 1, 896, [16384, 5000, 31]),      # many splits per sequence
+    ("int4", 4, 32, 8, 1, 864, [16384, 2000, 865, 33]),  # a 32-token split step
     ("int4", 4, 32, 8, 2, 512, [900, 30]),              # multi-query on the persistent kernel
     ("int4", 2, 32, 8, 1, 256, [300, 0, 129]),          # the general int4 kernel
     ("int4", 4, 32, 4, 1, 2048, [900, 2]),              # G = 8, Hkv 4: the general kernel

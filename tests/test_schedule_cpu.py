@@ -116,25 +116,30 @@ def _balanced_cost(split, B, groups, L, sms, unit_cost=64):
     return max(load)
 
 
+@pytest.mark.parametrize("tile", [32, 64])
 @pytest.mark.parametrize("sms,B,groups,L", [
     (152, 16, 1, 16384), (152, 64, 1, 32768), (152, 2, 1, 131372), (148, 7, 2, 5000), (1, 3, 1, 700),
     (7, 1, 3, 64), (152, 40, 1, 1),
 ])
-def test_balanced_decode_split_minimises_the_busiest_cta(attn, sms, B, groups, L):
-    """The persistent int4 decode's split: the multiple of 64 whose round-robin
-    walk gives the smallest busiest-CTA sum (64 tokens per unit for its fixed
-    cost), the larger split on ties; checked against every candidate."""
-    got = attn.attn_decode_split_tokens_balanced_for(sms, B, groups, L)
-    assert got % 64 == 0 and 64 <= got <= 64 * -(-L // 64)
-    costs = {sp: _balanced_cost(sp, B, groups, L, sms) for sp in range(64, 64 * -(-L // 64) + 1, 64)}
+def test_balanced_decode_split_minimises_the_busiest_cta(attn, sms, B, groups, L, tile):
+    """The persistent int4 decode's split: the multiple of `tile` whose
+    round-robin walk gives the smallest busiest-CTA sum (64 tokens per unit for
+    its fixed cost), the larger split on ties; checked against every candidate."""
+    got = attn.attn_decode_split_tokens_balanced_for(sms, B, groups, L, tile)
+    top = tile * -(-L // tile)
+    assert got % tile == 0 and tile <= got <= top
+    costs = {sp: _balanced_cost(sp, B, groups, L, sms) for sp in range(tile, top + 1, tile)}
     best = min(costs.values())
     assert costs[got] == best and got == max(sp for sp, c in costs.items() if c == best)
 
 
 def test_balanced_decode_split_of_the_int4_workload(attn):
-    """16 sequences of 16384 tokens, one group of 8 KV heads, 152 SMs: 9 chunks
-    of 1856 tokens (144 units, one per CTA) tie with 19 of 896 (two per CTA)
-    and the larger split is taken; non-positive sizes give 0."""
-    assert attn.attn_decode_split_tokens_balanced_for(152, 16, 1, 16384) == 1856
-    assert attn.attn_decode_split_tokens_balanced_for(0, 16, 1, 16384) == 0
-    assert attn.attn_decode_split_tokens_balanced_for(152, 16, 0, 16384) == 0
+    """16 sequences of 16384 tokens, one group of 8 KV heads, 152 SMs: in
+    32-token steps, 19 chunks of 864 tokens (304 units, two per CTA, busiest
+    CTA 1728 tokens); in 64-token steps 1856 (9 chunks, one unit per CTA) ties
+    with 896 and the larger is taken.  Bad sizes give 0."""
+    assert attn.attn_decode_split_tokens_balanced_for(152, 16, 1, 16384, 32) == 864
+    assert attn.attn_decode_split_tokens_balanced_for(152, 16, 1, 16384, 64) == 1856
+    assert attn.attn_decode_split_tokens_balanced_for(0, 16, 1, 16384, 32) == 0
+    assert attn.attn_decode_split_tokens_balanced_for(152, 16, 0, 16384, 32) == 0
+    assert attn.attn_decode_split_tokens_balanced_for(152, 16, 1, 16384, 48) == 0
