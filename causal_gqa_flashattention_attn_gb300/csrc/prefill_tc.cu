@@ -20,6 +20,9 @@
 //   * warp roles: warps 0-3 softmax of tile 0, warps 4-7 softmax of tile 1,
 //     warp 8 TMA producer, warp 9 MMA issuer (one elected lane), warps 10-11
 //     idle; registers move from the control warpgroup to the softmax ones;
+//   * one elected lane of the MMA warp issues every tcgen05.mma with
+//     prebuilt descriptor words, a handful of instructions per MMA, so the
+//     tensor core is not left waiting on the issuing thread;
 //   * TMA (128-byte swizzle) stages Q once per work item and K/V through a
 //     two-stage ring whose K and V stages are freed separately (K once both
 //     S MMAs have read it, V after both P.V); tcgen05.mma accumulates S
@@ -991,23 +994,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool cp_async_tiles = kVarlen && !p.gathered;
                 constexpr uint32_t idesc_qk = idesc_bf16_f32(kBM, kBN, false);
                 constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, kD, true);
-                const uint32_t q_s = smem_u32(smem + kOffQ), k_s = smem_u32(smem + kOffK), v_s = smem_u32(smem + kOffV);
+                // This one thread issues every MMA of the CTA, so its instruction
+                // count per MMA bounds the tensor core: the descriptors' low words
+                // are built once and an MMA only adds a constant start-address
+                // offset (>> 4); the high word is an immediate in the instruction.
+                // (Full 64-bit descriptors rebuilt per MMA left the tensor core idle
+                // about a third of the time.)
+                const uint32_t d_base = sw128_desc_lo(smem_u32(smem), 16);   // low word of a descriptor at smem
                 auto issue_s = [&](int t, int stage) {  // S_t = Q_t K^T
-                    const uint32_t qa = q_s + t * kTile, kb = k_s + stage * kTile;
+                    const uint32_t dq = d_base + ((kOffQ + t * kTile) >> 4), dk = d_base + ((kOffK + stage * kTile) >> 4);
+                    const uint32_t d = tmem + kColS + 128 * t;
+                    umma_ss_lo<0>(d, dq, dk, idesc_qk);
     #pragma unroll
-                    for (int kk = 0; kk < kD / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-                        umma_ss(tmem + kColS + 128 * t, sw128_desc(qa + off, 16, 1024), sw128_desc(kb + off, 16, 1024),
-                                idesc_qk, kk > 0);
+                    for (int kk = 1; kk < kD / 16; ++kk) {
+                        const uint32_t off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
+                        umma_ss_lo<1>(d, dq + off, dk + off, idesc_qk);
                     }
                 };
                 auto issue_pv = [&](int t, int stage, bool acc) {  // O_t (+)= P_t V
-                    const uint32_t vb = v_s + stage * kTile;
+                    // V: leading offset kHalf (the two 64-column halves) in bits 16-29
+                    const uint32_t dv = d_base + ((kOffV + stage * kTile) >> 4) + (((kHalf - 16) >> 4) << 16);
+                    const uint32_t d = tmem + kColO + 128 * t, a = tmem + kColS + 128 * t;
+                    umma_ts_lo(d, a, dv, idesc_pv, acc ? 1u : 0u);
     #pragma unroll
-                    for (int kk = 0; kk < kBN / 16; ++kk) {
-                        umma_ts(tmem + kColO + 128 * t, tmem + kColS + 128 * t + kk * 8,
-                                sw128_desc(vb + kk * 16 * 128, kHalf, 1024), idesc_pv, (acc || kk > 0) ? 1u : 0u);
-                    }
+                    for (int kk = 1; kk < kBN / 16; ++kk) umma_ts_lo(d, a + kk * 8, dv + ((kk * 16 * 128) >> 4), idesc_pv, 1u);
                 };
                 uint32_t kv_iter = 0, item_iter = 0;
                 bool ok = true;
