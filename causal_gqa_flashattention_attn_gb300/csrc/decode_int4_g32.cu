@@ -279,7 +279,6 @@ __device__ __forceinline__ void subtiles(WarpState& st, const uint8_t* kt, const
     }
 #pragma unroll
     for (int sb = 0; sb < 2; ++sb) {
-        const uint32_t sbo = sb * 2 * kRow8;
         float pr[4];
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
@@ -481,7 +480,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_int4_g32_kernel(const __gr
         // waits, so a role that gave up cannot leave the others waiting.
         auto fused_tail = [&]() -> bool {
             if constexpr (!kFused) return true;
-            __threadfence();   // this lane's partials, before the CTA counts itself in
+            // the warps' partials are ordered before warp 0's fence by the warp
+            // barrier and the CTA's mbarrier; that one fence (cumulative) makes
+            // them visible device-wide before the CTA counts itself in
             __syncwarp();
             if (lane == 0) mbar_arrive(&unit_bar);
             if (!mbar_wait(&unit_bar, unit_phase, &s_abort)) return false;
@@ -500,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_int4_g32_kernel(const __gr
             last_phase ^= 1u;
             if (volatile_load(&s_last)) {
                 __threadfence();
-                merge_head(p.o_part, p.lse_part, p.n_split, out_row(0), n_rows, p.fused, 0, 1, lane);
+                merge_head<16>(p.o_part, p.lse_part, p.n_split, out_row(0), n_rows, p.fused, 0, 1, lane);
             }
             return true;
         };

@@ -4,7 +4,7 @@
 // maximum partial LSE M, weights w_s = exp(LSE_s - M), O = sum w_s O_s / sum w_s,
 // LSE = M + log(sum w_s); a row whose partial LSEs are all -inf gives O = 0
 // and LSE = -inf.  One warp per row, lanes across D in float4 chunks; splits
-// with LSE = -inf add nothing, whatever bits their O holds (rows of up to 16
+// with LSE = -inf add nothing, whatever bits their O holds (rows of up to 32
 // splits and D <= 128 load every partial at once, the rest skip reading them).
 #include <cuda_bf16.h>
 
@@ -88,6 +88,38 @@ __device__ __forceinline__ void row_weights(const float* lp, int S, int lane, fl
     wsum = warp_sum(wsum);
 }
 
+// A row of at most kN splits with D <= 128: the partial LSEs (one per lane)
+// and every partial-O chunk are loaded at once, so the row costs one round
+// trip; the same weights, sums and order as the general path.
+template <int kN, typename OutT>
+__device__ __forceinline__ void merge_row_at_once(const float* op, const float* lp, int S, int D, OutT* orow,
+                                                  float* lse, int row, int lane) {
+    const int d = 4 * lane;
+    const float l = lane < S ? lp[lane] : -INFINITY;
+    float4 v[kN];
+#pragma unroll
+    for (int u = 0; u < kN; ++u)
+        v[u] = (u < S && d < D) ? ld4(op + static_cast<size_t>(u) * D + d) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float mx = warp_max(l);
+    const bool alive = mx != -INFINITY;
+    const float w = (l == -INFINITY) ? 0.f : expf(l - mx);
+    const float wsum = warp_sum(w);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int u = 0; u < kN; ++u) {
+        const float wu = __shfl_sync(0xffffffffu, w, u);
+        if (wu != 0.f) {   // splits of weight 0 may hold any bits
+            acc.x = fmaf(wu, v[u].x, acc.x);
+            acc.y = fmaf(wu, v[u].y, acc.y);
+            acc.z = fmaf(wu, v[u].z, acc.z);
+            acc.w = fmaf(wu, v[u].w, acc.w);
+        }
+    }
+    const float inv = alive ? 1.f / wsum : 0.f;
+    if (d < D) store4(orow + d, make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
+    if (lse != nullptr && lane == 0) lse[row] = alive ? mx + logf(wsum) : -INFINITY;
+}
+
 template <typename OutT>
 __global__ void __launch_bounds__(32 * kWarps) lse_merge_kernel(const float* __restrict__ o_part,
                                                                 const float* __restrict__ lse_part, int N, int S,
@@ -98,33 +130,12 @@ __global__ void __launch_bounds__(32 * kWarps) lse_merge_kernel(const float* __r
     const float* lp = lse_part + static_cast<size_t>(row) * S;
     const float* op = o_part + static_cast<size_t>(row) * S * D;
     OutT* orow = o + static_cast<size_t>(row) * D;
-    if (S <= kFastSplits && D <= 128) {
-        // the row's partial LSEs (one per lane) and all its partial-O chunks are
-        // loaded together; the same weights, sums and order as the general path
-        const int d = 4 * lane;
-        const float l = lane < S ? lp[lane] : -INFINITY;
-        float4 v[kFastSplits];
-#pragma unroll
-        for (int u = 0; u < kFastSplits; ++u)
-            v[u] = (u < S && d < D) ? ld4(op + static_cast<size_t>(u) * D + d) : make_float4(0.f, 0.f, 0.f, 0.f);
-        const float mx = warp_max(l);
-        const bool alive = mx != -INFINITY;
-        const float w = (l == -INFINITY) ? 0.f : expf(l - mx);
-        const float wsum = warp_sum(w);
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int u = 0; u < kFastSplits; ++u) {
-            const float wu = __shfl_sync(0xffffffffu, w, u);
-            if (wu != 0.f) {   // splits of weight 0 may hold any bits
-                acc.x = fmaf(wu, v[u].x, acc.x);
-                acc.y = fmaf(wu, v[u].y, acc.y);
-                acc.z = fmaf(wu, v[u].z, acc.z);
-                acc.w = fmaf(wu, v[u].w, acc.w);
-            }
-        }
-        const float inv = alive ? 1.f / wsum : 0.f;
-        if (d < D) store4(orow + d, make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
-        if (lse != nullptr && lane == 0) lse[row] = alive ? mx + logf(wsum) : -INFINITY;
+    if (D <= 128 && S <= kFastSplits) {
+        merge_row_at_once<kFastSplits>(op, lp, S, D, orow, lse, row, lane);
+        return;
+    }
+    if (D <= 128 && S <= 32) {
+        merge_row_at_once<32>(op, lp, S, D, orow, lse, row, lane);
         return;
     }
     float mx, wsum;

@@ -7,9 +7,9 @@
 // O = 0 and LSE = -inf, and a split of weight 0 adds nothing whatever its O
 // holds.
 //
-// Arrival protocol (no waits): every CTA (or warp) that has written the
-// partials of its rows of a (sequence, KV head) makes them visible device-wide
-// (threadfence) and then adds 1 to that head's counter; the one that brings
+// Arrival protocol (no waits): every CTA that has written the partials of its
+// rows of a (sequence, KV head) makes them visible device-wide (its threads
+// meet, then one thread fences) and adds 1 to that head's counter; the one that brings
 // the counter to the number of expected arrivals reads everyone's partials
 // from L2, writes O and LSE and puts the counter back to 0, so a workspace
 // whose counters start at 0 is left at 0 by every call that completes.  A
@@ -25,11 +25,15 @@ namespace gb300 {
 // Arrival of a group of `nthreads` threads (whole warps, meeting at named
 // barrier `bar_id`, thread `leader` among them) on `counter`; true in every
 // one of them when this group arrived last.  `flag` is a shared word.
+// Only the leader fences: the barrier orders every thread's partials before
+// the leader's fence, a GPU-scope fence is cumulative (it orders what its
+// thread has observed through the barrier, not only its own writes), and the
+// fence orders them before the counter update that the last arriver reads.
 __device__ __forceinline__ bool split_arrive(int32_t* counter, int expected, int32_t* status, int* flag, int bar_id,
                                              int nthreads, int leader) {
-    __threadfence();
     named_barrier_sync(bar_id, nthreads);
     if (threadIdx.x == leader) {
+        __threadfence();
         const int old = atomicAdd(counter, 1);
         if (old >= expected) flag_status(status, ATTN_DEV_WORKSPACE_STATE);
         *flag = old == expected - 1;
@@ -40,30 +44,72 @@ __device__ __forceinline__ bool split_arrive(int32_t* counter, int expected, int
     return last;
 }
 
-// The same for one warp (lane 0 takes the ticket).
-__device__ __forceinline__ bool split_arrive_warp(int32_t* counter, int expected, int32_t* status, int lane) {
-    __threadfence();
-    __syncwarp();
-    int last = 0;
-    if (lane == 0) {
-        const int old = atomicAdd(counter, 1);
-        if (old >= expected) flag_status(status, ATTN_DEV_WORKSPACE_STATE);
-        last = old == expected - 1;
+// One row of a warp's merge, S <= 32 splits (lane j holds split j's LSE),
+// the partial O loaded kN splits at a time: one round trip per kN splits
+// (D = 128: four elements per lane).  Sums in split order, as
+// attn_lse_merge's do.
+template <int kN>
+__device__ __forceinline__ void merge_row_at_once(const float* o_part, const float* lse_part, int S, size_t row,
+                                                  __nv_bfloat16* o, float* lse, int lane) {
+    const float l = lane < S ? __ldcg(lse_part + row * S + lane) : -INFINITY;
+    float4 v[kN];
+#pragma unroll
+    for (int u = 0; u < kN; ++u)
+        v[u] = u < S ? __ldcg(reinterpret_cast<const float4*>(o_part + (row * S + u) * 128) + lane)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+    float mx = l;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    const float w = (l == -INFINITY || mx == -INFINITY) ? 0.f : expf(l - mx);
+    float wsum = w;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c0 = 0; c0 < S; c0 += kN) {
+        if (c0 > 0) {
+#pragma unroll
+            for (int u = 0; u < kN; ++u)
+                v[u] = c0 + u < S ? __ldcg(reinterpret_cast<const float4*>(o_part + (row * S + c0 + u) * 128) + lane)
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < kN; ++u) {
+            const float wu = __shfl_sync(0xffffffffu, w, (c0 + u) & 31);
+            if (c0 + u < S && wu != 0.f) {   // a split of weight 0 adds nothing, whatever its O holds
+                acc.x = fmaf(wu, v[u].x, acc.x);
+                acc.y = fmaf(wu, v[u].y, acc.y);
+                acc.z = fmaf(wu, v[u].z, acc.z);
+                acc.w = fmaf(wu, v[u].w, acc.w);
+            }
+        }
     }
-    last = __shfl_sync(0xffffffffu, last, 0);
-    if (last) __threadfence();
-    return last != 0;
+    const bool alive = mx != -INFINITY;
+    const float inv = alive ? 1.f / wsum : 0.f;
+    const __nv_bfloat162 a = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+    const __nv_bfloat162 b = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+    uint2 u2;
+    u2.x = *reinterpret_cast<const uint32_t*>(&a);
+    u2.y = *reinterpret_cast<const uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(o + row * 128 + 4 * lane) = u2;
+    if (lse != nullptr && lane == 0) lse[row] = alive ? mx + logf(wsum) : -INFINITY;
 }
 
 // One warp merges up to 4 partial rows row0 + k * stride (k < nr; D = 128:
 // four elements per lane) of o_part [rows][S][128] / lse_part [rows][S] into
 // o [rows][128] (bf16) and lse [rows] (may be NULL).  Partials are read through
-// L2 (other SMs wrote them); every load of a batch of 4 splits of all the rows
-// is issued before any is used, so a merge costs a few L2 round trips, and
-// the sums run in split order as attn_lse_merge's do.  Not inlined: its
-// registers do not add to the decode loop's.
+// L2 (other SMs wrote them).  Up to 32 splits, a row's partials are loaded
+// kN splits at a time (kN = 32: one round trip per row; kN = 16 keeps the
+// registers of kernels launched with fewer); more splits go in batches of 4
+// splits of all the rows, every load of a batch issued before any is used.
+// Either way the sums run in split order as attn_lse_merge's do.  Not
+// inlined: its registers do not add to the decode loop's.
+template <int kN>
 static __device__ __noinline__ void merge_rows_warp(const float* o_part, const float* lse_part, int S, size_t row0,
                                                     size_t stride, int nr, __nv_bfloat16* o, float* lse, int lane) {
+    if (S <= 32) {
+        for (int k = 0; k < nr; ++k) merge_row_at_once<kN>(o_part, lse_part, S, row0 + k * stride, o, lse, lane);
+        return;
+    }
     constexpr int kR = 4, kB = 4;
     float mx[kR], wsum[kR];
     float4 acc[kR];
@@ -148,11 +194,12 @@ struct FusedOut {
 
 // Rows [row0, row0 + n_rows) of a (sequence, KV head), merged by warps
 // warp, warp + n_warps, ... of the caller, up to four rows per pass.
+template <int kN = 16>
 __device__ __forceinline__ void merge_head(const float* o_part, const float* lse_part, int S, size_t row0, int n_rows,
                                            const FusedOut& f, int warp, int n_warps, int lane) {
     for (int r = warp; r < n_rows; r += 4 * n_warps)
-        merge_rows_warp(o_part, lse_part, S, row0 + r, n_warps, min(4, (n_rows - r + n_warps - 1) / n_warps), f.o,
-                        f.lse, lane);
+        merge_rows_warp<kN>(o_part, lse_part, S, row0 + r, n_warps, min(4, (n_rows - r + n_warps - 1) / n_warps),
+                            f.o, f.lse, lane);
 }
 
 // Fused tail of a decode CTA whose `nthreads` threads (warps 0.., meeting at

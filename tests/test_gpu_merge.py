@@ -11,8 +11,11 @@ from parity import check_lse, check_o, gpu_or_skip
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("n,s,d", [(1, 1, 128), (37, 5, 128), (300, 16, 128), (64, 3, 64), (9, 40, 1024), (5, 2, 4)])
+@pytest.mark.parametrize("n,s,d", [(1, 1, 128), (37, 5, 128), (300, 16, 128), (64, 3, 64), (9, 40, 1024), (5, 2, 4),
+                                   (200, 17, 128), (70, 19, 128), (33, 32, 128), (33, 33, 128), (21, 19, 64)])
 def test_merge_fp32_matches_oracle(n, s, d):
+    """Rows of up to 16 and of 17-32 splits (D <= 128) take the one-round-trip
+    paths; more splits, or wider rows, the batched one."""
     dev = gpu_or_skip()
     import causal_gqa_flashattention_attn_gb300 as attn
     o_part, lse_part = synth.merge_inputs(n, s, d, seed=n * 7 + s)
