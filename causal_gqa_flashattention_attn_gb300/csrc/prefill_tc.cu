@@ -2,7 +2,7 @@
 //
 // What it computes follows "causal_forward_kernel.py" (flash-attention-scratch),
 // _flash_attention_forward_gqa_kernel: Q tiles against streamed K/V tiles,
-// S = Q K^T scaled into the exp2 domain (qk_scale = softmax_scale * log2 e),
+// S = Q K^T times the softmax scale and log2(e), so that the exponentials are powers of 2,
 // an online softmax (running max m, running sum l, rescale by exp2(m_old -
 // m_new)), P rounded to bf16 before O += P V, skipping of tiles above the
 // causal diagonal and masking of the diagonal tiles only, then O = acc / l
