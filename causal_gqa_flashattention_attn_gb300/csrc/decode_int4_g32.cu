@@ -501,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_int4_g32_kernel(const __gr
             last_phase ^= 1u;
             if (volatile_load(&s_last)) {
                 __threadfence();
-                merge_head<16>(p.o_part, p.lse_part, p.n_split, out_row(0), n_rows, p.fused, 0, 1, lane);
+                merge_head(p.o_part, p.lse_part, p.n_split, out_row(0), n_rows, p.fused, 0, 1, lane);
             }
             return true;
         };

@@ -45,12 +45,12 @@ __device__ __forceinline__ bool split_arrive(int32_t* counter, int expected, int
 }
 
 // One row of a warp's merge, S <= 32 splits (lane j holds split j's LSE),
-// the partial O loaded kN splits at a time: one round trip per kN splits
-// (D = 128: four elements per lane).  Sums in split order, as
-// attn_lse_merge's do.
-template <int kN>
+// the partial O loaded kN = 16 splits at a time, all in flight together: one
+// round trip per 16 splits (D = 128: four elements per lane).  Sums in split
+// order, as attn_lse_merge's do.
 __device__ __forceinline__ void merge_row_at_once(const float* o_part, const float* lse_part, int S, size_t row,
                                                   __nv_bfloat16* o, float* lse, int lane) {
+    constexpr int kN = 16;
     const float l = lane < S ? __ldcg(lse_part + row * S + lane) : -INFINITY;
     float4 v[kN];
 #pragma unroll
@@ -97,17 +97,15 @@ __device__ __forceinline__ void merge_row_at_once(const float* o_part, const flo
 // One warp merges up to 4 partial rows row0 + k * stride (k < nr; D = 128:
 // four elements per lane) of o_part [rows][S][128] / lse_part [rows][S] into
 // o [rows][128] (bf16) and lse [rows] (may be NULL).  Partials are read through
-// L2 (other SMs wrote them).  Up to 32 splits, a row's partials are loaded
-// kN splits at a time (kN = 32: one round trip per row; kN = 16 keeps the
-// registers of kernels launched with fewer); more splits go in batches of 4
-// splits of all the rows, every load of a batch issued before any is used.
-// Either way the sums run in split order as attn_lse_merge's do.  Not
-// inlined: its registers do not add to the decode loop's.
-template <int kN>
+// L2 (other SMs wrote them).  Up to 32 splits, a row's partials are loaded 16
+// splits at a time; more splits go in batches of 4 splits of all the rows,
+// every load of a batch issued before any is used.  Either way the sums run in
+// split order as attn_lse_merge's do.  Not inlined: its registers do not add
+// to the decode loop's.
 static __device__ __noinline__ void merge_rows_warp(const float* o_part, const float* lse_part, int S, size_t row0,
                                                     size_t stride, int nr, __nv_bfloat16* o, float* lse, int lane) {
     if (S <= 32) {
-        for (int k = 0; k < nr; ++k) merge_row_at_once<kN>(o_part, lse_part, S, row0 + k * stride, o, lse, lane);
+        for (int k = 0; k < nr; ++k) merge_row_at_once(o_part, lse_part, S, row0 + k * stride, o, lse, lane);
         return;
     }
     constexpr int kR = 4, kB = 4;
@@ -194,12 +192,11 @@ struct FusedOut {
 
 // Rows [row0, row0 + n_rows) of a (sequence, KV head), merged by warps
 // warp, warp + n_warps, ... of the caller, up to four rows per pass.
-template <int kN = 16>
 __device__ __forceinline__ void merge_head(const float* o_part, const float* lse_part, int S, size_t row0, int n_rows,
                                            const FusedOut& f, int warp, int n_warps, int lane) {
     for (int r = warp; r < n_rows; r += 4 * n_warps)
-        merge_rows_warp<kN>(o_part, lse_part, S, row0 + r, n_warps, min(4, (n_rows - r + n_warps - 1) / n_warps),
-                            f.o, f.lse, lane);
+        merge_rows_warp(o_part, lse_part, S, row0 + r, n_warps, min(4, (n_rows - r + n_warps - 1) / n_warps), f.o,
+                        f.lse, lane);
 }
 
 // Fused tail of a decode CTA whose `nthreads` threads (warps 0.., meeting at
