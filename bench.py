@@ -85,9 +85,10 @@ def load_peaks():
 
 
 def filled_split(shape):
-    """The int4 and fp8 decode workloads fix no split size: take the one that
-    fills the GPU with whole waves of CTAs (attn_decode_split_tokens).  The
-    bf16 workload keeps its stated 2048."""
+    """The int4 and fp8 decode workloads fix no split size: take the library's
+    choice (attn_decode_split_tokens: for the persistent int4 kernel the split
+    that balances its CTAs, 864 tokens here; for fp8 the one that fills whole
+    waves of CTAs).  The bf16 workload keeps its stated 2048."""
     import causal_gqa_flashattention_attn_gb300 as attn
     if shape.kv_format not in ("int4", "fp8"):
         return shape
