@@ -180,7 +180,7 @@ attn_status_t varlen_impl(const void* q, const void* k_cache, const void* v_cach
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o)) return ATTN_ERR_INVALID_ARG;
     if (D != 128) return ATTN_ERR_UNSUPPORTED;
     const int G = Hq / Hkv;
-    if (G > 128 || 128 % G != 0) return ATTN_ERR_UNSUPPORTED;
+    if (G > 128) return ATTN_ERR_UNSUPPORTED;
     if (B > varlen_max_seqs()) return ATTN_ERR_UNSUPPORTED;
     if (static_cast<long long>(num_pages) * page_size >= (1LL << 31) - 1) return ATTN_ERR_UNSUPPORTED;
     // work items (query blocks x KV heads) are counted in int and a query
@@ -210,7 +210,7 @@ const char* attn_status_string(attn_status_t status) {
     }
 }
 
-int attn_abi_version(void) { return 109; }
+int attn_abi_version(void) { return 110; }
 
 attn_status_t attn_selftest_wait_timeout(int32_t* dev_status, unsigned int limit_us, void* stream) {
     if (dev_status == nullptr || limit_us == 0 || limit_us > 1000000u) return ATTN_ERR_INVALID_ARG;

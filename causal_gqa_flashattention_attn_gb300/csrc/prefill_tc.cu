@@ -12,9 +12,10 @@
 // fully-masked-row guard is that of "splitk_kernels.py", _fwd_kernel_splitK.
 //
 // GB300 design:
-//   * GQA packing: a 128-row Q tile holds P = 128/G consecutive query
+//   * GQA packing: a 128-row Q tile holds P = floor(128/G) consecutive query
 //     positions for each of the G query heads that share one KV head, so every
-//     K/V tile brought on chip serves the whole group;
+//     K/V tile brought on chip serves the whole group (when G does not divide
+//     128, the last 128 - P G rows are never loaded and never stored);
 //   * a CTA owns two such tiles (2P positions) and one KV head: the two
 //     softmax warpgroups ping-pong so the tensor core always has work;
 //   * warp roles: warps 0-3 softmax of tile 0, warps 4-7 softmax of tile 1,
@@ -519,6 +520,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t kv_iter = 0, item_iter = 0;
         bool ok = true;
         // this thread's row of item `it`: query position, head, output row
+        // rows past P G are padding when G does not divide 128: never stored
+        const bool row_used = r < p.P * p.G;
         auto row_of = [&](const Item& it, int& pos, size_t& row_id) {
             // head-major rows for the dense layout, position-major rows for
             // the ragged [total_q, Hq, D] layout
@@ -540,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int pos;
                 size_t row_id;
                 row_of(dense_item(p, k / zq, k % zq), pos, row_id);
-                if (pos < p.q_len) write_empty(row_id);
+                if (row_used && pos < p.q_len) write_empty(row_id);
             }
         }
         Walker wk = walk_begin();
@@ -549,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int pos;
             size_t row_id;
             row_of(it, pos, row_id);
-            const bool row_real = pos < it.q_len;
+            const bool row_real = row_used && pos < it.q_len;
             if (it.n_kv == 0) {
                 if (row_real) write_empty(row_id);
                 continue;
@@ -849,7 +852,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (Item it; ok && walk_next(wk, it);) {
                     if (it.n_kv == 0) continue;
                     if (item_iter > 0 && !(ok = wait(&q_empty, (item_iter - 1) & 1))) break;
-                    mbar_arrive_expect_tx(&q_full, 2 * kTile);
+                    mbar_arrive_expect_tx(&q_full, 2 * p.P * p.G * 256);
                     for (int t = 0; t < 2; ++t)
                         for (int h = 0; h < 2; ++h)
                             tma_load_3d(smem + kOffQ + t * kTile + h * kHalf, &q_map, &q_full, h * 64,
@@ -894,7 +897,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) {
                     if (item_iter > 0) ok = wait(&q_empty, (item_iter - 1) & 1);
                     if (ok) {
-                        mbar_arrive_expect_tx(&q_full, 2 * kTile);
+                        mbar_arrive_expect_tx(&q_full, 2 * p.P * p.G * 256);
                         for (int t = 0; t < 2; ++t)
                             for (int h = 0; h < 2; ++h)
                                 tma_load_3d(smem + kOffQ + t * kTile + h * kHalf, &q_map, &q_full, h * 64,
@@ -964,7 +967,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (Item it; ok && walk_next(wk, it);) {
                     if (it.n_kv == 0) continue;
                     if (item_iter > 0 && !(ok = wait(&q_empty, (item_iter - 1) & 1))) break;
-                    mbar_arrive_expect_tx(&q_full, 2 * kTile);
+                    mbar_arrive_expect_tx(&q_full, 2 * p.P * p.G * 256);
                     const int head0 = it.b * p.Hq + it.kvh * p.G;
                     for (int t = 0; t < 2; ++t)
                         for (int h = 0; h < 2; ++h)
@@ -1243,7 +1246,7 @@ int prefill_tc_plan(const PrefillArgs& a, int sms, int* grid) {
 bool prefill_tc_supported(const PrefillArgs& a) {
     if (a.dtype != ATTN_BF16 || a.D != kD) return false;
     const int G = a.Hq / a.Hkv;
-    if (G < 1 || G > 128 || (128 % G) != 0) return false;
+    if (G < 1 || G > 128) return false;
     return true;
 }
 

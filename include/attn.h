@@ -73,9 +73,9 @@ typedef enum {
  *   v    [B, Hkv, kv_len, D]  dtype            (read)
  *   o    [B, Hq,  q_len,  D]  dtype            (written)
  *   lse  [B, Hq,  q_len]      float32, natural log (written; may be NULL)
- *   dtype   ATTN_BF16 (tensor-core path; D = 128 needs Hq/Hkv to divide 128,
- *           other shapes use the CUDA-core path) or ATTN_F32 (exact fp32
- *           CUDA-core path, no TF32).
+ *   dtype   ATTN_BF16 (tensor-core path for D = 128 and Hq/Hkv <= 128; D = 64
+ *           uses the CUDA-core path) or ATTN_F32 (exact fp32 CUDA-core path,
+ *           no TF32).
  *   D       64 or 128.
  *   scale   softmax scale; pass 1/sqrt(D) for the usual attention.
  *   Requires Hq % Hkv == 0, all sizes > 0.
@@ -222,7 +222,7 @@ int attn_decode_split_tokens_balanced_for(int sms, int B, int head_groups, int m
  *                (NULL: every page full); kv_len_b = (pages_b - 1) *
  *                page_size + last_b                                  (read, device)
  *   o            [total_q, Hq, D] bfloat16; lse [total_q, Hq] fp32 (written; lse may be NULL)
- *   D = 128, Hq / Hkv dividing 128, B <= 2048, total_q < 2^22 and
+ *   D = 128, Hq / Hkv <= 128, B <= 2048, total_q < 2^22 and
  *   (total_q + B) * Hkv < 2^31 (ATTN_ERR_UNSUPPORTED otherwise).
  * A page id outside [0, num_pages) sets ATTN_DEV_PAGE_OUT_OF_RANGE and is
  * read as zeros.
@@ -499,7 +499,8 @@ const char* attn_status_string(attn_status_t status);
  * 106 attn_prefill_plan_sms, attn_decode_split_tokens_for.
  * 107 attn_decode_split_tokens_balanced_for; bad decode pages are left out.
  * 108 attn_decode_paged_fused, attn_decode_fused_workspace_bytes.
- * 109 32-token splits for the persistent int4 decode; the balanced split takes a tile. */
+ * 109 32-token splits for the persistent int4 decode; the balanced split takes a tile.
+ * 110 the tensor-core prefill takes any Hq / Hkv up to 128 (not only divisors of 128). */
 int attn_abi_version(void);
 
 #ifdef __cplusplus

@@ -39,7 +39,7 @@ def test_library_exports_every_declared_symbol(L):
     for name in declared_functions():
         assert hasattr(L, name), name
         assert name in attn.EXPORTED
-    assert L.attn_abi_version() == 109
+    assert L.attn_abi_version() == 110
 
 
 def test_status_strings(L):
@@ -179,7 +179,7 @@ def test_varlen_host_validation(L):
     assert _varlen(L, scale=float("inf")) == -1
     assert _varlen(L, o=ctypes.c_void_p(0x10008)) == -1   # misaligned
     assert _varlen(L, D=64) == -2
-    assert _varlen(L, Hq=24, Hkv=8) == -2                 # group of 3 does not divide 128
+    assert _varlen(L, Hq=129, Hkv=1) == -2                # a group of more than 128 heads
     assert _varlen(L, B=2049) == -2                       # prefix table holds 2048 sequences
     assert _varlen(L, total_q=1 << 22) == -2              # query block index packed in 21 bits
     assert _varlen(L, Hq=1024, Hkv=1024, total_q=(1 << 21) + 1) == -2   # item count overflows int

@@ -62,6 +62,11 @@ BF16_CASES = [
     (1, 8, 1, 1, 333),      # a single query row
     (1, 8, 2, 260, 120),    # q_len > kv_len: the first rows see no key
     (3, 8, 8, 64, 64),      # G = 1, short
+    (1, 28, 4, 300, 500),   # G = 7: 18 positions x 7 heads = 126 of the 128 tile rows
+    (2, 12, 4, 200, 200),   # G = 3: 42 x 3 = 126 rows
+    (1, 20, 4, 150, 350),   # G = 5: 25 x 5 = 125 rows
+    (1, 24, 4, 140, 100),   # G = 6, q_len > kv_len
+    (1, 100, 1, 5, 300),    # G = 100: one position per tile, 28 rows unused
 ]
 
 

@@ -19,6 +19,8 @@ CASES = [
     (8, 8, 1, [260, 5], [300, 5]),                           # G = 1
     (32, 2, 256, [100, 500], [1000, 700]),                   # G = 16, large pages
     (32, 4, 1, [90, 10], [40, 10]),                          # q_len > kv_len: early rows see nothing
+    (28, 4, 16, [300, 19, 40], [500, 19, 300]),              # G = 7: 18 positions x 7 heads per tile
+    (12, 4, 1, [100, 43], [260, 43]),                        # G = 3: 42 x 3 rows
 ]
 
 

@@ -33,6 +33,7 @@ def test_prefill_schedule_of_the_benchmark_workloads(attn):
 @pytest.mark.parametrize("b,hq,hkv,lq,lk", [
     (1, 32, 4, 2048, 4096), (8, 32, 8, 4096, 4096), (1, 8, 1, 512, 65536), (1, 8, 2, 160, 1100),
     (2, 16, 4, 33, 4000), (1, 8, 2, 900, 500), (3, 8, 8, 64, 64), (1, 128, 1, 777, 1500), (1, 4, 4, 1, 1),
+    (1, 28, 4, 2048, 4096), (2, 24, 8, 300, 300), (1, 100, 1, 90, 700),   # groups of 7, 3, 100
 ])
 def test_prefill_schedule_bounds(attn, sms, b, hq, hkv, lq, lk):
     """Whatever the choice, the grid is at least one CTA and at most one per
@@ -51,7 +52,10 @@ def test_prefill_schedule_refusals(attn):
     assert attn.attn_prefill_plan_sms(BF16, 1, 32, 5, 2048, 4096, 128, 152) == (-1, 0)    # Hq % Hkv
     assert attn.attn_prefill_plan_sms(BF16, 0, 32, 4, 2048, 4096, 128, 152) == (-1, 0)
     assert attn.attn_prefill_plan_sms(torch.float32, 1, 4, 2, 128, 128, 64, 152) == (0, 0)  # CUDA-core path
-    assert attn.attn_prefill_plan_sms(BF16, 1, 6, 2, 128, 128, 128, 152) == (0, 0)          # G = 3: CUDA cores
+    assert attn.attn_prefill_plan_sms(BF16, 1, 4, 2, 128, 128, 64, 152) == (0, 0)           # D = 64: CUDA cores
+    # a group of 3 heads takes the tensor cores: P = 42 positions per tile, 2 blocks of 84
+    kind, grid = attn.attn_prefill_plan_sms(BF16, 1, 6, 2, 128, 128, 128, 152)
+    assert kind in (0, 1) and grid > 0
 
 
 def _waves(units, n, slots):
