@@ -91,6 +91,7 @@ struct Params {
     float* lse;
     int32_t* status;
     int B, Hq, Hkv, q_len, kv_len, G, P, n_qb, n_items;
+    int halves;   // 64-column halves of a head's row, D / 64 (dense: 1 or 2; ragged: 2)
     int sec_bh;   // whole items: (batch, KV head) pairs per section of the order (their K/V fits in L2)
     float scale_log2;
     // ragged batch over a paged cache (varlen mode only)
@@ -438,6 +439,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(&tmem_base_sh, kTmemCols);
         tmem_relinquish();
     }
+    if (!kVarlen && p.halves == 1) {
+        // D = 64: the tiles' second 64-column halves are never loaded; zeros
+        // there leave S = Q K^T and P V as they are (the MMAs run at D = 128)
+        static_assert(kStages == 2, "six tiles: two Q, two K, two V");
+        constexpr int kVecs = kHalf / 16;
+        for (int i = threadIdx.x; i < 6 * kVecs; i += kThreads) {
+            const int tile = i / kVecs;   // Q0, Q1, K0, K1, V0, V1: consecutive 32 KB tiles from kOffQ
+            *reinterpret_cast<uint4*>(smem + kOffQ + tile * kTile + kHalf + (i % kVecs) * 16) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();   // generic-proxy writes -> the tensor core's reads
+    }
     int n_items = p.n_items;
     if constexpr (kVarlen) {
         if (warp == 0) {
@@ -531,9 +543,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                              : (static_cast<size_t>(it.b) * p.Hq + head) * p.q_len + pos;
         };
         // a row that sees no key: O = 0, LSE = -inf
+        const int d_out = 64 * p.halves;   // D: the row stride of O
         auto write_empty = [&](size_t row_id) {
-            uint4* orow = reinterpret_cast<uint4*>(p.o + row_id * kD);
-            for (int c = 0; c < kD / 8; ++c) orow[c] = make_uint4(0, 0, 0, 0);
+            uint4* orow = reinterpret_cast<uint4*>(p.o + row_id * d_out);
+            for (int c = 0; c < d_out / 8; ++c) orow[c] = make_uint4(0, 0, 0, 0);
             if (p.lse != nullptr) p.lse[row_id] = -INFINITY;
         };
         if constexpr (kSplit) {
@@ -700,6 +713,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const bool tile_real = it.p0 + t * p.P < p.q_len;
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {
+                            if (h >= p.halves) break;
                             if (r == 0) bulk_wait_read_all();   // the stage's last store has read it
                             mbar_arrive(&epi_bar[t]);
                             if (!(ok = wait(&epi_bar[t], 0))) break;
@@ -788,9 +802,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const bool alive = lsum > 0.f;
                 const float inv = alive ? 1.f / lsum : 0.f;
-                uint4* orow = reinterpret_cast<uint4*>(p.o + row_id * kD);
+                uint4* orow = reinterpret_cast<uint4*>(p.o + row_id * d_out);
 #pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < 2 * p.halves; ++c) {
                     uint32_t orr[32];
                     tmem_ld32(o_addr + 32 * c, orr);
                     tmem_ld_wait();
@@ -967,10 +981,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (Item it; ok && walk_next(wk, it);) {
                     if (it.n_kv == 0) continue;
                     if (item_iter > 0 && !(ok = wait(&q_empty, (item_iter - 1) & 1))) break;
-                    mbar_arrive_expect_tx(&q_full, 2 * p.P * p.G * 256);
+                    mbar_arrive_expect_tx(&q_full, 2 * p.P * p.G * 128 * p.halves);
                     const int head0 = it.b * p.Hq + it.kvh * p.G;
                     for (int t = 0; t < 2; ++t)
-                        for (int h = 0; h < 2; ++h)
+                        for (int h = 0; h < p.halves; ++h)
                             tma_load_3d(smem + kOffQ + t * kTile + h * kHalf, &q_map, &q_full, h * 64, it.p0 + t * p.P,
                                         head0);
                     const int kvrow = it.b * p.Hkv + it.kvh;
@@ -978,13 +992,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int s = kv_iter % kStages;
                         const uint32_t par = ((kv_iter / kStages) - 1) & 1;
                         if (kv_iter >= kStages && !(ok = wait(&k_empty[s], par))) break;
-                        mbar_arrive_expect_tx(&k_full[s], kTile);
+                        mbar_arrive_expect_tx(&k_full[s], kHalf * p.halves);
                         tma_load_3d(smem + kOffK + s * kTile, &k_map, &k_full[s], 0, j * kBN, kvrow);
-                        tma_load_3d(smem + kOffK + s * kTile + kHalf, &k_map, &k_full[s], 64, j * kBN, kvrow);
+                        if (p.halves == 2)
+                            tma_load_3d(smem + kOffK + s * kTile + kHalf, &k_map, &k_full[s], 64, j * kBN, kvrow);
                         if (kv_iter >= kStages && !(ok = wait(&v_empty[s], par))) break;
-                        mbar_arrive_expect_tx(&v_full[s], kTile);
+                        mbar_arrive_expect_tx(&v_full[s], kHalf * p.halves);
                         tma_load_3d(smem + kOffV + s * kTile, &v_map, &v_full[s], 0, j * kBN, kvrow);
-                        tma_load_3d(smem + kOffV + s * kTile + kHalf, &v_map, &v_full[s], 64, j * kBN, kvrow);
+                        if (p.halves == 2)
+                            tma_load_3d(smem + kOffV + s * kTile + kHalf, &v_map, &v_full[s], 64, j * kBN, kvrow);
                     }
                     ++item_iter;
                 }
@@ -1203,7 +1219,7 @@ size_t round16(size_t x) { return (x + 15) & ~static_cast<size_t>(15); }
 // section (all pairs, the plain longest-first order).
 constexpr double kSectionBytes = 64.0 * (1 << 20);
 int section_pairs(const PrefillArgs& a, int n_qb, int grid) {
-    const double kv_pair = 2.0 * a.kv_len * kD * 2;   // K and V of one pair, bf16
+    const double kv_pair = 2.0 * a.kv_len * a.D * 2;   // K and V of one pair, bf16
     const int bh = a.B * a.Hkv;
     const int most = static_cast<int>(kSectionBytes / kv_pair);
     if (most >= bh) return bh;
@@ -1244,7 +1260,7 @@ int prefill_tc_plan(const PrefillArgs& a, int sms, int* grid) {
 }
 
 bool prefill_tc_supported(const PrefillArgs& a) {
-    if (a.dtype != ATTN_BF16 || a.D != kD) return false;
+    if (a.dtype != ATTN_BF16 || (a.D != kD && a.D != 64)) return false;
     const int G = a.Hq / a.Hkv;
     if (G < 1 || G > 128) return false;
     return true;
@@ -1253,18 +1269,19 @@ bool prefill_tc_supported(const PrefillArgs& a) {
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream) {
     const int G = a.Hq / a.Hkv;
     const int P = kBM / G;
+    const uint64_t D = static_cast<uint64_t>(a.D);   // 128, or 64 (loaded into the first half of each tile)
     CUtensorMap q_map, k_map, v_map;
     {
-        const uint64_t dims[3] = {kD, static_cast<uint64_t>(a.q_len), static_cast<uint64_t>(a.B) * a.Hq};
-        const uint64_t strides[2] = {kD * 2, static_cast<uint64_t>(a.q_len) * kD * 2};
+        const uint64_t dims[3] = {D, static_cast<uint64_t>(a.q_len), static_cast<uint64_t>(a.B) * a.Hq};
+        const uint64_t strides[2] = {D * 2, static_cast<uint64_t>(a.q_len) * D * 2};
         const uint32_t box[3] = {64, static_cast<uint32_t>(P), static_cast<uint32_t>(G)};
         if (!encode_tiled_map(&q_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.q, dims, strides, box,
                               CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
     }
     {
-        const uint64_t dims[3] = {kD, static_cast<uint64_t>(a.kv_len), static_cast<uint64_t>(a.B) * a.Hkv};
-        const uint64_t strides[2] = {kD * 2, static_cast<uint64_t>(a.kv_len) * kD * 2};
+        const uint64_t dims[3] = {D, static_cast<uint64_t>(a.kv_len), static_cast<uint64_t>(a.B) * a.Hkv};
+        const uint64_t strides[2] = {D * 2, static_cast<uint64_t>(a.kv_len) * D * 2};
         const uint32_t box[3] = {64, kBN, 1};
         if (!encode_tiled_map(&k_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.k, dims, strides, box,
                               CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -1274,8 +1291,8 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream) {
     }
     CUtensorMap o_map;   // O [B * Hq, q_len, D]: the Q map's geometry over the output
     {
-        const uint64_t dims[3] = {kD, static_cast<uint64_t>(a.q_len), static_cast<uint64_t>(a.B) * a.Hq};
-        const uint64_t strides[2] = {kD * 2, static_cast<uint64_t>(a.q_len) * kD * 2};
+        const uint64_t dims[3] = {D, static_cast<uint64_t>(a.q_len), static_cast<uint64_t>(a.B) * a.Hq};
+        const uint64_t strides[2] = {D * 2, static_cast<uint64_t>(a.q_len) * D * 2};
         const uint32_t box[3] = {64, static_cast<uint32_t>(P), static_cast<uint32_t>(G)};
         if (!encode_tiled_map(&o_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.o, dims, strides, box,
                               CU_TENSOR_MAP_SWIZZLE_128B))
@@ -1294,6 +1311,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream) {
     p.P = P;
     p.n_qb = (a.q_len + 2 * P - 1) / (2 * P);
     p.n_items = a.B * a.Hkv * p.n_qb;
+    p.halves = a.D / 64;
     p.scale_log2 = a.scale * kLog2e;
     p.qo_indptr = p.kv_indptr = p.kv_indices = p.kv_last = nullptr;
     p.k_pool = p.v_pool = nullptr;
@@ -1356,6 +1374,7 @@ cudaError_t launch_prefill_varlen_tc(const VarlenArgs& a, cudaStream_t stream) {
     p.P = P;
     p.n_qb = 0;
     p.n_items = 0;   // counted on the device from qo_indptr
+    p.halves = 2;
     p.sec_bh = 1;
     p.scale_log2 = a.scale * kLog2e;
     p.qo_indptr = a.qo_indptr;

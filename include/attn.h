@@ -73,9 +73,9 @@ typedef enum {
  *   v    [B, Hkv, kv_len, D]  dtype            (read)
  *   o    [B, Hq,  q_len,  D]  dtype            (written)
  *   lse  [B, Hq,  q_len]      float32, natural log (written; may be NULL)
- *   dtype   ATTN_BF16 (tensor-core path for D = 128 and Hq/Hkv <= 128; D = 64
- *           uses the CUDA-core path) or ATTN_F32 (exact fp32 CUDA-core path,
- *           no TF32).
+ *   dtype   ATTN_BF16 (tensor-core path for Hq/Hkv <= 128, larger groups use
+ *           the CUDA-core path) or ATTN_F32 (exact fp32 CUDA-core path, no
+ *           TF32).
  *   D       64 or 128.
  *   scale   softmax scale; pass 1/sqrt(D) for the usual attention.
  *   Requires Hq % Hkv == 0, all sizes > 0.
@@ -500,7 +500,7 @@ const char* attn_status_string(attn_status_t status);
  * 107 attn_decode_split_tokens_balanced_for; bad decode pages are left out.
  * 108 attn_decode_paged_fused, attn_decode_fused_workspace_bytes.
  * 109 32-token splits for the persistent int4 decode; the balanced split takes a tile.
- * 110 the tensor-core prefill takes any Hq / Hkv up to 128 (not only divisors of 128). */
+ * 110 the tensor-core prefill takes any Hq / Hkv up to 128 (not only divisors of 128), and D = 64. */
 int attn_abi_version(void);
 
 #ifdef __cplusplus

@@ -92,16 +92,30 @@ def test_bf16_sharp_softmax_k_scaled():
     check_lse(lse, lse_ref)
 
 
-def test_bf16_head_dim_64_cuda_core_path():
-    shape = replace(synth.LLAMA_GQA_PREFILL, B=1, Hq=4, Hkv=2, q_len=150, kv_len=200, D=64)
-    (q, k, v), o, lse = _run(shape, seed=1)
+D64_CASES = [
+    # (B, Hq, Hkv, q_len, kv_len) at D = 64: the tiles' second halves stay zero
+    (1, 4, 2, 150, 200),    # G = 2
+    (2, 32, 4, 300, 500),   # G = 8, several blocks and a ragged tail
+    (1, 8, 8, 129, 129),    # G = 1
+    (1, 28, 4, 100, 60),    # G = 7, q_len > kv_len
+    (1, 16, 1, 40, 700),    # G = 16, long KV
+]
+
+
+@pytest.mark.parametrize("entry", ["plain", "ws"])
+@pytest.mark.parametrize("bsz,hq,hkv,lq,lk", D64_CASES)
+def test_bf16_head_dim_64_tensor_core_path(bsz, hq, hkv, lq, lk, entry):
+    shape = replace(synth.LLAMA_GQA_PREFILL, B=bsz, Hq=hq, Hkv=hkv, q_len=lq, kv_len=lk, D=64)
+    (q, k, v), o, lse = _run(shape, seed=lq + 3, entry=entry)
     o_ref, lse_ref = oracle.prefill(_np(q), _np(k), _np(v))
     check_o(o, o_ref)
     check_lse(lse, lse_ref)
 
 
-def test_bf16_group_of_three_cuda_core_path():
-    shape = replace(synth.LLAMA_GQA_PREFILL, B=1, Hq=6, Hkv=2, q_len=90, kv_len=150)
+def test_bf16_group_over_128_cuda_core_path():
+    """More than 128 query heads per KV head do not fit a tile's rows: the
+    CUDA-core path."""
+    shape = replace(synth.LLAMA_GQA_PREFILL, B=1, Hq=256, Hkv=1, q_len=20, kv_len=50)
     (q, k, v), o, lse = _run(shape, seed=2)
     o_ref, lse_ref = oracle.prefill(_np(q), _np(k), _np(v))
     check_o(o, o_ref)

@@ -52,7 +52,8 @@ def test_prefill_schedule_refusals(attn):
     assert attn.attn_prefill_plan_sms(BF16, 1, 32, 5, 2048, 4096, 128, 152) == (-1, 0)    # Hq % Hkv
     assert attn.attn_prefill_plan_sms(BF16, 0, 32, 4, 2048, 4096, 128, 152) == (-1, 0)
     assert attn.attn_prefill_plan_sms(torch.float32, 1, 4, 2, 128, 128, 64, 152) == (0, 0)  # CUDA-core path
-    assert attn.attn_prefill_plan_sms(BF16, 1, 4, 2, 128, 128, 64, 152) == (0, 0)           # D = 64: CUDA cores
+    assert attn.attn_prefill_plan_sms(BF16, 1, 256, 1, 128, 128, 128, 152) == (0, 0)        # G = 256: CUDA cores
+    assert attn.attn_prefill_plan_sms(BF16, 1, 4, 2, 128, 128, 64, 152) == (0, 2)           # D = 64: tensor cores, 2 items
     # a group of 3 heads takes the tensor cores: P = 42 positions per tile, 2 blocks of 84
     kind, grid = attn.attn_prefill_plan_sms(BF16, 1, 6, 2, 128, 128, 128, 152)
     assert kind in (0, 1) and grid > 0
