@@ -45,12 +45,12 @@ __device__ __forceinline__ bool split_arrive(int32_t* counter, int expected, int
 }
 
 // One row of a warp's merge, S <= 32 splits (lane j holds split j's LSE),
-// the partial O loaded kN = 16 splits at a time, all in flight together: one
-// round trip per 16 splits (D = 128: four elements per lane).  Sums in split
+// the partial O loaded kN splits at a time, all in flight together: one
+// round trip per kN splits (D = 128: four elements per lane).  Sums in split
 // order, as attn_lse_merge's do.
+template <int kN>
 __device__ __forceinline__ void merge_row_at_once(const float* o_part, const float* lse_part, int S, size_t row,
                                                   __nv_bfloat16* o, float* lse, int lane) {
-    constexpr int kN = 16;
     const float l = lane < S ? __ldcg(lse_part + row * S + lane) : -INFINITY;
     float4 v[kN];
 #pragma unroll
@@ -97,15 +97,19 @@ __device__ __forceinline__ void merge_row_at_once(const float* o_part, const flo
 // One warp merges up to 4 partial rows row0 + k * stride (k < nr; D = 128:
 // four elements per lane) of o_part [rows][S][128] / lse_part [rows][S] into
 // o [rows][128] (bf16) and lse [rows] (may be NULL).  Partials are read through
-// L2 (other SMs wrote them).  Up to 32 splits, a row's partials are loaded 16
-// splits at a time; more splits go in batches of 4 splits of all the rows,
-// every load of a batch issued before any is used.  Either way the sums run in
+// L2 (other SMs wrote them).  Up to 24 splits, a row's partials are loaded in
+// one round trip, up to 32 in rounds of 16; more splits go in batches of 4
+// splits of all the rows, every load of a batch issued before any is used.  Either way the sums run in
 // split order as attn_lse_merge's do.  Not inlined: its registers do not add
 // to the decode loop's.
 static __device__ __noinline__ void merge_rows_warp(const float* o_part, const float* lse_part, int S, size_t row0,
                                                     size_t stride, int nr, __nv_bfloat16* o, float* lse, int lane) {
+    if (S <= 24) {
+        for (int k = 0; k < nr; ++k) merge_row_at_once<24>(o_part, lse_part, S, row0 + k * stride, o, lse, lane);
+        return;
+    }
     if (S <= 32) {
-        for (int k = 0; k < nr; ++k) merge_row_at_once(o_part, lse_part, S, row0 + k * stride, o, lse, lane);
+        for (int k = 0; k < nr; ++k) merge_row_at_once<16>(o_part, lse_part, S, row0 + k * stride, o, lse, lane);
         return;
     }
     constexpr int kR = 4, kB = 4;
