@@ -391,7 +391,11 @@ __device__ __forceinline__ int cta_item(int i) {
 // 128-byte-swizzled tile layout (TMA tile loads need contiguous rows).
 // kSplit (dense only): the split schedule, where an item whose KV tiles are
 // cut between CTAs is finished by the piece that ends last (see the epilogue).
-template <bool kVarlen, bool kSplit>
+// kD64 (dense, D = 64): the tiles hold only their first 64-column half, so
+// S = Q K^T takes that half's 4 K steps and P.V runs at N = 64 (an
+// instantiation of its own: the D = 128 kernels' MMA-issuing loop is left as
+// it is, which the tensor core's rate is sensitive to).
+template <bool kVarlen, bool kSplit, bool kD64 = false>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap k_map,
                       const __grid_constant__ CUtensorMap v_map, const __grid_constant__ CUtensorMap o_map,
@@ -440,8 +444,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_relinquish();
     }
     if (!kVarlen && p.halves == 1) {
-        // D = 64: the tiles' second 64-column halves are never loaded; zeros
-        // there leave S = Q K^T and P V as they are (the MMAs run at D = 128)
+        // D = 64: the tiles' second 64-column halves are never loaded, and the
+        // kD64 kernel's MMAs never read them; they are zeroed all the same
         static_assert(kStages == 2, "six tiles: two Q, two K, two V");
         constexpr int kVecs = kHalf / 16;
         for (int i = threadIdx.x; i < 6 * kVecs; i += kThreads) {
@@ -1012,7 +1016,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // before the tensor core reads them; TMA-written tiles do not
                 const bool cp_async_tiles = kVarlen && !p.gathered;
                 constexpr uint32_t idesc_qk = idesc_bf16_f32(kBM, kBN, false);
-                constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, kD, true);
+                constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, kD64 ? 64 : kD, true);
                 // This one thread issues every MMA of the CTA, so its instruction
                 // count per MMA bounds the tensor core: the descriptors' low words
                 // are built once and an MMA only adds a constant start-address
@@ -1025,7 +1029,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t d = tmem + kColS + 128 * t;
                     umma_ss_lo<0>(d, dq, dk, idesc_qk);
     #pragma unroll
-                    for (int kk = 1; kk < kD / 16; ++kk) {
+                    for (int kk = 1; kk < (kD64 ? 4 : kD / 16); ++kk) {
                         const uint32_t off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
                         umma_ss_lo<1>(d, dq + off, dk + off, idesc_qk);
                     }
@@ -1333,17 +1337,17 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream) {
         p.sk_count = reinterpret_cast<int32_t*>(w);
         p.sk_o = reinterpret_cast<float*>(w + prefill_tc_counter_bytes(a));
         p.sk_ml = p.sk_o + static_cast<size_t>(2) * sms * 2 * kD * kBM;
-        cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<false, true>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        auto kern = p.halves == 1 ? prefill_tc_kernel<false, true, true> : prefill_tc_kernel<false, true>;
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         if (e != cudaSuccess) return e;
-        prefill_tc_kernel<false, true><<<pl.grid, kThreads, smem, stream>>>(q_map, k_map, v_map, o_map, p);
+        kern<<<pl.grid, kThreads, smem, stream>>>(q_map, k_map, v_map, o_map, p);
         return cudaGetLastError();
     }
     const int grid = p.n_items < sms ? p.n_items : sms;
-    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    auto kern = p.halves == 1 ? prefill_tc_kernel<false, false, true> : prefill_tc_kernel<false, false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    prefill_tc_kernel<false, false><<<grid, kThreads, smem, stream>>>(q_map, k_map, v_map, o_map, p);
+    kern<<<grid, kThreads, smem, stream>>>(q_map, k_map, v_map, o_map, p);
     return cudaGetLastError();
 }
 
