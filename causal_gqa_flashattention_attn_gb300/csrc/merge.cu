@@ -39,6 +39,23 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// Sums over the warp of 16 per-lane values at once: each butterfly step
+// halves the values a lane holds (it keeps one half and adds its partner's
+// copy of that half), 8 + 4 + 2 + 1 shuffles, and a last one joins the two
+// lanes that share a value.  Lanes 2u and 2u + 1 return the sum of value u.
+__device__ __forceinline__ float warp_sum16(const float (&v)[16], int lane) {
+    float a[8], b[4], c[2];
+    const bool u16 = lane & 16, u8 = lane & 8, u4 = lane & 4, u2 = lane & 2;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a[i] = (u16 ? v[i + 8] : v[i]) + __shfl_xor_sync(0xffffffffu, u16 ? v[i] : v[i + 8], 16);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) b[i] = (u8 ? a[i + 4] : a[i]) + __shfl_xor_sync(0xffffffffu, u8 ? a[i] : a[i + 4], 8);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) c[i] = (u4 ? b[i + 2] : b[i]) + __shfl_xor_sync(0xffffffffu, u4 ? b[i] : b[i + 2], 4);
+    float d = (u2 ? c[1] : c[0]) + __shfl_xor_sync(0xffffffffu, u2 ? c[0] : c[1], 2);
+    return d + __shfl_xor_sync(0xffffffffu, d, 1);
+}
+
 constexpr int kBatch = 8;   // splits whose loads are in flight together
 constexpr int kFastSplits = 16;   // rows of at most this many splits load everything at once
 
@@ -197,18 +214,23 @@ __global__ void __launch_bounds__(32 * kWarps) lse_merge_bwd_kernel(
         const float4 o = make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
         const float lse = alive ? mx + logf(wsum) : -INFINITY;
         const float wl = (alive && l != -INFINITY) ? expf(l - lse) : 0.f;   // lane s: weight of split s
+        // per split, this lane's share of sum_d (O_s - O)_d dO_d; splits past S
+        // (zero O, weight 0) give 0
+        float dot[kFastSplits];
 #pragma unroll
         for (int u = 0; u < kFastSplits; ++u) {
-            if (u >= S) break;   // S is the same in every lane
             const float wu = __shfl_sync(0xffffffffu, wl, u);
             const float4 x = wu != 0.f ? v[u] : o;
-            const float dot = (x.x - o.x) * g.x + (x.y - o.y) * g.y + (x.z - o.z) * g.z + (x.w - o.w) * g.w;
-            if (d < D)
+            dot[u] = (x.x - o.x) * g.x + (x.y - o.y) * g.y + (x.z - o.z) * g.z + (x.w - o.w) * g.w;
+            if (u < S && d < D)
                 *reinterpret_cast<float4*>(dop + static_cast<size_t>(u) * D + d) =
                     make_float4(wu * g.x, wu * g.y, wu * g.z, wu * g.w);
-            const float t = warp_sum(dot);
-            if (lane == 0) dlp[u] = wu * (dl + t);
         }
+        static_assert(kFastSplits == 16, "warp_sum16 reduces 16 values");
+        const float t = warp_sum16(dot, lane);   // lanes 2u, 2u + 1: split u
+        const int u = lane >> 1;
+        const float wu = __shfl_sync(0xffffffffu, wl, u);
+        if ((lane & 1) == 0 && u < S) dlp[u] = wu * (dl + t);
         return;
     }
     float mx, wsum;
