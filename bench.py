@@ -86,9 +86,9 @@ def load_peaks():
 
 def filled_split(shape):
     """The int4 and fp8 decode workloads fix no split size: take the library's
-    choice (attn_decode_split_tokens: for the persistent int4 kernel the split
-    that balances its CTAs, 864 tokens here; for fp8 the one that fills whole
-    waves of CTAs).  The bf16 workload keeps its stated 2048."""
+    choice (attn_decode_split_tokens: for the persistent int4 and fp8 kernels
+    the split that balances their CTAs, 864 tokens here).  The bf16 workload
+    keeps its stated 2048."""
     import causal_gqa_flashattention_attn_gb300 as attn
     if shape.kv_format not in ("int4", "fp8"):
         return shape
@@ -611,7 +611,7 @@ def run_ours(args, rank, world, dist):
                             unit="GB/s", work=mqb, src="decode.cu", kernel="decode_bf16_kernel (q_len 4)")
     fp8b = decode_bytes(d8, lens8)["kernel"]
     rep["decode_fp8"] = dict(bound="hbm", achieved=fp8b / (ms["decode_fp8"] * 1e-3) / 1e9, peak=peaks["hbm_gbs"],
-                             unit="GB/s", work=fp8b, src="decode_fp8.cu", kernel="decode_fp8_kernel")
+                             unit="GB/s", work=fp8b, src="decode_fp8_g32.cu", kernel="decode_fp8_g32_kernel")
     rep["prefill_varlen"] = dict(bound="tensor", achieved=vl_flops / (ms["prefill_varlen"] * 1e-3) / 1e12,
                                  peak=peaks["bf16_tflops"], unit="TFLOP/s", work=vl_flops, src="prefill_tc.cu",
                                  kernel="prefill_tc_kernel (ragged, paged)")

@@ -115,11 +115,12 @@ attn_status_t decode_impl(const void* q, const void* k_cache, const void* v_cach
     const int G = Hq / Hkv;
     if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return ATTN_ERR_UNSUPPORTED;
     if (q_len > 16) return ATTN_ERR_UNSUPPORTED;
-    // the persistent int4 kernel (N_GROUPS 4, Hkv a multiple of 8, at most 8 rows
-    // per KV head) takes splits in 32-token steps, the others in 64-token steps
-    const bool int4_g32 = kv_dtype == ATTN_INT4_PACKED && n_groups == 4 && D == 128 && Hkv % 8 == 0 &&
-                          G * q_len <= 8;
-    if (page_size % 64 != 0 || split_tokens % (int4_g32 ? 32 : 64) != 0) return ATTN_ERR_UNSUPPORTED;
+    // the persistent int4 and fp8 kernels (int4 with N_GROUPS 4; Hkv a multiple
+    // of 8, at most 8 rows per KV head) take splits in 32-token steps, the
+    // others in 64-token steps
+    const bool tile32 = ((kv_dtype == ATTN_INT4_PACKED && n_groups == 4) || kv_dtype == ATTN_FP8_E4M3) && D == 128 &&
+                        Hkv % 8 == 0 && G * q_len <= 8;
+    if (page_size % 64 != 0 || split_tokens % (tile32 ? 32 : 64) != 0) return ATTN_ERR_UNSUPPORTED;
     if (static_cast<long long>(num_pages) * page_size >= (1LL << 31)) return ATTN_ERR_UNSUPPORTED;
     int fmt = 0;
     if (kv_dtype == ATTN_BF16) {
@@ -410,7 +411,7 @@ int attn_decode_split_tokens(attn_dtype_t kv_dtype, int n_groups, int B, int Hq,
     a.Hkv = Hkv;
     a.D = D;
     a.q_len = q_len;
-    if (fmt == 1 && decode_int4_g32_shape_ok(a))
+    if ((fmt == 1 && decode_int4_g32_shape_ok(a)) || (fmt == 2 && decode_fp8_g32_shape_ok(a)))
         return attn_decode_split_tokens_balanced_for(device_sm_count(), B, Hkv / 8, max_kv_len, 32);
     int occ = 0;
     const cudaError_t e = (fmt == 2) ? launch_decode_fp8(a, nullptr, nullptr, nullptr, &occ)

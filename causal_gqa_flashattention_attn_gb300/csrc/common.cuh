@@ -68,6 +68,12 @@ cudaError_t launch_decode_int4(const DecodeArgs& a, cudaStream_t stream, int* oc
 bool decode_int4_g32_shape_ok(const DecodeArgs& a);   // shape only (no page or split size)
 bool decode_int4_g32_supported(const DecodeArgs& a);
 cudaError_t launch_decode_int4_g32(const DecodeArgs& a, cudaStream_t stream, int* occ = nullptr);
+// fp8 rows, KV head counts that are multiples of 8 and at most 8 (query, head)
+// rows per KV head: the persistent kernel of decode_fp8_g32.cu.
+bool decode_fp8_g32_shape_ok(const DecodeArgs& a);   // shape only (no page or split size)
+bool decode_fp8_g32_supported(const DecodeArgs& a);
+cudaError_t launch_decode_fp8_g32(const DecodeArgs& a, const void* k_scale_shift, const void* v_scale_shift,
+                                  cudaStream_t stream, int* occ = nullptr);
 cudaError_t launch_decode_fp8(const DecodeArgs& a, const void* k_scale_shift, const void* v_scale_shift,
                               cudaStream_t stream, int* occ = nullptr);
 int rows_per_cta(const DecodeArgs& a);

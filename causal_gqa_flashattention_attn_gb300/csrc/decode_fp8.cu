@@ -464,6 +464,7 @@ cudaError_t launch_r(const DecodeArgs& a, const void* k_ss, const void* v_ss, cu
 
 cudaError_t launch_decode_fp8(const DecodeArgs& a, const void* k_scale_shift, const void* v_scale_shift,
                               cudaStream_t stream, int* occ) {
+    if (decode_fp8_g32_supported(a)) return launch_decode_fp8_g32(a, k_scale_shift, v_scale_shift, stream, occ);
     switch (rows_per_cta(a)) {
         case 1: return launch_r<1>(a, k_scale_shift, v_scale_shift, stream, occ);
         case 2: return launch_r<2>(a, k_scale_shift, v_scale_shift, stream, occ);

@@ -360,37 +360,6 @@ __device__ __forceinline__ Unit unit_of(const Params& p, int u, bool flag) {
     return w;
 }
 
-// Fused mode, after a unit: the 8 warps have written their rows of the unit's
-// (sequence, head group); the CTA counts itself in once (on `cnt`) and, if its
-// split is the last to arrive, every warp merges its own head's rows.  The
-// warps' partials are ordered before warp 0's fence by the warp barrier and the
-// CTA's mbarrier; that one fence (cumulative) makes them visible device-wide
-// before the count.  Kept out of line so the decode loop's registers do not
-// carry any of it.
-static __device__ __noinline__ bool fused_tail_fn(FusedOut f, const float* o_part, const float* lse_part, int n_split,
-                                                  int32_t* status, int32_t* cnt, size_t row0, int n_rows, uint32_t ph,
-                                                  uint64_t* unit_bar, uint64_t* last_bar, int* s_last,
-                                                  const int* s_abort, int warp, int lane) {
-    __syncwarp();
-    if (lane == 0) mbar_arrive(unit_bar);
-    if (!mbar_wait(unit_bar, ph, s_abort)) return false;
-    if (warp == 0 && lane == 0) {
-        __threadfence();
-        const int old = atomicAdd(cnt, 1);
-        if (old >= n_split) flag_status(status, ATTN_DEV_WORKSPACE_STATE);
-        const bool last = old == n_split - 1;
-        if (last) atomicExch(cnt, 0);
-        *s_last = last;
-        mbar_arrive(last_bar);
-    }
-    if (!mbar_wait(last_bar, ph, s_abort)) return false;
-    if (volatile_load(s_last)) {
-        __threadfence();
-        merge_head(o_part, lse_part, n_split, row0, n_rows, f, 0, 1, lane);
-    }
-    return true;
-}
-
 template <bool kFused>
 __global__ void __launch_bounds__(kThreads, 1) decode_int4_g32_kernel(const __grid_constant__ CUtensorMap k_map,
                                                                       const __grid_constant__ CUtensorMap v_map,
@@ -504,13 +473,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_int4_g32_kernel(const __gr
             const int i = r / p.G, h = r % p.G;
             return (static_cast<size_t>(w.b) * p.Hq + kvh * p.G + h) * p.nq + i;
         };
-        // fused mode: fused_tail_fn after every unit (an empty split included),
+        // fused mode: unit_fused_tail after every unit (an empty split included),
         // so its barriers' phase is the parity of the units this CTA took before
         auto fused_tail = [&]() -> bool {
             if constexpr (!kFused) return true;
             const uint32_t ph = static_cast<uint32_t>((u - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x)) & 1u;
             int32_t* cnt = p.fused.counters + static_cast<size_t>(w.b) * p.Hkv + w.hg * kHeads;
-            return fused_tail_fn(p.fused, p.o_part, p.lse_part, p.n_split, p.status, cnt, out_row(0), n_rows, ph,
+            return unit_fused_tail(p.fused, p.o_part, p.lse_part, p.n_split, p.status, cnt, out_row(0), n_rows, ph,
                                  &unit_bar, &last_bar, &s_last, &s_abort, warp, lane);
         };
         if (w.n_tiles == 0) {   // empty split: O = 0, LSE = -inf

@@ -19,6 +19,7 @@
 #include <cuda_bf16.h>
 
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace gb300 {
 
@@ -216,6 +217,40 @@ __device__ __forceinline__ void fused_tail_cta(const FusedOut& f, int n_arrivals
         merge_head(o_part, lse_part, S, row0, G * nq, f, threadIdx.x >> 5, nthreads >> 5, threadIdx.x & 31);
         if (threadIdx.x == 0) atomicExch(cnt, 0);
     }
+}
+
+// Fused mode of a persistent decode whose CTA takes one unit (sequence, split,
+// group of KV heads) at a time, one warp per KV head: after a unit the warps
+// have written their rows of the unit's (sequence, head group); the CTA counts
+// itself in once (on `cnt`) and, if its split is the last to arrive, every warp
+// merges its own head's rows.  `ph` is the phase of the CTA's `unit_bar` (all
+// of its warps arrive) and `last_bar` (warp 0 arrives) for this unit.  The
+// warps' partials are ordered before warp 0's fence by the warp barrier and the
+// CTA's mbarrier; that one fence (cumulative) makes them visible device-wide
+// before the count.  Kept out of line so the decode loop's registers do not
+// carry any of it.
+static __device__ __noinline__ bool unit_fused_tail(FusedOut f, const float* o_part, const float* lse_part,
+                                                    int n_split, int32_t* status, int32_t* cnt, size_t row0,
+                                                    int n_rows, uint32_t ph, uint64_t* unit_bar, uint64_t* last_bar,
+                                                    int* s_last, const int* s_abort, int warp, int lane) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(unit_bar);
+    if (!mbar_wait(unit_bar, ph, s_abort)) return false;
+    if (warp == 0 && lane == 0) {
+        __threadfence();
+        const int old = atomicAdd(cnt, 1);
+        if (old >= n_split) flag_status(status, ATTN_DEV_WORKSPACE_STATE);
+        const bool last = old == n_split - 1;
+        if (last) atomicExch(cnt, 0);
+        *s_last = last;
+        mbar_arrive(last_bar);
+    }
+    if (!mbar_wait(last_bar, ph, s_abort)) return false;
+    if (*reinterpret_cast<const volatile int*>(s_last) != 0) {
+        __threadfence();
+        merge_head(o_part, lse_part, n_split, row0, n_rows, f, 0, 1, lane);
+    }
+    return true;
 }
 
 }  // namespace gb300

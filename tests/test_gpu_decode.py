@@ -219,14 +219,14 @@ def test_full_size_paged_decode_int4_sampled():
 def test_split_tokens_fills_the_gpu():
     """attn_decode_split_tokens on the int4 and fp8 workloads (16 sequences x
     8 KV heads, 16384 tokens): a multiple of 64 (32 for the persistent int4
-    kernel) whose CTA count is not the 2.25 waves of 2048-token splits, and
-    never more pieces than tiles."""
+    and fp8 kernels) whose CTA count is not the 2.25 waves of 2048-token
+    splits, and never more pieces than tiles."""
     gpu_or_skip()
     import causal_gqa_flashattention_attn_gb300 as attn
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     for fmt in ("int4", "fp8", "bf16"):
         split = attn.attn_decode_split_tokens(fmt, 16, 32, 8, 16384, n_groups=4)
-        assert split > 0 and split % (32 if fmt == "int4" else 64) == 0 and split <= 16384
+        assert split > 0 and split % (32 if fmt in ("int4", "fp8") else 64) == 0 and split <= 16384
         ctas = 16 * 8 * -(-16384 // split)
         assert ctas >= sms
     assert attn.attn_decode_split_tokens("int4", 16, 32, 8, 16384, n_groups=3) == 0

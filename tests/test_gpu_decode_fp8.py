@@ -24,6 +24,11 @@ CASES = [
     (32, 8, 9, 256, 512, [900, 30]),         # multi-query, 36 rows in 3 groups
     (16, 8, 1, 128, 256, [600, 129]),        # G = 2, page 128
     (64, 4, 1, 256, 1024, [1500, 99]),       # G = 16
+    # the persistent kernel (Hkv a multiple of 8, at most 8 rows): 32-token
+    # split steps, two queries of 4 heads (8 rows), two groups of 8 KV heads
+    (32, 8, 1, 64, 96, [0, 65, 200, 31, 97]),
+    (32, 8, 2, 256, 512, [700, 3, 2]),
+    (64, 16, 1, 256, 512, [900, 40]),
 ]
 
 

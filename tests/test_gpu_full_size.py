@@ -82,7 +82,7 @@ def _decode_whole(shape, fused=False):
     if shape.kv_format in ("int4", "fp8"):
         split = attn.attn_decode_split_tokens(shape.kv_format, shape.B, shape.Hq, shape.Hkv, shape.len_hi,
                                               n_groups=shape.n_groups, D=shape.D)
-        assert split > 0 and split % (32 if shape.kv_format == "int4" else 64) == 0
+        assert split > 0 and split % (32 if shape.kv_format in ("int4", "fp8") else 64) == 0
         shape = replace(shape, split_tokens=split)
     inp = synth.decode_inputs(shape, seed=0)
     lens = inp["lens"]
