@@ -211,7 +211,7 @@ const char* attn_status_string(attn_status_t status) {
     }
 }
 
-int attn_abi_version(void) { return 110; }
+int attn_abi_version(void) { return 111; }
 
 attn_status_t attn_selftest_wait_timeout(int32_t* dev_status, unsigned int limit_us, void* stream) {
     if (dev_status == nullptr || limit_us == 0 || limit_us > 1000000u) return ATTN_ERR_INVALID_ARG;
@@ -467,7 +467,8 @@ size_t attn_decode_fused_workspace_bytes(int B, int Hq, int Hkv, int q_len, int 
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || q_len <= 0 || Hq % Hkv != 0) return 0;
     const size_t partials = attn_decode_workspace_bytes(B, Hq * q_len, max_kv_len, split_tokens, D);
     if (partials == 0) return 0;
-    return partials + round16(static_cast<size_t>(B) * Hkv * sizeof(int32_t));
+    // the arrival counters, then the three words of the cooperative kernels' grid barrier
+    return partials + round16((static_cast<size_t>(B) * Hkv + 3) * sizeof(int32_t));
 }
 
 attn_status_t attn_decode_paged_fused(const void* q, const void* k_cache, const void* v_cache,

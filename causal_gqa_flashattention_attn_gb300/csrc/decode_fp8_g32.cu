@@ -309,7 +309,10 @@ __device__ __forceinline__ Unit unit_of(const Params& p, int u, bool flag) {
     return w;
 }
 
-template <bool kFused>
+// kMode 0: partials only; 1: fused, the split that arrives last merges its
+// (sequence, head group); 2: fused, cooperative launch, the whole grid merges
+// every row once all CTAs have passed a grid barrier.
+template <int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_fp8_g32_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
                           const __grid_constant__ CUtensorMap kw_map, const __grid_constant__ CUtensorMap vw_map,
@@ -326,6 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ __align__(8) uint64_t unit_bar;   // fused mode: the consumer warps have written a unit
     __shared__ __align__(8) uint64_t last_bar;   // fused mode: warp 0 has counted the CTA in
     __shared__ int s_last;                       // fused mode: this CTA's split arrived last
+    __shared__ __align__(8) uint64_t exit_bar;   // cooperative mode: the consumer warps are done
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_rows = p.G * p.nq;    // <= 8 (query, head) rows per KV head
@@ -340,6 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&q_empty, kConsumers);
         mbar_init(&unit_bar, kConsumers);
         mbar_init(&last_bar, 1);
+        mbar_init(&exit_bar, kConsumers);
         s_abort = 0;
         fence_mbar_init();
     }
@@ -430,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // fused mode: unit_fused_tail after every unit (an empty split included),
         // so its barriers' phase is the parity of the units this CTA took before
         auto fused_tail = [&]() -> bool {
-            if constexpr (!kFused) return true;
+            if constexpr (kMode != 1) return true;
             const uint32_t ph = static_cast<uint32_t>((u - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x)) & 1u;
             int32_t* cnt = p.fused.counters + static_cast<size_t>(w.b) * p.Hkv + w.hg * kHeads;
             return unit_fused_tail(p.fused, p.o_part, p.lse_part, p.n_split, p.status, cnt, out_row(0), n_rows, ph,
@@ -565,6 +570,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
         }
     }
+    if constexpr (kMode == 2) {
+        // every consumer warp of the CTA is done (bounded meeting); one thread
+        // meets the grid, then every warp merges its share of the rows
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&exit_bar);
+        if (threadIdx.x == 0)
+            s_last = mbar_wait(&exit_bar, 0, &s_abort) && volatile_load(&s_abort) == 0 &&
+                     grid_barrier_once(p.fused.counters + p.B * p.Hkv, p.status);
+        if (threadIdx.x == 0) mbar_arrive(&last_bar);
+        if (mbar_wait(&last_bar, 0, &s_abort) && volatile_load(&s_last))
+            grid_merge(p.o_part, p.lse_part, p.n_split, p.B * p.Hq * p.nq, p.fused, warp, kConsumers, lane);
+    }
 }
 
 }  // namespace
@@ -582,7 +599,7 @@ bool decode_fp8_g32_supported(const DecodeArgs& a) {
 cudaError_t launch_decode_fp8_g32(const DecodeArgs& a, const void* k_scale_shift, const void* v_scale_shift,
                                   cudaStream_t stream, int* occ) {
     const size_t smem = kStages * kStageBytes + kQBytes + 1024;
-    auto kern = a.counters != nullptr ? decode_fp8_g32_kernel<true> : decode_fp8_g32_kernel<false>;
+    auto kern = a.counters != nullptr ? decode_fp8_g32_kernel<1> : decode_fp8_g32_kernel<0>;
     if (occ != nullptr) {
         int ctas = 0;
         const cudaError_t e = ctas_per_sm(kern, kThreads, smem, &ctas);
@@ -636,11 +653,32 @@ cudaError_t launch_decode_fp8_g32(const DecodeArgs& a, const void* k_scale_shift
     p.fused.counters = a.counters;
     p.fused.o = static_cast<__nv_bfloat16*>(a.o_final);
     p.fused.lse = a.lse_final;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
     const int sms = device_sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
     const int grid = p.n_units < sms ? p.n_units : sms;
+    cudaError_t e;
+    if (a.counters != nullptr) {
+        // fused: a cooperative launch (every CTA resident at once) lets the whole
+        // grid merge after one grid barrier; if it is refused, the split that
+        // arrives last merges its (sequence, head group)
+        e = cudaFuncSetAttribute(decode_fp8_g32_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = stream;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, decode_fp8_g32_kernel<2>, k_map, v_map, kw_map, vw_map, p);
+        if (e != cudaErrorCooperativeLaunchTooLarge) return e;
+        (void)cudaGetLastError();
+    }
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
     kern<<<grid, kThreads, smem, stream>>>(k_map, v_map, kw_map, vw_map, p);
     return cudaGetLastError();
 }

@@ -253,4 +253,59 @@ static __device__ __noinline__ bool unit_fused_tail(FusedOut f, const float* o_p
     return true;
 }
 
+// Cooperative fused mode of a persistent decode (launched with the
+// cooperative attribute, so every CTA of the grid is resident at once): after
+// its last unit each CTA sends one thread to a grid barrier made of three words
+// of the workspace, zero between launches.  w[0] counts arrivals; the last to
+// arrive raises w[1] (release); each CTA that passes counts itself out in
+// w[2], and the last to leave puts all three back to zero (no CTA reads them
+// after it has left).  Every CTA fences its partials before arriving, the
+// waiters acquire w[1], so after the barrier every partial of the launch can be
+// read.  A count found out of its range (a workspace that was not zeroed)
+// sets ATTN_DEV_WORKSPACE_STATE and that CTA gives up the merge; the wait is
+// bounded (ATTN_DEV_WAIT_TIMEOUT).  Either leaves words set: the caller must
+// zero the workspace again.  Returns whether the barrier was passed.
+__device__ __forceinline__ bool grid_barrier_once(int32_t* w, int32_t* status) {
+    const int n = static_cast<int>(gridDim.x);
+    __threadfence();
+    const int a = atomicAdd(&w[0], 1);
+    if (a < 0 || a >= n) {
+        flag_status(status, ATTN_DEV_WORKSPACE_STATE);
+        return false;
+    }
+    if (a == n - 1) {
+        __threadfence();
+        if (atomicExch(&w[1], 1) != 0) flag_status(status, ATTN_DEV_WORKSPACE_STATE);
+    } else {
+        const uint64_t t0 = global_ns();
+        while (ld_acquire_gpu(&w[1]) == 0) {
+            if (global_ns() - t0 > kWaitLimitNs) {
+                flag_status(status, ATTN_DEV_WAIT_TIMEOUT);
+                return false;
+            }
+            __nanosleep(64);
+        }
+    }
+    __threadfence();
+    const int d = atomicAdd(&w[2], 1);
+    if (d < 0 || d >= n) {
+        flag_status(status, ATTN_DEV_WORKSPACE_STATE);
+    } else if (d == n - 1) {
+        atomicExch(&w[0], 0);
+        atomicExch(&w[1], 0);
+        atomicExch(&w[2], 0);
+    }
+    return true;
+}
+
+// The merge of every row of the launch, spread over all the grid's warps
+// (`warp` of `n_warps` per CTA): rows [0, n_rows) of o_part / lse_part, row r
+// to warp r / gridDim.x of CTA r mod gridDim.x, so every SM takes a share.
+__device__ __forceinline__ void grid_merge(const float* o_part, const float* lse_part, int S, int n_rows,
+                                           const FusedOut& f, int warp, int n_warps, int lane) {
+    const int g = static_cast<int>(gridDim.x);
+    for (int r = warp * g + static_cast<int>(blockIdx.x); r < n_rows; r += n_warps * g)
+        merge_rows_warp(o_part, lse_part, S, static_cast<size_t>(r), 1, 1, f.o, f.lse, lane);
+}
+
 }  // namespace gb300

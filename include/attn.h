@@ -368,6 +368,12 @@ attn_status_t attn_decode_paged_splitk_fp8(const void* q, const void* k_cache, c
  * M = max_s LSE_s, w_s = exp(LSE_s - M), O = sum_s w_s O_s / sum_s w_s,
  * LSE = M + log sum_s w_s; O = 0 and LSE = -inf when every LSE_s is -inf).
  * No CTA waits for another: arrival is counted, and the last arrival merges.
+ * The persistent int4 and fp8 kernels (KV head counts that are multiples of 8,
+ * at most 8 rows per KV head) are launched cooperatively instead, every CTA
+ * resident at once: after its last split each CTA meets the others at one
+ * grid barrier (a bounded wait; ATTN_DEV_WAIT_TIMEOUT if it runs out), and then
+ * every warp of the grid merges a share of the rows.  If the device refuses
+ * the cooperative launch, they fall back to the last-arrival merge.
  *
  *   kv_dtype       ATTN_BF16, ATTN_INT4_PACKED (with n_groups) or
  *                  ATTN_FP8_E4M3 (with k_scale_shift / v_scale_shift, as for
@@ -377,10 +383,11 @@ attn_status_t attn_decode_paged_splitk_fp8(const void* q, const void* k_cache, c
  *   workspace      >= attn_decode_fused_workspace_bytes(...) bytes: the split
  *                  partials (layout as for attn_decode_paged_splitk with
  *                  Hq * q_len rows per sequence), then one int32 arrival
- *                  counter per (sequence, KV head).  The counters must be 0
- *                  when a call starts: zero the workspace once; every call
- *                  that completes without a device error leaves them 0
- *                  again (so a replayed CUDA graph needs no re-zeroing).  A
+ *                  counter per (sequence, KV head) and three int32 words of
+ *                  the grid barrier.  The counters and words must be 0 when a
+ *                  call starts: zero the workspace once; every call that
+ *                  completes without a device error leaves them 0 again (so a
+ *                  replayed CUDA graph needs no re-zeroing).  A
  *                  counter found past its range sets ATTN_DEV_WORKSPACE_STATE.
  *                  Calls that share a workspace must not overlap on the GPU.
  *   o              [B, Hq, q_len, D] bfloat16 (written, required); lse
@@ -500,7 +507,8 @@ const char* attn_status_string(attn_status_t status);
  * 107 attn_decode_split_tokens_balanced_for; bad decode pages are left out.
  * 108 attn_decode_paged_fused, attn_decode_fused_workspace_bytes.
  * 109 32-token splits for the persistent int4 decode; the balanced split takes a tile.
- * 110 the tensor-core prefill takes any Hq / Hkv up to 128 (not only divisors of 128), and D = 64. */
+ * 110 the tensor-core prefill takes any Hq / Hkv up to 128 (not only divisors of 128), and D = 64.
+ * 111 the fused decode's workspace holds three more words (the cooperative grid merge). */
 int attn_abi_version(void);
 
 #ifdef __cplusplus

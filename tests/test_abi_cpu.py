@@ -39,7 +39,7 @@ def test_library_exports_every_declared_symbol(L):
     for name in declared_functions():
         assert hasattr(L, name), name
         assert name in attn.EXPORTED
-    assert L.attn_abi_version() == 110
+    assert L.attn_abi_version() == 111
 
 
 def test_status_strings(L):
@@ -277,9 +277,9 @@ def test_decode_fused_host_validation(L):
     assert _decode_fused(L, ws=None) == -3
     partial = attn.attn_decode_workspace_bytes(2, 32, 1024, 512, 128)
     fused = attn.attn_decode_fused_workspace_bytes(2, 32, 8, 1024, 512, 128)
-    assert fused == partial + 64                                  # 2 x 8 int32 counters
+    assert fused == partial + 80          # 2 x 8 int32 counters and 3 grid-barrier words, rounded to 16 bytes
     assert attn.attn_decode_fused_workspace_bytes(2, 32, 8, 1024, 512, 128, q_len=4) == \
-        attn.attn_decode_workspace_bytes(2, 128, 1024, 512, 128) + 64
+        attn.attn_decode_workspace_bytes(2, 128, 1024, 512, 128) + 80
     assert _decode_fused(L, ws_bytes=partial) == -3               # room for the partials only
     assert attn.attn_decode_fused_workspace_bytes(2, 12, 8, 1024, 512, 128) == 0
 
