@@ -41,7 +41,7 @@ ATTN_DEV_WORKSPACE_STATE = 0x8
 
 EXPORTED = ("attn_prefill_fwd", "attn_prefill_workspace_bytes", "attn_prefill_plan", "attn_prefill_plan_sms", "attn_prefill_fwd_ws", "attn_prefill_host_workspace_bytes", "attn_prefill_fwd_host", "attn_prefill_paged_varlen", "attn_prefill_varlen_workspace_bytes",
             "attn_prefill_paged_varlen_ws", "attn_decode_workspace_bytes", "attn_decode_split_tokens", "attn_decode_split_tokens_for", "attn_decode_split_tokens_balanced_for", "attn_decode_paged_splitk", "attn_decode_paged_splitk_mq",
-            "attn_decode_paged_splitk_fp8", "attn_decode_paged_fused", "attn_decode_fused_workspace_bytes",
+            "attn_decode_paged_splitk_fp8", "attn_decode_paged_fused", "attn_decode_fused_workspace_bytes", "attn_decode_cooperative",
             "attn_decode_paged_splitk_static", "attn_lse_merge", "attn_lse_merge_bwd", "attn_selftest_wait_timeout",
             "attn_status_string", "attn_abi_version")
 ATTN_DECODE_STATIC_SCRATCH_BYTES = 32 << 20
@@ -122,8 +122,17 @@ def lib():
     L.attn_status_string.restype = ctypes.c_char_p
     L.attn_abi_version.argtypes = []
     L.attn_abi_version.restype = i32
+    L.attn_decode_cooperative.argtypes = [i32]
+    L.attn_decode_cooperative.restype = i32
     _lib = L
     return L
+
+
+def attn_decode_cooperative(enable=None):
+    """Allow (True) or forbid (False) cooperative launches in the fused
+    decodes, process-wide; None only reads the setting.  Returns the setting
+    before the call."""
+    return bool(lib().attn_decode_cooperative(-1 if enable is None else int(bool(enable))))
 
 
 def attn_status_string(status):

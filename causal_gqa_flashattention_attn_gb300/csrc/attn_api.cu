@@ -5,6 +5,7 @@
 // Hq % Hkv assertion of "causal_forward_kernel.py" flash_attention_forward,
 // the shape checks of "gpt-o3 / triton6fd1ef" run, and the static_asserts of
 // "splitk_kernels.py" _fwd_kernel_splitK (N_GROUPS in {1, 2, 4, 8}).
+#include <atomic>
 #include <cudaTypedefs.h>
 
 #include <cmath>
@@ -51,6 +52,10 @@ bool encode_tiled_map(CUtensorMap* map, CUtensorMapDataType dtype, int rank, con
                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
+
+std::atomic<int> g_cooperative{1};
+
+bool cooperative_launch_enabled() { return g_cooperative.load(std::memory_order_relaxed) != 0; }
 
 int device_sm_count() {
     int dev = 0;
@@ -211,7 +216,12 @@ const char* attn_status_string(attn_status_t status) {
     }
 }
 
-int attn_abi_version(void) { return 111; }
+int attn_abi_version(void) { return 112; }
+
+int attn_decode_cooperative(int enable) {
+    if (enable < 0) return g_cooperative.load();
+    return g_cooperative.exchange(enable != 0 ? 1 : 0);
+}
 
 attn_status_t attn_selftest_wait_timeout(int32_t* dev_status, unsigned int limit_us, void* stream) {
     if (dev_status == nullptr || limit_us == 0 || limit_us > 1000000u) return ATTN_ERR_INVALID_ARG;

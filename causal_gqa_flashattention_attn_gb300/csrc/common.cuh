@@ -36,6 +36,8 @@ bool encode_tiled_map(CUtensorMap* map, CUtensorMapDataType dtype, int rank, con
                       CUtensorMapSwizzle swizzle);
 
 int device_sm_count();
+// Whether the fused decodes may use cooperative launches (attn_decode_cooperative).
+bool cooperative_launch_enabled();
 
 // Launchers (return a cudaError_t from the launch).
 struct DecodeArgs {

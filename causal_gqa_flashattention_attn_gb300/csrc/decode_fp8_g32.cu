@@ -657,7 +657,7 @@ cudaError_t launch_decode_fp8_g32(const DecodeArgs& a, const void* k_scale_shift
     if (sms <= 0) return cudaErrorInvalidDevice;
     const int grid = p.n_units < sms ? p.n_units : sms;
     cudaError_t e;
-    if (a.counters != nullptr) {
+    if (a.counters != nullptr && cooperative_launch_enabled()) {
         // fused: a cooperative launch (every CTA resident at once) lets the whole
         // grid merge after one grid barrier; if it is refused, the split that
         // arrives last merges its (sequence, head group)

@@ -698,7 +698,7 @@ cudaError_t launch_decode_int4_g32(const DecodeArgs& a, cudaStream_t stream, int
     if (sms <= 0) return cudaErrorInvalidDevice;
     const int grid = p.n_units < sms ? p.n_units : sms;
     cudaError_t e;
-    if (a.counters != nullptr) {
+    if (a.counters != nullptr && cooperative_launch_enabled()) {
         // fused: a cooperative launch (every CTA resident at once) lets the whole
         // grid merge after one grid barrier; if it is refused, the split that
         // arrives last merges its (sequence, head group)

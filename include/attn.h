@@ -393,6 +393,12 @@ attn_status_t attn_decode_paged_splitk_fp8(const void* q, const void* k_cache, c
  *   o              [B, Hq, q_len, D] bfloat16 (written, required); lse
  *                  [B, Hq, q_len] fp32 (written, may be NULL)
  * Other arguments, limits and errors as the entries named above.
+ *
+ * attn_decode_cooperative - whether attn_decode_paged_fused may use
+ * cooperative launches (process-wide, default on).  enable = 1 allows them,
+ * 0 makes every fused decode use the last-arrival merge (for callers whose
+ * device or sharing mode refuses cooperative launches, or to compare the
+ * two), -1 only reads the setting.  Returns the setting before the call.
  */
 size_t attn_decode_fused_workspace_bytes(int B, int Hq, int Hkv, int q_len, int max_kv_len, int split_tokens,
                                          int D);
@@ -403,6 +409,7 @@ attn_status_t attn_decode_paged_fused(const void* q, const void* k_cache, const 
                                       int num_pages, int page_size, int split_tokens, int max_kv_len, float scale,
                                       void* workspace, size_t workspace_bytes, void* o, float* lse,
                                       int32_t* dev_status, void* stream);
+int attn_decode_cooperative(int enable);
 
 /*
  * attn_decode_paged_splitk_static - attn_decode_paged_splitk without a workspace.
@@ -508,7 +515,8 @@ const char* attn_status_string(attn_status_t status);
  * 108 attn_decode_paged_fused, attn_decode_fused_workspace_bytes.
  * 109 32-token splits for the persistent int4 decode; the balanced split takes a tile.
  * 110 the tensor-core prefill takes any Hq / Hkv up to 128 (not only divisors of 128), and D = 64.
- * 111 the fused decode's workspace holds three more words (the cooperative grid merge). */
+ * 111 the fused decode's workspace holds three more words (the cooperative grid merge).
+ * 112 attn_decode_cooperative. */
 int attn_abi_version(void);
 
 #ifdef __cplusplus

@@ -39,7 +39,7 @@ def test_library_exports_every_declared_symbol(L):
     for name in declared_functions():
         assert hasattr(L, name), name
         assert name in attn.EXPORTED
-    assert L.attn_abi_version() == 111
+    assert L.attn_abi_version() == 112
 
 
 def test_status_strings(L):

@@ -1,8 +1,10 @@
 """The paged decode with the LSE merge inside the same launch
 (attn_decode_paged_fused: the last split of each (sequence, KV head) to
-finish merges its partials, "splitk_kernels.py" _splitK_reduce) against the
-oracle, through the C ABI; and its workspace contract (arrival counters that
-start at zero and are left at zero)."""
+finish merges its partials, or, in the persistent int4 and fp8 kernels'
+cooperative launch, the whole grid merges after one grid barrier;
+"splitk_kernels.py" _splitK_reduce) against the oracle, through the C ABI;
+and its workspace contract (arrival counters and barrier words that start at
+zero and are left at zero)."""
 
 from dataclasses import replace
 
@@ -91,6 +93,37 @@ def test_fused_decode_matches_oracle_and_leaves_counters_zero(fmt, ng, hq, hkv, 
     torch.cuda.synchronize()
     assert status.item() == 0
     assert torch.equal(o, o2) and torch.equal(lse, lse2)
+
+
+@pytest.mark.parametrize("fmt,ng", [("int4", 4), ("fp8", 1)])
+def test_cooperative_and_last_arrival_merges_agree(fmt, ng):
+    """The persistent kernels' fused modes: with cooperative launches (the grid
+    merges after a grid barrier) and without (attn_decode_cooperative(False):
+    the last split to arrive merges), both against the oracle, with the same
+    bits, and both leave the workspace's counters and barrier words zero."""
+    dev = gpu_or_skip()
+    import causal_gqa_flashattention_attn_gb300 as attn
+    lens = [3000, 700, 64, 0, 1]
+    shape, inp, q = _inputs(fmt, ng, 32, 8, 1, 256, lens, seed=61)
+    partial = attn.attn_decode_workspace_bytes(len(lens), 32, 3000, 256, 128)
+    assert attn.attn_decode_cooperative() is True           # the default
+    outs = []
+    try:
+        for coop in (True, False):
+            attn.attn_decode_cooperative(coop)
+            status = torch.zeros(1, dtype=torch.int32, device=dev)
+            o, lse, ws = _fused(attn, dev, shape, inp, q, 256, 3000, status=status)
+            torch.cuda.synchronize()
+            assert status.item() == 0, (coop, status.item())
+            assert int(ws[partial:].count_nonzero()) == 0, coop
+            outs.append((o, lse))
+    finally:
+        attn.attn_decode_cooperative(True)
+    o_ref, lse_ref = _oracle(shape, inp, q, 256, 3000)
+    for o, lse in outs:
+        check_o(o, o_ref)
+        check_lse(lse, lse_ref)
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
 
 
 @pytest.mark.parametrize("fmt", ["dense", "int4"])
