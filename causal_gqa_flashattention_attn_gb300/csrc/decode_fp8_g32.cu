@@ -274,7 +274,8 @@ __device__ __forceinline__ void subtiles(WarpState& st, const uint8_t* kt, const
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
             const int wi = mt >> 1;
-            const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;   // bytes 2, 3 or 0, 1 of word wi, two tokens interleaved
+            // bytes 2, 3 (odd mt) or 0, 1 of word wi, the two tokens interleaved
+            const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
             const uint32_t xab = __byte_perm(xa[wi], xb[wi], sel);   // tokens 2t4, 2t4 + 1
             const uint32_t xcd = __byte_perm(xc[wi], xd[wi], sel);   // tokens 2t4 + 8, 2t4 + 9
             mma16816(st.o_acc[mt], e4m3x2_lo(xab), e4m3x2_hi(xab), e4m3x2_lo(xcd), e4m3x2_hi(xcd), pt0, pt1);
@@ -327,8 +328,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ int s_abort;
     __shared__ int s_skip[kStages];   // the stage was not loaded: its page id was out of range
     __shared__ __align__(8) uint64_t unit_bar;   // fused mode: the consumer warps have written a unit
-    __shared__ __align__(8) uint64_t last_bar;   // fused mode: warp 0 has counted the CTA in
-    __shared__ int s_last;                       // fused mode: this CTA's split arrived last
+    __shared__ __align__(8) uint64_t last_bar;   // fused modes: thread 0 has counted the CTA in (1) or met the grid (2)
+    __shared__ int s_last;                       // mode 1: the CTA's split arrived last; 2: the grid barrier passed
     __shared__ __align__(8) uint64_t exit_bar;   // cooperative mode: the consumer warps are done
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -436,7 +437,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // so its barriers' phase is the parity of the units this CTA took before
         auto fused_tail = [&]() -> bool {
             if constexpr (kMode != 1) return true;
-            const uint32_t ph = static_cast<uint32_t>((u - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x)) & 1u;
+            const uint32_t ph =
+                static_cast<uint32_t>((u - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x)) & 1u;
             int32_t* cnt = p.fused.counters + static_cast<size_t>(w.b) * p.Hkv + w.hg * kHeads;
             return unit_fused_tail(p.fused, p.o_part, p.lse_part, p.n_split, p.status, cnt, out_row(0), n_rows, ph,
                                    &unit_bar, &last_bar, &s_last, &s_abort, warp, lane);
@@ -661,7 +663,8 @@ cudaError_t launch_decode_fp8_g32(const DecodeArgs& a, const void* k_scale_shift
         // fused: a cooperative launch (every CTA resident at once) lets the whole
         // grid merge after one grid barrier; if it is refused, the split that
         // arrives last merges its (sequence, head group)
-        e = cudaFuncSetAttribute(decode_fp8_g32_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        e = cudaFuncSetAttribute(decode_fp8_g32_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem));
         if (e != cudaSuccess) return e;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeCooperative;
