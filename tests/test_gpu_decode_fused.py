@@ -34,6 +34,10 @@ CASES = [
     ("int4", 4, 32, 8, 9, 512, [900, 30]),              # 36 rows: the general kernel, row groups
     ("fp8", 1, 32, 8, 1, 2048, [700, 1, 2049, 3000]),
     ("fp8", 1, 32, 8, 4, 2048, [700, 4, 2100]),
+    # the persistent kernels' cooperative merge: about 7 units per CTA (64-token
+    # splits), and two groups of 8 KV heads with an empty sequence
+    ("int4", 4, 32, 8, 1, 64, [16384, 16384, 16000, 16383]),
+    ("fp8", 1, 64, 16, 1, 256, [3000, 700, 5, 0]),
 ]
 
 
