@@ -661,8 +661,7 @@ cudaError_t launch_decode_fp8_g32(const DecodeArgs& a, const void* k_scale_shift
     cudaError_t e;
     if (a.counters != nullptr && cooperative_launch_enabled()) {
         // fused: a cooperative launch (every CTA resident at once) lets the whole
-        // grid merge after one grid barrier; if it is refused, the split that
-        // arrives last merges its (sequence, head group)
+        // grid merge after one grid barrier
         e = cudaFuncSetAttribute(decode_fp8_g32_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(smem));
         if (e != cudaSuccess) return e;
@@ -677,7 +676,10 @@ cudaError_t launch_decode_fp8_g32(const DecodeArgs& a, const void* k_scale_shift
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         e = cudaLaunchKernelEx(&cfg, decode_fp8_g32_kernel<2>, k_map, v_map, kw_map, vw_map, p);
-        if (e != cudaErrorCooperativeLaunchTooLarge) return e;
+        if (e == cudaSuccess) return e;
+        // refused (too large to be resident at once, or a sharing mode without
+        // cooperative launches): clear the launch error and merge by last arrival;
+        // an error that is not the launch's own comes back from that launch too
         (void)cudaGetLastError();
     }
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
