@@ -4,7 +4,8 @@ Each check ties the oracle to something outside itself: hand-derived fixtures
 (tests/golden), brute force with scalar Python loops on tiny inputs, closed
 forms, a library routine (torch's scaled_dot_product_attention with an explicit
 boolean mask, and scipy's logsumexp), and invariants of the definition.  The
-last tests plant plausible mistakes in the oracle and check that a pin fails.
+tests at the end plant plausible mistakes in the oracle (a wrong mask, scale, sign,
+index, operand, bias or dropped term, one at a time) and check that a pin fails.
 """
 
 import math
@@ -164,6 +165,26 @@ def test_matches_torch_sdpa_with_explicit_mask(lq, lk):
     o, lse = oracle.prefill(q.numpy(), k.numpy(), v.numpy(), scale=0.37)
     np.testing.assert_allclose(o, ref.numpy(), rtol=1e-12, atol=1e-12)
     np.testing.assert_allclose(lse, ref_lse.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_default_scale_matches_torch_sdpa_default():
+    """With no scale given, the prefill and the decode use torch's own default
+    softmax scale (scaled_dot_product_attention without ``scale=``)."""
+    g = torch.Generator().manual_seed(9)
+    d = 16
+    q = torch.randn(1, 4, 6, d, generator=g, dtype=torch.float64) * 3
+    k = torch.randn(1, 2, 6, d, generator=g, dtype=torch.float64) * 3
+    v = torch.randn(1, 2, 6, d, generator=g, dtype=torch.float64)
+    kr, vr = k.repeat_interleave(2, dim=1), v.repeat_interleave(2, dim=1)
+    mask = torch.ones(6, 6, dtype=torch.bool).tril()
+    ref = torch.nn.functional.scaled_dot_product_attention(q, kr, vr, attn_mask=mask)
+    o, _ = oracle.prefill(q.numpy(), k.numpy(), v.numpy())
+    np.testing.assert_allclose(o, ref.numpy(), rtol=1e-12, atol=1e-12)
+    # the decode: the last query row against a one-page cache of the 6 rows
+    kc = k.numpy()[0].transpose(1, 0, 2)[None]       # [1 page, 6, Hkv, D]
+    vc = v.numpy()[0].transpose(1, 0, 2)[None]
+    od, _ = oracle.decode_unsplit(q.numpy()[:, :, -1], kc, vc, np.array([[0]]), [6], 6)
+    np.testing.assert_allclose(od[0], ref.numpy()[0, :, -1], rtol=1e-12, atol=1e-12)
 
 
 # ------------------------------------------------------------- invariants
@@ -658,3 +679,102 @@ def test_varlen_paged_prefill_equals_dense_prefill_per_sequence(page_size):
         ob, lb = _brute_prefill(qb, kk.transpose(1, 0, 2)[None], vv.transpose(1, 0, 2)[None], 0.3)
         np.testing.assert_allclose(o[qo[b]:qo[b + 1]], ob[0].transpose(1, 0, 2), rtol=1e-12, atol=1e-12)
         np.testing.assert_allclose(lse[qo[b]:qo[b + 1]], lb[0].T, rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------- more planted mistakes, one each
+
+def test_planted_default_scale_of_one_over_d_is_caught(monkeypatch):
+    """A default scale of 1/D instead of 1/sqrt(D) fails the library default."""
+    monkeypatch.setattr(oa, "_default_scale", lambda d: 1.0 / d)
+    with pytest.raises(AssertionError):
+        test_default_scale_matches_torch_sdpa_default()
+
+
+def test_planted_strict_causal_mask_is_caught(monkeypatch):
+    """A mask that hides the diagonal (j < i + delta) fails the brute force."""
+    def strict(q_len, kv_len, rows=None):
+        i = np.arange(q_len) if rows is None else np.asarray(rows)
+        return np.arange(kv_len)[None, :] < i[:, None] + (kv_len - q_len)
+    monkeypatch.setattr(oa, "visible_mask", strict)
+    with pytest.raises(AssertionError):
+        test_brute_force_tiny(2, 4, 2, 3, 6, 2)
+
+
+def test_planted_k_in_place_of_v_is_caught(monkeypatch):
+    """Weighting the key rows instead of the value rows fails the brute force."""
+    real = oa.attend
+    monkeypatch.setattr(oa, "attend", lambda q, k, v, mask, scale: real(q, k, k, mask, scale))
+    with pytest.raises(AssertionError):
+        test_brute_force_tiny(1, 2, 1, 4, 4, 3)
+
+
+def test_planted_merge_weights_of_the_wrong_sign_are_caught(monkeypatch, golden):
+    """Weights proportional to exp(-LSE_s) fail the merge fixture."""
+    real = oracle.lse_merge
+    monkeypatch.setattr(oracle, "lse_merge", lambda o, lse: real(o, -np.asarray(lse)))
+    with pytest.raises(AssertionError):
+        test_golden_merge_two_splits(golden)
+
+
+def test_planted_page_and_slot_swapped_are_caught(monkeypatch, golden):
+    """Taking the page from t % page_size and the slot from t // page_size
+    fails the block-table fixture."""
+    def swapped(block_table, b, t, page_size):
+        return int(block_table[b][t % page_size]) * page_size + t // page_size
+    monkeypatch.setattr(oracle, "paged_row_index", swapped)
+    with pytest.raises(AssertionError):
+        test_golden_block_table(golden)
+
+
+def test_planted_gather_without_the_block_table_is_caught(monkeypatch):
+    """Reading logical page t // page_size as if it were the physical page
+    fails the decode's page-by-page brute force."""
+    def no_table(cache, block_table, b, t_lo, t_hi, page_size):
+        rows = [np.asarray(cache[t // page_size, t % page_size]) for t in range(t_lo, t_hi)]
+        return np.stack(rows) if rows else np.zeros((0,) + tuple(cache.shape[2:]))
+    monkeypatch.setattr(oa, "gather_paged_rows", no_table)
+    with pytest.raises(AssertionError):
+        test_decode_matches_dense_attention_on_gathered_rows("dense", 1)
+
+
+def test_planted_one_split_short_is_caught(monkeypatch):
+    """One split too few drops the tail of the longest sequence and fails the
+    multi-query brute force."""
+    real = oa.num_splits
+    monkeypatch.setattr(oa, "num_splits", lambda n, s: max(1, real(n, s) - 1))
+    with pytest.raises(AssertionError):
+        test_multi_query_decode_equals_prefill_over_the_gathered_sequence()
+
+
+def test_planted_fp8_exponent_bias_of_eight_is_caught(monkeypatch, golden):
+    """An e4m3 decoder with exponent bias 8 fails the fp8 fixture."""
+    real = oracle.fp8_e4m3_value
+    monkeypatch.setattr(oracle, "fp8_e4m3_value", lambda b: real(b) / 2)
+    with pytest.raises(AssertionError):
+        test_golden_fp8_e4m3(golden)
+
+
+def test_planted_merge_bwd_without_the_output_term_is_caught(monkeypatch):
+    """Dropping sum_d (O_s - O)_d dO_d from dLSE_s fails torch autograd."""
+    real = oracle.lse_merge_bwd
+
+    def dropped(o_part, lse_part, d_o, d_lse=None):
+        g_o, _ = real(o_part, lse_part, d_o, d_lse)
+        _, g_l = real(o_part, lse_part, np.zeros_like(np.asarray(d_o)), d_lse)
+        return g_o, g_l
+    monkeypatch.setattr(oracle, "lse_merge_bwd", dropped)
+    with pytest.raises(AssertionError):
+        test_merge_bwd_matches_torch_autograd()
+
+
+def test_planted_varlen_full_last_page_is_caught(monkeypatch):
+    """Treating every last page as full fails the ragged prefill's per-sequence
+    brute force on a cache of page size 3 (kv lengths 4 and 7 end mid-page)."""
+    real = oracle.prefill_paged_varlen
+
+    def full_pages(q, k_cache, v_cache, qo_indptr, kv_indptr, kv_indices, page_size=1,
+                   kv_last_page_len=None, scale=None):
+        return real(q, k_cache, v_cache, qo_indptr, kv_indptr, kv_indices, page_size, None, scale)
+    monkeypatch.setattr(oracle, "prefill_paged_varlen", full_pages)
+    with pytest.raises(AssertionError):
+        test_varlen_paged_prefill_equals_dense_prefill_per_sequence(3)
