@@ -605,7 +605,7 @@ def run_ours(args, rank, world, dist):
     # algorithmic bytes: partials read once, gradients in, gradient partials out
     mbb = n_rows * s_max * (dd + 1) * 4 * 2 + n_rows * (dd + 1) * 4
     rep["merge_bwd"] = dict(bound="hbm", achieved=mbb / (ms["merge_bwd"] * 1e-3) / 1e9, peak=peaks["hbm_gbs"],
-                            unit="GB/s", work=mbb, src="merge.cu", kernel="lse_merge_bwd_kernel")
+                            unit="GB/s", work=mbb, src="merge.cu", kernel="lse_merge_bwd_short_kernel")
     mqb = dec["decode_bf16"]["bytes"]["kernel"] + mq_q.numel() * 2 - d16.B * d16.Hq * d16.D * 2
     rep["decode_mq"] = dict(bound="hbm", achieved=mqb / (ms["decode_mq"] * 1e-3) / 1e9, peak=peaks["hbm_gbs"],
                             unit="GB/s", work=mqb, src="decode.cu", kernel="decode_bf16_kernel (q_len 4)")

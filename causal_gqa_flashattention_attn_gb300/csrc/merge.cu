@@ -171,10 +171,71 @@ __global__ void __launch_bounds__(32 * kWarps) lse_merge_kernel(const float* __r
 // with w_s = exp(LSE_s - LSE) the weight of split s,
 //   dO_s = w_s * dO,   dLSE_s = w_s * dLSE + sum_d (O_s - O)_d * w_s * dO_d.
 // The merged O and LSE are recomputed here from the partials (fp32), so the
-// caller needs to keep only the partials.  One warp per row.  Rows of up to 16
-// splits with D <= 128 load every partial once, with dO, and keep them in
-// registers for both the merged O and the dot products; longer rows go in
-// batches of splits whose loads are in flight together.
+// caller needs to keep only the partials.  One warp per row.
+//
+// Rows of up to 16 splits with D <= 128: every partial is loaded once, with
+// dO, and kept in registers for both the merged O and the dot products.  This
+// kernel is separate from the general one so that its register count is its
+// own: four CTAs fit on an SM, and 2048 rows take one wave of 152 SMs.
+__global__ void __launch_bounds__(32 * kWarps, 4) lse_merge_bwd_short_kernel(
+    const float* __restrict__ o_part, const float* __restrict__ lse_part, const float* __restrict__ d_o,
+    const float* __restrict__ d_lse, int N, int S, int D, float* __restrict__ d_o_part,
+    float* __restrict__ d_lse_part) {
+    const int row = blockIdx.x * kWarps + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= N) return;
+    const float* lp = lse_part + static_cast<size_t>(row) * S;
+    const float* op = o_part + static_cast<size_t>(row) * S * D;
+    float* dop = d_o_part + static_cast<size_t>(row) * S * D;
+    float* dlp = d_lse_part + static_cast<size_t>(row) * S;
+    const int d = 4 * lane;
+    const float l = lane < S ? lp[lane] : -INFINITY;
+    float4 v[kFastSplits];
+#pragma unroll
+    for (int u = 0; u < kFastSplits; ++u)
+        v[u] = (u < S && d < D) ? ld4(op + static_cast<size_t>(u) * D + d) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4 g = d < D ? ld4(d_o + static_cast<size_t>(row) * D + d) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float dl = (d_lse != nullptr) ? d_lse[row] : 0.f;
+    const float mx = warp_max(l);
+    const bool alive = mx != -INFINITY;
+    const float w0 = (l == -INFINITY) ? 0.f : expf(l - mx);
+    const float wsum = warp_sum(w0);
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int u = 0; u < kFastSplits; ++u) {
+        const float wu = __shfl_sync(0xffffffffu, w0, u);
+        if (wu != 0.f) {
+            a.x = fmaf(wu, v[u].x, a.x);
+            a.y = fmaf(wu, v[u].y, a.y);
+            a.z = fmaf(wu, v[u].z, a.z);
+            a.w = fmaf(wu, v[u].w, a.w);
+        }
+    }
+    const float inv = alive ? 1.f / wsum : 0.f;
+    const float4 o = make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
+    const float lse = alive ? mx + logf(wsum) : -INFINITY;
+    const float wl = (alive && l != -INFINITY) ? expf(l - lse) : 0.f;   // lane s: weight of split s
+    // per split, this lane's share of sum_d (O_s - O)_d dO_d; splits past S
+    // (zero O, weight 0) give 0
+    float dot[kFastSplits];
+#pragma unroll
+    for (int u = 0; u < kFastSplits; ++u) {
+        const float wu = __shfl_sync(0xffffffffu, wl, u);
+        const float4 x = wu != 0.f ? v[u] : o;
+        dot[u] = (x.x - o.x) * g.x + (x.y - o.y) * g.y + (x.z - o.z) * g.z + (x.w - o.w) * g.w;
+        if (u < S && d < D)
+            *reinterpret_cast<float4*>(dop + static_cast<size_t>(u) * D + d) =
+                make_float4(wu * g.x, wu * g.y, wu * g.z, wu * g.w);
+    }
+    static_assert(kFastSplits == 16, "warp_sum16 reduces 16 values");
+    const float t = warp_sum16(dot, lane);   // lanes 2u, 2u + 1: split u
+    const int u = lane >> 1;
+    const float wu = __shfl_sync(0xffffffffu, wl, u);
+    if ((lane & 1) == 0 && u < S) dlp[u] = wu * (dl + t);
+}
+
+// The general case: longer rows, or D > 128, in batches of splits whose loads
+// are in flight together.
 __global__ void __launch_bounds__(32 * kWarps) lse_merge_bwd_kernel(
     const float* __restrict__ o_part, const float* __restrict__ lse_part, const float* __restrict__ d_o,
     const float* __restrict__ d_lse, int N, int S, int D, float* __restrict__ d_o_part,
@@ -186,53 +247,6 @@ __global__ void __launch_bounds__(32 * kWarps) lse_merge_bwd_kernel(
     const float* op = o_part + static_cast<size_t>(row) * S * D;
     float* dop = d_o_part + static_cast<size_t>(row) * S * D;
     float* dlp = d_lse_part + static_cast<size_t>(row) * S;
-    if (S <= kFastSplits && D <= 128) {
-        const int d = 4 * lane;
-        const float l = lane < S ? lp[lane] : -INFINITY;
-        float4 v[kFastSplits];
-#pragma unroll
-        for (int u = 0; u < kFastSplits; ++u)
-            v[u] = (u < S && d < D) ? ld4(op + static_cast<size_t>(u) * D + d) : make_float4(0.f, 0.f, 0.f, 0.f);
-        const float4 g = d < D ? ld4(d_o + static_cast<size_t>(row) * D + d) : make_float4(0.f, 0.f, 0.f, 0.f);
-        const float dl = (d_lse != nullptr) ? d_lse[row] : 0.f;
-        const float mx = warp_max(l);
-        const bool alive = mx != -INFINITY;
-        const float w0 = (l == -INFINITY) ? 0.f : expf(l - mx);
-        const float wsum = warp_sum(w0);
-        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int u = 0; u < kFastSplits; ++u) {
-            const float wu = __shfl_sync(0xffffffffu, w0, u);
-            if (wu != 0.f) {
-                a.x = fmaf(wu, v[u].x, a.x);
-                a.y = fmaf(wu, v[u].y, a.y);
-                a.z = fmaf(wu, v[u].z, a.z);
-                a.w = fmaf(wu, v[u].w, a.w);
-            }
-        }
-        const float inv = alive ? 1.f / wsum : 0.f;
-        const float4 o = make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
-        const float lse = alive ? mx + logf(wsum) : -INFINITY;
-        const float wl = (alive && l != -INFINITY) ? expf(l - lse) : 0.f;   // lane s: weight of split s
-        // per split, this lane's share of sum_d (O_s - O)_d dO_d; splits past S
-        // (zero O, weight 0) give 0
-        float dot[kFastSplits];
-#pragma unroll
-        for (int u = 0; u < kFastSplits; ++u) {
-            const float wu = __shfl_sync(0xffffffffu, wl, u);
-            const float4 x = wu != 0.f ? v[u] : o;
-            dot[u] = (x.x - o.x) * g.x + (x.y - o.y) * g.y + (x.z - o.z) * g.z + (x.w - o.w) * g.w;
-            if (u < S && d < D)
-                *reinterpret_cast<float4*>(dop + static_cast<size_t>(u) * D + d) =
-                    make_float4(wu * g.x, wu * g.y, wu * g.z, wu * g.w);
-        }
-        static_assert(kFastSplits == 16, "warp_sum16 reduces 16 values");
-        const float t = warp_sum16(dot, lane);   // lanes 2u, 2u + 1: split u
-        const int u = lane >> 1;
-        const float wu = __shfl_sync(0xffffffffu, wl, u);
-        if ((lane & 1) == 0 && u < S) dlp[u] = wu * (dl + t);
-        return;
-    }
     float mx, wsum;
     row_weights(lp, S, lane, mx, wsum);
     const bool alive = mx != -INFINITY;
@@ -292,8 +306,12 @@ cudaError_t launch_merge_bwd(const float* o_part, const float* lse_part, const f
                              int S, int D, float* d_o_part, float* d_lse_part, cudaStream_t stream) {
     if (N == 0) return cudaSuccess;
     const dim3 grid((N + kWarps - 1) / kWarps);
-    lse_merge_bwd_kernel<<<grid, 32 * kWarps, 0, stream>>>(o_part, lse_part, d_o, d_lse, N, S, D, d_o_part,
-                                                           d_lse_part);
+    if (S <= kFastSplits && D <= 128)
+        lse_merge_bwd_short_kernel<<<grid, 32 * kWarps, 0, stream>>>(o_part, lse_part, d_o, d_lse, N, S, D,
+                                                                     d_o_part, d_lse_part);
+    else
+        lse_merge_bwd_kernel<<<grid, 32 * kWarps, 0, stream>>>(o_part, lse_part, d_o, d_lse, N, S, D, d_o_part,
+                                                               d_lse_part);
     return cudaGetLastError();
 }
 

@@ -39,7 +39,11 @@ def test_merge_bf16_output():
     check_lse(lse, lse_ref)
 
 
-@pytest.mark.parametrize("n,s,d", [(1, 1, 128), (37, 5, 128), (300, 16, 128), (9, 40, 1024), (5, 2, 4)])
+# the short-row kernel takes up to 16 splits with D <= 128; (2048, 16, 128) is
+# the bf16 decode's partial shape, a whole wave of it; 17 splits or D = 132
+# go to the general kernel
+@pytest.mark.parametrize("n,s,d", [(1, 1, 128), (37, 5, 128), (300, 16, 128), (2048, 16, 128), (9, 40, 1024),
+                                   (5, 2, 4), (64, 17, 128), (33, 16, 132)])
 def test_merge_bwd_matches_oracle(n, s, d):
     """Gradient of the merge ("splitk_kernels.py", _splitK_reduce_varargs_backward)."""
     dev = gpu_or_skip()
