@@ -818,6 +818,18 @@ def run_profile(args):
             else:
                 attn.attn_prefill_paged_varlen(t["q"], t["k_cache"], t["v_cache"], t["qo_indptr"], t["kv_indptr"],
                                                t["kv_indices"], t["kv_last_page_len"])
+    elif args.profile == "merge_bwd":
+        # partials of the bf16 decode's shape (rows = B * Hq, its split count, D), synthetic values
+        shape = synth.PAGED_DECODE_BF16
+        n_split = -(-shape.len_hi // shape.split_tokens)
+        o_part, lse_part = synth.merge_inputs(shape.B * shape.Hq, n_split, shape.D, seed=0)
+        g = torch.Generator().manual_seed(1)
+        d_o = torch.randn(shape.B * shape.Hq, shape.D, generator=g).to(dev)
+        d_lse = torch.randn(shape.B * shape.Hq, generator=g).to(dev)
+        op, lp = o_part.to(dev), lse_part.to(dev)
+        go, gl = torch.empty_like(op), torch.empty_like(lp)
+        for _ in range(n):
+            attn.attn_lse_merge_bwd(op, lp, d_o, d_lse, d_o_part=go, d_lse_part=gl)
     elif args.profile.startswith("prefill"):
         shape = synth.LLAMA_GQA_PREFILL if args.profile == "prefill" else synth.BATCHED_SQUARE_PREFILL
         q, k, v = (t.to(dev) for t in synth.prefill_inputs(shape, seed=0))
@@ -858,7 +870,7 @@ def main():
     ap.add_argument("--clock-window", type=float, default=2.0,
                     help="seconds of loaded, untimed steps sampled by nvidia-smi before the timed region")
     ap.add_argument("--profile", choices=["prefill", "prefill_batched", "prefill_varlen", "prefill_varlen_ws", "decode_bf16", "decode_int4",
-                                          "decode_fp8"],
+                                          "decode_fp8", "merge_bwd"],
                     help="run only one kernel on its workload (for ncu captures); prints no JSON line")
     ap.add_argument("--decode-batch", type=int, default=0, help="with --profile: shrink the decode batch")
     args = ap.parse_args()
